@@ -1,0 +1,327 @@
+"""Oracle: SageBwd forward and backward (TEST INFRASTRUCTURE, not product code).
+
+The algorithm is taken in the pages' order and notation:
+
+Forward -- "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps,
+forward (1)-(5); "SageAttention3 ..." (review), eq. (1) (online softmax) and eq. (8)
+(INT8 forward: S_ij = MM(Q^_i, K^_j) s_Q s_K, per-token P with s_P = exp(rowmax(S_ij) - m_ij)/127,
+O_ij update); section summary A.1 (returns O and the log-sum-exp L).
+
+Backward -- "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps,
+backward (1)-(7); "SageAttention3 ..." (review), INT8 backward (Algorithm 3 equations): dV, dP kept
+16-bit, dS = P o (dP - D), dQ, dK with per-block INT8 products; section summary A.2.
+
+Readings where the pages are silent, garbled or at odds (listed again in the design doc):
+  R1  the softmax scale 1/sqrt(d) is applied after dequantisation, in float32, folded with
+      log2(e): t = fl32(acc * fl32(fl32(s_Q s_K) * fl32(log2(e)/sqrt(d)))) -- logits in log2 units;
+      dQ and dK carry 1/sqrt(d) by the chain rule.
+  R7  forward P^ is per token per 64-key tile: P^ = rne(fl32(127 * fl32(2^(fl32(t - r))))) with r
+      the row max over the tile's unmasked entries; s_P = 2^(r - m)/127; l accumulates the
+      unquantised P~ (eq. 1); eq. (8)'s inverted rescale "diag(...)^-1" is read as eq. (1)'s
+      non-inverted one.
+  R8  backward P and dS are quantised per 64x64 tile: s = fl32(max|x|/127), q =
+      rne(fl32(x * fl32(1/s))); a tile whose max|x| is below 2^-120 (zero, or so small that
+      1/s would overflow float32) gets s = 0, q = 0.
+  R9  dP = dO V^T uses the unquantised 16-bit dO and V, float32 result, never rounded to 16 bits.
+  R10 D = rowsum(dO o O) uses the stored 16-bit O.
+  R11 no K-smoothing correction in the backward pass.
+  R12 causal = top-left-aligned mask (key index <= query index); fully masked tiles are skipped.
+  R13 L is natural-log, float32, in units of the scaled logits.
+  R5  with Q-smoothing, S gets the bias mu_Qi K_sm,j^T (before 1/sqrt(d)) and dK gets
+      (dS_ij^T 1) mu_Qi^T / sqrt(d) from the unquantised dS.
+
+Where float decides an integer code (P^, dS^), the decision is taken in float32 as the kernel
+does; everything that only accumulates (m, l, O, dV, dQ, dK, D) is float64.
+
+The ``DEQUANTISED`` arithmetic replaces every quantiser by the identity and drops every float32
+rounding; the very same tiled code must then equal float64 full-precision attention, which pins
+the tiling, the online-softmax bookkeeping, L and the backward structure (tests/test_oracle_sage.py).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from .quant import BLOCK, quantize_per_block, quantize_smooth, k_mean, q_block_mean
+
+LOG2E = 1.4426950408889634      # log2(e), the double nearest 1/ln(2)
+LN2 = 0.6931471805599453
+F32 = np.float32
+# R8b: a backward P / dS tile whose max|x| is below 2^-120 is a zero tile (s = 0, q = 0); below
+# that bound the float32 reciprocal 1/s of its scale would overflow.
+TILE_ZERO_BELOW = np.float32(2.0 ** -120)
+
+
+class Arith:
+    """The arithmetic of the quantisation steps: SageBwd's (quantised) or the identity limit."""
+
+    def __init__(self, quantised: bool):
+        self.quantised = quantised
+
+    # -- plain float helpers --------------------------------------------------------------
+    def r32(self, x):
+        return np.asarray(x, np.float64).astype(np.float32) if self.quantised else np.asarray(x, np.float64)
+
+    def scale_log2(self, d: int):
+        return F32(LOG2E / math.sqrt(d)) if self.quantised else LOG2E / math.sqrt(d)
+
+    def logit_scale(self, sq, sk, sl2):
+        """c = fl32(fl32(s_Q s_K) * sl2): the float32 factor taking an integer product to log2 units."""
+        if self.quantised:
+            return F32(F32(sq) * F32(sk)) * F32(sl2)
+        return float(sq) * float(sk) * float(sl2)
+
+    # -- exact integer block products ------------------------------------------------------
+    def int_mm(self, a, b):
+        """MM(A^, B^): exact for integer codes (every partial sum is far below 2^53)."""
+        p = np.asarray(a, np.float64) @ np.asarray(b, np.float64)
+        if not self.quantised:
+            return p
+        r = np.rint(p)
+        assert np.array_equal(r, p), "integer block product is not integral"
+        return r.astype(np.int64)
+
+    def logits(self, s_int, c):
+        """t = fl32(acc * c); |acc| < 2^24 so the int -> float32 conversion is exact."""
+        if self.quantised:
+            return np.asarray(s_int, np.float64).astype(np.float32) * F32(c)
+        return np.asarray(s_int, np.float64) * c
+
+    # -- the quantisers --------------------------------------------------------------------
+    def block_quant(self, x):
+        """Per-64-token-block quantiser of Q, K, V, dO (see oracle.quant)."""
+        if self.quantised:
+            return quantize_per_block(x)
+        x = np.asarray(x, np.float64)
+        return x, np.ones(x.shape[:-2] + (x.shape[-2] // BLOCK,))
+
+    def token_quant(self, t, r):
+        """Forward per-token P^ of one tile (R7).  Returns (2^(t - r) in float64, P^)."""
+        diff64 = t.astype(np.float64) - r[:, None].astype(np.float64)
+        e64 = np.exp2(diff64)
+        if not self.quantised:
+            return e64, 127.0 * e64
+        e32 = np.exp2((t - r[:, None].astype(np.float32)).astype(np.float64)).astype(np.float32)
+        x = F32(127) * e32
+        return e64, np.clip(np.rint(x), 0, 127).astype(np.int64)
+
+    def tile_quant(self, x):
+        """Backward per-tile quantiser of P and dS (R8).  Returns (scale, codes)."""
+        if not self.quantised:
+            return 1.0, np.asarray(x, np.float64)
+        x = np.asarray(x, np.float32)
+        mx = np.max(np.abs(x)) if x.size else F32(0)
+        if mx < TILE_ZERO_BELOW:
+            return F32(0), np.zeros(x.shape, np.int64)
+        s = F32(mx) / F32(127)
+        inv = F32(1) / s
+        q = np.clip(np.rint(x * inv), -127, 127).astype(np.int64)
+        return s, q
+
+    def exp2_32(self, x):
+        if self.quantised:
+            return np.exp2(np.asarray(x, np.float32).astype(np.float64)).astype(np.float32)
+        return np.exp2(np.asarray(x, np.float64))
+
+
+QUANTISED = Arith(True)
+DEQUANTISED = Arith(False)
+
+
+def prepare(Q, K, V, smooth_k: bool = True, smooth_q: bool = False, arith: Arith = QUANTISED) -> dict:
+    """Steps a1 + a2 in the chosen arithmetic: K-mean, smoothing and the per-block quantisers."""
+    if arith.quantised:
+        return quantize_smooth(Q, K, V, smooth_k=smooth_k, smooth_q=smooth_q)
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    B, H, N, d = K.shape
+    ones = np.ones((B, H, N // BLOCK))
+    muK = K.mean(axis=-2) if smooth_k else np.zeros((B, H, d))
+    Ksm = K - muK[:, :, None, :]
+    if smooth_q:
+        muQ = Q.reshape(B, H, N // BLOCK, BLOCK, d).mean(axis=-2)
+        Qsm = (Q.reshape(B, H, N // BLOCK, BLOCK, d) - muQ[:, :, :, None, :]).reshape(B, H, N, d)
+    else:
+        muQ, Qsm = None, Q
+    return dict(Qh=Qsm, Kh=Ksm, Vh=V, sQ=ones, sK=ones.copy(), sV=ones.copy(), muK=muK, muQ=muQ, Ksm=Ksm)
+
+
+def _bias_log2(prep, b, h, i, sl2, arith: Arith):
+    """Q-smoothing bias of query block i in log2 units: fl32(fl32(mu_Qi . K_sm[n]) * sl2) per key n."""
+    mu = np.asarray(prep["muQ"][b, h, i], np.float64)
+    ksm = np.asarray(prep["Ksm"][b, h], np.float64)
+    bias = ksm @ mu
+    if arith.quantised:
+        return bias.astype(np.float32) * F32(sl2)
+    return bias * sl2
+
+
+def _causal_mask(n: int) -> np.ndarray:
+    """True where a key lies after the query inside a diagonal tile (top-left aligned)."""
+    return np.triu(np.ones((n, n), bool), k=1)
+
+
+def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=None, heads=None,
+                 record: dict | None = None):
+    """SageBwd forward (steps a3-a6).  Returns (O float64 (B,H,N,d), L float64 (B,H,N)).
+
+    ``q_blocks`` limits the query blocks computed (others stay zero), ``heads`` the (b, h) pairs.
+    ``record`` (small N only) receives, per head, the integer S products, the P^ codes and the
+    integer P^ V^ products of every tile.
+    """
+    Qh, Kh, Vh = prep["Qh"], prep["Kh"], prep["Vh"]
+    sQ, sK, sV = prep["sQ"], prep["sK"], prep["sV"]
+    B, H, N, d = Qh.shape
+    T = N // BLOCK
+    sl2 = arith.scale_log2(d)
+    O = np.zeros((B, H, N, d))
+    L = np.zeros((B, H, N))
+    mask = _causal_mask(BLOCK)
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for (b, h) in heads:
+        if record is not None:
+            rec = record.setdefault((b, h), {})
+            rec["S_int"] = np.zeros((N, N), np.int64)
+            rec["P_hat"] = np.zeros((N, N), np.int64)
+            rec["PV_int"] = {}
+        for i in (range(T) if q_blocks is None else q_blocks):
+            rows = slice(i * BLOCK, (i + 1) * BLOCK)
+            m = np.full(BLOCK, -np.inf)
+            l = np.zeros(BLOCK)
+            acc = np.zeros((BLOCK, d))
+            bias = _bias_log2(prep, b, h, i, sl2, arith) if prep.get("muQ") is not None else None
+            for j in range(T):
+                if causal and j > i:
+                    break
+                cols = slice(j * BLOCK, (j + 1) * BLOCK)
+                # (3) S_ij = MM(Q^_i, K^_j) * s_Q * s_K  (and * 1/sqrt(d), in log2 units)
+                s_int = arith.int_mm(Qh[b, h, rows], np.swapaxes(Kh[b, h, cols], 0, 1))
+                t = arith.logits(s_int, arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2))
+                if bias is not None:
+                    t = t + bias[cols][None, :]
+                if causal and j == i:
+                    t = np.where(mask, -np.inf, t)
+                # (4) online softmax statistics and per-token quantisation of P~
+                r = t.max(axis=1)
+                m_new = np.maximum(m, r.astype(np.float64))
+                e64, p_hat = arith.token_quant(t, r)
+                alpha = np.exp2(m - m_new)
+                grow = np.exp2(r.astype(np.float64) - m_new)
+                s_p = grow / 127.0
+                l = alpha * l + grow * e64.sum(axis=1)
+                # (5) O_ij = diag(e^{m_old - m_new}) O + MM(P^_ij, V^_j) * s_P * s_V
+                pv = arith.int_mm(p_hat, Vh[b, h, cols])
+                acc = alpha[:, None] * acc + (s_p * float(sV[b, h, j]))[:, None] * pv
+                m = m_new
+                if record is not None:
+                    rec["S_int"][rows, cols] = s_int
+                    rec["P_hat"][rows, cols] = p_hat
+                    rec["PV_int"][(i, j)] = pv
+            O[b, h, rows] = acc / l[:, None]
+            L[b, h, rows] = (m + np.log2(l)) * LN2
+    return O, L
+
+
+def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUANTISED,
+                  q_blocks=None, kv_blocks=None, heads=None, record: dict | None = None):
+    """SageBwd backward (steps a7-a13).  Returns dict(dQ, dK, dV float64 (B,H,N,d), D, dOh, sdO).
+
+    ``O_stored`` is the forward output as stored (16-bit values), ``L`` the stored float32 LSE.
+    ``q_blocks`` / ``kv_blocks`` restrict which dQ rows / dK, dV rows are completed (for sampled
+    checks at large N); by default everything is computed, looping over key/value blocks and,
+    inside, query blocks.  ``record`` receives the per-tile dequantised P, dP, dequantised dS.
+    """
+    Qh, Kh = prep["Qh"], prep["Kh"]
+    sQ, sK = prep["sQ"], prep["sK"]
+    B, H, N, d = Qh.shape
+    T = N // BLOCK
+    sl2 = arith.scale_log2(d)
+    inv_sqrt_d = 1.0 / math.sqrt(d)
+    if "V16" not in prep:
+        raise ValueError("prep must carry the unquantised 16-bit V as prep['V16']")
+    V64 = np.asarray(prep["V16"], np.float64)
+    dO = np.asarray(dO, np.float32)
+    O64 = np.asarray(O_stored, np.float64)
+    # (1) D = rowsum(dO o O) from the cached forward output
+    D = (dO.astype(np.float64) * O64).sum(axis=-1)
+    D32 = arith.r32(D)
+    dOh, sdO = arith.block_quant(dO)
+    L2 = arith.r32(np.asarray(L, np.float32 if arith.quantised else np.float64) * (F32(LOG2E) if arith.quantised else LOG2E))
+    dQ = np.zeros((B, H, N, d))
+    dK = np.zeros((B, H, N, d))
+    dV = np.zeros((B, H, N, d))
+    mask = _causal_mask(BLOCK)
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+
+    def tile(b, h, i, j, bias, want_dq, want_dkv):
+        rows = slice(i * BLOCK, (i + 1) * BLOCK)
+        cols = slice(j * BLOCK, (j + 1) * BLOCK)
+        # (2) recompute S_ij (same formula as the forward) and P_ij = exp(S_ij - L_i)
+        s_int = arith.int_mm(Qh[b, h, rows], np.swapaxes(Kh[b, h, cols], 0, 1))
+        t = arith.logits(s_int, arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2))
+        if bias is not None:
+            t = t + bias[cols][None, :]
+        if causal and i == j:
+            t = np.where(mask, -np.inf, t)
+        P = arith.exp2_32(arith.r32(t - L2[b, h, rows][:, None]))
+        # (3) dV_j += MM(P^_ij^T, dO^_i) * s_P * s_dO
+        s_p, p_hat = arith.tile_quant(P)
+        if want_dkv:
+            dV[b, h, cols] += (float(s_p) * float(sdO[b, h, i])) * arith.int_mm(p_hat.T, dOh[b, h, rows])
+        # (4) dP_ij = dO_i V_j^T, 16-bit operands, float32 result
+        dP = arith.r32(dO[b, h, rows].astype(np.float64) @ V64[b, h, cols].T)
+        # (5) dS_ij = P_ij o (dP_ij - D_i), then per-tile quantisation
+        dS = arith.r32(P * arith.r32(dP - D32[b, h, rows][:, None]))
+        s_ds, ds_hat = arith.tile_quant(dS)
+        # (6) dQ_i += MM(dS^_ij, K^_j) * s_dS * s_K   (and * 1/sqrt(d))
+        if want_dq:
+            dQ[b, h, rows] += (float(s_ds) * float(sK[b, h, j]) * inv_sqrt_d) * arith.int_mm(ds_hat, Kh[b, h, cols])
+        # (7) dK_j += MM(dS^_ij^T, Q^_i) * s_dS * s_Q   (and * 1/sqrt(d))
+        if want_dkv:
+            dK[b, h, cols] += (float(s_ds) * float(sQ[b, h, i]) * inv_sqrt_d) * arith.int_mm(ds_hat.T, Qh[b, h, rows])
+            if prep.get("muQ") is not None:
+                colsum = np.asarray(dS, np.float64).sum(axis=0)
+                dK[b, h, cols] += inv_sqrt_d * np.outer(colsum, np.asarray(prep["muQ"][b, h, i], np.float64))
+        if record is not None:
+            rec = record.setdefault((b, h), {})
+            for key in ("P", "dP", "dS"):
+                rec.setdefault(key, np.zeros((N, N)))
+            rec["P"][rows, cols] = float(s_p) * np.asarray(p_hat, np.float64)
+            rec["dP"][rows, cols] = dP
+            rec["dS"][rows, cols] = float(s_ds) * np.asarray(ds_hat, np.float64)
+
+    for (b, h) in heads:
+        biases = {}
+        def bias_of(i):
+            if prep.get("muQ") is None:
+                return None
+            if i not in biases:
+                biases[i] = _bias_log2(prep, b, h, i, sl2, arith)
+            return biases[i]
+        if q_blocks is None and kv_blocks is None:
+            for j in range(T):
+                for i in range(j if causal else 0, T):
+                    tile(b, h, i, j, bias_of(i), True, True)
+        else:
+            for j in (kv_blocks or []):
+                for i in range(j if causal else 0, T):
+                    tile(b, h, i, j, bias_of(i), False, True)
+            for i in (q_blocks or []):
+                for j in range(0, (i + 1) if causal else T):
+                    tile(b, h, i, j, bias_of(i), True, False)
+    return dict(dQ=dQ, dK=dK, dV=dV, D=D, dOh=dOh, sdO=sdO)
+
+
+def run(Q, K, V, dO, causal: bool, dtype_round, smooth_k: bool = True, smooth_q: bool = False,
+        arith: Arith = QUANTISED, record: dict | None = None):
+    """Whole path on full tensors: quantise, forward, backward.  ``dtype_round`` rounds O to the
+    stored 16-bit type (identity in the dequantised limit)."""
+    prep = prepare(Q, K, V, smooth_k=smooth_k, smooth_q=smooth_q, arith=arith)
+    prep["V16"] = np.asarray(V, np.float64)
+    O, L = sage_forward(prep, causal, arith=arith, record=record)
+    O_stored = dtype_round(O.astype(np.float32)) if arith.quantised else O
+    L_stored = L.astype(np.float32) if arith.quantised else L
+    g = sage_backward(prep, O_stored, L_stored, dO, causal, arith=arith, record=record)
+    return dict(prep=prep, O=O, L=L, O_stored=O_stored, L_stored=L_stored, **g)
