@@ -1,0 +1,225 @@
+"""Thin ctypes binding of libsage_gb300.so -- argument marshalling only.
+
+Every function here has the name of the C entry point it wraps.  Device memory (outputs and the
+workspace) comes from PyTorch; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: without the built library, or without a CUDA device, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsage_gb300.so")
+
+SAGE_OK, SAGE_ERR_ARG, SAGE_ERR_UNSUPPORTED, SAGE_ERR_ALIGN = 0, 1, 2, 3
+SAGE_ERR_CUDA, SAGE_ERR_TIMEOUT, SAGE_ERR_WORKSPACE = 4, 5, 6
+SAGE_FP16, SAGE_BF16 = 0, 1
+SAGE_FLAG_DUMP = 1
+
+EXPORTED = (
+    "sage_quantize_workspace_bytes", "sage_quantize_smooth", "sage_fwd_workspace_bytes",
+    "sage_attn_fwd", "sage_bwd_workspace_bytes", "sage_attn_bwd", "sage_dump_bytes",
+    "sage_device_status", "sage_status_string", "sage_version",
+)
+
+
+class SageParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int), ("d", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("causal", ctypes.c_int), ("smooth_k", ctypes.c_int),
+        ("smooth_q", ctypes.c_int), ("flags", ctypes.c_uint), ("dump", ctypes.c_void_p),
+        ("dump_bytes", ctypes.c_size_t),
+    ]
+
+
+class SageError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m bit_trainable_attention_sage_gb300.build` "
+            "(the SageBwd library has no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(SageParams)
+    vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    for name in ("sage_quantize_workspace_bytes", "sage_fwd_workspace_bytes", "sage_bwd_workspace_bytes"):
+        getattr(L, name).argtypes = [P]
+        getattr(L, name).restype = sz
+    L.sage_dump_bytes.argtypes = [P, ci]
+    L.sage_dump_bytes.restype = sz
+    L.sage_quantize_smooth.argtypes = [P] + [vp] * 12 + [sz, vp]
+    L.sage_quantize_smooth.restype = ci
+    L.sage_attn_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
+    L.sage_attn_fwd.restype = ci
+    L.sage_attn_bwd.argtypes = [P] + [vp] * 15 + [sz, vp]
+    L.sage_attn_bwd.restype = ci
+    L.sage_device_status.argtypes = [vp]
+    L.sage_device_status.restype = ci
+    L.sage_status_string.argtypes = [ci]
+    L.sage_status_string.restype = ctypes.c_char_p
+    L.sage_version.argtypes = []
+    L.sage_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(fn: str, status: int):
+    if status != SAGE_OK:
+        raise SageError(fn, status, lib().sage_status_string(status).decode())
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return SAGE_FP16
+    if t.dtype == torch.bfloat16:
+        return SAGE_BF16
+    raise TypeError(f"SageBwd takes fp16 or bf16 tensors, got {t.dtype}")
+
+
+def make_params(B: int, H: int, N: int, d: int, dtype: int, causal: bool, smooth_k: bool = True,
+                smooth_q: bool = False, dump: torch.Tensor | None = None) -> SageParams:
+    p = SageParams(B, H, N, d, dtype, int(causal), int(smooth_k), int(smooth_q), 0, None, 0)
+    if dump is not None:
+        p.flags = SAGE_FLAG_DUMP
+        p.dump = dump.data_ptr()
+        p.dump_bytes = dump.numel() * dump.element_size()
+    return p
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("SageBwd tensors must be contiguous CUDA tensors")
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+@dataclass
+class Quantized:
+    """The quantised forward inputs (codes, scales, means) and the problem description."""
+    Qh: torch.Tensor
+    Kh: torch.Tensor
+    Vh: torch.Tensor
+    sQ: torch.Tensor
+    sK: torch.Tensor
+    sV: torch.Tensor
+    muK: torch.Tensor
+    muQ: torch.Tensor | None
+    dtype: int
+    smooth_k: bool
+    smooth_q: bool
+
+
+def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, smooth_k: bool = True,
+                         smooth_q: bool = False, stream=None) -> Quantized:
+    """K-smoothing (+ optional Q-smoothing) and per-block INT8 quantisation of (B,H,N,d) Q, K, V."""
+    _require_cuda(Q, K, V)
+    B, H, N, d = Q.shape
+    dt = _dtype_code(Q)
+    dev = Q.device
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q)
+    Qh = torch.empty((B, H, N, d), dtype=torch.int8, device=dev)
+    Kh, Vh = torch.empty_like(Qh), torch.empty_like(Qh)
+    sQ = torch.empty((B, H, N // 64), dtype=torch.float32, device=dev)
+    sK, sV = torch.empty_like(sQ), torch.empty_like(sQ)
+    muK = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    muQ = torch.empty((B, H, N // 64, d), dtype=torch.float32, device=dev) if smooth_q else None
+    L = lib()
+    nws = L.sage_quantize_workspace_bytes(ctypes.byref(p))
+    ws = _workspace(nws, dev)
+    st = L.sage_quantize_smooth(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(Qh), _ptr(Kh), _ptr(Vh),
+                                _ptr(sQ), _ptr(sK), _ptr(sV), _ptr(muK), _ptr(muQ), _ptr(ws), nws,
+                                _stream(stream))
+    _check("sage_quantize_smooth", st)
+    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q)
+
+
+def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, dump: torch.Tensor | None = None,
+                  stream=None):
+    """SageBwd forward.  Returns (O (B,H,N,d) in the input dtype, L (B,H,N) float32)."""
+    B, H, N, d = q.Qh.shape
+    dev = q.Qh.device
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump)
+    odt = torch.float16 if q.dtype == SAGE_FP16 else torch.bfloat16
+    O = torch.empty((B, H, N, d), dtype=odt, device=dev) if out is None else out
+    Lse = torch.empty((B, H, N), dtype=torch.float32, device=dev) if lse is None else lse
+    _require_cuda(O, Lse, K)
+    L = lib()
+    nws = L.sage_fwd_workspace_bytes(ctypes.byref(p))
+    ws = workspace if workspace is not None else _workspace(nws, dev)
+    st = L.sage_attn_fwd(ctypes.byref(p), _ptr(q.Qh), _ptr(q.Kh), _ptr(q.Vh), _ptr(q.sQ), _ptr(q.sK),
+                         _ptr(q.sV), _ptr(K), _ptr(q.muK), _ptr(q.muQ), _ptr(O), _ptr(Lse), _ptr(ws),
+                         nws if ws is None else ws.numel(), _stream(stream))
+    _check("sage_attn_fwd", st)
+    return O, Lse
+
+
+def sage_attn_bwd(q: Quantized, V: torch.Tensor, O: torch.Tensor, L: torch.Tensor, dO: torch.Tensor, *,
+                  causal: bool, K: torch.Tensor | None = None, grads=None,
+                  workspace: torch.Tensor | None = None, dump: torch.Tensor | None = None, stream=None):
+    """SageBwd backward.  Returns (dQ, dK, dV), float32 (B,H,N,d)."""
+    _require_cuda(V, O, L, dO, K)
+    B, H, N, d = q.Qh.shape
+    dev = q.Qh.device
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump)
+    if grads is None:
+        grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3))
+    dQ, dK, dV = grads
+    lb = lib()
+    nws = lb.sage_bwd_workspace_bytes(ctypes.byref(p))
+    ws = workspace if workspace is not None else _workspace(nws, dev)
+    st = lb.sage_attn_bwd(ctypes.byref(p), _ptr(q.Qh), _ptr(q.Kh), _ptr(q.sQ), _ptr(q.sK), _ptr(K),
+                          _ptr(q.muK), _ptr(q.muQ), _ptr(V), _ptr(O), _ptr(L), _ptr(dO), _ptr(dQ),
+                          _ptr(dK), _ptr(dV), _ptr(ws), nws if ws is None else ws.numel(),
+                          _stream(stream))
+    _check("sage_attn_bwd", st)
+    return dQ, dK, dV
+
+
+def sage_dump_bytes(B, H, N, d, which: int) -> int:
+    p = make_params(B, H, N, d, SAGE_FP16, False)
+    return lib().sage_dump_bytes(ctypes.byref(p), which)
+
+
+def sage_device_status(stream=None) -> int:
+    """Waits for the stream; SAGE_OK or SAGE_ERR_TIMEOUT (a bounded device wait expired)."""
+    return lib().sage_device_status(_stream(stream))
+
+
+def sage_version() -> str:
+    return lib().sage_version().decode()
+
+
+def sage_status_string(status: int) -> str:
+    return lib().sage_status_string(status).decode()

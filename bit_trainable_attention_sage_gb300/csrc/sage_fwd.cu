@@ -1,0 +1,424 @@
+// sage_fwd.cu -- SageBwd forward on sm_103a tensor cores (tcgen05, TMA, TMEM).
+//
+// Method: "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps, forward
+// (3)-(5); "SageAttention3 ..." (review) eq. (1) (online softmax) and eq. (8) (INT8 forward:
+// S_ij = MM(Q^_i, K^_j) s_Q s_K, per-token P codes with s_P = exp(rowmax(S_ij) - m_ij) / 127,
+// O_ij = diag(e^{m_{i,j-1} - m_ij}) O_{i,j-1} + MM(P^_ij, V^_j) s_P s_V); section summary A.1
+// (the forward returns O and the log-sum-exp L).
+//
+// GB300 design.  sm_103a has no INT8 tcgen05 MMA, so the int8 codes run through kind::f16 MMAs as
+// integer-valued fp16: every |code| <= 127 is exact in fp16, every product <= 127^2 and every
+// partial sum over a 128-long contraction <= 2 064 512 < 2^24 is exact in the fp32 accumulator,
+// so the block products are the exact integers the method defines.
+//
+// One CTA owns two 128-row query tiles (four 64-row quantisation blocks) of one head and walks
+// the keys in steps of 128 (two 64-key blocks); both tiles share every K and V tile it loads:
+//   warp 8      TMA producer: both Q tiles once, then K and V tiles (single-buffered each; K(j+1)
+//               streams in while the softmax and PV of step j run)
+//   warp 9      allocates TMEM; one lane issues every MMA, for each tile t:
+//                 S_t    = Q^_t K^T                 M=128 N=128 K=d  -> TMEM cols 256t + [0,128)
+//                 PV_t,h = P^_t[:,64h:64h+64] V^_h  M=128 N=d   K=64 -> TMEM cols 256t + [128,256)
+//   warps 0-3   softmax of tile 0, warps 4-7 of tile 1: thread = query row = TMEM lane.  Per step:
+//               logits, row max per 64-key block, P codes (written back to TMEM over the consumed
+//               S columns, as the A operand of the PV MMA), running max and sum, then
+//               O = alpha O + s_P s_V PV_h in registers.
+// While one warpgroup turns S into codes the tensor core works on the other tile, so the two
+// softmax warpgroups and the MMA pipe overlap.  TMEM: all 512 columns; one CTA per SM.
+
+// Numerics (the CPU oracle mirrors these float32 steps):
+//   c   = fl32(fl32(sQ_i sK_j) * fl32(log2(e)/sqrt(d)))
+//   r   = fl32(max_k(acc_k) * c)                 (row max of the 64-key block, log2 units)
+//   x_k = fl32(acc_k * c - r)                    (one rounding: fused multiply-add)
+//   P^_k = rint(fl32(127 * ex2(x_k)))            (round half to even)
+//   with Q-smoothing: t_k = fl32(acc_k * c + bias_k), r = max t_k, x_k = fl32(t_k - r)
+//   l <- 2^(m - m') l + 2^(r - m') sum_k ex2(x_k);  O <- 2^(m - m') O + (2^(r - m') / 127) s_V PV
+//   O_out = O / l;  L = (m + log2 l) ln 2
+#include "sage_device.cuh"
+#include "sage_internal.h"
+
+namespace sage {
+
+__device__ unsigned int g_fwd_err;
+
+namespace fwd {
+
+// warps 0-3: softmax of tile 0, 4-7: tile 1, 8: TMA producer, 9: MMA issuer, 10-11: idle.
+// Launched at 168 registers a thread (384 x 168 = 64512); the control warpgroup gives registers
+// back (40) and the softmax warpgroups take them (232): 2 x 128 x 232 + 128 x 40 = 64512.
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kRegsSoftmax = 232;
+constexpr uint32_t kRegsControl = 40;
+
+template <int D>
+struct Smem {
+    alignas(1024) uint8_t q[2][D / 64][128 * 128];   // [tile][chunk][row][64 halves], 128B swizzle
+    alignas(1024) uint8_t k[D / 64][128 * 128];
+    alignas(1024) uint8_t v[D / 64][128 * 128];
+    uint64_t q_full, k_full, k_free, v_full, v_free, mma_done;
+    uint64_t s_full[2], p_full[2], pv_full[2], pv_free[2];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// number of keys a CTA tile visits: causal tiles stop at their last row
+__device__ __forceinline__ int tile_kv_end(int q0, int N, int causal) {
+    if (q0 >= N) return 0;
+    return causal ? min(N, q0 + 128) : N;
+}
+
+template <int D, typename OutT, bool BIAS, bool DUMP>
+__global__ void __launch_bounds__(kThreads, 1)
+sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                const __grid_constant__ CUtensorMap mapV, const FwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem<D> &s = *reinterpret_cast<Smem<D> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int N = a.N;
+    const int bh = blockIdx.y;
+    const int npair = gridDim.x;
+    // causal: longest tile pairs first
+    const int ip = a.causal ? (npair - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    const int q0 = ip * 256;
+    int kv_end_t[2], nsteps_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        kv_end_t[t] = tile_kv_end(q0 + 128 * t, N, a.causal);
+        nsteps_t[t] = (kv_end_t[t] + 127) / 128;
+    }
+    const int nsteps = max(nsteps_t[0], nsteps_t[1]);
+    constexpr uint32_t kTileBytes = (D / 64) * 128 * 128;
+
+    if (warp == kMmaWarp) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        s.abort_flag = 0;
+        mbar_init(&s.q_full, 1);
+        mbar_init(&s.k_full, 1);
+        mbar_init(&s.k_free, 1);
+        mbar_init(&s.v_full, 1);
+        mbar_init(&s.v_free, 1);
+        mbar_init(&s.mma_done, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s.s_full[t], 1);
+            mbar_init(&s.p_full[t], 4);
+            mbar_init(&s.pv_full[t], 1);
+            mbar_init(&s.pv_free[t], 4);
+        }
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    volatile int *abort_flag = &s.abort_flag;
+    if (warp >= 8) {
+        regs_dec<kRegsControl>();
+        if (warp == kProducerWarp) {
+        // ------------------------------------------------------------------ TMA producer
+        if (elect_one()) {
+            tma_prefetch_desc(&mapQ);
+            tma_prefetch_desc(&mapK);
+            tma_prefetch_desc(&mapV);
+            mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.q[t][c], &mapQ, &s.q_full, 64 * c, q0 + 128 * t, bh);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < nsteps; ++j) {
+                if (j > 0 && !mbar_wait(&s.k_free, (j - 1) & 1, abort_flag, &g_fwd_err, 1)) break;
+                mbar_arrive_expect_tx(&s.k_full, kTileBytes);
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.k[c], &mapK, &s.k_full, 64 * c, 128 * j, bh);
+                k_issued = j + 1;
+                if (j > 0 && !mbar_wait(&s.v_free, (j - 1) & 1, abort_flag, &g_fwd_err, 2)) break;
+                mbar_arrive_expect_tx(&s.v_full, kTileBytes);
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.v[c], &mapV, &s.v_full, 64 * c, 128 * j, bh);
+                v_issued = j + 1;
+            }
+            // drain: every load issued must land before the CTA may exit
+            mbar_wait_drain(&s.q_full, 0, &g_fwd_err, 3);
+            if (k_issued > 0) mbar_wait_drain(&s.k_full, (k_issued - 1) & 1, &g_fwd_err, 3);
+            if (v_issued > 0) mbar_wait_drain(&s.v_full, (v_issued - 1) & 1, &g_fwd_err, 4);
+        }
+        } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (elect_one()) {
+            constexpr uint32_t idS = idesc_f16(128, 128, false, false, false);
+            constexpr uint32_t idPV = idesc_f16(128, D, false, false, true);
+            const uint32_t k_addr = smem_u32(s.k[0]), v_addr = smem_u32(s.v[0]);
+            int pv_count[2] = {0, 0};
+            mbar_wait(&s.q_full, 0, abort_flag, &g_fwd_err, 5);
+            for (int j = 0; j < nsteps; ++j) {
+                if (!mbar_wait(&s.k_full, j & 1, abort_flag, &g_fwd_err, 6)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= nsteps_t[t]) continue;
+                    const uint32_t q_addr = smem_u32(s.q[t][0]);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                        umma_ss(tmem + 256 * t, sdesc_sw128(q_addr + off, 16, 1024),
+                                sdesc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
+                    }
+                    umma_commit(&s.s_full[t]);
+                }
+                umma_commit(&s.k_free);
+                if (!mbar_wait(&s.v_full, j & 1, abort_flag, &g_fwd_err, 8)) break;
+                bool ok = true;
+                for (int h = 0; h < 2 && ok; ++h) {
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= nsteps_t[t]) continue;
+                        if (h == 1 && 128 * j + 64 >= kv_end_t[t]) continue;
+                        if (h == 0 && !mbar_wait(&s.p_full[t], j & 1, abort_flag, &g_fwd_err, 7)) { ok = false; break; }
+                        // the tile's PV accumulator must have been read out
+                        if (pv_count[t] > 0 &&
+                            !mbar_wait(&s.pv_free[t], (pv_count[t] - 1) & 1, abort_flag, &g_fwd_err, 9)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t vrow = 64 * h + 16 * kk;
+                            umma_ts(tmem + 256 * t + 128, tmem + 256 * t + 32 * h + 8 * kk,
+                                    sdesc_sw128(v_addr + vrow * 128, 16384, 1024), idPV, kk > 0);
+                        }
+                        umma_commit(&s.pv_full[t]);
+                        ++pv_count[t];
+                    }
+                }
+                umma_commit(&s.v_free);
+                if (!ok) break;
+            }
+            // every MMA must have finished before the tensor memory is released
+            umma_commit(&s.mma_done);
+            mbar_wait_drain(&s.mma_done, 0, &g_fwd_err, 12);
+        }
+        }
+    } else {
+        regs_inc<kRegsSoftmax>();
+        // ------------------------------------------------------------------ softmax warps
+        const int t = warp >> 2;                      // query tile of this warpgroup
+        const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+        const int row = 32 * quarter + static_cast<int>(lane_id());
+        const int grow = q0 + 128 * t + row;          // query index within the head
+        const int qblk = min(grow, N - 1) >> 6;
+        const size_t bhN = static_cast<size_t>(bh) * N;
+        const int nblk = N >> 6;
+        const int kv_end = kv_end_t[t];
+        const int my_steps = nsteps_t[t];
+        const float sq = a.sQ[static_cast<size_t>(bh) * nblk + qblk];
+        const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 256 * t);
+        float o[D];
+#pragma unroll
+        for (int c = 0; c < D; ++c) o[c] = 0.0f;
+        float m = -INFINITY, l = 0.0f;
+        int pv_uses = 0;
+        for (int j = 0; j < my_steps; ++j) {
+            if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, &g_fwd_err, 10)) break;
+            tc_fence_after();
+            const bool has_b = 128 * j + 64 < kv_end;
+            float r_h[2] = {-INFINITY, -INFINITY}, sum_h[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !has_b) break;
+                const int kb = 2 * j + h;                     // key block index
+                const int key0 = 64 * kb;
+                const float c = __fmul_rn(__fmul_rn(sq, a.sK[static_cast<size_t>(bh) * nblk + kb]), a.sl2);
+                // keys allowed for this row inside the block: [key0, key0 + nvalid)
+                int nvalid = a.causal ? min(64, grow - key0 + 1) : 64;
+                if (grow >= N) nvalid = 0;
+                const float *bias = BIAS ? a.qbias + (static_cast<size_t>(bh) * nblk + qblk) * N + key0 : nullptr;
+                // pass 1: row maximum over the block (of the integer products, or of the biased logits)
+                float r = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t raw[16];
+                    tmem_ld16(lane_base + 64 * h + cc, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float acc = __uint_as_float(raw[k]);
+                        const float v = BIAS ? __fmaf_rn(acc, c, bias[cc + k]) : acc;
+                        if (cc + k < nvalid) r = fmaxf(r, v);
+                        if (DUMP) {
+                            if (grow < N) a.dump_s[(bhN + grow) * N + key0 + cc + k] = static_cast<int32_t>(acc);
+                        }
+                    }
+                }
+                if (!BIAS && nvalid > 0) r = __fmul_rn(r, c);
+                const float rs = (r == -INFINITY) ? 0.0f : r;
+                r_h[h] = r;
+                // pass 2: codes, row sum; codes go to TMEM cols [32h, 32h+32) over consumed S columns
+                float sum = 0.0f;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t raw[16];
+                    tmem_ld16(lane_base + 64 * h + cc, raw);
+                    tmem_wait_ld();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int k = 0; k < 16; k += 2) {
+                        float x0, x1;
+                        const float a0 = __uint_as_float(raw[k]), a1 = __uint_as_float(raw[k + 1]);
+                        if (BIAS) {
+                            x0 = __fsub_rn(__fmaf_rn(a0, c, bias[cc + k]), rs);
+                            x1 = __fsub_rn(__fmaf_rn(a1, c, bias[cc + k + 1]), rs);
+                        } else {
+                            x0 = __fmaf_rn(a0, c, -rs);
+                            x1 = __fmaf_rn(a1, c, -rs);
+                        }
+                        x0 = (cc + k < nvalid) ? x0 : -INFINITY;
+                        x1 = (cc + k + 1 < nvalid) ? x1 : -INFINITY;
+                        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+                        sum += e0;
+                        sum += e1;
+                        const float p0 = rintf(__fmul_rn(127.0f, e0)), p1 = rintf(__fmul_rn(127.0f, e1));
+                        pk[k / 2] = pack_half2(p0, p1);
+                        if (DUMP) {
+                            if (grow < N) {
+                                a.dump_p[(bhN + grow) * N + key0 + cc + k] = static_cast<int16_t>(p0);
+                                a.dump_p[(bhN + grow) * N + key0 + cc + k + 1] = static_cast<int16_t>(p1);
+                            }
+                        }
+                    }
+                    tmem_st8(lane_base + 32 * h + cc / 2, pk);
+                }
+                sum_h[h] = sum;
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane_id() == 0) mbar_arrive(&s.p_full[t]);
+            // online softmax statistics
+            const float m_new = fmaxf(m, fmaxf(r_h[0], r_h[1]));
+            const float alpha = (m == -INFINITY) ? 0.0f : ex2_approx(__fsub_rn(m, m_new));
+            float cpv[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const bool live = r_h[h] != -INFINITY;
+                const float g = live ? ex2_approx(__fsub_rn(r_h[h], m_new)) : 0.0f;
+                l = (h == 0) ? __fmaf_rn(alpha, l, g * sum_h[h]) : __fmaf_rn(g, sum_h[h], l);
+                const int kb = min(2 * j + h, nblk - 1);
+                cpv[h] = (g * (1.0f / 127.0f)) * a.sV[static_cast<size_t>(bh) * nblk + kb];
+            }
+            m = m_new;
+            // O = alpha O + c_h PV_h
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !has_b) break;
+                if (!mbar_wait(&s.pv_full[t], pv_uses & 1, abort_flag, &g_fwd_err, 11)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < D; cc += 16) {
+                    uint32_t raw[16];
+                    tmem_ld16(lane_base + 128 + cc, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float pv = __uint_as_float(raw[k]);
+                        o[cc + k] = (h == 0) ? __fmaf_rn(alpha, o[cc + k], cpv[0] * pv)
+                                             : __fmaf_rn(cpv[1], pv, o[cc + k]);
+                        if (DUMP) {
+                            if (grow < N)
+                                a.dump_pv[(((static_cast<size_t>(bh) * nblk + qblk) * nblk + 2 * j + h) * 64 + (grow & 63)) * D + cc + k] =
+                                    static_cast<int32_t>(pv);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane_id() == 0) mbar_arrive(&s.pv_free[t]);
+                ++pv_uses;
+            }
+        }
+        // epilogue: O / l in the output type, L = (m + log2 l) ln 2
+        if (grow < N && !*abort_flag) {
+            const float inv_l = 1.0f / l;
+            OutT *dst = static_cast<OutT *>(a.O) + (bhN + grow) * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 8) {
+                uint4 w;
+                w.x = pack2<OutT>(o[c] * inv_l, o[c + 1] * inv_l);
+                w.y = pack2<OutT>(o[c + 2] * inv_l, o[c + 3] * inv_l);
+                w.z = pack2<OutT>(o[c + 4] * inv_l, o[c + 5] * inv_l);
+                w.w = pack2<OutT>(o[c + 6] * inv_l, o[c + 7] * inv_l);
+                *reinterpret_cast<uint4 *>(dst + c) = w;
+            }
+            a.L[bhN + grow] = (m + __log2f(l)) * 0.69314718055994531f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace fwd
+
+template <int D, typename OutT, bool BIAS, bool DUMP>
+static cudaError_t launch_fwd_t(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                                const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
+    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP>;
+    const int smem = static_cast<int>(sizeof(fwd::Smem<D>)) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + 255) / 256, p.B * p.H);
+    kern<<<grid, fwd::kThreads, smem, st>>>(mq, mk, mv, a);
+    return cudaGetLastError();
+}
+
+template <int D, typename OutT>
+static cudaError_t launch_fwd_d(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                                const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
+    const bool bias = a.qbias != nullptr, dump = a.dump_s != nullptr;
+    if (dump) return bias ? launch_fwd_t<D, OutT, true, true>(p, mq, mk, mv, a, st)
+                          : launch_fwd_t<D, OutT, false, true>(p, mq, mk, mv, a, st);
+    return bias ? launch_fwd_t<D, OutT, true, false>(p, mq, mk, mv, a, st)
+                : launch_fwd_t<D, OutT, false, false>(p, mq, mk, mv, a, st);
+}
+
+cudaError_t launch_fwd(const sage_params &p, const __half *Q16, const __half *K16,
+                       const __half *V16, FwdArgs a, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    const uint64_t bh = static_cast<uint64_t>(p.B) * p.H;
+    if (!make_tmap_3d(&mq, Q16, p.d, p.N, bh) || !make_tmap_3d(&mk, K16, p.d, p.N, bh) ||
+        !make_tmap_3d(&mv, V16, p.d, p.N, bh))
+        return cudaErrorInvalidValue;
+    if (p.d == 128)
+        return p.dtype == SAGE_FP16 ? launch_fwd_d<128, __half>(p, mq, mk, mv, a, st)
+                                    : launch_fwd_d<128, __nv_bfloat16>(p, mq, mk, mv, a, st);
+    return p.dtype == SAGE_FP16 ? launch_fwd_d<64, __half>(p, mq, mk, mv, a, st)
+                                : launch_fwd_d<64, __nv_bfloat16>(p, mq, mk, mv, a, st);
+}
+
+unsigned int take_fwd_error() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_fwd_err, sizeof(v));
+    cudaMemcpyToSymbol(g_fwd_err, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace sage

@@ -1,0 +1,91 @@
+// sage_internal.h -- declarations shared by the translation units of libsage_gb300.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <type_traits>
+
+#include "../../include/sage.h"
+
+namespace sage {
+
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e) rounded to float32
+
+// log2(e) / sqrt(d) rounded once to float32 (the double is formed first, as the oracle does)
+inline float scale_log2(int d) {
+    return static_cast<float>(1.4426950408889634 / __builtin_sqrt(static_cast<double>(d)));
+}
+
+struct QuantArgs {
+    const void *Q, *K, *V;
+    int8_t *Qh, *Kh, *Vh;
+    float *sQ, *sK, *sV, *muK, *muQ;
+    const double *kpartial;   // (B*H, ksplits, d) float64 partial sums of K (workspace)
+    int ksplits;
+    int N, d, smooth_k, smooth_q;
+};
+
+struct BwdPrologueArgs {
+    const void *dO, *O;
+    float *D;          // (B,H,N)
+    __half *dO16;      // (B,H,N,d) integer-valued fp16 codes of dO
+    int8_t *dOh;       // optional int8 codes of dO (debug dump), may be NULL
+    float *sdO;        // (B,H,N/64)
+    int N, d;
+};
+
+// Forward kernel arguments (device pointers; tensor maps are separate __grid_constant__ params)
+struct FwdArgs {
+    const float *sQ, *sK, *sV;
+    const float *qbias;   // (B,H,N/64,N) log2-unit Q-smoothing bias or NULL
+    void *O;              // (B,H,N,d) 16-bit
+    float *L;             // (B,H,N)
+    int32_t *dump_s;      // debug: (B,H,N,N) integer S products, or NULL
+    int16_t *dump_p;      // debug: (B,H,N,N) P codes, or NULL
+    int32_t *dump_pv;     // debug: (B,H,N/64,N/64,64,d) integer P V products, or NULL
+    int N, H, causal, dtype;
+    float sl2;            // log2(e)/sqrt(d)
+};
+
+struct BwdArgs {
+    const float *sQ, *sK, *sdO, *D, *L;
+    const float *qbias;   // (B,H,N/64,N) or NULL
+    const float *muQ;     // (B,H,N/64,d) or NULL (Q-smoothing dK bias term)
+    float *dQ, *dK, *dV;  // (B,H,N,d) float32
+    int32_t *dump_s;      // debug: (B,H,N,N) integer S products
+    int16_t *dump_p;      // debug: (B,H,N,N) backward P codes
+    int16_t *dump_ds;     // debug: (B,H,N,N) dS codes
+    float *dump_sp;       // debug: (B,H,N/64,N/64) P tile scales
+    float *dump_sds;      // debug: (B,H,N/64,N/64) dS tile scales
+    int N, H, causal, dtype;
+    float sl2, inv_sqrt_d;
+};
+
+// sage_quant.cu
+int kmean_splits(const sage_params &p);
+cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st);
+cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, cudaStream_t st);
+cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStream_t st);
+cudaError_t launch_qbias(const sage_params &p, const void *K, const float *muK, const float *muQ,
+                         float *bias, float sl2, cudaStream_t st);
+
+// sage_fwd.cu
+cudaError_t launch_fwd(const sage_params &p, const __half *Q16, const __half *K16,
+                       const __half *V16, FwdArgs a, cudaStream_t st);
+unsigned int take_fwd_error();
+
+// sage_bwd.cu
+cudaError_t launch_bwd(const sage_params &p, const __half *Q16, const __half *K16,
+                       const void *V, const void *dO, const __half *dO16, BwdArgs a,
+                       cudaStream_t st);
+unsigned int take_bwd_error();
+
+// tensor maps (sage_capi.cu)
+// (d, N, B*H) 16-bit tensor maps with 64 x 128 boxes and the 128-byte swizzle
+bool make_tmap_3d(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh);
+bool make_tmap_3d_bf16(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh);
+
+}  // namespace sage

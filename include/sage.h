@@ -1,0 +1,161 @@
+/*
+ * sage.h -- C ABI of the GB300 (sm_103a) SageBwd attention library (libsage_gb300.so).
+ *
+ * SageBwd is the trainable INT8 attention of "SageBwd: A Trainable Low-bit Attention" and of the
+ * SageBwd part of "SageAttention3: Microscaling FP4 Attention for Inference and An Exploration of
+ * 8-Bit Training".  The library exposes the method's three steps:
+ *
+ *   sage_quantize_smooth  K-smoothing (and optional Q-smoothing) plus per-block INT8 quantisation
+ *   sage_attn_fwd         tiled online-softmax forward with per-token P codes; writes O and L
+ *   sage_attn_bwd         backward with 16-bit dP and per-tile INT8 P / dS codes; writes dQ, dK, dV
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous, row-major (B, H, N, d): token n of head (b, h) starts at element
+ *     ((b * H + h) * N + n) * d.  Per-block scales are float32 (B, H, N / 64).
+ *   - Every pointer is DEVICE memory allocated and owned by the caller, except `p` (host).  The
+ *     library allocates nothing and keeps no state between calls; scratch memory is the caller's
+ *     `workspace` of at least the size the matching *_workspace_bytes() query returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  The
+ *     return value reports argument and launch errors only; a device-side timeout of a bounded
+ *     wait is reported by sage_device_status().
+ *   - Supported: N a multiple of 64 (N >= 64), d in {64, 128}, dtype fp16 or bf16, self-attention
+ *     (queries and keys share N).  Inputs must be finite.  All device pointers must be 16-byte
+ *     aligned.
+ *   - Causal masking is top-left aligned: query n attends to keys m <= n.
+ */
+#ifndef SAGE_GB300_H
+#define SAGE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SAGE_OK 0
+#define SAGE_ERR_ARG 1          /* null pointer, non-positive size, bad flag value            */
+#define SAGE_ERR_UNSUPPORTED 2  /* d not in {64,128}, N % 64 != 0, unknown dtype              */
+#define SAGE_ERR_ALIGN 3        /* a device pointer is not 16-byte aligned                     */
+#define SAGE_ERR_CUDA 4         /* a kernel launch or CUDA runtime call failed                 */
+#define SAGE_ERR_TIMEOUT 5      /* a bounded device-side wait expired (see sage_device_status) */
+#define SAGE_ERR_WORKSPACE 6    /* workspace missing or smaller than the query says            */
+
+/* Element types of the 16-bit tensors (Q, K, V, dO, O). */
+#define SAGE_FP16 0
+#define SAGE_BF16 1
+
+/* Flags. */
+#define SAGE_FLAG_DUMP 1u       /* debug: write the integer block products and the in-kernel
+                                   codes to `dump` (small problems only; see sage_dump_bytes) */
+
+typedef struct CUstream_st *sage_stream_t;   /* identical to cudaStream_t */
+
+#if defined(__GNUC__)
+#define SAGE_API __attribute__((visibility("default")))
+#else
+#define SAGE_API
+#endif
+
+typedef struct sage_params {
+    int B;           /* batch                                                                */
+    int H;           /* heads                                                                */
+    int N;           /* sequence length (queries = keys), multiple of 64                    */
+    int d;           /* head dimension, 64 or 128                                            */
+    int dtype;       /* SAGE_FP16 or SAGE_BF16: type of Q, K, V, dO and O                    */
+    int causal;      /* 0 or 1                                                               */
+    int smooth_k;    /* 1 (default): subtract the mean over tokens of K before quantising   */
+    int smooth_q;    /* 0 (default): 1 subtracts each 64-row block mean of Q and adds the
+                        bias mu_Q K_sm^T to the logits (and its gradient to dK)              */
+    unsigned flags;  /* SAGE_FLAG_*                                                          */
+    void *dump;      /* device buffer for SAGE_FLAG_DUMP, else NULL                          */
+    size_t dump_bytes;
+} sage_params;
+
+/* ------------------------------------------------------------------------------------------ *
+ * Step 1 -- smoothing and per-block INT8 quantisation.
+ * "SageBwd: A Trainable Low-bit Attention" (structured summary): prerequisites, INT8
+ * quantisation (X^ = round(X / delta), delta = max|X| / 127) and K-/Q-smoothing (mu_K = mean over
+ * tokens of K, K_sm = K - mu_K; mu_Qi = mean over the rows of query block i); method steps,
+ * forward (2).  "SageAttention3 ..." (review), eq. (7).
+ *
+ * In:  Q, K, V      (B,H,N,d) fp16/bf16.
+ * Out: Qh, Kh, Vh   (B,H,N,d) int8 codes in [-127, 127] of Q (or Q - mu_Q), K - mu_K (or K), V.
+ *      sQ, sK, sV   (B,H,N/64) float32 block scales delta = fl32(max|x| / 127); a block whose max
+ *                   is zero gets delta = 0 and all-zero codes.
+ *      muK          (B,H,d) float32: float64 sum over the N tokens / N, rounded once (zeros when
+ *                   smooth_k = 0).
+ *      muQ          (B,H,N/64,d) float32 block means (same rule), required iff smooth_q = 1.
+ * Codes are round-half-even of fl32(x / delta) with IEEE float32 division, x = fl32(v - mu).
+ * ------------------------------------------------------------------------------------------ */
+SAGE_API size_t sage_quantize_workspace_bytes(const sage_params *p);
+SAGE_API int sage_quantize_smooth(const sage_params *p, const void *Q, const void *K, const void *V,
+                         int8_t *Qh, int8_t *Kh, int8_t *Vh, float *sQ, float *sK, float *sV,
+                         float *muK, float *muQ, void *workspace, size_t workspace_bytes,
+                         sage_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ *
+ * Step 2 -- forward.
+ * "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps, forward (3)-(5);
+ * "SageAttention3 ..." (review) eq. (1) online softmax and eq. (8): S_ij = MM(Q^_i, K^_j) s_Q s_K,
+ * s_P = exp(rowmax(S_ij) - m_ij) / 127 per token, P^_ij = P~_ij / s_P, O_ij accumulation; section
+ * summary, A.1: the forward returns O and the log-sum-exp L.
+ *
+ * In:  Qh, Kh, Vh, sQ, sK, sV  as written by sage_quantize_smooth.
+ *      K, muK, muQ             only when smooth_q = 1 (the bias mu_Qi . (K - mu_K)); else NULL.
+ * Out: O  (B,H,N,d) fp16/bf16 (the dtype of p).
+ *      L  (B,H,N) float32 natural-log log-sum-exp of the scaled logits S / sqrt(d) as formed
+ *         (with K-smoothing these differ from the unsmoothed logits by a per-row constant).
+ * Logits: t = acc * fl32(fl32(sQ sK) * fl32(log2(e) / sqrt(d))) in log2 units; P codes are
+ * round-half-even of 2^(t - r) * 127 with r the row max over the 64-key tile; the running sum l
+ * accumulates the unquantised probabilities.
+ * ------------------------------------------------------------------------------------------ */
+SAGE_API size_t sage_fwd_workspace_bytes(const sage_params *p);
+SAGE_API int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, const int8_t *Vh,
+                  const float *sQ, const float *sK, const float *sV, const void *K,
+                  const float *muK, const float *muQ, void *O, float *L, void *workspace,
+                  size_t workspace_bytes, sage_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ *
+ * Step 3 -- backward.
+ * "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps, backward (1)-(7):
+ * D = rowsum(dO o O); recompute S_ij, P_ij; dV_j += MM(P^_ij^T, dO^_i) s_P s_dO; dP_ij = dO V_j^T in
+ * 16 bits; dS_ij = P_ij o (dP_ij - D_i) quantised; dQ_i += MM(dS^_ij, K^_j) s_dS s_K;
+ * dK_j += MM(dS^_ij^T, Q^_i) s_dS s_Q.  "SageAttention3 ..." (review), INT8 backward equations.
+ *
+ * In:  Qh, Kh, sQ, sK          the forward's codes and scales.
+ *      K, muK, muQ             only when smooth_q = 1; else NULL.
+ *      V, O, dO                (B,H,N,d) fp16/bf16: unquantised V, the stored forward output, dO.
+ *      L                       (B,H,N) float32 from sage_attn_fwd.
+ * Out: dQ, dK, dV              (B,H,N,d) float32, fully overwritten (the library zeroes them).
+ * P and dS are quantised per 64x64 tile: s = fl32(max|x| / 127), codes round-half-even of
+ * fl32(x * fl32(1 / s)); a tile whose max|x| is below 2^-120 is a zero tile.  dO is quantised
+ * per 64-token block like Q.  dQ sums tiles with float32 atomic adds, so its last bits vary
+ * from run to run.
+ * ------------------------------------------------------------------------------------------ */
+SAGE_API size_t sage_bwd_workspace_bytes(const sage_params *p);
+SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, const float *sQ,
+                  const float *sK, const void *K, const float *muK, const float *muQ,
+                  const void *V, const void *O, const float *L, const void *dO, float *dQ,
+                  float *dK, float *dV, void *workspace, size_t workspace_bytes,
+                  sage_stream_t stream);
+
+/* Bytes the SAGE_FLAG_DUMP buffer needs for a forward (which = 0) or backward (which = 1). */
+SAGE_API size_t sage_dump_bytes(const sage_params *p, int which);
+
+/* Waits for `stream`, then reads and clears the device-side error word of the current device:
+ * SAGE_OK, or SAGE_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call. */
+SAGE_API int sage_device_status(sage_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+SAGE_API const char *sage_status_string(int status);
+
+/* Library version string. */
+SAGE_API const char *sage_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_GB300_H */

@@ -13,13 +13,16 @@ backward (1)-(7); "SageAttention3 ..." (review), INT8 backward (Algorithm 3 equa
 
 Readings where the pages are silent, garbled or at odds (listed again in the design doc):
   R1  the softmax scale 1/sqrt(d) is applied after dequantisation, in float32, folded with
-      log2(e): t = fl32(acc * fl32(fl32(s_Q s_K) * fl32(log2(e)/sqrt(d)))) -- logits in log2 units;
-      dQ and dK carry 1/sqrt(d) by the chain rule.
-  R7  forward P^ is per token per 64-key tile: P^ = rne(fl32(127 * fl32(2^(fl32(t - r))))) with r
-      the row max over the tile's unmasked entries; s_P = 2^(r - m)/127; l accumulates the
+      log2(e) into c = fl32(fl32(s_Q s_K) * fl32(log2(e)/sqrt(d))): the logits in log2 units are
+      acc * c; dQ and dK carry 1/sqrt(d) by the chain rule.
+  R7  forward P^ is per token per 64-key tile: with r = fl32(max_k(acc_k) * c) the row max over the
+      tile's unmasked entries and x_k = fl32(acc_k * c - r) (one rounding, as a fused
+      multiply-add), P^_k = rne(fl32(127 * fl32(2^x_k))); s_P = 2^(r - m)/127; l accumulates the
       unquantised P~ (eq. 1); eq. (8)'s inverted rescale "diag(...)^-1" is read as eq. (1)'s
-      non-inverted one.
-  R8  backward P and dS are quantised per 64x64 tile: s = fl32(max|x|/127), q =
+      non-inverted one.  With Q-smoothing t_k = fl32(acc_k * c + bias_k), r = max t_k,
+      x_k = fl32(t_k - r).
+  R8  backward P_k = fl32(2^(fl32(acc_k * c - L2))) with L2 = fl32(L * fl32(log2(e))) (with
+      Q-smoothing fl32(t_k - L2)); P and dS are quantised per 64x64 tile: s = fl32(max|x|/127), q =
       rne(fl32(x * fl32(1/s))); a tile whose max|x| is below 2^-120 (zero, or so small that
       1/s would overflow float32) gets s = 0, q = 0.
   R9  dP = dO V^T uses the unquantised 16-bit dO and V, float32 result, never rounded to 16 bits.
@@ -82,11 +85,40 @@ class Arith:
         assert np.array_equal(r, p), "integer block product is not integral"
         return r.astype(np.int64)
 
-    def logits(self, s_int, c):
-        """t = fl32(acc * c); |acc| < 2^24 so the int -> float32 conversion is exact."""
-        if self.quantised:
-            return np.asarray(s_int, np.float64).astype(np.float32) * F32(c)
-        return np.asarray(s_int, np.float64) * c
+    def fma_logits(self, s_int, c, sub=None, bias=None):
+        """Logits in log2 units minus ``sub`` (a per-row array), as the kernel forms them.
+
+        Without a bias: fl32(acc * c - sub) with a single rounding (a fused multiply-add; acc * c
+        is exact in float64 and so is the difference, so one cast rounds once).
+        With a bias: t = fl32(acc * c + bias) (one rounding), then fl32(t - sub).
+        """
+        acc = np.asarray(s_int, np.float64)
+        if not self.quantised:
+            t = acc * c + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+            return t if sub is None else t - np.asarray(sub, np.float64)[:, None]
+        c64 = float(F32(c))
+        if bias is None:
+            if sub is None:
+                return (acc * c64).astype(np.float32)
+            return (acc * c64 - np.asarray(sub, np.float32).astype(np.float64)[:, None]).astype(np.float32)
+        t = (acc * c64 + np.asarray(bias, np.float32).astype(np.float64)[None, :]).astype(np.float32)
+        if sub is None:
+            return t
+        return t - np.asarray(sub, np.float32)[:, None]
+
+    def row_max_logit(self, s_int, c, valid, bias=None):
+        """r = the row max of the logits over ``valid`` entries, -inf where a row has none.
+        Without a bias it is formed from the integer maximum: fl32(max_k(acc_k) * c), c >= 0."""
+        acc = np.asarray(s_int, np.float64)
+        anyv = valid.any(axis=1)
+        if bias is None:
+            amax = np.where(valid, acc, -np.inf).max(axis=1)
+            if self.quantised:
+                r = (np.where(anyv, amax, 0.0) * float(F32(c))).astype(np.float32)
+                return np.where(anyv, r, np.float32(-np.inf)).astype(np.float32)
+            return np.where(anyv, np.where(anyv, amax, 0.0) * c, -np.inf)
+        t = self.fma_logits(s_int, c, None, bias)
+        return np.where(valid, t, -np.inf).max(axis=1).astype(np.float32 if self.quantised else np.float64)
 
     # -- the quantisers --------------------------------------------------------------------
     def block_quant(self, x):
@@ -96,15 +128,14 @@ class Arith:
         x = np.asarray(x, np.float64)
         return x, np.ones(x.shape[:-2] + (x.shape[-2] // BLOCK,))
 
-    def token_quant(self, t, r):
-        """Forward per-token P^ of one tile (R7).  Returns (2^(t - r) in float64, P^)."""
-        diff64 = t.astype(np.float64) - r[:, None].astype(np.float64)
-        e64 = np.exp2(diff64)
+    def token_quant(self, x):
+        """Forward per-token P^ of one tile (R7) from x = logits - r.
+        Returns (2^x in float64, P^)."""
+        e64 = np.exp2(np.asarray(x, np.float64))
         if not self.quantised:
             return e64, 127.0 * e64
-        e32 = np.exp2((t - r[:, None].astype(np.float32)).astype(np.float64)).astype(np.float32)
-        x = F32(127) * e32
-        return e64, np.clip(np.rint(x), 0, 127).astype(np.int64)
+        e32 = e64.astype(np.float32)
+        return e64, np.clip(np.rint(F32(127) * e32), 0, 127).astype(np.int64)
 
     def tile_quant(self, x):
         """Backward per-tile quantiser of P and dS (R8).  Returns (scale, codes)."""
@@ -198,15 +229,15 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
                 cols = slice(j * BLOCK, (j + 1) * BLOCK)
                 # (3) S_ij = MM(Q^_i, K^_j) * s_Q * s_K  (and * 1/sqrt(d), in log2 units)
                 s_int = arith.int_mm(Qh[b, h, rows], np.swapaxes(Kh[b, h, cols], 0, 1))
-                t = arith.logits(s_int, arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2))
-                if bias is not None:
-                    t = t + bias[cols][None, :]
-                if causal and j == i:
-                    t = np.where(mask, -np.inf, t)
+                c = arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2)
+                bias_j = None if bias is None else bias[cols]
+                valid = ~mask if (causal and j == i) else np.ones((BLOCK, BLOCK), bool)
                 # (4) online softmax statistics and per-token quantisation of P~
-                r = t.max(axis=1)
+                r = arith.row_max_logit(s_int, c, valid, bias_j)
+                x = arith.fma_logits(s_int, c, np.where(np.isfinite(r), r, 0), bias_j)
+                x = np.where(valid, x, -np.inf)
                 m_new = np.maximum(m, r.astype(np.float64))
-                e64, p_hat = arith.token_quant(t, r)
+                e64, p_hat = arith.token_quant(x)
                 alpha = np.exp2(m - m_new)
                 grow = np.exp2(r.astype(np.float64) - m_new)
                 s_p = grow / 127.0
@@ -260,12 +291,11 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
         cols = slice(j * BLOCK, (j + 1) * BLOCK)
         # (2) recompute S_ij (same formula as the forward) and P_ij = exp(S_ij - L_i)
         s_int = arith.int_mm(Qh[b, h, rows], np.swapaxes(Kh[b, h, cols], 0, 1))
-        t = arith.logits(s_int, arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2))
-        if bias is not None:
-            t = t + bias[cols][None, :]
+        c = arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2)
+        x = arith.fma_logits(s_int, c, L2[b, h, rows], None if bias is None else bias[cols])
         if causal and i == j:
-            t = np.where(mask, -np.inf, t)
-        P = arith.exp2_32(arith.r32(t - L2[b, h, rows][:, None]))
+            x = np.where(mask, -np.inf, x)
+        P = arith.exp2_32(x)
         # (3) dV_j += MM(P^_ij^T, dO^_i) * s_P * s_dO
         s_p, p_hat = arith.tile_quant(P)
         if want_dkv:

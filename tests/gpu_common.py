@@ -1,0 +1,97 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path and the oracle on the same inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads
+from oracle import sage as osage
+
+TORCH_DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_dev(x: np.ndarray, dtype: str) -> torch.Tensor:
+    """float32 values that are exact in ``dtype`` -> contiguous CUDA tensor of that dtype."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(TORCH_DT[dtype]).cuda()
+
+
+def carve(buf: torch.Tensor, specs):
+    """Split a dump buffer into consecutive 256-byte-aligned typed regions (the library's layout)."""
+    out, off = [], 0
+    for dtype, count in specs:
+        off = (off + 255) & ~255
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        out.append(buf[off:off + nbytes].view(dtype))
+        off += nbytes
+    return out
+
+
+def fwd_dump_views(buf, B, H, N, d):
+    nn = B * H * N * N
+    nb = B * H * (N // 64)
+    s, p, pv = carve(buf, [(torch.int32, nn), (torch.int16, nn), (torch.int32, nb * (N // 64) * 64 * d)])
+    return (s.view(B, H, N, N), p.view(B, H, N, N), pv.view(B, H, N // 64, N // 64, 64, d))
+
+
+def bwd_dump_views(buf, B, H, N, d):
+    nn = B * H * N * N
+    nb = B * H * (N // 64)
+    s, p, ds, sp, sds, doh, sdo, D = carve(buf, [
+        (torch.int32, nn), (torch.int16, nn), (torch.int16, nn), (torch.float32, nb * (N // 64)),
+        (torch.float32, nb * (N // 64)), (torch.int8, B * H * N * d), (torch.float32, nb),
+        (torch.float32, B * H * N)])
+    return dict(S=s.view(B, H, N, N), P=p.view(B, H, N, N), dS=ds.view(B, H, N, N),
+                sP=sp.view(B, H, N // 64, N // 64), sdS=sds.view(B, H, N // 64, N // 64),
+                dOh=doh.view(B, H, N, d), sdO=sdo.view(B, H, N // 64), D=D.view(B, H, N))
+
+
+def make_case(N, d, dtype, causal, B=1, H=2, seed=0, qk="normal", sigma=1.0, k_offset_var=0.0,
+              do_var=1e-2, smooth_q=False):
+    w = workloads.Workload("case", B, H, N, d, dtype, causal, qk=qk, sigma=sigma,
+                           k_offset_var=k_offset_var, do_var=do_var, smooth_q=smooth_q)
+    return w, workloads.make_inputs(w, seed=seed)
+
+
+def oracle_run(w, x, record=True):
+    rec = {} if record else None
+    out = osage.run(x["Q"], x["K"], x["V"], x["dO"], w.causal,
+                    lambda a: workloads.round_to(a, w.dtype), smooth_q=w.smooth_q, record=rec)
+    out["record"] = rec
+    return out
+
+
+def visited_blocks(N, causal):
+    """(i, j) 64-blocks the method computes: all, or j <= i when causal."""
+    T = N // 64
+    return [(i, j) for i in range(T) for j in range(T) if not causal or j <= i]
+
+
+def causal_mask_full(N):
+    return np.triu(np.ones((N, N), bool), 1)
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+def oracle_fwd(w, x, record=True):
+    prep = osage.prepare(x["Q"], x["K"], x["V"], smooth_q=w.smooth_q)
+    rec = {} if record else None
+    O, L = osage.sage_forward(prep, w.causal, record=rec)
+    return prep, O, L, rec
+
+
+def gpu_fwd(w, x, dump=False):
+    import bit_trainable_attention_sage_gb300 as sg
+    Q, K, V = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V"))
+    q = sg.sage_quantize_smooth(Q, K, V, smooth_q=w.smooth_q)
+    buf = None
+    if dump:
+        nbytes = sg.sage_dump_bytes(w.B, w.H, w.N, w.d, 0)
+        buf = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    O, L = sg.sage_attn_fwd(q, causal=w.causal, K=K if w.smooth_q else None, dump=buf)
+    assert sg.sage_device_status() == 0
+    return dict(q=q, O=O, L=L, dump=buf, dev=dict(Q=Q, K=K, V=V))

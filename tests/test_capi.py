@@ -1,0 +1,84 @@
+"""The C-ABI library: it loads, exports every entry point include/sage.h declares, sizes its
+workspaces, and rejects bad arguments before touching the GPU (CPU-only checks)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sg():
+    from bit_trainable_attention_sage_gb300 import build
+    build.build()
+    import bit_trainable_attention_sage_gb300 as sg
+    return sg
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "sage.h")).read()
+    return sorted(set(re.findall(r"SAGE_API\s+[\w\s\*]+?\b(sage_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("sage_quantize_smooth", "sage_attn_fwd", "sage_attn_bwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(sg):
+    L = sg.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert "sm_103a" in sg.sage_version()
+
+
+def test_workspace_sizes(sg):
+    L = sg.lib()
+    p = sg.make_params(2, 16, 8192, 128, 0, False)
+    n = 2 * 16 * 8192 * 128
+    fwd = L.sage_fwd_workspace_bytes(ctypes.byref(p))
+    bwd = L.sage_bwd_workspace_bytes(ctypes.byref(p))
+    assert fwd >= 3 * 2 * n
+    assert bwd >= 3 * 2 * n + 4 * 2 * 16 * 8192
+    pq = sg.make_params(2, 16, 8192, 128, 0, False, smooth_q=True)
+    assert L.sage_fwd_workspace_bytes(ctypes.byref(pq)) >= fwd + 4 * 2 * 16 * 128 * 8192
+    bad = sg.make_params(1, 1, 100, 128, 0, False)
+    assert L.sage_fwd_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def _fake(i):
+    return 0x10000 * (i + 1)    # aligned non-null addresses; never dereferenced (calls fail first)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("d", 96, 2), ("N", 100, 2), ("dtype", 7, 2), ("B", 0, 1), ("causal", 2, 1), ("flags", 8, 1),
+])
+def test_bad_params_rejected(sg, field, value, status):
+    L = sg.lib()
+    p = sg.make_params(1, 1, 128, 64, 0, False)
+    setattr(p, field, value)
+    args = [_fake(i) for i in range(12)]
+    st = L.sage_attn_fwd(ctypes.byref(p), *args, 1 << 30, None)
+    assert st == status
+    assert sg.sage_status_string(st)
+
+
+def test_null_misaligned_and_workspace(sg):
+    L = sg.lib()
+    p = sg.make_params(1, 1, 128, 64, 0, False)
+    args = [_fake(i) for i in range(12)]
+    args[0] = None
+    assert L.sage_attn_fwd(ctypes.byref(p), *args, 1 << 30, None) == 1
+    args = [_fake(i) for i in range(12)]
+    args[3] = _fake(3) + 4
+    assert L.sage_attn_fwd(ctypes.byref(p), *args, 1 << 30, None) == 3
+    args = [_fake(i) for i in range(12)]
+    assert L.sage_attn_fwd(ctypes.byref(p), *args, 16, None) == 6
+    args = [_fake(i) for i in range(15)]
+    assert L.sage_attn_bwd(ctypes.byref(p), *args, 16, None) == 6
+    qargs = [_fake(i) for i in range(12)]
+    qargs[9] = None   # muK
+    assert L.sage_quantize_smooth(ctypes.byref(p), *qargs, 1 << 30, None) == 1

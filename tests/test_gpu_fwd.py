@@ -1,0 +1,81 @@
+"""GPU parity of sage_quantize_smooth and sage_attn_fwd against the CPU oracle.
+
+Bit-exact: int8 codes, block scales, mu_K / mu_Q, and the integer Q^ K^T block products (read from
+the kernel's debug dump).  P codes: within one code of the oracle's on at most 1e-3 of the entries
+(both take the decision in float32, but the kernel's exp2 is the hardware approximation).  P^ V^
+products: exactly the integer product of the kernel's own codes with V^ (a property at any size).
+O: rel-l2 <= 1e-3 against the oracle's O rounded to the output type; L: max error <= 1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_common import (causal_mask_full, fwd_dump_views, gpu_fwd, make_case, oracle_fwd,
+                              rel_l2, visited_blocks)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # N, d, dtype, causal, extra
+    (128, 64, "fp16", False, {}),                                    # the tiny workload
+    (320, 128, "fp16", True, {}),                                    # ragged tail, causal
+    (384, 64, "bf16", True, dict(smooth_q=True)),                    # Q-smoothing bias
+    (512, 128, "bf16", False, dict(qk="qknorm", k_offset_var=4.0)),  # QK-norm + K channel offsets
+    (256, 128, "fp16", False, dict(sigma=5.0)),                      # large logits (sweep sigma 5)
+    (192, 64, "fp16", False, dict(qk="outlier", smooth_q=True)),     # outlier channels
+]
+
+
+def _ids(c):
+    return f"N{c[0]}-d{c[1]}-{c[2]}-{'causal' if c[3] else 'full'}-{'-'.join(f'{k}={v}' for k, v in c[4].items())}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_quantize_bit_exact(case):
+    N, d, dtype, causal, extra = case
+    w, x = make_case(N, d, dtype, causal, **extra)
+    g = gpu_fwd(w, x)
+    prep, _, _, _ = oracle_fwd(w, x, record=False)
+    q = g["q"]
+    for name in ("Qh", "Kh", "Vh"):
+        assert np.array_equal(getattr(q, name).cpu().numpy(), prep[name]), name
+    for name in ("sQ", "sK", "sV"):
+        got = getattr(q, name).cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), prep[name].view(np.uint32)), name
+    assert np.array_equal(q.muK.cpu().numpy().view(np.uint32), prep["muK"].view(np.uint32))
+    if w.smooth_q:
+        assert np.array_equal(q.muQ.cpu().numpy().view(np.uint32), prep["muQ"].view(np.uint32))
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_forward_parity(case):
+    N, d, dtype, causal, extra = case
+    w, x = make_case(N, d, dtype, causal, **extra)
+    g = gpu_fwd(w, x, dump=True)
+    prep, O, L, rec = oracle_fwd(w, x)
+    import workloads
+    O_ref = workloads.round_to(O.astype(np.float32), dtype)
+    O_gpu = g["O"].float().cpu().numpy()
+    L_gpu = g["L"].cpu().numpy()
+    assert np.all(np.isfinite(O_gpu)) and np.all(np.isfinite(L_gpu))
+    assert rel_l2(O_gpu, O_ref) <= 1e-3
+    assert np.max(np.abs(L_gpu - L)) <= 1e-4 * max(1.0, np.abs(L).max())
+    S, P, PV = (t.cpu().numpy() for t in fwd_dump_views(g["dump"], w.B, w.H, N, d))
+    Vh = prep["Vh"]
+    mask = causal_mask_full(N) if causal else np.zeros((N, N), bool)
+    n_codes = n_diff = 0
+    for b in range(w.B):
+        for h in range(w.H):
+            r = rec[(b, h)]
+            for (i, j) in visited_blocks(N, causal):
+                rows, cols = slice(64 * i, 64 * i + 64), slice(64 * j, 64 * j + 64)
+                assert np.array_equal(S[b, h, rows, cols], r["S_int"][rows, cols]), (b, h, i, j)
+                live = ~mask[rows, cols]
+                dp = np.abs(P[b, h, rows, cols].astype(np.int64) - r["P_hat"][rows, cols])
+                assert dp[live].max(initial=0) <= 1, (b, h, i, j)
+                n_codes += int(live.sum())
+                n_diff += int((dp[live] != 0).sum())
+                assert np.all(P[b, h, rows, cols][~live] == 0)
+                want = P[b, h, rows, cols].astype(np.int64) @ Vh[b, h, cols].astype(np.int64)
+                assert np.array_equal(PV[b, h, i, j].astype(np.int64), want), (b, h, i, j)
+    assert n_diff <= 1e-3 * n_codes, (n_diff, n_codes)

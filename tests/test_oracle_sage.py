@@ -56,7 +56,9 @@ def test_dequantised_limit_equals_fpa(N, d, causal, smooth_k, smooth_q):
 
 
 def _closed_form_O(prep, causal):
-    """Order-independent closed form of the quantised forward, evaluated row by row."""
+    """Order-independent closed form of the quantised forward, evaluated row by row:
+    O_i = sum_j 2^(r_ij - M_i) (s_V,j / 127) P^_ij V^_j / sum_j 2^(r_ij - M_i) sum_k 2^(x_ijk),
+    with the per-tile codes P^ = rint(127 * 2^x), x = fl32(acc c - r), r = fl32(max acc * c)."""
     Qh, Kh, Vh, sQ, sK, sV = (prep[k] for k in ("Qh", "Kh", "Vh", "sQ", "sK", "sV"))
     B, H, N, d = Qh.shape
     T = N // 64
@@ -64,23 +66,26 @@ def _closed_form_O(prep, causal):
     O = np.zeros((B, H, N, d))
     for b in range(B):
         for h in range(H):
-            acc = np.einsum("nc,mc->nm", Qh[b, h].astype(np.int64), Kh[b, h].astype(np.int64))
-            c = (np.repeat(sQ[b, h], 64)[:, None] * np.repeat(sK[b, h], 64)[None, :]).astype(np.float32) * sl2
-            t = acc.astype(np.float32) * c
-            if causal:
-                t = np.where(np.triu(np.ones((N, N), bool), 1), -np.inf, t)
-            tj = t.reshape(N, T, 64)
-            r = tj.max(axis=2)                                           # r_ij
-            Mrow = r.max(axis=1)                                         # global row max
-            live = np.isfinite(r)                                        # tile j has unmasked keys
-            r_safe = np.where(live, r, np.float32(0))
-            e32 = np.exp2((tj - r_safe[:, :, None]).astype(np.float64)).astype(np.float32)
-            p_hat = np.where(live[:, :, None], np.rint(np.float32(127) * e32), 0)   # per-token codes
+            acc = np.einsum("nc,mc->nm", Qh[b, h].astype(np.int64), Kh[b, h].astype(np.int64)).astype(np.float64)
+            c = ((np.repeat(sQ[b, h], 64)[:, None] * np.repeat(sK[b, h], 64)[None, :]).astype(np.float32) * sl2).astype(np.float64)
+            valid = ~np.triu(np.ones((N, N), bool), 1) if causal else np.ones((N, N), bool)
+            accj = acc.reshape(N, T, 64)
+            cj = c.reshape(N, T, 64)[:, :, 0]
+            vj = valid.reshape(N, T, 64)
+            live = vj.any(axis=2)
+            amax = np.where(vj, accj, -np.inf).max(axis=2)
+            r = np.where(live, (np.where(live, amax, 0) * cj).astype(np.float32), -np.inf)
+            x = (accj * cj[:, :, None] - np.where(live, r, 0)[:, :, None]).astype(np.float32)
+            x = np.where(vj, x, -np.inf)
+            e64 = np.exp2(x.astype(np.float64))
+            p_hat = np.rint(np.float32(127) * e64.astype(np.float32))
+            r64 = r.astype(np.float64)
+            Mrow = r64.max(axis=1)
+            w = np.where(live, np.exp2(np.where(live, r64, 0.0) - Mrow[:, None]), 0.0)
             num = np.zeros((N, d))
             for j in range(T):
-                w = np.where(live[:, j], np.exp2(r_safe[:, j].astype(np.float64) - Mrow), 0) / 127.0 * sV[b, h, j]
-                num += w[:, None] * (p_hat[:, j, :] @ Vh[b, h, 64 * j:64 * j + 64].astype(np.float64))
-            den = np.exp2(t.astype(np.float64) - Mrow[:, None]).sum(axis=1)
+                num += (w[:, j] / 127.0 * sV[b, h, j])[:, None] * (p_hat[:, j, :] @ Vh[b, h, 64 * j:64 * j + 64].astype(np.float64))
+            den = (w * e64.sum(axis=2)).sum(axis=1)
             O[b, h] = num / den[:, None]
     return O
 
@@ -113,9 +118,8 @@ def test_integer_products_exact():
 
 
 def test_token_quantiser():
-    t = np.array([[0.0, -1.0, -0.5, -np.inf, -30.0]], np.float32)
-    r = t.max(axis=1)
-    e64, q = sage.QUANTISED.token_quant(t, r)
+    x = np.array([[0.0, -1.0, -0.5, -np.inf, -30.0]], np.float32)
+    e64, q = sage.QUANTISED.token_quant(x)
     assert q.tolist() == [[127, 64, 90, 0, 0]]    # 127, 63.5 -> 64 (even), 127/sqrt(2) = 89.8
     assert e64[0, 0] == 1.0 and e64[0, 3] == 0.0
 
@@ -157,7 +161,13 @@ def test_special_case_causal_first_row():
     Q, K, V, _ = _inputs(128, 64, seed=10)
     prep = sage.prepare(Q, K, V)
     O, L = sage.sage_forward(prep, True)
-    want = prep["sV"][:, :, 0, None].astype(np.float64) * prep["Vh"][:, :, 0, :]
+    # row 0 sees key 0 only: its code is 127 and s_P = 1/127, so O_0 = s_V,0 V^_0 / 2^x_0 where
+    # x_0 = fl32(acc c - fl32(acc c)) is the float32 rounding residual of its own logit
+    acc = (prep["Qh"][:, :, 0, :].astype(np.int64) * prep["Kh"][:, :, 0, :].astype(np.int64)).sum(-1)
+    c = (prep["sQ"][:, :, 0] * prep["sK"][:, :, 0]).astype(np.float32) * np.float32(sage.LOG2E / math.sqrt(64))
+    ac = acc.astype(np.float64) * c.astype(np.float64)
+    x0 = (ac - ac.astype(np.float32).astype(np.float64)).astype(np.float32).astype(np.float64)
+    want = prep["sV"][:, :, 0, None].astype(np.float64) * prep["Vh"][:, :, 0, :] / np.exp2(x0)[..., None]
     assert np.allclose(O[:, :, 0, :], want, rtol=1e-15, atol=0)
 
 
