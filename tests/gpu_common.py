@@ -95,3 +95,24 @@ def gpu_fwd(w, x, dump=False):
     O, L = sg.sage_attn_fwd(q, causal=w.causal, K=K if w.smooth_q else None, dump=buf)
     assert sg.sage_device_status() == 0
     return dict(q=q, O=O, L=L, dump=buf, dev=dict(Q=Q, K=K, V=V))
+
+
+def gpu_run(w, x, dump=False):
+    """quantise -> forward -> backward on the GPU; returns numpy results (+ backward dump views)."""
+    import bit_trainable_attention_sage_gb300 as sg
+    Q, K, V, dO = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V", "dO"))
+    q = sg.sage_quantize_smooth(Q, K, V, smooth_q=w.smooth_q)
+    Kb = K if w.smooth_q else None
+    O, L = sg.sage_attn_fwd(q, causal=w.causal, K=Kb)
+    buf = None
+    if dump:
+        nbytes = sg.sage_dump_bytes(w.B, w.H, w.N, w.d, 1)
+        buf = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    dQ, dK, dV = sg.sage_attn_bwd(q, V, O, L, dO, causal=w.causal, K=Kb, dump=buf)
+    st = sg.sage_device_status()
+    assert st == 0, sg.sage_status_string(st)
+    out = dict(O=O.float().cpu().numpy(), L=L.cpu().numpy(), dQ=dQ.cpu().numpy(),
+               dK=dK.cpu().numpy(), dV=dV.cpu().numpy())
+    if dump:
+        out["dump"] = {k: v.cpu().numpy() for k, v in bwd_dump_views(buf, w.B, w.H, w.N, w.d).items()}
+    return out

@@ -78,4 +78,6 @@ def test_forward_parity(case):
                 assert np.all(P[b, h, rows, cols][~live] == 0)
                 want = P[b, h, rows, cols].astype(np.int64) @ Vh[b, h, cols].astype(np.int64)
                 assert np.array_equal(PV[b, h, i, j].astype(np.int64), want), (b, h, i, j)
+    print(f"\n{_ids(case)}: P code flips {n_diff}/{n_codes}, O rel-l2 {rel_l2(O_gpu, O_ref):.2e}, "
+          f"L max err {np.max(np.abs(L_gpu - L)):.2e}")
     assert n_diff <= 1e-3 * n_codes, (n_diff, n_codes)
