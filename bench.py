@@ -1,0 +1,420 @@
+"""Benchmark of the SageBwd hot path on GB300: one step = quantise + forward + backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--causal]
+
+Workload: the headline configuration, B=2 H=16 N=8192 d=128 fp16, non-causal (``--causal`` for
+the causal variant), synthetic seeded inputs (Q, K, V ~ N(0,1), dO ~ N(0,1e-4)); each rank under
+torchrun processes its own batch (weak scaling, no data-path collective).
+
+Metric: effective TOPS = 14 B H N^2 d / step time (the 6 integer GEMMs and the 16-bit dP GEMM
+of forward + backward; halved when causal).  One JSON line on rank 0 carries the device-timed
+value, the end-to-end value through the public API with host buffers (``e2e``), the roofline of
+the dominant call, the clocks seen during the timed region, the number of library kernels
+launched, and the CPU oracle timed on a bounded sample (``cpu_baseline``).
+
+``--impl reference`` times the CPU oracle alone (the reference arm of this build: there is no
+published GPU implementation of the method), each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+if "reference" in sys.argv:
+    # the reference arm times the oracle on one host core: pin BLAS before numpy loads
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import workloads  # noqa: E402
+
+METRIC = "fwd+bwd effective TOPS (N=8192,d=128) and % of INT8/FP16 tensor-core roofline"
+UNIT = "TOPS"
+KERNELS_PER_STEP = 10   # kmean_partial, quantize, 3 widen + fwd, 2 widen + bwd prologue + bwd
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "bwd_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "bit_trainable_attention_sage_gb300", "csrc", f)
+                  for f in ("sage_bwd.cu", "sage_device.cuh", "sage_internal.h")]
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU under torchrun; nothing on the data path)
+# ------------------------------------------------------------------------------------------
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def step_ops(w: workloads.Workload) -> float:
+    """Algorithmic tensor ops of one quantise + forward + backward: 14 B H N^2 d (x 1/2 causal)."""
+    ops = 14.0 * w.B * w.H * w.N * w.N * w.d
+    return ops / 2 if w.causal else ops
+
+
+def bwd_ops(w: workloads.Workload) -> float:
+    ops = 10.0 * w.B * w.H * w.N * w.N * w.d
+    return ops / 2 if w.causal else ops
+
+
+def fwd_ops(w: workloads.Workload) -> float:
+    ops = 4.0 * w.B * w.H * w.N * w.N * w.d
+    return ops / 2 if w.causal else ops
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self, path: str):
+        self.path = path
+        try:
+            self.fh = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------
+# the GPU arm
+# ------------------------------------------------------------------------------------------
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(w) -> float | None:
+    """DRAM bytes per launch of the backward kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        rec = json.load(open(PROFILE_TRAFFIC))
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha") != source_sha():
+        return None
+    scale = (w.B * w.H) / rec["heads"] * (w.N / rec["N"]) ** 2 if rec.get("scale_with_work") else 1.0
+    return rec["dram_bytes_per_launch"] * scale
+
+
+def run_gpu(args, w: workloads.Workload):
+    import numpy as np
+    import torch
+    import bit_trainable_attention_sage_gb300 as sg
+
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    x = workloads.make_inputs(w, seed=rank)
+    dt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+    host = {k: torch.from_numpy(v).to(dt).pin_memory() for k, v in x.items()}
+    del x
+    dev = {k: v.to(device) for k, v in host.items()}
+    stream = torch.cuda.current_stream(device)
+    B, H, N, d = w.B, w.H, w.N, w.d
+
+    # outputs and workspaces allocated once (the library allocates nothing)
+    p = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal)
+    import ctypes
+    L = sg.lib()
+    ws_f = torch.empty(L.sage_fwd_workspace_bytes(ctypes.byref(p)), dtype=torch.uint8, device=device)
+    ws_b = torch.empty(L.sage_bwd_workspace_bytes(ctypes.byref(p)), dtype=torch.uint8, device=device)
+    O = torch.empty((B, H, N, d), dtype=dt, device=device)
+    Lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=device) for _ in range(3))
+
+    def step(ev=None):
+        q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q)
+        if ev is not None:
+            ev[0].record(stream)
+        sg.sage_attn_fwd(q, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
+        if ev is not None:
+            ev[1].record(stream)
+        sg.sage_attn_bwd(q, dev["V"], O, Lse, dev["dO"], causal=w.causal, grads=grads, workspace=ws_b)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    st = sg.sage_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {sg.sage_status_string(st)}")
+
+    # ---- device-timed region -------------------------------------------------------------
+    clocks = ClockSampler(local)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks.start(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+    st = sg.sage_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {sg.sage_status_string(st)}")
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms_max = max_over_ranks(dist, ms, device)
+
+    # ---- end to end through the public API with host buffers ------------------------------
+    host_out = {"O": torch.empty_like(O, device="cpu").pin_memory(),
+                "dQ": torch.empty_like(grads[0], device="cpu").pin_memory(),
+                "dK": torch.empty_like(grads[1], device="cpu").pin_memory(),
+                "dV": torch.empty_like(grads[2], device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        step()
+        host_out["O"].copy_(O, non_blocking=True)
+        for name, g in zip(("dQ", "dK", "dV"), grads):
+            host_out[name].copy_(g, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
+    assert np.isfinite(host_out["dQ"].float().numpy()).all()
+
+    ops = step_ops(w)
+    value = world * ops * args.steps / (ms_max * 1e-3) / 1e12
+    e2e_value = world * ops * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    peak_src = "measured (bf16_tflops_sustained; fp16 runs at the bf16 rate)" if peaks else "fallback"
+    bwd_tflops = bwd_ops(w) / (bwd_ms * 1e-3) / 1e12
+    fwd_tflops = fwd_ops(w) / (fwd_ms * 1e-3) / 1e12
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "s8 codes as f16 (f32 accumulate); dP f16", "data": "synthetic",
+        "config": {"workload": f"headline {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "smooth_k": True, "smooth_q": w.smooth_q,
+                   "per_rank": "own batch", "l2": "inputs larger than L2 (Q,K,V,dO = 268 MB per step)"},
+        "roofline": {"kernel": "sage_attn_bwd call (bwd prologue + tcgen05 backward kernel)",
+                     "bound": "tensor", "achieved": round(bwd_tflops, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
+                     "traffic": profiled_traffic(w), "flops_per_launch": bwd_ops(w)},
+        "fwd_call": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 1), "frac": round(fwd_tflops / peak, 4)},
+        "bwd_call": {"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 1), "frac": round(bwd_tflops / peak, 4)},
+        "step_frac_of_fp16_peak": round(value / world / peak, 4),
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+# ------------------------------------------------------------------------------------------
+# the CPU oracle (baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------------
+def oracle_sample(w: workloads.Workload, q_blocks, kv_blocks, seed: int = 0) -> tuple[float, float]:
+    """Time the oracle on head (0, 0) of the workload: quantise, forward over ``q_blocks`` (None =
+    all) and backward over ``kv_blocks`` (None = all).  Returns (seconds, algorithmic ops)."""
+    import numpy as np
+    from oracle import sage as osage
+    x = workloads.make_inputs(w, seed=seed, heads=1)
+    x = {k: np.ascontiguousarray(v[:1]) for k, v in x.items()}
+    T = w.N // 64
+    qb = list(range(T)) if q_blocks is None else list(q_blocks)
+    kb = list(range(T)) if kv_blocks is None else list(kv_blocks)
+    t0 = time.perf_counter()
+    prep = osage.prepare(x["Q"], x["K"], x["V"], smooth_q=w.smooth_q)
+    prep["V16"] = x["V"]
+    O, L = osage.sage_forward(prep, w.causal, q_blocks=None if q_blocks is None else qb)
+    Os = workloads.round_to(O.astype(np.float32), w.dtype)
+    if kv_blocks is None:
+        osage.sage_backward(prep, Os, L.astype(np.float32), x["dO"], w.causal)
+    else:
+        osage.sage_backward(prep, Os, L.astype(np.float32), x["dO"], w.causal, kv_blocks=kb)
+    secs = time.perf_counter() - t0
+    tile = 64 * 64 * w.d
+    n_f = sum((i + 1) if w.causal else T for i in qb)
+    n_b = sum((T - j) if w.causal else T for j in kb)
+    return secs, 4.0 * tile * n_f + 10.0 * tile * n_b
+
+
+def cpu_baseline_subprocess(w: workloads.Workload, q_blocks, kv_blocks, label: str) -> dict:
+    """Run the oracle in a fresh interpreter (single BLAS thread) and describe the sample."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, workloads; "
+            "w = workloads.get(%r, causal=%r); s, ops = bench.oracle_sample(w, %r, %r); "
+            "print(json.dumps({'s': s, 'ops': ops}))" % (ROOT, w.name, w.causal, q_blocks, kv_blocks))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label,
+                "error": r.stderr[-300:]}
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(out["ops"] / out["s"] / 1e12, 8), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "sample": label, "seconds": round(out["s"], 2),
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+def run_reference(args, w: workloads.Workload):
+    """The reference arm: the CPU oracle as it stands, each step a bounded sample."""
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return None
+    qb = list(range(4))
+    kb = list(range(4))
+    label = f"head (0,0) of the workload; forward over 4 of {w.N // 64} query blocks and backward " \
+            f"over 4 of {w.N // 64} key blocks per step"
+    for _ in range(args.warmup):
+        oracle_sample(w, qb, kb)
+    secs = ops = 0.0
+    for _ in range(args.steps):
+        s, o = oracle_sample(w, qb, kb)
+        secs += s
+        ops += o
+    value = ops / secs / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (f32 codes)",
+        "data": "synthetic",
+        "config": {"workload": f"headline {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": round(value, 8), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label},
+        "e2e": {"value": round(value, 8), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    over = {"causal": args.causal}
+    if args.batch:
+        over["B"] = args.batch
+    if args.heads:
+        over["H"] = args.heads
+    w = workloads.get("headline", **over)
+    if args.impl == "reference":
+        line = run_reference(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    from __graft_entry__ import build
+    build()
+    line = run_gpu(args, w)
+    if line is None:
+        return
+    rank, world, _ = rank_info()
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_subprocess(
+            w, None, None, "head (0,0) of 32: full quantise + forward + backward of one head, "
+                           "value = its 14 N^2 d ops / CPU seconds")
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

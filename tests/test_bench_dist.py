@@ -1,0 +1,49 @@
+"""Host-side logic of the multi-GPU benchmark, run as world-size-2 gloo ranks on CPU.
+
+Each rank processes its own batch (weak scaling); the only communication is a barrier and the
+max-reduction of the timed region, so the job time is the slowest rank's.
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    r, w, local = bench.rank_info()
+    dist = bench.init_dist(w, "gloo")
+    bench.barrier(dist)
+    slowest = bench.max_over_ranks(dist, 10.0 + rank)       # rank 1 is the slow one
+    out[rank] = (r, w, local, slowest)
+    dist.destroy_process_group()
+
+
+def test_two_rank_barrier_and_max():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0][:3] == (0, 2, 0) and res[1][:3] == (1, 2, 1)
+    assert res[0][3] == res[1][3] == 11.0
+
+
+def test_weak_scaling_value():
+    import bench
+    import workloads
+    w = workloads.get("headline")
+    ops = bench.step_ops(w)
+    assert ops == 14.0 * 2 * 16 * 8192 * 8192 * 128
+    assert bench.step_ops(workloads.get("headline", causal=True)) == ops / 2
+    assert bench.fwd_ops(w) + bench.bwd_ops(w) == ops
