@@ -6,5 +6,6 @@ functions carry the C entry points' names.
 """
 from .binding import (  # noqa: F401
     Quantized, SageError, SageParams, lib, make_params, sage_attn_bwd, sage_attn_fwd,
-    sage_device_status, sage_dump_bytes, sage_quantize_smooth, sage_status_string, sage_version,
+    sage_device_status, sage_dump_bytes, sage_quantize_smooth, sage_quantize_smooth_noalloc,
+    sage_status_string, sage_version,
 )

@@ -223,3 +223,31 @@ def sage_version() -> str:
 
 def sage_status_string(status: int) -> str:
     return lib().sage_status_string(status).decode()
+
+
+def sage_quantize_smooth_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *,
+                                 smooth_k: bool = True, smooth_q: bool = False, out=None,
+                                 stream=None) -> Quantized:
+    """sage_quantize_smooth for callers that cannot allocate device memory while they run: the
+    K-mean scratch lives in a fixed array inside the library.  ``out`` (a Quantized whose tensors
+    the caller allocated beforehand) receives the results; without it they are allocated here."""
+    _require_cuda(Q, K, V)
+    B, H, N, d = Q.shape
+    dt = _dtype_code(Q)
+    dev = Q.device
+    if out is None:
+        Qh = torch.empty((B, H, N, d), dtype=torch.int8, device=dev)
+        sQ = torch.empty((B, H, N // 64), dtype=torch.float32, device=dev)
+        out = Quantized(Qh, torch.empty_like(Qh), torch.empty_like(Qh), sQ, torch.empty_like(sQ),
+                        torch.empty_like(sQ), torch.empty((B, H, d), dtype=torch.float32, device=dev),
+                        torch.empty((B, H, N // 64, d), dtype=torch.float32, device=dev) if smooth_q else None,
+                        dt, smooth_k, smooth_q)
+    L = lib()
+    fn = L.sage_quantize_smooth_noalloc
+    fn.argtypes = [ctypes.POINTER(SageParams)] + [ctypes.c_void_p] * 12
+    fn.restype = ctypes.c_int
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q)
+    st = fn(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(out.Qh), _ptr(out.Kh), _ptr(out.Vh),
+            _ptr(out.sQ), _ptr(out.sK), _ptr(out.sV), _ptr(out.muK), _ptr(out.muQ), _stream(stream))
+    _check("sage_quantize_smooth_noalloc", st)
+    return out

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsage_gb300.so")
-SOURCES = ["sage_quant.cu", "sage_fwd.cu", "sage_bwd.cu", "sage_capi.cu"]
+SOURCES = ["sage_quant.cu", "sage_fwd.cu", "sage_bwd.cu", "sage_capi.cu", "sage_noalloc.cu"]
 HEADERS = ["sage_device.cuh", "sage_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

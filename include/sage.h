@@ -141,6 +141,31 @@ SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t 
                   float *dK, float *dV, void *workspace, size_t workspace_bytes,
                   sage_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------ *
+ * Step 1 without a workspace (the paper has no counterpart: this is a calling convenience).
+ *
+ * For callers that cannot allocate device memory while they run -- for example a plug-in whose
+ * host framework owns all device memory and offers it no allocator, or a latency-critical loop
+ * that must not pay for (or synchronise on) an allocation.  Same inputs, outputs, results and
+ * errors as sage_quantize_smooth, but the float64 K-mean partial sums live in a fixed array
+ * inside the library (sage_quantize_noalloc_max_partials() entries, 1 MiB, held on every device
+ * that loads the library until the process exits) instead of in a caller workspace.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Returns SAGE_ERR_WORKSPACE when B * H * splits * d exceeds that capacity (splits is the
+ *     K-mean split count the library chooses: about ceil(304 / (B*H)), at most N / 64).
+ *   - The first call on a device looks up the array's device address on that device (the
+ *     current device); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's partial sums.  Nothing has to
+ *     start at zero (each call writes every entry it reads first), but calls that overlap on the
+ *     GPU -- on different streams, or from different host threads -- race on it.
+ *   - `flags` must be 0 (no debug dump).
+ * ------------------------------------------------------------------------------------------ */
+SAGE_API size_t sage_quantize_noalloc_max_partials(void);
+SAGE_API int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, const void *K,
+                                          const void *V, int8_t *Qh, int8_t *Kh, int8_t *Vh,
+                                          float *sQ, float *sK, float *sV, float *muK, float *muQ,
+                                          sage_stream_t stream);
+
 /* Bytes the SAGE_FLAG_DUMP buffer needs for a forward (which = 0) or backward (which = 1). */
 SAGE_API size_t sage_dump_bytes(const sage_params *p, int which);
 
