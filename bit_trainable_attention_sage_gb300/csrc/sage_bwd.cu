@@ -11,25 +11,31 @@
 // the forward); dP runs on the unquantised fp16/bf16 dO and V.  One CTA owns a 128-key tile
 // (two 64-key quantisation blocks) of one head and loops over 128-row query chunks (two 64-row
 // blocks).  Everything is transposed so that keys are TMEM lanes:
-//   S^T  = K^ Q^T    (M=128 keys, N=128 q, K=d)    TMEM R_S  = cols [0,128)
-//   dP^T = V dO^T    (M=128 keys, N=128 q, K=d)    TMEM R_dP = cols [128,256)
-//   dV_h = P^T_h dO^_h (A from TMEM, K=64 q)       TMEM R_V  = cols [256,384)  (h = q block)
-//   dK_h = dS^T_h Q^_h (A from TMEM, K=64 q)       TMEM R_K  = cols [384,512)
-//   dQ_g = dS^_g K^_g (A from smem, K=64 keys)     TMEM R_S (g = 0) / R_dP (g = 1), once their
-//                                                  codes have been read by the dV / dK MMAs
+//   S^T  = K^ Q^T      (M=128 keys, N=128 q, K=d)    TMEM R_S  = cols [0,128)
+//   dP^T = V dO^T      (M=128 keys, N=128 q, K=d)    TMEM R_dP = cols [128,256)
+//   two product slots R_A = cols [256,384), R_B = [384,512), each filled three times a chunk:
+//     dK_h = dS^T_h Q^_h  (A from TMEM, K=64 q)    h = 0 -> R_A, 1 -> R_B
+//     dV_h = P^T_h dO^_h  (A from TMEM, K=64 q)
+//     dQ_g = dS^_g K^_g   (A from smem, K=64 keys)  g = key block
+// The MMA order per chunk is dK, dV, then the next chunk's S^T and dP^T (their regions' codes
+// are consumed by then: the tensor pipe runs in issue order), then dQ: the score warpgroup starts
+// on the next chunk while the dQ products are added to global memory.
 // Warp roles (12 warps; registers 232 for the two math warpgroups, 40 for the control one):
 //   warps 0-3  "score" warpgroup, thread = key: P = 2^(acc c - L2), dS = P o (dP - D) in place in
 //              TMEM; per 64x64 tile max reductions; P and dS codes back into TMEM (A operands)
 //              and dS codes into shared memory (A operand of dQ); dV rows in registers.
-//   warps 4-7  "grad" warpgroup: dK rows in registers (thread = key); dQ products read with
-//              thread = query row, scaled, and added to global dQ with vector float32 atomics.
-//   warp 8     TMA producer; warp 9 TMEM allocation and the single MMA-issuing thread.
+//   warps 4-7  "grad" warpgroup: dK rows in registers (thread = key); the two dQ products of a
+//              chunk read with thread = query row, scaled, summed and added to global dQ with
+//              one vector float32 atomic per four elements.
+//   warp 8     TMA producer (tiles, and L2 / D rows by bulk copy); warp 9 TMEM allocation and the
+//              single MMA-issuing thread.
 //
 // Numerics (the CPU oracle mirrors these float32 steps):
 //   c = fl32(fl32(sQ sK) * fl32(log2(e)/sqrt(d)));  L2 = fl32(L * fl32(log2(e)))
 //   P = fl32(ex2(fl32(acc * c - L2)))   (with Q-smoothing ex2(fl32(fl32(acc * c + bias) - L2)))
 //   dS = fl32(P * fl32(dP - D))
-//   per 64x64 tile: s = fl32(max|x| / 127), code = rint(fl32(x * fl32(1/s))); max|x| < 2^-120 -> 0
+//   per 64x64 tile: s = fl32(max|x| / 127), code = rne16(fl32(x * fl32(1/s) + 1536)) - 1536;
+//   max|x| < 2^-120 -> zero tile
 #include "sage_device.cuh"
 #include "sage_internal.h"
 
@@ -44,7 +50,7 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kRegsMath = 232;
 constexpr uint32_t kRegsControl = 40;
-constexpr uint32_t R_S = 0, R_DP = 128, R_V = 256, R_K = 384;
+constexpr uint32_t R_S = 0, R_DP = 128, R_A = 256, R_B = 384;
 constexpr float kTileZero = 7.52316384526264e-37f;   // 2^-120
 
 template <int D>
@@ -55,13 +61,17 @@ struct Smem {
     alignas(1024) uint8_t doc[D / 64][128 * 128];   // dO chunk  (16-bit input type)
     alignas(1024) uint8_t dohc[D / 64][128 * 128];  // dO^ chunk (codes)
     alignas(1024) uint8_t dss[2][128 * 128];        // dS^ as MN-major A: [q block][key][64 q]
-    float L2s[128], Ds[128];
-    float red[4][2][4];                             // [warp][kb pair slot][4 maxima]
+    alignas(16) float L2s[2][128];                  // [chunk parity][q]: fl32(L log2 e)
+    alignas(16) float Ds[2][128];                   // [chunk parity][q]: D
+    float red[4][2][4];                             // [warp][chunk parity][4 maxima]
     float sds[2][2][2];                             // [chunk parity][kb][qb] dS tile scales
     float colsum[2][128];                           // [qb][key] column sums of dS (Q-smoothing)
-    uint64_t kv_full, q_full, q_free, do_full, do_free, doh_full, doh_free;
+    uint64_t kv_full, q_full, q_free, do_full, do_free, doh_full, doh_free, meta_full[2];
     uint64_t s_full, dp_full, codes_ready, dss_free;
-    uint64_t rv_full, rv_free, rk_full, rk_free, rs_full, rs_free, rdp_full, rdp_free;
+    // the two product slots R_A, R_B: "full" per consumer (the grad warpgroup takes dK and dQ,
+    // the score warpgroup dV), so that every waiter sees every phase of its barrier; "free" is
+    // shared (the MMA thread waits for each use in turn)
+    uint64_t a_full_g, a_full_s, a_free, b_full_g, b_full_s, b_free;
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -76,15 +86,35 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// plain bulk copy global -> shared (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
                  "f"(c), "f"(d)
                  : "memory");
 }
 
-// code of x with reciprocal scale inv (inv = 0 for a zero tile)
-__device__ __forceinline__ float tile_code(float x, float inv) {
-    return fminf(127.0f, fmaxf(-127.0f, rintf(__fmul_rn(x, inv))));
+// Two tile codes packed as fp16: rne16(fl32(x * inv + 1536)) - 1536 (inv = 0 for a zero tile).
+// Values x * inv lie in [-127, 127], so x * inv + 1536 lies in [1024, 2048) where fp16 spacing is
+// 1: the fp16 conversion rounds to an integer and the subtraction is exact.
+__device__ __forceinline__ uint32_t codes2(float x0, float x1, float inv) {
+    const __half2 h = __floats2half2_rn(__fmaf_rn(x0, inv, 1536.0f), __fmaf_rn(x1, inv, 1536.0f));
+    const __half2 r = __hsub2(h, __float2half2_rn(1536.0f));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+__device__ __forceinline__ int16_t code_lo(uint32_t w) {
+    return static_cast<int16_t>(__half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))));
+}
+__device__ __forceinline__ int16_t code_hi(uint32_t w) {
+    return static_cast<int16_t>(__half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
 }
 
 template <int D, bool BF16, bool BIAS, bool DUMP>
@@ -114,14 +144,13 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     if (threadIdx.x == 0) {
         s.abort_flag = 0;
         uint64_t *one[] = {&s.kv_full, &s.q_full, &s.q_free, &s.do_full, &s.do_free, &s.doh_full,
-                           &s.doh_free, &s.s_full, &s.dp_full, &s.dss_free, &s.rv_full, &s.rk_full,
-                           &s.rs_full, &s.rdp_full, &s.mma_done};
+                           &s.doh_free, &s.meta_full[0], &s.meta_full[1], &s.s_full, &s.dp_full,
+                           &s.dss_free, &s.a_full_g, &s.a_full_s, &s.b_full_g, &s.b_full_s,
+                           &s.mma_done};
         for (uint64_t *b : one) mbar_init(b, 1);
         mbar_init(&s.codes_ready, 4);
-        mbar_init(&s.rv_free, 4);
-        mbar_init(&s.rk_free, 4);
-        mbar_init(&s.rs_free, 4);
-        mbar_init(&s.rdp_free, 4);
+        mbar_init(&s.a_free, 4);
+        mbar_init(&s.b_free, 4);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -145,13 +174,20 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                     tma_load_3d(s.kt[c], &mapK, &s.kv_full, 64 * c, k0, bh);
                     tma_load_3d(s.vt[c], &mapV, &s.kv_full, 64 * c, k0, bh);
                 }
-                int nq = 0, ndo = 0, ndoh = 0;
+                int nq = 0, ndo = 0, ndoh = 0, nmeta[2] = {0, 0};
                 for (int it = 0; it < nmine; ++it) {
                     const int q0 = 128 * (c_first + it);
+                    const uint32_t rows = static_cast<uint32_t>(min(128, N - q0));
+                    const int slot = it & 1;
                     if (it > 0 && !mbar_wait(&s.do_free, (it - 1) & 1, abort_flag, &g_bwd_err, 1)) break;
                     mbar_arrive_expect_tx(&s.do_full, kTileBytes);
                     for (int c = 0; c < D / 64; ++c) tma_load_3d(s.doc[c], &mapdO, &s.do_full, 64 * c, q0, bh);
                     ndo = it + 1;
+                    // row data of the chunk: L2 = fl32(L log2 e) and D (written by the prologue)
+                    mbar_arrive_expect_tx(&s.meta_full[slot], 8 * rows);
+                    bulk_load(s.L2s[slot], a.L2 + bhN + q0, 4 * rows, &s.meta_full[slot]);
+                    bulk_load(s.Ds[slot], a.D + bhN + q0, 4 * rows, &s.meta_full[slot]);
+                    ++nmeta[slot];
                     if (it > 0 && !mbar_wait(&s.q_free, (it - 1) & 1, abort_flag, &g_bwd_err, 2)) break;
                     mbar_arrive_expect_tx(&s.q_full, kTileBytes);
                     for (int c = 0; c < D / 64; ++c) tma_load_3d(s.qc[c], &mapQ, &s.q_full, 64 * c, q0, bh);
@@ -163,11 +199,16 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 }
                 mbar_wait_drain(&s.kv_full, 0, &g_bwd_err, 4);
                 if (ndo > 0) mbar_wait_drain(&s.do_full, (ndo - 1) & 1, &g_bwd_err, 4);
+                for (int sl = 0; sl < 2; ++sl)
+                    if (nmeta[sl] > 0) mbar_wait_drain(&s.meta_full[sl], (nmeta[sl] - 1) & 1, &g_bwd_err, 4);
                 if (nq > 0) mbar_wait_drain(&s.q_full, (nq - 1) & 1, &g_bwd_err, 4);
                 if (ndoh > 0) mbar_wait_drain(&s.doh_full, (ndoh - 1) & 1, &g_bwd_err, 4);
             }
         } else if (warp == kMmaWarp) {
             // -------------------------------------------------------------- MMA issuer
+            // Per chunk: dK_0 -> A, dK_1 -> B (Q^ is then free for the next chunk), dV_0 -> A,
+            // dV_1 -> B, the next chunk's S^T and dP^T, then dQ_0 -> A, dQ_1 -> B.  Each product
+            // slot is refilled only after its consumer warpgroup has read it out.
             if (elect_one()) {
                 constexpr uint32_t idKK = idesc_f16(128, 128, false, false, false);    // S^T
                 constexpr uint32_t idDP = idesc_f16(128, 128, BF16, false, false);     // dP^T
@@ -182,12 +223,9 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 const uint64_t dQmn = sdesc_sw128(smem_u32(s.qc[0]), 16384, 1024);
                 const uint64_t dKmn = sdesc_sw128(smem_u32(s.kt[0]), 16384, 1024);
                 const uint64_t dDss = sdesc_sw128(smem_u32(s.dss[0]), 16384, 1024);
-                bool ok = mbar_wait(&s.kv_full, 0, abort_flag, &g_bwd_err, 5);
-                for (int it = 0; it < nmine && ok; ++it) {
-                    const uint32_t ph = it & 1;
-                    // S^T = K^ Q^T
-                    if (!mbar_wait(&s.q_full, ph, abort_flag, &g_bwd_err, 6)) break;
-                    if (it > 0 && !mbar_wait(&s.rs_free, (it - 1) & 1, abort_flag, &g_bwd_err, 7)) break;
+                int ua = 0, ub = 0;                        // products issued into each slot
+                auto issue_s_dp = [&](int it) -> bool {
+                    if (!mbar_wait(&s.q_full, it & 1, abort_flag, &g_bwd_err, 6)) return false;
                     tc_fence_after();
 #pragma unroll 1
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -195,9 +233,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                         umma_ss(tmem + R_S, dKt + o, dQc + o, idKK, kk > 0);
                     }
                     umma_commit(&s.s_full);
-                    // dP^T = V dO^T
-                    if (!mbar_wait(&s.do_full, ph, abort_flag, &g_bwd_err, 8)) break;
-                    if (it > 0 && !mbar_wait(&s.rdp_free, (it - 1) & 1, abort_flag, &g_bwd_err, 9)) break;
+                    if (!mbar_wait(&s.do_full, it & 1, abort_flag, &g_bwd_err, 8)) return false;
                     tc_fence_after();
 #pragma unroll 1
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -206,40 +242,62 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                     }
                     umma_commit(&s.dp_full);
                     umma_commit(&s.do_free);
-                    // the score warpgroup turns S^T, dP^T into P / dS codes
-                    if (!mbar_wait(&s.codes_ready, ph, abort_flag, &g_bwd_err, 10)) break;
-                    if (!mbar_wait(&s.doh_full, ph, abort_flag, &g_bwd_err, 11)) break;
+                    return true;
+                };
+                auto slot_ready = [&](bool is_a) -> bool {
+                    const int u = is_a ? ua : ub;
+                    if (u == 0) return true;
+                    if (!mbar_wait(is_a ? &s.a_free : &s.b_free, (u - 1) & 1, abort_flag, &g_bwd_err, is_a ? 12 : 13)) return false;
                     tc_fence_after();
+                    return true;
+                };
+                bool ok = mbar_wait(&s.kv_full, 0, abort_flag, &g_bwd_err, 5);
+                if (ok && nmine > 0) ok = issue_s_dp(0);
+                for (int it = 0; it < nmine && ok; ++it) {
+                    if (!mbar_wait(&s.codes_ready, it & 1, abort_flag, &g_bwd_err, 10)) break;
+                    tc_fence_after();
+                    // dK_h = dS^T[:, h] Q^_h
+#pragma unroll 1
                     for (int h = 0; h < 2 && ok; ++h) {
-                        // dV_h = P^T[:, h] dO^_h  -> R_V
-                        const int uv = 2 * it + h;
-                        if (uv > 0 && !mbar_wait(&s.rv_free, (uv - 1) & 1, abort_flag, &g_bwd_err, 12)) { ok = false; break; }
-                        tc_fence_after();
+                        if (!(ok = slot_ready(h == 0))) break;
+                        const uint32_t dst = tmem + (h == 0 ? R_A : R_B);
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_ts(tmem + R_V, tmem + R_S + 32 * h + 8 * kk, dDoh + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
-                        umma_commit(&s.rv_full);
-                        // dK_h = dS^T[:, h] Q^_h  -> R_K
-                        if (uv > 0 && !mbar_wait(&s.rk_free, (uv - 1) & 1, abort_flag, &g_bwd_err, 13)) { ok = false; break; }
-                        tc_fence_after();
+                            umma_ts(dst, tmem + R_DP + 32 * h + 8 * kk, dQmn + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
+                        umma_commit(h == 0 ? &s.a_full_g : &s.b_full_g);
+                        if (h == 0) ++ua; else ++ub;
+                    }
+                    if (!ok) break;
+                    umma_commit(&s.q_free);
+                    if (!mbar_wait(&s.doh_full, it & 1, abort_flag, &g_bwd_err, 11)) break;
+                    // dV_h = P^T[:, h] dO^_h
+#pragma unroll 1
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!(ok = slot_ready(h == 0))) break;
+                        const uint32_t dst = tmem + (h == 0 ? R_A : R_B);
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_ts(tmem + R_K, tmem + R_DP + 32 * h + 8 * kk, dQmn + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
-                        umma_commit(&s.rk_full);
+                            umma_ts(dst, tmem + R_S + 32 * h + 8 * kk, dDoh + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
+                        umma_commit(h == 0 ? &s.a_full_s : &s.b_full_s);
+                        if (h == 0) ++ua; else ++ub;
                     }
                     if (!ok) break;
                     umma_commit(&s.doh_free);
-                    umma_commit(&s.q_free);
-                    // dQ_g = dS^[:, keys of g] K^_g -> R_S (g = 0), R_DP (g = 1); the tensor pipe
-                    // runs in issue order, so the codes these regions held are already consumed
+                    // the next chunk's scores: the tensor pipe runs in issue order, so the codes in
+                    // R_S / R_DP have been read by the dV / dK MMAs above before they are replaced
+                    if (it + 1 < nmine && !(ok = issue_s_dp(it + 1))) break;
+                    // dQ_g = dS^[:, keys of g] K^_g
 #pragma unroll 1
-                    for (int g = 0; g < 2; ++g) {
+                    for (int g = 0; g < 2 && ok; ++g) {
+                        if (!(ok = slot_ready(g == 0))) break;
+                        const uint32_t dst = tmem + (g == 0 ? R_A : R_B);
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t o = ((64 * g + 16 * kk) * 128) >> 4;
-                            umma_ss(tmem + (g ? R_DP : R_S), dDss + o, dKmn + o, idQ, kk > 0);
+                            umma_ss(dst, dDss + o, dKmn + o, idQ, kk > 0);
                         }
-                        umma_commit(g ? &s.rdp_full : &s.rs_full);
+                        umma_commit(g == 0 ? &s.a_full_g : &s.b_full_g);
+                        if (g == 0) ++ua; else ++ub;
                     }
                     umma_commit(&s.dss_free);
                 }
@@ -250,7 +308,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     } else if (warp < 4) {
         regs_inc<kRegsMath>();
         // ------------------------------------------------------------------ score warpgroup
-        const int tq = threadIdx.x;                       // 0..127: key lane / query index
+        const int tq = threadIdx.x;                       // 0..127: key lane
         const int quarter = warp;
         const int key = k0 + tq;                          // key index within the head
         const int kb = tq >> 6;                           // key block of this lane (0/1)
@@ -261,28 +319,32 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
         float dv[D];
 #pragma unroll
         for (int c = 0; c < D; ++c) dv[c] = 0.0f;
-        for (int it = 0; it < nmine; ++it) {
-            const uint32_t ph = it & 1;
-            const int ic = c_first + it;
-            const int q0 = 128 * ic;
-            // per-chunk row data: L2 = fl32(L log2 e), D
-            {
-                const int r = q0 + tq;
-                s.L2s[tq] = r < N ? __fmul_rn(a.L[bhN + r], kLog2e) : 0.0f;
-                s.Ds[tq] = r < N ? a.D[bhN + r] : 0.0f;
-            }
-            named_bar_sync(1, 128);
-            float cq[2], biasv[2] = {0.0f, 0.0f};
-            int qblk[2];
+        // per-chunk scalars, fetched one chunk ahead
+        auto fetch = [&](int ic, float (&sq)[2], float (&sdo)[2], float (&bias)[2]) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                qblk[h] = min(2 * ic + h, nblk - 1);
-                cq[h] = __fmul_rn(__fmul_rn(a.sQ[static_cast<size_t>(bh) * nblk + qblk[h]], sk), a.sl2);
-                if (BIAS && key_ok) biasv[h] = a.qbias[(static_cast<size_t>(bh) * nblk + qblk[h]) * N + key];
+                const int qb = min(2 * ic + h, nblk - 1);
+                sq[h] = a.sQ[static_cast<size_t>(bh) * nblk + qb];
+                sdo[h] = a.sdO[static_cast<size_t>(bh) * nblk + qb];
+                bias[h] = (BIAS && key_ok) ? a.qbias[(static_cast<size_t>(bh) * nblk + qb) * N + key] : 0.0f;
             }
+        };
+        float sq[2], sdo[2], biasv[2], nsq[2], nsdo[2], nbias[2];
+        if (nmine > 0) fetch(c_first, sq, sdo, biasv);
+        for (int it = 0; it < nmine; ++it) {
+            const uint32_t ph = it & 1;
+            const int slot = it & 1;
+            const int ic = c_first + it;
+            const int q0 = 128 * ic;
+            if (it + 1 < nmine) fetch(ic + 1, nsq, nsdo, nbias);
+            float cq[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) cq[h] = __fmul_rn(__fmul_rn(sq[h], sk), a.sl2);
             // valid query columns for this key: [qlo, qhi) relative to q0
             const int qhi = min(128, N - q0);
             const int qlo = a.causal ? max(0, key - q0) : 0;
+            const bool edge = (a.causal && ic == jt) || q0 + 128 > N || k0 + 128 > N;
+            if (!mbar_wait(&s.meta_full[slot], (it >> 1) & 1, abort_flag, &g_bwd_err, 19)) break;
             if (!mbar_wait(&s.s_full, ph, abort_flag, &g_bwd_err, 20)) break;
             if (!mbar_wait(&s.dp_full, ph, abort_flag, &g_bwd_err, 21)) break;
             tc_fence_after();
@@ -295,23 +357,35 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 uint32_t sr[16], dr[16];
                 tmem_ld16(lane_base + R_S + cc, sr);
                 tmem_ld16(lane_base + R_DP + cc, dr);
+                float l2v[16], dvv[16];
+#pragma unroll
+                for (int k = 0; k < 16; k += 4) {
+                    *reinterpret_cast<float4 *>(&l2v[k]) = *reinterpret_cast<const float4 *>(&s.L2s[slot][cc + k]);
+                    *reinterpret_cast<float4 *>(&dvv[k]) = *reinterpret_cast<const float4 *>(&s.Ds[slot][cc + k]);
+                }
                 tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int col = cc + k;
                     const float acc = __uint_as_float(sr[k]);
                     float x;
-                    if (BIAS) x = __fsub_rn(__fmaf_rn(acc, cq[h], biasv[h]), s.L2s[col]);
-                    else x = __fmaf_rn(acc, cq[h], -s.L2s[col]);
-                    const bool ok = key_ok && col >= qlo && col < qhi;
-                    const float p = ok ? ex2_approx(x) : 0.0f;
-                    const float ds = __fmul_rn(p, __fsub_rn(__uint_as_float(dr[k]), s.Ds[col]));
+                    if (BIAS) x = __fsub_rn(__fmaf_rn(acc, cq[h], biasv[h]), l2v[k]);
+                    else x = __fmaf_rn(acc, cq[h], -l2v[k]);
+                    float p = ex2_approx(x);
+                    float ds = __fmul_rn(p, __fsub_rn(__uint_as_float(dr[k]), dvv[k]));
+                    if (edge) {
+                        const bool ok = key_ok && col >= qlo && col < qhi;
+                        p = ok ? p : 0.0f;
+                        ds = ok ? ds : 0.0f;
+                        if (DUMP) {
+                            if (ok) a.dump_s[(bhN + q0 + col) * N + key] = static_cast<int32_t>(acc);
+                        }
+                    } else if (DUMP) {
+                        a.dump_s[(bhN + q0 + col) * N + key] = static_cast<int32_t>(acc);
+                    }
                     mp[h] = fmaxf(mp[h], p);
                     md[h] = fmaxf(md[h], fabsf(ds));
-                    cs[h] += ds;
-                    if (DUMP) {
-                        if (ok) a.dump_s[(bhN + q0 + col) * N + key] = static_cast<int32_t>(acc);
-                    }
+                    if (BIAS) cs[h] += ds;
                     sr[k] = __float_as_uint(p);
                     dr[k] = __float_as_uint(ds);
                 }
@@ -329,10 +403,10 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 }
             }
             if (lane_id() == 0) {
-                s.red[warp][it & 1][0] = mp[0];
-                s.red[warp][it & 1][1] = mp[1];
-                s.red[warp][it & 1][2] = md[0];
-                s.red[warp][it & 1][3] = md[1];
+                s.red[warp][slot][0] = mp[0];
+                s.red[warp][slot][1] = mp[1];
+                s.red[warp][slot][2] = md[0];
+                s.red[warp][slot][3] = md[1];
             }
             if (BIAS) {
                 s.colsum[0][tq] = cs[0];
@@ -343,16 +417,16 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
             float sp[2], sd[2], ip[2], id[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float mxp = fmaxf(s.red[w0][it & 1][h], s.red[w0 + 1][it & 1][h]);
-                const float mxd = fmaxf(s.red[w0][it & 1][2 + h], s.red[w0 + 1][it & 1][2 + h]);
+                const float mxp = fmaxf(s.red[w0][slot][h], s.red[w0 + 1][slot][h]);
+                const float mxd = fmaxf(s.red[w0][slot][2 + h], s.red[w0 + 1][slot][2 + h]);
                 sp[h] = mxp < kTileZero ? 0.0f : __fdiv_rn(mxp, 127.0f);
                 ip[h] = mxp < kTileZero ? 0.0f : __frcp_rn(sp[h]);
                 sd[h] = mxd < kTileZero ? 0.0f : __fdiv_rn(mxd, 127.0f);
                 id[h] = mxd < kTileZero ? 0.0f : __frcp_rn(sd[h]);
             }
             if ((tq & 63) == 0) {
-                s.sds[it & 1][kb][0] = sd[0];
-                s.sds[it & 1][kb][1] = sd[1];
+                s.sds[slot][kb][0] = sd[0];
+                s.sds[slot][kb][1] = sd[1];
                 if (DUMP) {
                     for (int h = 0; h < 2; ++h) {
                         if (key_ok && q0 + 64 * h < N) {
@@ -377,21 +451,17 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 uint32_t pk[8], dk[8];
 #pragma unroll
                 for (int k = 0; k < 16; k += 2) {
-                    const float p0 = tile_code(__uint_as_float(pr[k]), ip[h]);
-                    const float p1 = tile_code(__uint_as_float(pr[k + 1]), ip[h]);
-                    const float d0 = tile_code(__uint_as_float(dr[k]), id[h]);
-                    const float d1 = tile_code(__uint_as_float(dr[k + 1]), id[h]);
-                    pk[k / 2] = pack_half2(p0, p1);
-                    dk[k / 2] = pack_half2(d0, d1);
+                    pk[k / 2] = codes2(__uint_as_float(pr[k]), __uint_as_float(pr[k + 1]), ip[h]);
+                    dk[k / 2] = codes2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1]), id[h]);
                     if (DUMP) {
                         const int col = cc + k;
                         if (key_ok && q0 + col < N) {
-                            a.dump_p[(bhN + q0 + col) * N + key] = static_cast<int16_t>(p0);
-                            a.dump_ds[(bhN + q0 + col) * N + key] = static_cast<int16_t>(d0);
+                            a.dump_p[(bhN + q0 + col) * N + key] = code_lo(pk[k / 2]);
+                            a.dump_ds[(bhN + q0 + col) * N + key] = code_lo(dk[k / 2]);
                         }
                         if (key_ok && q0 + col + 1 < N) {
-                            a.dump_p[(bhN + q0 + col + 1) * N + key] = static_cast<int16_t>(p1);
-                            a.dump_ds[(bhN + q0 + col + 1) * N + key] = static_cast<int16_t>(d1);
+                            a.dump_p[(bhN + q0 + col + 1) * N + key] = code_hi(pk[k / 2]);
+                            a.dump_ds[(bhN + q0 + col + 1) * N + key] = code_hi(dk[k / 2]);
                         }
                     }
                 }
@@ -409,24 +479,33 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane_id() == 0) mbar_arrive(&s.codes_ready);
-            // dV += s_P s_dO (P^T dO^)_h
+            // dV += s_P s_dO (P^T dO^)_h: product h sits in slot A (h = 0) or B (h = 1); the score
+            // warpgroup's barrier of the slot completes once per chunk
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int uv = 2 * it + h;
-                if (!mbar_wait(&s.rv_full, uv & 1, abort_flag, &g_bwd_err, 23)) break;
+                if (!mbar_wait(h == 0 ? &s.a_full_s : &s.b_full_s, it & 1, abort_flag, &g_bwd_err, 23)) break;
                 tc_fence_after();
-                const float sc = __fmul_rn(sp[h], a.sdO[static_cast<size_t>(bh) * nblk + qblk[h]]);
+                const float sc = __fmul_rn(sp[h], sdo[h]);
+                const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_base + R_V + cc, r);
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(src + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
+                    for (int k = 0; k < 32; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane_id() == 0) mbar_arrive(&s.rv_free);
+                if (lane_id() == 0) mbar_arrive(h == 0 ? &s.a_free : &s.b_free);
+            }
+            if (it + 1 < nmine) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    sq[h] = nsq[h];
+                    sdo[h] = nsdo[h];
+                    biasv[h] = nbias[h];
+                }
             }
         }
         if (key_ok && !*abort_flag) {
@@ -448,65 +527,84 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
         for (int c = 0; c < D; ++c) dk[c] = 0.0f;
         float skb[2];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) skb[g] = a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)];
+        for (int g = 0; g < 2; ++g)
+            skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
+        float sq[2], nsq[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) sq[h] = nmine > 0 ? a.sQ[static_cast<size_t>(bh) * nblk + min(2 * c_first + h, nblk - 1)] : 0.0f;
         for (int it = 0; it < nmine; ++it) {
             const int ic = c_first + it;
             const int q0 = 128 * ic;
-            int qblk[2];
+            const int slot = it & 1;
+            if (it + 1 < nmine) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) qblk[h] = min(2 * ic + h, nblk - 1);
-            // dK += s_dS s_Q / sqrt(d) (dS^T Q^)_h   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d))
+                for (int h = 0; h < 2; ++h) nsq[h] = a.sQ[static_cast<size_t>(bh) * nblk + min(2 * ic + 2 + h, nblk - 1)];
+            }
+            // dK += s_dS s_Q / sqrt(d) (dS^T Q^)_h   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d));
+            // the grad warpgroup's barrier of a slot completes twice per chunk: dK, then dQ
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int uk = 2 * it + h;
-                if (!mbar_wait(&s.rk_full, uk & 1, abort_flag, &g_bwd_err, 30)) break;
+                if (!mbar_wait(h == 0 ? &s.a_full_g : &s.b_full_g, 0, abort_flag, &g_bwd_err, 30)) break;
                 tc_fence_after();
-                const float sc = __fmul_rn(__fmul_rn(s.sds[it & 1][kb][h], a.sQ[static_cast<size_t>(bh) * nblk + qblk[h]]), a.inv_sqrt_d);
+                const float sc = __fmul_rn(__fmul_rn(s.sds[slot][kb][h], sq[h]), a.inv_sqrt_d);
+                const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_base + R_K + cc, r);
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(src + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
+                    for (int k = 0; k < 32; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
                 }
                 if (BIAS && q0 + 64 * h < N) {
                     const float w = __fmul_rn(s.colsum[h][tq], a.inv_sqrt_d);
-                    const float *mu = a.muQ + (static_cast<size_t>(bh) * nblk + qblk[h]) * D;
+                    const float *mu = a.muQ + (static_cast<size_t>(bh) * nblk + min(2 * ic + h, nblk - 1)) * D;
 #pragma unroll
                     for (int c = 0; c < D; ++c) dk[c] = __fmaf_rn(w, mu[c], dk[c]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane_id() == 0) mbar_arrive(&s.rk_free);
+                if (lane_id() == 0) mbar_arrive(h == 0 ? &s.a_free : &s.b_free);
             }
-            // dQ rows: thread = query row of the chunk
-            const int qrow = q0 + tq;
-            const int h_row = tq >> 6;
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                uint64_t *full = g ? &s.rdp_full : &s.rs_full;
-                uint64_t *freeb = g ? &s.rdp_free : &s.rs_free;
-                if (!mbar_wait(full, it & 1, abort_flag, &g_bwd_err, 31)) break;
+            // dQ rows (thread = query row of the chunk): both key blocks' products, each scaled by
+            // its own s_dS s_K / sqrt(d), summed, then one float32 atomic add per element
+            {
+                const int qrow = q0 + tq;
+                const int h_row = tq >> 6;
+                if (!mbar_wait(&s.a_full_g, 1, abort_flag, &g_bwd_err, 31)) break;
+                if (!mbar_wait(&s.b_full_g, 1, abort_flag, &g_bwd_err, 32)) break;
                 tc_fence_after();
-                const float sc = __fmul_rn(__fmul_rn(s.sds[it & 1][g][h_row], skb[g]), a.inv_sqrt_d);
-                const bool live = qrow < N && k0 + 64 * g < N;
+                const float s0 = __fmul_rn(__fmul_rn(s.sds[slot][0][h_row], skb[0]), a.inv_sqrt_d);
+                const float s1 = __fmul_rn(__fmul_rn(s.sds[slot][1][h_row], skb[1]), a.inv_sqrt_d);
+                const bool live = qrow < N;
                 float *dst = a.dQ + (bhN + min(qrow, N - 1)) * D;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_base + (g ? R_DP : R_S) + cc, r);
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(lane_base + R_A + cc, r0);
+                    tmem_ld16(lane_base + R_B + cc, r1);
                     tmem_wait_ld();
                     if (live) {
 #pragma unroll
-                        for (int k = 0; k < 16; k += 4)
-                            red_add_v4(dst + cc + k, sc * __uint_as_float(r[k]), sc * __uint_as_float(r[k + 1]),
-                                       sc * __uint_as_float(r[k + 2]), sc * __uint_as_float(r[k + 3]));
+                        for (int k = 0; k < 16; k += 4) {
+                            float v[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                v[e] = __fmaf_rn(s1, __uint_as_float(r1[k + e]), __fmul_rn(s0, __uint_as_float(r0[k + e])));
+                            red_add_v4(dst + cc + k, v[0], v[1], v[2], v[3]);
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane_id() == 0) mbar_arrive(freeb);
+                if (lane_id() == 0) {
+                    mbar_arrive(&s.a_free);
+                    mbar_arrive(&s.b_free);
+                }
+            }
+            if (it + 1 < nmine) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) sq[h] = nsq[h];
             }
         }
         if (key_ok && !*abort_flag) {
@@ -529,6 +627,13 @@ static cudaError_t launch_bwd_t(const sage_params &p, const CUtensorMap *maps, c
     const int smem = static_cast<int>(sizeof(bwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // the warpgroup register split must fit in what the block is launched with, or the
+    // setmaxnreg increase could never be granted
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * bwd::kThreads < 2 * 128 * static_cast<int>(bwd::kRegsMath) + 128 * static_cast<int>(bwd::kRegsControl))
+        return cudaErrorInvalidConfiguration;
     dim3 grid((p.N + 127) / 128, p.B * p.H);
     kern<<<grid, bwd::kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
     return cudaGetLastError();

@@ -102,7 +102,7 @@ static FwdWs fwd_ws(const sage_params &p, void *w, size_t *bytes) {
 
 struct BwdWs {
     __half *q16, *k16, *do16;
-    float *D, *sdO, *qbias;
+    float *D, *L2, *sdO, *qbias;
 };
 static BwdWs bwd_ws(const sage_params &p, void *w, size_t *bytes) {
     Carve c(w);
@@ -111,6 +111,7 @@ static BwdWs bwd_ws(const sage_params &p, void *w, size_t *bytes) {
     r.k16 = c.take<__half>(elems(p));
     r.do16 = c.take<__half>(elems(p));
     r.D = c.take<float>(rows(p));
+    r.L2 = c.take<float>(rows(p));
     r.sdO = c.take<float>(nblocks(p));
     r.qbias = p.smooth_q ? c.take<float>(nblocks(p) * p.N) : nullptr;
     if (bytes) *bytes = c.off;
@@ -311,7 +312,7 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     SAGE_CUDA(launch_widen(Qh, w.q16, n, st));
     SAGE_CUDA(launch_widen(Kh, w.k16, n, st));
     BwdPrologueArgs pa;
-    pa.dO = dO; pa.O = O; pa.D = w.D; pa.dO16 = w.do16; pa.dOh = dd.doh; pa.sdO = w.sdO;
+    pa.dO = dO; pa.O = O; pa.L = L; pa.L2 = w.L2; pa.D = w.D; pa.dO16 = w.do16; pa.dOh = dd.doh; pa.sdO = w.sdO;
     pa.N = p->N; pa.d = p->d;
     SAGE_CUDA(launch_bwd_prologue(*p, pa, st));
     const float sl2 = scale_log2(p->d);
@@ -319,7 +320,7 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     SAGE_CUDA(cudaMemsetAsync(dQ, 0, n * sizeof(float), st));
     BwdArgs a;
     memset(&a, 0, sizeof(a));
-    a.sQ = sQ; a.sK = sK; a.sdO = w.sdO; a.D = w.D; a.L = L;
+    a.sQ = sQ; a.sK = sK; a.sdO = w.sdO; a.D = w.D; a.L2 = w.L2;
     a.qbias = w.qbias; a.muQ = p->smooth_q ? muQ : nullptr;
     a.dQ = dQ; a.dK = dK; a.dV = dV;
     if (p->flags & SAGE_FLAG_DUMP) {

@@ -385,6 +385,13 @@ static cudaError_t launch_fwd_t(const sage_params &p, const CUtensorMap &mq, con
     const int smem = static_cast<int>(sizeof(fwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // the warpgroup register split must fit in what the block is launched with, or the
+    // setmaxnreg increase could never be granted
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * fwd::kThreads < 2 * 128 * static_cast<int>(fwd::kRegsSoftmax) + 128 * static_cast<int>(fwd::kRegsControl))
+        return cudaErrorInvalidConfiguration;
     dim3 grid((p.N + 255) / 256, p.B * p.H);
     kern<<<grid, fwd::kThreads, smem, st>>>(mq, mk, mv, a);
     return cudaGetLastError();

@@ -257,7 +257,11 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(BwdPrologueArgs a) {
         }
         // reduce over the vec_per_row consecutive lanes that share row r (fixed tree order)
         for (int o2 = 1; o2 < vec_per_row; o2 <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-        if (cv == 0) a.D[static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r] = part;
+        if (cv == 0) {
+            const size_t row = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r;
+            a.D[row] = part;
+            a.L2[row] = __fmul_rn(a.L[row], kLog2e);
+        }
     }
     mx = block_max_256(mx, red);
     const float delta = __fdiv_rn(mx, 127.0f);

@@ -22,9 +22,11 @@ Readings where the pages are silent, garbled or at odds (listed again in DESIGN.
       non-inverted one.  With Q-smoothing t_k = fl32(acc_k * c + bias_k), r = max t_k,
       x_k = fl32(t_k - r).
   R8  backward P_k = fl32(2^(fl32(acc_k * c - L2))) with L2 = fl32(L * fl32(log2(e))) (with
-      Q-smoothing fl32(t_k - L2)); P and dS are quantised per 64x64 tile: s = fl32(max|x|/127), q =
-      rne(fl32(x * fl32(1/s))); a tile whose max|x| is below 2^-120 (zero, or so small that
-      1/s would overflow float32) gets s = 0, q = 0.
+      Q-smoothing fl32(t_k - L2)); P and dS are quantised per 64x64 tile: s = fl32(max|x|/127),
+      q = rne16(fl32(x * fl32(1/s) + 1536)) - 1536, i.e. the value x/s rounded once to float32
+      at the 2^-13 spacing of [1024, 2048) and then to the nearest integer, ties to even (the
+      pages say only "round"; this is the kernel's two-instruction rounding); a tile whose
+      max|x| is below 2^-120 (zero, or so small that 1/s would overflow float32) gets s = 0, q = 0.
   R9  dP = dO V^T uses the unquantised 16-bit dO and V, float32 result, never rounded to 16 bits.
   R10 D = rowsum(dO o O) uses the stored 16-bit O.
   R11 no K-smoothing correction in the backward pass.
@@ -147,7 +149,10 @@ class Arith:
             return F32(0), np.zeros(x.shape, np.int64)
         s = F32(mx) / F32(127)
         inv = F32(1) / s
-        q = np.clip(np.rint(x * inv), -127, 127).astype(np.int64)
+        # round half to even of y = fl32(x * inv + 1536) at fp16 resolution (1 in [1024, 2048)):
+        # x * inv is exact in float64 and so is the sum, so one cast gives the fused rounding
+        y = (x.astype(np.float64) * float(inv) + 1536.0).astype(np.float32)
+        q = y.astype(np.float16).astype(np.int64) - 1536
         return s, q
 
     def exp2_32(self, x):

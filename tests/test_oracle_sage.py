@@ -136,10 +136,23 @@ def test_tile_quantiser_against_exact_rationals():
         se = fl32(mx / 127)
         inv = fl32(1 / se)
         assert Fr(float(s)) == se
-        qe = [max(-127, min(127, rne(fl32(Fr(float(v)) * inv)))) for v in x.ravel()]
+        # one float32 rounding of x * inv + 1536, then to an integer (fp16 spacing is 1 there)
+        qe = [rne(fl32(Fr(float(v)) * inv + 1536)) - 1536 for v in x.ravel()]
         assert q.ravel().tolist() == qe
+        assert max(abs(v) for v in qe) == 127
     s, q = sage.QUANTISED.tile_quant(np.zeros((64, 64), np.float32))
     assert s == 0 and not q.any()
+
+
+def test_tile_quantiser_rounding_boundaries():
+    """Hand-worked: max = 127 gives s = 1 and inv = 1 exactly, so the codes are x rounded to the
+    float32 spacing 2^-13 around 1536 and then half to even: 62.5 -> 62, 63.5 -> 64,
+    -2.5 -> -2, and 62.5 - 2^-15 -> 62.5 (float32 spacing) -> 62."""
+    x = np.zeros((64, 64), np.float32)
+    x.ravel()[:6] = [127.0, 62.5, 63.5, -2.5, 62.5 - 2.0 ** -15, 0.49999997]
+    s, q = sage.QUANTISED.tile_quant(x)
+    assert s == np.float32(1.0)
+    assert q.ravel()[:6].tolist() == [127, 62, 64, -2, 62, 0]
 
 
 def test_special_case_constant_keys():
