@@ -16,17 +16,21 @@
 //   two product slots R_A = cols [256,384), R_B = [384,512), each filled three times a chunk:
 //     dK_h = dS^T_h Q^_h  (A from TMEM, K=64 q)    h = 0 -> R_A, 1 -> R_B
 //     dV_h = P^T_h dO^_h  (A from TMEM, K=64 q)
-//     dQ_g = dS^_g K^_g   (A from smem, K=64 keys)  g = key block
+//     dQ_g = dS^_g K^_g   (A from smem, K=64 keys)  g = key block; for d = 128 formed as
+//            dQ_g^T = K^_g^T dS^_g^T (M = d) so that the dQ atomics are coalesced
 // The MMA order per chunk is dK, dV, then the next chunk's S^T and dP^T (their regions' codes
 // are consumed by then: the tensor pipe runs in issue order), then dQ: the score warpgroup starts
 // on the next chunk while the dQ products are added to global memory.
-// Warp roles (12 warps; registers 232 for the two math warpgroups, 40 for the control one):
-//   warps 0-3  "score" warpgroup, thread = key: P = 2^(acc c - L2), dS = P o (dP - D) in place in
-//              TMEM; per 64x64 tile max reductions; P and dS codes back into TMEM (A operands)
-//              and dS codes into shared memory (A operand of dQ); dV rows in registers.
-//   warps 4-7  "grad" warpgroup: dK rows in registers (thread = key); the two dQ products of a
-//              chunk read with thread = query row, scaled, summed and added to global dQ with
-//              one vector float32 atomic per four elements.
+// Warp roles (16 warps in four warpgroups):
+//   warps 0-3   "score": thread = key; P = 2^(acc c - L2), dS = P o (dP - D) in place in TMEM,
+//               per 64x64 tile max reductions, P and dS codes back into TMEM (A operands) and dS
+//               codes into shared memory (A operand of dQ).  It holds no accumulator, so its
+//               registers go to instruction-level parallelism over 16 columns at a time.
+//   warps 4-7   "dV": dV rows in registers (thread = key); it also adds the two dQ products of
+//               each chunk to global dQ: d = 128 stages their scaled sum in shared memory and
+//               adds it with TMA bulk reductions (32 KB row blocks); d = 64 uses vector float32
+//               atomics along each query row.
+//   warps 8-11  "dK": dK rows in registers (thread = key).
 //   warp 8     TMA producer (tiles, and L2 / D rows by bulk copy); warp 9 TMEM allocation and the
 //              single MMA-issuing thread.
 //
@@ -45,10 +49,14 @@ __device__ unsigned int g_bwd_err;
 
 namespace bwd {
 
-constexpr int kThreads = 384;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kRegsMath = 232;
+// Four warpgroups, launched at 128 registers a thread (512 x 128 = 65536).  setmaxnreg then gives
+// score 152, dV 160, dK 160 and control 40: 128 x (152 + 160 + 160 + 40) = 65536.
+constexpr int kThreads = 512;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr uint32_t kRegsScore = 152;
+constexpr uint32_t kRegsDV = 160;
+constexpr uint32_t kRegsDK = 160;
 constexpr uint32_t kRegsControl = 40;
 constexpr uint32_t R_S = 0, R_DP = 128, R_A = 256, R_B = 384;
 constexpr float kTileZero = 7.52316384526264e-37f;   // 2^-120
@@ -65,13 +73,14 @@ struct Smem {
     alignas(16) float Ds[2][128];                   // [chunk parity][q]: D
     float red[4][2][4];                             // [warp][chunk parity][4 maxima]
     float sds[2][2][2];                             // [chunk parity][kb][qb] dS tile scales
+    float sps[2][2][2];                             // [chunk parity][kb][qb] P tile scales
     float colsum[2][128];                           // [qb][key] column sums of dS (Q-smoothing)
     uint64_t kv_full, q_full, q_free, do_full, do_free, doh_full, doh_free, meta_full[2];
     uint64_t s_full, dp_full, codes_ready, dss_free;
-    // the two product slots R_A, R_B: "full" per consumer (the grad warpgroup takes dK and dQ,
-    // the score warpgroup dV), so that every waiter sees every phase of its barrier; "free" is
-    // shared (the MMA thread waits for each use in turn)
-    uint64_t a_full_g, a_full_s, a_free, b_full_g, b_full_s, b_free;
+    // the two product slots R_A, R_B: "full" per consumer (the dK warpgroup takes dK, the dV
+    // warpgroup dV and dQ), so that every waiter sees every phase of its barrier; "free" is shared
+    // (the MMA thread waits for each use in turn)
+    uint64_t a_full_k, a_full_v, a_free, b_full_k, b_full_v, b_free;
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -94,6 +103,19 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+
+// TMA bulk reduction: global[dst .. dst+bytes) += shared[src ..] (float32 add), bulk-group tracked
+__device__ __forceinline__ void bulk_reduce_add_f32(float *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
@@ -145,7 +167,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
         s.abort_flag = 0;
         uint64_t *one[] = {&s.kv_full, &s.q_full, &s.q_free, &s.do_full, &s.do_free, &s.doh_full,
                            &s.doh_free, &s.meta_full[0], &s.meta_full[1], &s.s_full, &s.dp_full,
-                           &s.dss_free, &s.a_full_g, &s.a_full_s, &s.b_full_g, &s.b_full_s,
+                           &s.dss_free, &s.a_full_k, &s.a_full_v, &s.b_full_k, &s.b_full_v,
                            &s.mma_done};
         for (uint64_t *b : one) mbar_init(b, 1);
         mbar_init(&s.codes_ready, 4);
@@ -159,7 +181,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     const uint32_t tmem = s.tmem_base;
     volatile int *abort_flag = &s.abort_flag;
 
-    if (warp >= 8) {
+    if (warp >= 12) {
         regs_dec<kRegsControl>();
         if (warp == kProducerWarp) {
             // -------------------------------------------------------------- TMA producer
@@ -213,7 +235,8 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 constexpr uint32_t idKK = idesc_f16(128, 128, false, false, false);    // S^T
                 constexpr uint32_t idDP = idesc_f16(128, 128, BF16, false, false);     // dP^T
                 constexpr uint32_t idTS = idesc_f16(128, D, false, false, true);       // dV, dK
-                constexpr uint32_t idQ = idesc_f16(128, D, false, true, true);         // dQ
+                constexpr uint32_t idQ = D == 128 ? idesc_f16(128, 128, false, true, true)   // dQ^T
+                                                  : idesc_f16(128, D, false, true, true);    // dQ
                 // base descriptors; a byte offset `off` inside an operand adds off >> 4
                 const uint64_t dKt = sdesc_sw128(smem_u32(s.kt[0]), 16, 1024);
                 const uint64_t dVt = sdesc_sw128(smem_u32(s.vt[0]), 16, 1024);
@@ -264,7 +287,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk)
                             umma_ts(dst, tmem + R_DP + 32 * h + 8 * kk, dQmn + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
-                        umma_commit(h == 0 ? &s.a_full_g : &s.b_full_g);
+                        umma_commit(h == 0 ? &s.a_full_k : &s.b_full_k);
                         if (h == 0) ++ua; else ++ub;
                     }
                     if (!ok) break;
@@ -278,7 +301,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk)
                             umma_ts(dst, tmem + R_S + 32 * h + 8 * kk, dDoh + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
-                        umma_commit(h == 0 ? &s.a_full_s : &s.b_full_s);
+                        umma_commit(h == 0 ? &s.a_full_v : &s.b_full_v);
                         if (h == 0) ++ua; else ++ub;
                     }
                     if (!ok) break;
@@ -286,7 +309,10 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                     // the next chunk's scores: the tensor pipe runs in issue order, so the codes in
                     // R_S / R_DP have been read by the dV / dK MMAs above before they are replaced
                     if (it + 1 < nmine && !(ok = issue_s_dp(it + 1))) break;
-                    // dQ_g = dS^[:, keys of g] K^_g
+                    // dQ_g = dS^[:, keys of g] K^_g.  For d = 128 it is formed transposed,
+                    // dQ_g^T = K^_g^T dS^_g^T (M = d, N = 128 q): same two shared tiles with the
+                    // operand roles swapped, so that a thread then owns one d column and the
+                    // atomic adds of a warp hit 32 consecutive floats of one query row.
 #pragma unroll 1
                     for (int g = 0; g < 2 && ok; ++g) {
                         if (!(ok = slot_ready(g == 0))) break;
@@ -294,19 +320,22 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t o = ((64 * g + 16 * kk) * 128) >> 4;
-                            umma_ss(dst, dDss + o, dKmn + o, idQ, kk > 0);
+                            if (D == 128) umma_ss(dst, dKmn + o, dDss + o, idQ, kk > 0);
+                            else umma_ss(dst, dDss + o, dKmn + o, idQ, kk > 0);
                         }
-                        umma_commit(g == 0 ? &s.a_full_g : &s.b_full_g);
+                        umma_commit(g == 0 ? &s.a_full_v : &s.b_full_v);
                         if (g == 0) ++ua; else ++ub;
                     }
-                    umma_commit(&s.dss_free);
+                    // d = 64: the dS^ tile is free once the dQ MMAs have read it; d = 128: the dV
+                    // warpgroup frees it after staging the dQ reduction through it
+                    if (D != 128) umma_commit(&s.dss_free);
                 }
                 umma_commit(&s.mma_done);
                 mbar_wait_drain(&s.mma_done, 0, &g_bwd_err, 14);
             }
         }
     } else if (warp < 4) {
-        regs_inc<kRegsMath>();
+        regs_inc<kRegsScore>();
         // ------------------------------------------------------------------ score warpgroup
         const int tq = threadIdx.x;                       // 0..127: key lane
         const int quarter = warp;
@@ -316,27 +345,23 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
         const bool key_ok = key < N;
         const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
         const float sk = a.sK[static_cast<size_t>(bh) * nblk + kblk];
-        float dv[D];
-#pragma unroll
-        for (int c = 0; c < D; ++c) dv[c] = 0.0f;
         // per-chunk scalars, fetched one chunk ahead
-        auto fetch = [&](int ic, float (&sq)[2], float (&sdo)[2], float (&bias)[2]) {
+        auto fetch = [&](int ic, float (&sq)[2], float (&bias)[2]) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int qb = min(2 * ic + h, nblk - 1);
                 sq[h] = a.sQ[static_cast<size_t>(bh) * nblk + qb];
-                sdo[h] = a.sdO[static_cast<size_t>(bh) * nblk + qb];
                 bias[h] = (BIAS && key_ok) ? a.qbias[(static_cast<size_t>(bh) * nblk + qb) * N + key] : 0.0f;
             }
         };
-        float sq[2], sdo[2], biasv[2], nsq[2], nsdo[2], nbias[2];
-        if (nmine > 0) fetch(c_first, sq, sdo, biasv);
+        float sq[2], biasv[2], nsq[2], nbias[2];
+        if (nmine > 0) fetch(c_first, sq, biasv);
         for (int it = 0; it < nmine; ++it) {
             const uint32_t ph = it & 1;
             const int slot = it & 1;
             const int ic = c_first + it;
             const int q0 = 128 * ic;
-            if (it + 1 < nmine) fetch(ic + 1, nsq, nsdo, nbias);
+            if (it + 1 < nmine) fetch(ic + 1, nsq, nbias);
             float cq[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) cq[h] = __fmul_rn(__fmul_rn(sq[h], sk), a.sl2);
@@ -427,6 +452,8 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
             if ((tq & 63) == 0) {
                 s.sds[slot][kb][0] = sd[0];
                 s.sds[slot][kb][1] = sd[1];
+                s.sps[slot][kb][0] = sp[0];
+                s.sps[slot][kb][1] = sp[1];
                 if (DUMP) {
                     for (int h = 0; h < 2; ++h) {
                         if (key_ok && q0 + 64 * h < N) {
@@ -479,44 +506,170 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane_id() == 0) mbar_arrive(&s.codes_ready);
-            // dV += s_P s_dO (P^T dO^)_h: product h sits in slot A (h = 0) or B (h = 1); the score
-            // warpgroup's barrier of the slot completes once per chunk
+            if (it + 1 < nmine) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    sq[h] = nsq[h];
+                    biasv[h] = nbias[h];
+                }
+            }
+        }
+    } else if (warp < 8) {
+        regs_inc<kRegsDV>();
+        // ------------------------------------------------------------------ dV warpgroup
+        // dV rows in registers (thread = key); the two dQ products of each chunk (d = 128:
+        // thread = d column) scaled, summed and added to global dQ with float32 atomics
+        const int tq = threadIdx.x - 128;
+        const int quarter = warp & 3;
+        const int key = k0 + tq;
+        const int kb = tq >> 6;
+        const bool key_ok = key < N;
+        const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+        float dv[D];
+#pragma unroll
+        for (int c = 0; c < D; ++c) dv[c] = 0.0f;
+        float skb[2];
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+            skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
+        float sdo[2], nsdo[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) sdo[h] = nmine > 0 ? a.sdO[static_cast<size_t>(bh) * nblk + min(2 * c_first + h, nblk - 1)] : 0.0f;
+        for (int it = 0; it < nmine; ++it) {
+            const int ic = c_first + it;
+            const int q0 = 128 * ic;
+            const int slot = it & 1;
+            if (it + 1 < nmine) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) nsdo[h] = a.sdO[static_cast<size_t>(bh) * nblk + min(2 * ic + 2 + h, nblk - 1)];
+            }
+            // dV += s_P s_dO (P^T dO^)_h: product h in slot A (h = 0) or B (h = 1); this
+            // warpgroup's barrier of a slot completes twice a chunk: dV (parity 0), then dQ (1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                if (!mbar_wait(h == 0 ? &s.a_full_s : &s.b_full_s, it & 1, abort_flag, &g_bwd_err, 23)) break;
+                if (!mbar_wait(h == 0 ? &s.a_full_v : &s.b_full_v, 0, abort_flag, &g_bwd_err, 23)) break;
                 tc_fence_after();
-                const float sc = __fmul_rn(sp[h], sdo[h]);
+                const float sc = __fmul_rn(s.sps[slot][kb][h], sdo[h]);
                 const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(src + cc, r);
+                for (int cc = 0; cc < D; cc += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(src + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
+                    for (int k = 0; k < 16; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane_id() == 0) mbar_arrive(h == 0 ? &s.a_free : &s.b_free);
             }
-            if (it + 1 < nmine) {
+            // dQ: both key blocks' products, each scaled by its own s_dS s_K / sqrt(d) and summed
+            if (!mbar_wait(&s.a_full_v, 1, abort_flag, &g_bwd_err, 31)) break;
+            if (!mbar_wait(&s.b_full_v, 1, abort_flag, &g_bwd_err, 32)) break;
+            tc_fence_after();
+            if (D == 128) {
+                // transposed products: thread = d column c, TMEM columns = the chunk's query rows.
+                // The scaled sum goes to shared memory (the dS^ tile, which the dQ MMAs have
+                // finished reading) as 64 query rows x 128 floats at a time, and one TMA bulk
+                // reduction adds each 32 KB block of rows to global dQ.
+                const int c = tq;
+                float sg0[2], sg1[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    sq[h] = nsq[h];
-                    sdo[h] = nsdo[h];
-                    biasv[h] = nbias[h];
+                    sg0[h] = __fmul_rn(__fmul_rn(s.sds[slot][0][h], skb[0]), a.inv_sqrt_d);
+                    sg1[h] = __fmul_rn(__fmul_rn(s.sds[slot][1][h], skb[1]), a.inv_sqrt_d);
+                }
+                const int nrow = min(128, N - q0);
+                float *stage = reinterpret_cast<float *>(s.dss[0]);        // [64 rows][128 floats]
+                const bool leader = tq == 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int rows = min(64, nrow - 64 * h);
+                    if (rows <= 0) break;
+                    if (h == 1) {
+                        // the first block's reduction must have read the staging tile
+                        if (leader) bulk_wait_read_all();
+                        named_bar_sync(2, 128);
+                    }
+#pragma unroll 1
+                    for (int cc = 64 * h; cc < 64 * h + 64; cc += 8) {
+                        uint32_t r0[8], r1[8];
+                        tmem_ld8(lane_base + R_A + cc, r0);
+                        tmem_ld8(lane_base + R_B + cc, r1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            stage[(cc - 64 * h + k) * 128 + c] =
+                                __fmaf_rn(sg1[h], __uint_as_float(r1[k]), __fmul_rn(sg0[h], __uint_as_float(r0[k])));
+                    }
+                    fence_view_async_shared();
+                    named_bar_sync(2, 128);
+                    if (leader) {
+                        bulk_reduce_add_f32(a.dQ + (bhN + q0 + 64 * h) * D, stage, static_cast<uint32_t>(rows) * 128u * 4u);
+                        bulk_commit();
+                    }
+                }
+                // the products have been read out of TMEM: release both slots
+                tc_fence_before();
+                __syncwarp();
+                if (lane_id() == 0) {
+                    mbar_arrive(&s.a_free);
+                    mbar_arrive(&s.b_free);
+                }
+                // the staging tile goes back to the score warpgroup once the last reduction read it
+                if (leader) {
+                    bulk_wait_read_all();
+                    mbar_arrive(&s.dss_free);
+                }
+            } else {
+                // d = 64: thread = query row of the chunk, vector atomics along the row
+                const int qrow = q0 + tq;
+                const int h_row = tq >> 6;
+                const float s0 = __fmul_rn(__fmul_rn(s.sds[slot][0][h_row], skb[0]), a.inv_sqrt_d);
+                const float s1 = __fmul_rn(__fmul_rn(s.sds[slot][1][h_row], skb[1]), a.inv_sqrt_d);
+                const bool live = qrow < N;
+                float *dst = a.dQ + (bhN + min(qrow, N - 1)) * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 8) {
+                    uint32_t r0[8], r1[8];
+                    tmem_ld8(lane_base + R_A + cc, r0);
+                    tmem_ld8(lane_base + R_B + cc, r1);
+                    tmem_wait_ld();
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < 8; k += 4) {
+                            float v[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                v[e] = __fmaf_rn(s1, __uint_as_float(r1[k + e]), __fmul_rn(s0, __uint_as_float(r0[k + e])));
+                            red_add_v4(dst + cc + k, v[0], v[1], v[2], v[3]);
+                        }
+                    }
                 }
             }
+            if (D != 128) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane_id() == 0) {
+                    mbar_arrive(&s.a_free);
+                    mbar_arrive(&s.b_free);
+                }
+            }
+            if (it + 1 < nmine) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) sdo[h] = nsdo[h];
+            }
         }
+        if (D == 128 && tq == 0) bulk_wait_all();
         if (key_ok && !*abort_flag) {
             float *dst = a.dV + (bhN + key) * D;
 #pragma unroll
             for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(dv[c], dv[c + 1], dv[c + 2], dv[c + 3]);
         }
     } else {
-        regs_inc<kRegsMath>();
-        // ------------------------------------------------------------------ grad warpgroup
-        const int tq = threadIdx.x - 128;                 // key lane (dK) / query lane (dQ)
+        regs_inc<kRegsDK>();
+        // ------------------------------------------------------------------ dK warpgroup
+        const int tq = threadIdx.x - 256;                 // key lane
         const int quarter = warp & 3;
         const int key = k0 + tq;
         const int kb = tq >> 6;
@@ -541,20 +694,20 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 for (int h = 0; h < 2; ++h) nsq[h] = a.sQ[static_cast<size_t>(bh) * nblk + min(2 * ic + 2 + h, nblk - 1)];
             }
             // dK += s_dS s_Q / sqrt(d) (dS^T Q^)_h   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d));
-            // the grad warpgroup's barrier of a slot completes twice per chunk: dK, then dQ
+            // this warpgroup's barrier of a slot completes once a chunk
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                if (!mbar_wait(h == 0 ? &s.a_full_g : &s.b_full_g, 0, abort_flag, &g_bwd_err, 30)) break;
+                if (!mbar_wait(h == 0 ? &s.a_full_k : &s.b_full_k, it & 1, abort_flag, &g_bwd_err, 30)) break;
                 tc_fence_after();
                 const float sc = __fmul_rn(__fmul_rn(s.sds[slot][kb][h], sq[h]), a.inv_sqrt_d);
                 const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(src + cc, r);
+                for (int cc = 0; cc < D; cc += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(src + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
+                    for (int k = 0; k < 16; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
                 }
                 if (BIAS && q0 + 64 * h < N) {
                     const float w = __fmul_rn(s.colsum[h][tq], a.inv_sqrt_d);
@@ -565,42 +718,6 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 tc_fence_before();
                 __syncwarp();
                 if (lane_id() == 0) mbar_arrive(h == 0 ? &s.a_free : &s.b_free);
-            }
-            // dQ rows (thread = query row of the chunk): both key blocks' products, each scaled by
-            // its own s_dS s_K / sqrt(d), summed, then one float32 atomic add per element
-            {
-                const int qrow = q0 + tq;
-                const int h_row = tq >> 6;
-                if (!mbar_wait(&s.a_full_g, 1, abort_flag, &g_bwd_err, 31)) break;
-                if (!mbar_wait(&s.b_full_g, 1, abort_flag, &g_bwd_err, 32)) break;
-                tc_fence_after();
-                const float s0 = __fmul_rn(__fmul_rn(s.sds[slot][0][h_row], skb[0]), a.inv_sqrt_d);
-                const float s1 = __fmul_rn(__fmul_rn(s.sds[slot][1][h_row], skb[1]), a.inv_sqrt_d);
-                const bool live = qrow < N;
-                float *dst = a.dQ + (bhN + min(qrow, N - 1)) * D;
-#pragma unroll 1
-                for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(lane_base + R_A + cc, r0);
-                    tmem_ld16(lane_base + R_B + cc, r1);
-                    tmem_wait_ld();
-                    if (live) {
-#pragma unroll
-                        for (int k = 0; k < 16; k += 4) {
-                            float v[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                v[e] = __fmaf_rn(s1, __uint_as_float(r1[k + e]), __fmul_rn(s0, __uint_as_float(r0[k + e])));
-                            red_add_v4(dst + cc + k, v[0], v[1], v[2], v[3]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane_id() == 0) {
-                    mbar_arrive(&s.a_free);
-                    mbar_arrive(&s.b_free);
-                }
             }
             if (it + 1 < nmine) {
 #pragma unroll
@@ -632,7 +749,7 @@ static cudaError_t launch_bwd_t(const sage_params &p, const CUtensorMap *maps, c
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs * bwd::kThreads < 2 * 128 * static_cast<int>(bwd::kRegsMath) + 128 * static_cast<int>(bwd::kRegsControl))
+    if (fa.numRegs * bwd::kThreads < 128 * static_cast<int>(bwd::kRegsScore + bwd::kRegsDV + bwd::kRegsDK + bwd::kRegsControl))
         return cudaErrorInvalidConfiguration;
     dim3 grid((p.N + 127) / 128, p.B * p.H);
     kern<<<grid, bwd::kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
