@@ -50,13 +50,13 @@ __device__ unsigned int g_bwd_err;
 namespace bwd {
 
 // Four warpgroups, launched at 128 registers a thread (512 x 128 = 65536).  setmaxnreg then gives
-// score 152, dV 160, dK 160 and control 40: 128 x (152 + 160 + 160 + 40) = 65536.
+// score 152, dV 168, dK 152 and control 40: 128 x (152 + 168 + 152 + 40) = 65536.
 constexpr int kThreads = 512;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr uint32_t kRegsScore = 152;
-constexpr uint32_t kRegsDV = 160;
-constexpr uint32_t kRegsDK = 160;
+constexpr uint32_t kRegsDV = 168;
+constexpr uint32_t kRegsDK = 152;
 constexpr uint32_t kRegsControl = 40;
 constexpr uint32_t R_S = 0, R_DP = 128, R_A = 256, R_B = 384;
 constexpr float kTileZero = 7.52316384526264e-37f;   // 2^-120
@@ -127,9 +127,15 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
 // Values x * inv lie in [-127, 127], so x * inv + 1536 lies in [1024, 2048) where fp16 spacing is
 // 1: the fp16 conversion rounds to an integer and the subtraction is exact.
 __device__ __forceinline__ uint32_t codes2(float x0, float x1, float inv) {
-    const __half2 h = __floats2half2_rn(__fmaf_rn(x0, inv, 1536.0f), __fmaf_rn(x1, inv, 1536.0f));
-    const __half2 r = __hsub2(h, __float2half2_rn(1536.0f));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    const float y0 = __fmaf_rn(x0, inv, 1536.0f), y1 = __fmaf_rn(x1, inv, 1536.0f);
+    uint32_t r;
+    // cvt packs its first source into the upper half; 0x6600 is 1536 in fp16
+    asm("{\n\t.reg .b32 t;\n\t"
+        "cvt.rn.f16x2.f32 t, %2, %1;\n\t"
+        "sub.rn.f16x2 %0, t, %3;\n\t}"
+        : "=r"(r)
+        : "f"(y0), "f"(y1), "r"(0x66006600u));
+    return r;
 }
 
 __device__ __forceinline__ int16_t code_lo(uint32_t w) {
@@ -346,25 +352,33 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
         const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
         const float sk = a.sK[static_cast<size_t>(bh) * nblk + kblk];
         // per-chunk scalars, fetched one chunk ahead
-        auto fetch = [&](int ic, float (&sq)[2], float (&bias)[2]) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int qb = min(2 * ic + h, nblk - 1);
-                sq[h] = a.sQ[static_cast<size_t>(bh) * nblk + qb];
-                bias[h] = (BIAS && key_ok) ? a.qbias[(static_cast<size_t>(bh) * nblk + qb) * N + key] : 0.0f;
+        const float *sQh = a.sQ + static_cast<size_t>(bh) * nblk;
+        const float *biash = BIAS ? a.qbias + static_cast<size_t>(bh) * nblk * N + min(key, N - 1) : nullptr;
+        float sq0 = 0.0f, sq1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+        if (nmine > 0) {
+            sq0 = sQh[min(2 * c_first, nblk - 1)];
+            sq1 = sQh[min(2 * c_first + 1, nblk - 1)];
+            if (BIAS && key_ok) {
+                b0 = biash[static_cast<size_t>(min(2 * c_first, nblk - 1)) * N];
+                b1 = biash[static_cast<size_t>(min(2 * c_first + 1, nblk - 1)) * N];
             }
-        };
-        float sq[2], biasv[2], nsq[2], nbias[2];
-        if (nmine > 0) fetch(c_first, sq, biasv);
+        }
         for (int it = 0; it < nmine; ++it) {
             const uint32_t ph = it & 1;
             const int slot = it & 1;
             const int ic = c_first + it;
             const int q0 = 128 * ic;
-            if (it + 1 < nmine) fetch(ic + 1, nsq, nbias);
-            float cq[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) cq[h] = __fmul_rn(__fmul_rn(sq[h], sk), a.sl2);
+            float nsq0 = 0.0f, nsq1 = 0.0f, nb0 = 0.0f, nb1 = 0.0f;
+            if (it + 1 < nmine) {
+                nsq0 = sQh[min(2 * ic + 2, nblk - 1)];
+                nsq1 = sQh[min(2 * ic + 3, nblk - 1)];
+                if (BIAS && key_ok) {
+                    nb0 = biash[static_cast<size_t>(min(2 * ic + 2, nblk - 1)) * N];
+                    nb1 = biash[static_cast<size_t>(min(2 * ic + 3, nblk - 1)) * N];
+                }
+            }
+            const float cq[2] = {__fmul_rn(__fmul_rn(sq0, sk), a.sl2), __fmul_rn(__fmul_rn(sq1, sk), a.sl2)};
+            const float biasv[2] = {b0, b1};
             // valid query columns for this key: [qlo, qhi) relative to q0
             const int qhi = min(128, N - q0);
             const int qlo = a.causal ? max(0, key - q0) : 0;
@@ -378,19 +392,19 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll 1
-            for (int cc = 64 * h; cc < 64 * h + 64; cc += 16) {
-                uint32_t sr[16], dr[16];
-                tmem_ld16(lane_base + R_S + cc, sr);
-                tmem_ld16(lane_base + R_DP + cc, dr);
-                float l2v[16], dvv[16];
+            for (int cc = 64 * h; cc < 64 * h + 64; cc += 8) {
+                uint32_t sr[8], dr[8];
+                tmem_ld8(lane_base + R_S + cc, sr);
+                tmem_ld8(lane_base + R_DP + cc, dr);
+                float l2v[8], dvv[8];
 #pragma unroll
-                for (int k = 0; k < 16; k += 4) {
+                for (int k = 0; k < 8; k += 4) {
                     *reinterpret_cast<float4 *>(&l2v[k]) = *reinterpret_cast<const float4 *>(&s.L2s[slot][cc + k]);
                     *reinterpret_cast<float4 *>(&dvv[k]) = *reinterpret_cast<const float4 *>(&s.Ds[slot][cc + k]);
                 }
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
+                for (int k = 0; k < 8; ++k) {
                     const int col = cc + k;
                     const float acc = __uint_as_float(sr[k]);
                     float x;
@@ -414,8 +428,8 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                     sr[k] = __float_as_uint(p);
                     dr[k] = __float_as_uint(ds);
                 }
-                tmem_st16(lane_base + R_S + cc, sr);
-                tmem_st16(lane_base + R_DP + cc, dr);
+                tmem_st8(lane_base + R_S + cc, sr);
+                tmem_st8(lane_base + R_DP + cc, dr);
             }
             tmem_wait_st();
             // per 64x64 tile maxima: over the 32 lanes, then over the two warps of this key block
@@ -506,13 +520,10 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane_id() == 0) mbar_arrive(&s.codes_ready);
-            if (it + 1 < nmine) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    sq[h] = nsq[h];
-                    biasv[h] = nbias[h];
-                }
-            }
+            sq0 = nsq0;
+            sq1 = nsq1;
+            b0 = nb0;
+            b1 = nb1;
         }
     } else if (warp < 8) {
         regs_inc<kRegsDV>();
@@ -552,12 +563,12 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 const float sc = __fmul_rn(s.sps[slot][kb][h], sdo[h]);
                 const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(src + cc, r);
+                for (int cc = 0; cc < D; cc += 8) {
+                    uint32_t r[8];
+                    tmem_ld8(src + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
+                    for (int k = 0; k < 8; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -702,12 +713,12 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                 const float sc = __fmul_rn(__fmul_rn(s.sds[slot][kb][h], sq[h]), a.inv_sqrt_d);
                 const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(src + cc, r);
+                for (int cc = 0; cc < D; cc += 8) {
+                    uint32_t r[8];
+                    tmem_ld8(src + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
+                    for (int k = 0; k < 8; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
                 }
                 if (BIAS && q0 + 64 * h < N) {
                     const float w = __fmul_rn(s.colsum[h][tq], a.inv_sqrt_d);
