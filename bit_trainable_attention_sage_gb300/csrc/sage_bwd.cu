@@ -9,30 +9,35 @@
 //
 // GB300 design.  The integer GEMMs run as kind::f16 MMAs on integer-valued fp16 codes (exact, see
 // the forward); dP runs on the unquantised fp16/bf16 dO and V.  One CTA owns a 128-key tile
-// (two 64-key quantisation blocks) of one head and loops over 128-row query chunks (two 64-row
-// blocks).  Everything is transposed so that keys are TMEM lanes:
-//   S^T  = K^ Q^T      (M=128 keys, N=128 q, K=d)    TMEM R_S  = cols [0,128)
-//   dP^T = V dO^T      (M=128 keys, N=128 q, K=d)    TMEM R_dP = cols [128,256)
-//   two product slots R_A = cols [256,384), R_B = [384,512), each filled three times a chunk:
-//     dK_h = dS^T_h Q^_h  (A from TMEM, K=64 q)    h = 0 -> R_A, 1 -> R_B
-//     dV_h = P^T_h dO^_h  (A from TMEM, K=64 q)
-//     dQ_g = dS^_g K^_g   (A from smem, K=64 keys)  g = key block; for d = 128 formed as
-//            dQ_g^T = K^_g^T dS^_g^T (M = d) so that the dQ atomics are coalesced
-// The MMA order per chunk is dK, dV, then the next chunk's S^T and dP^T (their regions' codes
-// are consumed by then: the tensor pipe runs in issue order), then dQ: the score warpgroup starts
-// on the next chunk while the dQ products are added to global memory.
+// (two 64-key quantisation blocks) of one head and walks the head's 64-row query blocks, one
+// quantisation block of queries per step.  Keys are TMEM lanes throughout:
+//   S^T  = K^ Q^T   (M=128 keys, N=64 q, K=d)   } into score buffer b = step % 2, TMEM columns
+//   dP^T = V dO^T   (M=128 keys, N=64 q, K=d)   } [128b, 128b+64) and [128b+64, 128b+128)
+//   dK   = dS^T Q^  (M=128 keys, N=d, K=64 q; A = dS^ codes in shared memory)  -> R_B
+//   dV   = P^T dO^  (M=128 keys, N=d, K=64 q; A = P codes in TMEM over S^T)   -> R_A
+//   dQ   d = 128: dQ_g^T = K^_g^T dS^_g^T (M=d, N=64 q, K=64 keys of block g) -> R_A + 64 g,
+//          once the dV warpgroup has read the dV product out of R_A;  d = 64: dQ_g = dS^_g K^_g
+//          for two query blocks at once (M=128 q, N=d) into R_Q.
+// With two score buffers the tensor core computes the next block's S^T and dP^T while the score
+// warpgroup turns the current block into codes, so the two overlap; a score buffer is free again
+// as soon as the dV MMA has read the P codes (the tensor pipe runs in issue order).
+// Shared-memory bandwidth (128 B per clock per SM) is the bound to respect: the N = 64 MMAs read
+// their A operand once per 64 queries, so nothing else goes through shared memory that need not
+// (no dQ staging: dQ is reduced into global memory straight from registers).
 // Warp roles (16 warps in four warpgroups):
-//   warps 0-3   "score": thread = key; P = 2^(acc c - L2), dS = P o (dP - D) in place in TMEM,
-//               per 64x64 tile max reductions, P and dS codes back into TMEM (A operands) and dS
-//               codes into shared memory (A operand of dQ).  It holds no accumulator, so its
-//               registers go to instruction-level parallelism over 16 columns at a time.
-//   warps 4-7   "dV": dV rows in registers (thread = key); it also adds the two dQ products of
-//               each chunk to global dQ: d = 128 stages their scaled sum in shared memory and
-//               adds it with TMA bulk reductions (32 KB row blocks); d = 64 uses vector float32
-//               atomics along each query row.
-//   warps 8-11  "dK": dK rows in registers (thread = key).
-//   warp 8     TMA producer (tiles, and L2 / D rows by bulk copy); warp 9 TMEM allocation and the
-//              single MMA-issuing thread.
+//   warps 0-3   "score": thread = key; pass 1 reads S^T and dP^T and forms the two 64x64 tile
+//               maxima (P and dS) of its key block; pass 2 reads them again, recomputes P and dS
+//               bit for bit, writes P codes into TMEM (A operand of dV) and dS codes into shared
+//               memory (A operand of dK, B operand of dQ).  Recomputing costs less than writing P
+//               to TMEM and reading it back: TMEM traffic competes with the MMAs' accumulators.
+//   warps 4-7   "dV": dV rows in registers (thread = key), scaled per product; for d = 128 it also
+//               adds query rows 0-31 of each dQ product pair to global dQ (float32 reductions, a
+//               warp covering 32 consecutive d of one row), for d = 64 all of dQ by vector
+//               float32 reductions along each row.
+//   warps 8-11  "dK": dK rows in registers; for d = 128 also dQ query rows 32-63.
+//   warp 12     TMA producer: K and V once, then Q^ (3 stages), dO (2 stages), L2 / D rows (3).
+//   warp 13     TMEM allocation and the single MMA-issuing thread.
+//   warp 14     TMA producer of the dO^ codes (one stage).
 //
 // Numerics (the CPU oracle mirrors these float32 steps):
 //   c = fl32(fl32(sQ sK) * fl32(log2(e)/sqrt(d)));  L2 = fl32(L * fl32(log2(e)))
@@ -50,37 +55,50 @@ __device__ unsigned int g_bwd_err;
 namespace bwd {
 
 // Four warpgroups, launched at 128 registers a thread (512 x 128 = 65536).  setmaxnreg then gives
-// score 152, dV 168, dK 152 and control 40: 128 x (152 + 168 + 152 + 40) = 65536.
+// score 112, dV 184, dK 184 and control 32: 128 x (112 + 184 + 184 + 32) = 65536.
 constexpr int kThreads = 512;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr uint32_t kRegsScore = 152;
-constexpr uint32_t kRegsDV = 168;
-constexpr uint32_t kRegsDK = 152;
-constexpr uint32_t kRegsControl = 40;
-constexpr uint32_t R_S = 0, R_DP = 128, R_A = 256, R_B = 384;
+constexpr int kProducer2Warp = 14;
+constexpr uint32_t kRegsScore = 112;
+constexpr uint32_t kRegsDV = 184;
+constexpr uint32_t kRegsDK = 184;
+constexpr uint32_t kRegsControl = 32;
+constexpr uint32_t kRegsLaunch = 65536 / kThreads;
+static_assert(128 * (kRegsScore + kRegsDV + kRegsDK + kRegsControl) <= 65536, "register split");
+
+// Move this warpgroup from the launch register count to R: setmaxnreg.inc may only raise the
+// count and setmaxnreg.dec only lower it.
+template <uint32_t R>
+__device__ __forceinline__ void regs_to() {
+    if constexpr (R > kRegsLaunch) regs_inc<R>();
+    else if constexpr (R < kRegsLaunch) regs_dec<R>();
+}
+constexpr uint32_t R_A = 256;                         // dV product (d columns); d = 128: dQ^T
+constexpr uint32_t R_Q = 384;                         // d = 64: the two dQ products
+constexpr int kScaleSlots = 8;                        // tile scales kept for 8 steps
 constexpr float kTileZero = 7.52316384526264e-37f;   // 2^-120
 
 template <int D>
 struct Smem {
-    alignas(1024) uint8_t kt[D / 64][128 * 128];    // K^ tile   [chunk of 64 d][key][128 B]
-    alignas(1024) uint8_t vt[D / 64][128 * 128];    // V tile    (16-bit input type)
-    alignas(1024) uint8_t qc[D / 64][128 * 128];    // Q^ chunk  [chunk][q row][128 B]
-    alignas(1024) uint8_t doc[D / 64][128 * 128];   // dO chunk  (16-bit input type)
-    alignas(1024) uint8_t dohc[D / 64][128 * 128];  // dO^ chunk (codes)
-    alignas(1024) uint8_t dss[2][128 * 128];        // dS^ as MN-major A: [q block][key][64 q]
-    alignas(16) float L2s[2][128];                  // [chunk parity][q]: fl32(L log2 e)
-    alignas(16) float Ds[2][128];                   // [chunk parity][q]: D
-    float red[4][2][4];                             // [warp][chunk parity][4 maxima]
-    float sds[2][2][2];                             // [chunk parity][kb][qb] dS tile scales
-    float sps[2][2][2];                             // [chunk parity][kb][qb] P tile scales
-    float colsum[2][128];                           // [qb][key] column sums of dS (Q-smoothing)
-    uint64_t kv_full, q_full, q_free, do_full, do_free, doh_full, doh_free, meta_full[2];
-    uint64_t s_full, dp_full, codes_ready, dss_free;
-    // the two product slots R_A, R_B: "full" per consumer (the dK warpgroup takes dK, the dV
-    // warpgroup dV and dQ), so that every waiter sees every phase of its barrier; "free" is shared
-    // (the MMA thread waits for each use in turn)
-    uint64_t a_full_k, a_full_v, a_free, b_full_k, b_full_v, b_free;
+    alignas(1024) uint8_t kt[D / 64][128 * 128];       // K^ tile  [64-d chunk][key][128 B]
+    alignas(1024) uint8_t vt[D / 64][128 * 128];       // V tile   (16-bit input type)
+    alignas(1024) uint8_t qc[3][D / 64][64 * 128];     // Q^ blocks [stage][chunk][q][128 B]
+    alignas(1024) uint8_t doc[2][D / 64][64 * 128];    // dO blocks (16-bit input type)
+    alignas(1024) uint8_t dohc[D / 64][64 * 128];      // dO^ codes block
+    alignas(1024) uint8_t dss[2][128 * 128];           // dS^ codes [step % 2][key][64 q], 128-byte rows
+    alignas(16) float L2s[3][64];                      // [stage][q]: fl32(L log2 e)
+    alignas(16) float Ds[3][64];                       // [stage][q]: D
+    float red[4][2][2];                                // [warp][step parity][P max, |dS| max]
+    float sps[kScaleSlots][2];                         // [step % 8][key block] P tile scales
+    float sds[kScaleSlots][2];                         // [step % 8][key block] dS tile scales
+    float colsum[4][128];                              // [step % 4][key] column sums of dS
+    uint64_t kv_full, q_full[3], q_free[3], do_full[2], do_free[2], doh_full, doh_free;
+    uint64_t meta_full[3], meta_free[3], sd_full[2], codes_ready[2];
+    uint64_t a_full, a_free, b_full, b_free;           // dV product in R_A, dK product in R_B
+    uint64_t aq_full, aq_free;                         // d = 128: dQ^T products in R_A
+    uint64_t rq_full, rq_free;                         // d = 64: dQ products in R_Q
+    uint64_t dss_free;                                 // d = 64: the dQ MMAs are done with both dS^ tiles
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -104,18 +122,9 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
-// TMA bulk reduction: global[dst .. dst+bytes) += shared[src ..] (float32 add), bulk-group tracked
-__device__ __forceinline__ void bulk_reduce_add_f32(float *dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(dst)),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
+__device__ __forceinline__ void red_add(float *addr, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
@@ -145,6 +154,611 @@ __device__ __forceinline__ int16_t code_hi(uint32_t w) {
     return static_cast<int16_t>(__half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
 }
 
+// Row data of 8 query columns (L2 = fl32(L log2 e) and D), loaded ahead of use: the MMAs read
+// their operands from shared memory at a high rate, so a shared-memory load waited for at once
+// would stall the score warps.
+struct RowData8 {
+    float l2[8], dd[8];
+    __device__ __forceinline__ void load(const float *L2s, const float *Ds, int col0) {
+        *reinterpret_cast<float4 *>(&l2[0]) = *reinterpret_cast<const float4 *>(&L2s[col0]);
+        *reinterpret_cast<float4 *>(&l2[4]) = *reinterpret_cast<const float4 *>(&L2s[col0 + 4]);
+        *reinterpret_cast<float4 *>(&dd[0]) = *reinterpret_cast<const float4 *>(&Ds[col0]);
+        *reinterpret_cast<float4 *>(&dd[4]) = *reinterpret_cast<const float4 *>(&Ds[col0 + 4]);
+    }
+};
+
+// P and dS of 8 query columns [col0, col0 + 8) from S^T and dP^T: P = ex2(acc c - L2) (masked to
+// 0 where EDGE says the pair is not live), dS = P (dP - D).  Pass 1 and pass 2 both call this, so
+// the two passes see bit-identical values.
+template <bool EDGE, bool BIAS>
+__device__ __forceinline__ void score_p_ds_8(const uint32_t (&sr)[8], const uint32_t (&dr)[8],
+                                             const RowData8 &rd, int col0, float cq, float bias,
+                                             int qlo, bool key_ok, float (&pv)[8], float (&ds)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float acc = __uint_as_float(sr[k]);
+        float x;
+        if (BIAS) x = __fsub_rn(__fmaf_rn(acc, cq, bias), rd.l2[k]);
+        else x = __fmaf_rn(acc, cq, -rd.l2[k]);
+        if (EDGE) x = (key_ok && col0 + k >= qlo) ? x : -INFINITY;   // ex2(-inf) = +0: P = 0, dS = +-0
+        pv[k] = ex2_approx(x);
+        ds[k] = __fmul_rn(pv[k], __fsub_rn(__uint_as_float(dr[k]), rd.dd[k]));
+    }
+}
+
+// Walk the 64 query columns of a block in 8-column halves with the TMEM loads and the row data of
+// the next half in flight while one half is computed.  The loop is kept rolled (two halves a
+// trip): the four warp roles run different code on each SM sub-partition, and unrolled bodies
+// overflow the instruction cache.
+template <typename F>
+__device__ __forceinline__ void score_walk(uint32_t s_col, uint32_t dp_col, const float *L2s,
+                                           const float *Ds, F &&half) {
+    uint32_t sA[8], dA[8], sB[8], dB[8];
+    RowData8 rA, rB;
+    tmem_ld8(s_col, sA);
+    tmem_ld8(dp_col, dA);
+    rA.load(L2s, Ds, 0);
+#pragma unroll 1
+    for (int col0 = 0; col0 < 64; col0 += 16) {
+        tmem_wait_ld_regs(sA, dA);
+        tmem_ld8(s_col + col0 + 8, sB);
+        tmem_ld8(dp_col + col0 + 8, dB);
+        rB.load(L2s, Ds, col0 + 8);
+        half(sA, dA, rA, col0);
+        tmem_wait_ld_regs(sB, dB);
+        if (col0 + 16 < 64) {
+            tmem_ld8(s_col + col0 + 16, sA);
+            tmem_ld8(dp_col + col0 + 16, dA);
+            rA.load(L2s, Ds, col0 + 16);
+        }
+        half(sB, dB, rB, col0 + 8);
+    }
+}
+
+// Pass 1 over the 64 query columns of a block: tile maxima of P and |dS| and the dS column sum.
+template <bool EDGE, bool BIAS, bool DUMP>
+__device__ __forceinline__ void score_pass1(uint32_t s_col, uint32_t dp_col, const float *L2s,
+                                            const float *Ds, float cq, float bias, int qlo,
+                                            bool key_ok, float &mp, float &md, float &cs,
+                                            int32_t *dump_col0, int N) {
+    score_walk(s_col, dp_col, L2s, Ds, [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8 &rd, int col0) {
+        float pv[8], ds[8];
+        score_p_ds_8<EDGE, BIAS>(sr, dr, rd, col0, cq, bias, qlo, key_ok, pv, ds);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            mp = fmaxf(mp, pv[k]);
+            md = fmaxf(md, fabsf(ds[k]));
+            if (BIAS) cs += ds[k];
+            if (DUMP && key_ok && (!EDGE || col0 + k >= qlo))
+                dump_col0[static_cast<size_t>(col0 + k) * N] = static_cast<int32_t>(__uint_as_float(sr[k]));
+        }
+    });
+}
+
+// Pass 2: P and dS recomputed from a second read of S^T and dP^T, P codes -> TMEM over S^T
+// columns already read (4 packed columns at col0 / 2), dS codes -> this key's 128-byte row of the
+// shared dS^ tile (16-byte chunk j stored at j ^ (key % 8), the 128-byte swizzle the MMA
+// descriptors expect).
+template <bool EDGE, bool BIAS, bool DUMP>
+__device__ __forceinline__ void score_pass2(uint32_t s_col, uint32_t dp_col, const float *L2s,
+                                            const float *Ds, float cq, float bias, int qlo,
+                                            bool key_ok, float ip, float id, uint8_t *dss_row,
+                                            int swz, int16_t *dump_p0, int16_t *dump_ds0, int N) {
+    score_walk(s_col, dp_col, L2s, Ds, [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8 &rd, int col0) {
+        float pv[8], ds[8];
+        score_p_ds_8<EDGE, BIAS>(sr, dr, rd, col0, cq, bias, qlo, key_ok, pv, ds);
+        uint32_t pk[4], dk[4];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            pk[k / 2] = codes2(pv[k], pv[k + 1], ip);
+            dk[k / 2] = codes2(ds[k], ds[k + 1], id);
+            if (DUMP && key_ok) {
+                dump_p0[static_cast<size_t>(col0 + k) * N] = code_lo(pk[k / 2]);
+                dump_p0[static_cast<size_t>(col0 + k + 1) * N] = code_hi(pk[k / 2]);
+                dump_ds0[static_cast<size_t>(col0 + k) * N] = code_lo(dk[k / 2]);
+                dump_ds0[static_cast<size_t>(col0 + k + 1) * N] = code_hi(dk[k / 2]);
+            }
+        }
+        tmem_st4(s_col + col0 / 2, pk);
+        *reinterpret_cast<uint4 *>(dss_row + (((col0 >> 3) ^ swz) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+    });
+}
+
+// d = 128: this warpgroup's 32 query rows [32 half, 32 half + 32) of the step's two transposed dQ
+// products in R_A (thread = d column, TMEM columns = query rows): the scaled sum is added to
+// global dQ by float32 reductions, one row at a time, so a warp's 32 lanes cover 32 consecutive
+// floats of the row.  R_A is released once read.
+__device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, float sg0, float sg1,
+                                               int tq, float *dq_rows, uint64_t *aq_free) {
+    float *dst = dq_rows + (32 * half) * 128 + tq;
+#pragma unroll 1
+    for (int r0 = 0; r0 < 32; r0 += 8) {
+        uint32_t v0[8], v1[8];
+        tmem_ld8(lane_base + R_A + 32 * half + r0, v0);
+        tmem_ld8(lane_base + R_A + 64 + 32 * half + r0, v1);
+        tmem_wait_ld_regs(v0, v1);
+        if (r0 + 8 == 32) {
+            // every TMEM read of this warpgroup is done: R_A may be refilled
+            tc_fence_before();
+            __syncwarp();
+            if (lane_id() == 0) mbar_arrive(aq_free);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            red_add(dst + (r0 + k) * 128, __fmaf_rn(sg1, __uint_as_float(v1[k]), __fmul_rn(sg0, __uint_as_float(v0[k]))));
+    }
+}
+
+template <int D, bool BF16, bool BIAS, bool DUMP>
+__device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const CUtensorMap *mapK, const CUtensorMap *mapV,
+                                      const CUtensorMap *mapQ, const CUtensorMap *mapdO,
+                                      const CUtensorMap *mapdOh) {
+    const int warp = threadIdx.x >> 5;
+    const int N = a.N;
+    const int bh = blockIdx.y;
+    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const int k0 = 128 * jt;
+    const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
+    const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
+    const int n = nblk - c_first;                    // query blocks walked (>= 1)
+    const size_t bhN = static_cast<size_t>(bh) * N;
+    const uint32_t tmem = s.tmem_base;
+    volatile int *abort_flag = &s.abort_flag;
+    (void)warp; (void)k0; (void)bhN; (void)tmem;
+    constexpr uint32_t kKVBytes = (D / 64) * 128 * 128;
+    constexpr uint32_t kBlkBytes = (D / 64) * 64 * 128;
+    constexpr uint32_t R_B = R_A + D;
+    regs_to<kRegsControl>();
+    if (warp == kProducerWarp) {
+        // -------------------------------------------------------------- TMA producer
+        if (elect_one()) {
+            tma_prefetch_desc(mapK);
+            tma_prefetch_desc(mapV);
+            tma_prefetch_desc(mapQ);
+            tma_prefetch_desc(mapdO);
+            mbar_arrive_expect_tx(&s.kv_full, 2 * kKVBytes);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_3d(s.kt[c], mapK, &s.kv_full, 64 * c, k0, bh);
+                tma_load_3d(s.vt[c], mapV, &s.kv_full, 64 * c, k0, bh);
+            }
+            int last_do[2] = {-1, -1}, last_q[3] = {-1, -1, -1}, last_meta[3] = {-1, -1, -1};
+            for (int c = 0; c < n; ++c) {
+                const int q0 = 64 * (c_first + c);
+                const int s2 = c & 1, s3 = c % 3;
+                if (c >= 2 && !mbar_wait(&s.do_free[s2], ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 1)) break;
+                mbar_arrive_expect_tx(&s.do_full[s2], kBlkBytes);
+                for (int dc = 0; dc < D / 64; ++dc) tma_load_3d(s.doc[s2][dc], mapdO, &s.do_full[s2], 64 * dc, q0, bh);
+                last_do[s2] = c;
+                if (c >= 3 && !mbar_wait(&s.meta_free[s3], (c / 3 - 1) & 1, abort_flag, &g_bwd_err, 2)) break;
+                mbar_arrive_expect_tx(&s.meta_full[s3], 2 * 64 * 4);
+                bulk_load(s.L2s[s3], a.L2 + bhN + q0, 64 * 4, &s.meta_full[s3]);
+                bulk_load(s.Ds[s3], a.D + bhN + q0, 64 * 4, &s.meta_full[s3]);
+                last_meta[s3] = c;
+                if (c >= 3 && !mbar_wait(&s.q_free[s3], (c / 3 - 1) & 1, abort_flag, &g_bwd_err, 3)) break;
+                mbar_arrive_expect_tx(&s.q_full[s3], kBlkBytes);
+                for (int dc = 0; dc < D / 64; ++dc) tma_load_3d(s.qc[s3][dc], mapQ, &s.q_full[s3], 64 * dc, q0, bh);
+                last_q[s3] = c;
+            }
+            // drain: every copy issued into this CTA's shared memory has landed
+            mbar_wait_drain(&s.kv_full, 0, &g_bwd_err, 4);
+            for (int i = 0; i < 2; ++i)
+                if (last_do[i] >= 0) mbar_wait_drain(&s.do_full[i], (last_do[i] >> 1) & 1, &g_bwd_err, 4);
+            for (int i = 0; i < 3; ++i) {
+                if (last_meta[i] >= 0) mbar_wait_drain(&s.meta_full[i], (last_meta[i] / 3) & 1, &g_bwd_err, 4);
+                if (last_q[i] >= 0) mbar_wait_drain(&s.q_full[i], (last_q[i] / 3) & 1, &g_bwd_err, 4);
+            }
+        }
+    } else if (warp == kProducer2Warp) {
+        // -------------------------------------------------------------- dO^ producer
+        if (elect_one()) {
+            tma_prefetch_desc(mapdOh);
+            int last = -1;
+            for (int c = 0; c < n; ++c) {
+                if (c >= 1 && !mbar_wait(&s.doh_free, (c - 1) & 1, abort_flag, &g_bwd_err, 5)) break;
+                mbar_arrive_expect_tx(&s.doh_full, kBlkBytes);
+                for (int dc = 0; dc < D / 64; ++dc)
+                    tma_load_3d(s.dohc[dc], mapdOh, &s.doh_full, 64 * dc, 64 * (c_first + c), bh);
+                last = c;
+            }
+            if (last >= 0) mbar_wait_drain(&s.doh_full, last & 1, &g_bwd_err, 4);
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------------- MMA issuer
+        // Steady state per step c: dK(c), dV(c), dQ(c) (d = 128 into R_A once dV(c) has been read
+        // out of it), then S^T / dP^T of step c + 2 into the score buffer step c used.  S^T / dP^T
+        // of step c + 1 are already done, so the score warpgroup moves on at once; dQ(c) goes
+        // first because the score warpgroup's pass 2 of step c + 1 waits for it to release the
+        // dS^ tile.
+        if (elect_one()) {
+            constexpr uint32_t idS = idesc_f16(128, 64, false, false, false);      // S^T
+            constexpr uint32_t idDP = idesc_f16(128, 64, BF16, false, false);      // dP^T
+            constexpr uint32_t idKV = idesc_f16(128, D, false, false, true);       // dK, dV
+            constexpr uint32_t idQ = idesc_f16(128, 64, false, true, true);        // dQ(^T)
+            // base descriptors; a byte offset `off` inside an operand adds off >> 4
+            const uint64_t dKt = sdesc_sw128(smem_u32(s.kt[0]), 16, 1024);         // K-major A
+            const uint64_t dVt = sdesc_sw128(smem_u32(s.vt[0]), 16, 1024);
+            const uint64_t dKmn = sdesc_sw128(smem_u32(s.kt[0]), 16384, 1024);     // K^ as MN-major
+            const uint64_t dDoh = sdesc_sw128(smem_u32(s.dohc[0]), 8192, 1024);    // MN-major B
+            const uint64_t dDssM = sdesc_sw128(smem_u32(s.dss[0]), 16384, 1024);   // MN-major
+            auto issue_sd = [&](int c) -> bool {
+                const int b = c & 1, s3 = c % 3;
+                if (!mbar_wait(&s.q_full[s3], (c / 3) & 1, abort_flag, &g_bwd_err, 6)) return false;
+                tc_fence_after();
+                const uint64_t dQk = sdesc_sw128(smem_u32(s.qc[s3][0]), 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    umma_ss(tmem + 128 * b, dKt + oa, dQk + ob, idS, kk > 0);
+                }
+                if (!mbar_wait(&s.do_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 8)) return false;
+                tc_fence_after();
+                const uint64_t dDo = sdesc_sw128(smem_u32(s.doc[b][0]), 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    umma_ss(tmem + 128 * b + 64, dVt + oa, dDo + ob, idDP, kk > 0);
+                }
+                umma_commit(&s.sd_full[b]);
+                umma_commit(&s.do_free[b]);
+                return true;
+            };
+            bool ok = mbar_wait(&s.kv_full, 0, abort_flag, &g_bwd_err, 9);
+            if (ok) ok = issue_sd(0);
+            if (ok && n > 1) ok = issue_sd(1);
+            for (int c = 0; c < n && ok; ++c) {
+                const int b = c & 1, s3 = c % 3;
+                if (!(ok = mbar_wait(&s.codes_ready[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 10))) break;
+                if (c >= 1 && !(ok = mbar_wait(&s.b_free, (c - 1) & 1, abort_flag, &g_bwd_err, 11))) break;
+                tc_fence_after();
+                // dK = dS^T Q^: A = this step's dS^ codes (K-major rows of 64 q), B = Q^ block
+                // read as MN-major (N = d)
+                {
+                    const uint64_t dA = sdesc_sw128(smem_u32(s.dss[b]), 16, 1024);
+                    const uint64_t dB = sdesc_sw128(smem_u32(s.qc[s3][0]), 8192, 1024);
+#pragma unroll 1
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_ss(tmem + R_B, dA + ((kk * 32) >> 4), dB + ((kk * 2048) >> 4), idKV, kk > 0);
+                }
+                umma_commit(&s.b_full);
+                umma_commit(&s.q_free[s3]);
+                // dV = P^T dO^: A = the P codes in TMEM (8 columns per 16 q)
+                if (!(ok = mbar_wait(&s.doh_full, c & 1, abort_flag, &g_bwd_err, 12))) break;
+                // R_A must be empty: d = 128 the dQ(c - 1) products read out, d = 64 dV(c - 1)
+                if (c >= 1 && !(ok = mbar_wait(D == 128 ? &s.aq_free : &s.a_free, (c - 1) & 1, abort_flag, &g_bwd_err, 13))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_ts(tmem + R_A, tmem + 128 * b + 8 * kk, dDoh + ((kk * 2048) >> 4), idKV, kk > 0);
+                umma_commit(&s.a_full);
+                umma_commit(&s.doh_free);
+                if (D == 128) {
+                    // dQ_g^T = K^_g^T dS^_g^T: A = K^ tile read as MN-major (M = d), B = the dS^
+                    // tile read as MN-major (N = q); product g into R_A + 64 g once the dV
+                    // warpgroup has read dV(c) out of R_A
+                    if (!(ok = mbar_wait(&s.a_free, c & 1, abort_flag, &g_bwd_err, 16))) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int g = 0; g < 2; ++g)
+#pragma unroll 1
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t o = ((64 * g + 16 * kk) * 128) >> 4;
+                            umma_ss(tmem + R_A + 64 * g, dKmn + o, dDssM + ((b * 16384) >> 4) + o, idQ, kk > 0);
+                        }
+                    umma_commit(&s.aq_full);
+                } else if ((c & 1) || c == n - 1) {
+                    // dQ_g = dS^_g K^_g for the step pair (c - 1, c): A = both dS^ tiles as one
+                    // MN-major operand (M = 128 q), B = K^_g as MN-major (N = d)
+                    const int pr = c >> 1;
+                    if (pr >= 1 && !(ok = mbar_wait(&s.rq_free, (pr - 1) & 1, abort_flag, &g_bwd_err, 14))) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int g = 0; g < 2; ++g)
+#pragma unroll 1
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t o = ((64 * g + 16 * kk) * 128) >> 4;
+                            umma_ss(tmem + R_Q + 64 * g, dDssM + o, dKmn + o, idQ, kk > 0);
+                        }
+                    umma_commit(&s.rq_full);
+                    umma_commit(&s.dss_free);
+                }
+                if (c + 2 < n && !(ok = issue_sd(c + 2))) break;
+            }
+            umma_commit(&s.mma_done);
+            mbar_wait_drain(&s.mma_done, 0, &g_bwd_err, 15);
+        }
+    }
+}
+
+// Score warpgroup (warps 0-3).
+template <int D, bool BF16, bool BIAS, bool DUMP>
+__device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
+    const int warp = threadIdx.x >> 5;
+    const int N = a.N;
+    const int bh = blockIdx.y;
+    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const int k0 = 128 * jt;
+    const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
+    const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
+    const int n = nblk - c_first;                    // query blocks walked (>= 1)
+    const size_t bhN = static_cast<size_t>(bh) * N;
+    const uint32_t tmem = s.tmem_base;
+    volatile int *abort_flag = &s.abort_flag;
+    (void)warp; (void)k0; (void)bhN; (void)tmem;
+    regs_to<kRegsScore>();
+    // ------------------------------------------------------------------ score warpgroup
+    const int tq = threadIdx.x;                       // key lane
+    const int quarter = warp;
+    const int key = k0 + tq;
+    const int kb = tq >> 6;
+    const bool key_ok = key < N;
+    const int kblk = min(2 * jt + kb, nblk - 1);
+    const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    const float sk = key_ok ? a.sK[static_cast<size_t>(bh) * nblk + kblk] : 0.0f;
+    const float *sQh = a.sQ + static_cast<size_t>(bh) * nblk;
+    const float *biash = BIAS ? a.qbias + static_cast<size_t>(bh) * nblk * N + min(key, N - 1) : nullptr;
+    float sq_next = sQh[c_first];
+    float b_next = (BIAS && key_ok) ? biash[static_cast<size_t>(c_first) * N] : 0.0f;
+    for (int c = 0; c < n; ++c) {
+        const int qb = c_first + c;
+        const int q0 = 64 * qb;
+        const int b = c & 1, m3 = c % 3, z = c & (kScaleSlots - 1);
+        const float cq = __fmul_rn(__fmul_rn(sq_next, sk), a.sl2);
+        const float bias = b_next;
+        if (c + 1 < n) {
+            sq_next = sQh[qb + 1];
+            if (BIAS && key_ok) b_next = biash[static_cast<size_t>(qb + 1) * N];
+        }
+        const int qlo = a.causal ? max(0, key - q0) : 0;
+        const bool edge = (a.causal && q0 < k0 + 128) || k0 + 128 > N;
+        if (!mbar_wait(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19)) break;
+        if (!mbar_wait(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20)) break;
+        tc_fence_after();
+        const uint32_t s_col = lane_base + 128 * b;
+        float mp = 0.0f, md = 0.0f, cs = 0.0f;
+        int32_t *dump_s0 = DUMP ? a.dump_s + (bhN + q0) * N + key : nullptr;
+        if (edge)
+            score_pass1<true, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                          key_ok, mp, md, cs, dump_s0, N);
+        else
+            score_pass1<false, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                           key_ok, mp, md, cs, dump_s0, N);
+        // tile maxima of (this query block, this key block): over the 32 lanes, then over the
+        // two warps of the key block
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+            md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, o));
+        }
+        if (lane_id() == 0) {
+            s.red[warp][c & 1][0] = mp;
+            s.red[warp][c & 1][1] = md;
+        }
+        if (BIAS) s.colsum[c & 3][tq] = cs;
+        named_bar_sync(1, 128);
+        const int w0 = warp & ~1;
+        const float mxp = fmaxf(s.red[w0][c & 1][0], s.red[w0 + 1][c & 1][0]);
+        const float mxd = fmaxf(s.red[w0][c & 1][1], s.red[w0 + 1][c & 1][1]);
+        const float sp = mxp < kTileZero ? 0.0f : __fdiv_rn(mxp, 127.0f);
+        const float ip = mxp < kTileZero ? 0.0f : __frcp_rn(sp);
+        const float sd = mxd < kTileZero ? 0.0f : __fdiv_rn(mxd, 127.0f);
+        const float id = mxd < kTileZero ? 0.0f : __frcp_rn(sd);
+        if ((tq & 63) == 0) {
+            s.sps[z][kb] = sp;
+            s.sds[z][kb] = sd;
+            if (DUMP && key_ok) {
+                const size_t ti = (static_cast<size_t>(bh) * nblk + qb) * nblk + kblk;
+                a.dump_sp[ti] = sp;
+                a.dump_sds[ti] = sd;
+            }
+        }
+        // the dQ MMAs that read this dS^ tile two steps ago must be done: d = 128 they ran before
+        // this step's S^T / dP^T (the tensor pipe runs in issue order), d = 64 they are those of
+        // the previous step pair
+        if (D != 128 && c >= 2 && !mbar_wait(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
+        int16_t *dump_p0 = DUMP ? a.dump_p + (bhN + q0) * N + key : nullptr;
+        int16_t *dump_ds0 = DUMP ? a.dump_ds + (bhN + q0) * N + key : nullptr;
+        uint8_t *dss_row = s.dss[b] + tq * 128;
+        if (edge)
+            score_pass2<true, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
+                                          ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
+        else
+            score_pass2<false, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
+                                           ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
+        tmem_wait_st();
+        fence_view_async_shared();
+        tc_fence_before();
+        __syncwarp();
+        if (lane_id() == 0) {
+            mbar_arrive(&s.codes_ready[b]);
+            mbar_arrive(&s.meta_free[m3]);
+        }
+    }
+}
+
+// dV warpgroup (warps 4-7).
+template <int D, bool BF16, bool BIAS, bool DUMP>
+__device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
+    const int warp = threadIdx.x >> 5;
+    const int N = a.N;
+    const int bh = blockIdx.y;
+    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const int k0 = 128 * jt;
+    const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
+    const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
+    const int n = nblk - c_first;                    // query blocks walked (>= 1)
+    const size_t bhN = static_cast<size_t>(bh) * N;
+    const uint32_t tmem = s.tmem_base;
+    volatile int *abort_flag = &s.abort_flag;
+    (void)warp; (void)k0; (void)bhN; (void)tmem;
+    regs_to<kRegsDV>();
+    // ------------------------------------------------------------------ dV warpgroup
+    const int tq = threadIdx.x - 128;
+    const int quarter = warp & 3;
+    const int key = k0 + tq;
+    const int kb = tq >> 6;
+    const bool key_ok = key < N;
+    const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    float dv[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) dv[i] = 0.0f;
+    float skb[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+        skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
+    const float *sdOh = a.sdO + static_cast<size_t>(bh) * nblk;
+    float sdo_next = sdOh[c_first];
+    for (int c = 0; c < n; ++c) {
+        const int qb = c_first + c;
+        const int q0 = 64 * qb;
+        const int z = c & (kScaleSlots - 1);
+        const float sdo = sdo_next;
+        if (c + 1 < n) sdo_next = sdOh[qb + 1];
+        // dV += s_P s_dO (P^T dO^)
+        if (!mbar_wait(&s.a_full, c & 1, abort_flag, &g_bwd_err, 23)) break;
+        tc_fence_after();
+        {
+            const float sc = __fmul_rn(s.sps[z][kb], sdo);
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 8) {
+                uint32_t r[8];
+                tmem_ld8(lane_base + R_A + cc, r);
+                tmem_wait_ld_regs(r);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&s.a_free);
+        if (D == 128) {
+            // dQ rows 0-31 of this step: both key blocks' products, each scaled by its own
+            // s_dS s_K / sqrt(d), summed
+            if (!mbar_wait(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 24)) break;
+            tc_fence_after();
+            const float sg0 = __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
+            const float sg1 = __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
+            dq_consume_128(lane_base, 0, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free);
+        } else if ((c & 1) || c == n - 1) {
+            // d = 64, step pair (c - 1, c) (or the last step alone): thread = query row of the
+            // pair, vector atomics along the row
+            const int pr = c >> 1;
+            if (!mbar_wait(&s.rq_full, pr & 1, abort_flag, &g_bwd_err, 25)) break;
+            tc_fence_after();
+            const int zq = (2 * pr + (tq >> 6)) & (kScaleSlots - 1);
+            const int qrow = 64 * (c_first + 2 * pr) + tq;
+            const float s0 = __fmul_rn(__fmul_rn(s.sds[zq][0], skb[0]), a.inv_sqrt_d);
+            const float s1 = __fmul_rn(__fmul_rn(s.sds[zq][1], skb[1]), a.inv_sqrt_d);
+            const bool live = qrow < N && 2 * pr + (tq >> 6) < n;
+            float *dst = a.dQ + (bhN + min(qrow, N - 1)) * D;
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 8) {
+                uint32_t r0[8], r1[8];
+                tmem_ld8(lane_base + R_Q + cc, r0);
+                tmem_ld8(lane_base + R_Q + 64 + cc, r1);
+                tmem_wait_ld_regs(r0, r1);
+                if (live) {
+#pragma unroll
+                    for (int k = 0; k < 8; k += 4) {
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            v[e] = __fmaf_rn(s1, __uint_as_float(r1[k + e]), __fmul_rn(s0, __uint_as_float(r0[k + e])));
+                        red_add_v4(dst + cc + k, v[0], v[1], v[2], v[3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane_id() == 0) mbar_arrive(&s.rq_free);
+        }
+    }
+    if (key_ok && !*abort_flag) {
+        float *dst = a.dV + (bhN + key) * D;
+#pragma unroll
+        for (int i = 0; i < D; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(dv[i], dv[i + 1], dv[i + 2], dv[i + 3]);
+    }
+}
+
+// dK warpgroup (warps 8-11).
+template <int D, bool BF16, bool BIAS, bool DUMP>
+__device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
+    const int warp = threadIdx.x >> 5;
+    const int N = a.N;
+    const int bh = blockIdx.y;
+    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const int k0 = 128 * jt;
+    const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
+    const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
+    const int n = nblk - c_first;                    // query blocks walked (>= 1)
+    const size_t bhN = static_cast<size_t>(bh) * N;
+    const uint32_t tmem = s.tmem_base;
+    volatile int *abort_flag = &s.abort_flag;
+    (void)warp; (void)k0; (void)bhN; (void)tmem;
+    constexpr uint32_t R_B = R_A + D;
+    regs_to<kRegsDK>();
+    // ------------------------------------------------------------------ dK warpgroup
+    const int tq = threadIdx.x - 256;                 // key lane
+    const int quarter = warp & 3;
+    const int key = k0 + tq;
+    const int kb = tq >> 6;
+    const bool key_ok = key < N;
+    const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    float dk[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) dk[i] = 0.0f;
+    float skb[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+        skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
+    const float *sQh = a.sQ + static_cast<size_t>(bh) * nblk;
+    float sq_next = sQh[c_first];
+    for (int c = 0; c < n; ++c) {
+        const int qb = c_first + c;
+        const int q0 = 64 * qb;
+        const int z = c & (kScaleSlots - 1);
+        const float sq = sq_next;
+        if (c + 1 < n) sq_next = sQh[qb + 1];
+        // dK += s_dS s_Q / sqrt(d) (dS^T Q^)   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d))
+        if (!mbar_wait(&s.b_full, c & 1, abort_flag, &g_bwd_err, 30)) break;
+        tc_fence_after();
+        {
+            const float sc = __fmul_rn(__fmul_rn(s.sds[z][kb], sq), a.inv_sqrt_d);
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 8) {
+                uint32_t r[8];
+                tmem_ld8(lane_base + R_B + cc, r);
+                tmem_wait_ld_regs(r);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
+            }
+        }
+        if (BIAS) {
+            const float w = __fmul_rn(s.colsum[c & 3][tq], a.inv_sqrt_d);
+            const float *mu = a.muQ + (static_cast<size_t>(bh) * nblk + qb) * D;
+#pragma unroll
+            for (int i = 0; i < D; ++i) dk[i] = __fmaf_rn(w, mu[i], dk[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&s.b_free);
+        if (D == 128) {
+            // dQ rows 32-63 of this step
+            if (!mbar_wait(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 31)) break;
+            tc_fence_after();
+            const float sg0 = __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
+            const float sg1 = __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
+            dq_consume_128(lane_base, 1, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free);
+        }
+    }
+    if (key_ok && !*abort_flag) {
+        float *dst = a.dK + (bhN + key) * D;
+#pragma unroll
+        for (int i = 0; i < D; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(dk[i], dk[i + 1], dk[i + 2], dk[i + 3]);
+    }
+}
+
 template <int D, bool BF16, bool BIAS, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -154,16 +768,6 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
-    const int N = a.N;
-    const int bh = blockIdx.y;
-    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
-    const int k0 = 128 * jt;
-    const int nchunks = (N + 127) / 128;
-    const int c_first = a.causal ? jt : 0;           // query chunks [c_first, nchunks)
-    const int nmine = nchunks - c_first;
-    const int nblk = N >> 6;
-    const size_t bhN = static_cast<size_t>(bh) * N;
-    constexpr uint32_t kTileBytes = (D / 64) * 128 * 128;
 
     if (warp == kMmaWarp) {
         tmem_alloc(&s.tmem_base, 512);
@@ -171,579 +775,42 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     }
     if (threadIdx.x == 0) {
         s.abort_flag = 0;
-        uint64_t *one[] = {&s.kv_full, &s.q_full, &s.q_free, &s.do_full, &s.do_free, &s.doh_full,
-                           &s.doh_free, &s.meta_full[0], &s.meta_full[1], &s.s_full, &s.dp_full,
-                           &s.dss_free, &s.a_full_k, &s.a_full_v, &s.b_full_k, &s.b_full_v,
+        uint64_t *one[] = {&s.kv_full, &s.q_full[0], &s.q_full[1], &s.q_full[2], &s.q_free[0],
+                           &s.q_free[1], &s.q_free[2], &s.do_full[0], &s.do_full[1], &s.do_free[0],
+                           &s.do_free[1], &s.doh_full, &s.doh_free, &s.meta_full[0],
+                           &s.meta_full[1], &s.meta_full[2], &s.sd_full[0], &s.sd_full[1],
+                           &s.a_full, &s.b_full, &s.aq_full, &s.rq_full, &s.dss_free,
                            &s.mma_done};
         for (uint64_t *b : one) mbar_init(b, 1);
-        mbar_init(&s.codes_ready, 4);
-        mbar_init(&s.a_free, 4);
-        mbar_init(&s.b_free, 4);
+        uint64_t *four[] = {&s.meta_free[0], &s.meta_free[1], &s.meta_free[2], &s.codes_ready[0],
+                            &s.codes_ready[1], &s.a_free, &s.b_free, &s.rq_free};
+        for (uint64_t *b : four) mbar_init(b, 4);
+        mbar_init(&s.aq_free, 8);                    // both dQ-consuming warpgroups
         fence_barrier_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = s.tmem_base;
-    volatile int *abort_flag = &s.abort_flag;
-
+    // each role computes its own CTA geometry: a value computed here and used by several roles
+    // would have to sit in the same register in all of them, the 24-register control one included
     if (warp >= 12) {
-        regs_dec<kRegsControl>();
-        if (warp == kProducerWarp) {
-            // -------------------------------------------------------------- TMA producer
-            if (elect_one()) {
-                tma_prefetch_desc(&mapK);
-                tma_prefetch_desc(&mapV);
-                tma_prefetch_desc(&mapQ);
-                tma_prefetch_desc(&mapdO);
-                tma_prefetch_desc(&mapdOh);
-                mbar_arrive_expect_tx(&s.kv_full, 2 * kTileBytes);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_3d(s.kt[c], &mapK, &s.kv_full, 64 * c, k0, bh);
-                    tma_load_3d(s.vt[c], &mapV, &s.kv_full, 64 * c, k0, bh);
-                }
-                int nq = 0, ndo = 0, ndoh = 0, nmeta[2] = {0, 0};
-                for (int it = 0; it < nmine; ++it) {
-                    const int q0 = 128 * (c_first + it);
-                    const uint32_t rows = static_cast<uint32_t>(min(128, N - q0));
-                    const int slot = it & 1;
-                    if (it > 0 && !mbar_wait(&s.do_free, (it - 1) & 1, abort_flag, &g_bwd_err, 1)) break;
-                    mbar_arrive_expect_tx(&s.do_full, kTileBytes);
-                    for (int c = 0; c < D / 64; ++c) tma_load_3d(s.doc[c], &mapdO, &s.do_full, 64 * c, q0, bh);
-                    ndo = it + 1;
-                    // row data of the chunk: L2 = fl32(L log2 e) and D (written by the prologue)
-                    mbar_arrive_expect_tx(&s.meta_full[slot], 8 * rows);
-                    bulk_load(s.L2s[slot], a.L2 + bhN + q0, 4 * rows, &s.meta_full[slot]);
-                    bulk_load(s.Ds[slot], a.D + bhN + q0, 4 * rows, &s.meta_full[slot]);
-                    ++nmeta[slot];
-                    if (it > 0 && !mbar_wait(&s.q_free, (it - 1) & 1, abort_flag, &g_bwd_err, 2)) break;
-                    mbar_arrive_expect_tx(&s.q_full, kTileBytes);
-                    for (int c = 0; c < D / 64; ++c) tma_load_3d(s.qc[c], &mapQ, &s.q_full, 64 * c, q0, bh);
-                    nq = it + 1;
-                    if (it > 0 && !mbar_wait(&s.doh_free, (it - 1) & 1, abort_flag, &g_bwd_err, 3)) break;
-                    mbar_arrive_expect_tx(&s.doh_full, kTileBytes);
-                    for (int c = 0; c < D / 64; ++c) tma_load_3d(s.dohc[c], &mapdOh, &s.doh_full, 64 * c, q0, bh);
-                    ndoh = it + 1;
-                }
-                mbar_wait_drain(&s.kv_full, 0, &g_bwd_err, 4);
-                if (ndo > 0) mbar_wait_drain(&s.do_full, (ndo - 1) & 1, &g_bwd_err, 4);
-                for (int sl = 0; sl < 2; ++sl)
-                    if (nmeta[sl] > 0) mbar_wait_drain(&s.meta_full[sl], (nmeta[sl] - 1) & 1, &g_bwd_err, 4);
-                if (nq > 0) mbar_wait_drain(&s.q_full, (nq - 1) & 1, &g_bwd_err, 4);
-                if (ndoh > 0) mbar_wait_drain(&s.doh_full, (ndoh - 1) & 1, &g_bwd_err, 4);
-            }
-        } else if (warp == kMmaWarp) {
-            // -------------------------------------------------------------- MMA issuer
-            // Per chunk: dK_0 -> A, dK_1 -> B (Q^ is then free for the next chunk), dV_0 -> A,
-            // dV_1 -> B, the next chunk's S^T and dP^T, then dQ_0 -> A, dQ_1 -> B.  Each product
-            // slot is refilled only after its consumer warpgroup has read it out.
-            if (elect_one()) {
-                constexpr uint32_t idKK = idesc_f16(128, 128, false, false, false);    // S^T
-                constexpr uint32_t idDP = idesc_f16(128, 128, BF16, false, false);     // dP^T
-                constexpr uint32_t idTS = idesc_f16(128, D, false, false, true);       // dV, dK
-                constexpr uint32_t idQ = D == 128 ? idesc_f16(128, 128, false, true, true)   // dQ^T
-                                                  : idesc_f16(128, D, false, true, true);    // dQ
-                // base descriptors; a byte offset `off` inside an operand adds off >> 4
-                const uint64_t dKt = sdesc_sw128(smem_u32(s.kt[0]), 16, 1024);
-                const uint64_t dVt = sdesc_sw128(smem_u32(s.vt[0]), 16, 1024);
-                const uint64_t dQc = sdesc_sw128(smem_u32(s.qc[0]), 16, 1024);
-                const uint64_t dDo = sdesc_sw128(smem_u32(s.doc[0]), 16, 1024);
-                const uint64_t dDoh = sdesc_sw128(smem_u32(s.dohc[0]), 16384, 1024);
-                const uint64_t dQmn = sdesc_sw128(smem_u32(s.qc[0]), 16384, 1024);
-                const uint64_t dKmn = sdesc_sw128(smem_u32(s.kt[0]), 16384, 1024);
-                const uint64_t dDss = sdesc_sw128(smem_u32(s.dss[0]), 16384, 1024);
-                int ua = 0, ub = 0;                        // products issued into each slot
-                auto issue_s_dp = [&](int it) -> bool {
-                    if (!mbar_wait(&s.q_full, it & 1, abort_flag, &g_bwd_err, 6)) return false;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_ss(tmem + R_S, dKt + o, dQc + o, idKK, kk > 0);
-                    }
-                    umma_commit(&s.s_full);
-                    if (!mbar_wait(&s.do_full, it & 1, abort_flag, &g_bwd_err, 8)) return false;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_ss(tmem + R_DP, dVt + o, dDo + o, idDP, kk > 0);
-                    }
-                    umma_commit(&s.dp_full);
-                    umma_commit(&s.do_free);
-                    return true;
-                };
-                auto slot_ready = [&](bool is_a) -> bool {
-                    const int u = is_a ? ua : ub;
-                    if (u == 0) return true;
-                    if (!mbar_wait(is_a ? &s.a_free : &s.b_free, (u - 1) & 1, abort_flag, &g_bwd_err, is_a ? 12 : 13)) return false;
-                    tc_fence_after();
-                    return true;
-                };
-                bool ok = mbar_wait(&s.kv_full, 0, abort_flag, &g_bwd_err, 5);
-                if (ok && nmine > 0) ok = issue_s_dp(0);
-                for (int it = 0; it < nmine && ok; ++it) {
-                    if (!mbar_wait(&s.codes_ready, it & 1, abort_flag, &g_bwd_err, 10)) break;
-                    tc_fence_after();
-                    // dK_h = dS^T[:, h] Q^_h
-#pragma unroll 1
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        if (!(ok = slot_ready(h == 0))) break;
-                        const uint32_t dst = tmem + (h == 0 ? R_A : R_B);
-#pragma unroll 1
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_ts(dst, tmem + R_DP + 32 * h + 8 * kk, dQmn + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
-                        umma_commit(h == 0 ? &s.a_full_k : &s.b_full_k);
-                        if (h == 0) ++ua; else ++ub;
-                    }
-                    if (!ok) break;
-                    umma_commit(&s.q_free);
-                    if (!mbar_wait(&s.doh_full, it & 1, abort_flag, &g_bwd_err, 11)) break;
-                    // dV_h = P^T[:, h] dO^_h
-#pragma unroll 1
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        if (!(ok = slot_ready(h == 0))) break;
-                        const uint32_t dst = tmem + (h == 0 ? R_A : R_B);
-#pragma unroll 1
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_ts(dst, tmem + R_S + 32 * h + 8 * kk, dDoh + (((64 * h + 16 * kk) * 128) >> 4), idTS, kk > 0);
-                        umma_commit(h == 0 ? &s.a_full_v : &s.b_full_v);
-                        if (h == 0) ++ua; else ++ub;
-                    }
-                    if (!ok) break;
-                    umma_commit(&s.doh_free);
-                    // the next chunk's scores: the tensor pipe runs in issue order, so the codes in
-                    // R_S / R_DP have been read by the dV / dK MMAs above before they are replaced
-                    if (it + 1 < nmine && !(ok = issue_s_dp(it + 1))) break;
-                    // dQ_g = dS^[:, keys of g] K^_g.  For d = 128 it is formed transposed,
-                    // dQ_g^T = K^_g^T dS^_g^T (M = d, N = 128 q): same two shared tiles with the
-                    // operand roles swapped, so that a thread then owns one d column and the
-                    // atomic adds of a warp hit 32 consecutive floats of one query row.
-#pragma unroll 1
-                    for (int g = 0; g < 2 && ok; ++g) {
-                        if (!(ok = slot_ready(g == 0))) break;
-                        const uint32_t dst = tmem + (g == 0 ? R_A : R_B);
-#pragma unroll 1
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t o = ((64 * g + 16 * kk) * 128) >> 4;
-                            if (D == 128) umma_ss(dst, dKmn + o, dDss + o, idQ, kk > 0);
-                            else umma_ss(dst, dDss + o, dKmn + o, idQ, kk > 0);
-                        }
-                        umma_commit(g == 0 ? &s.a_full_v : &s.b_full_v);
-                        if (g == 0) ++ua; else ++ub;
-                    }
-                    // d = 64: the dS^ tile is free once the dQ MMAs have read it; d = 128: the dV
-                    // warpgroup frees it after staging the dQ reduction through it
-                    if (D != 128) umma_commit(&s.dss_free);
-                }
-                umma_commit(&s.mma_done);
-                mbar_wait_drain(&s.mma_done, 0, &g_bwd_err, 14);
-            }
-        }
+        control_role<D, BF16, BIAS, DUMP>(s, a, &mapK, &mapV, &mapQ, &mapdO, &mapdOh);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == kMmaWarp) tmem_dealloc(s.tmem_base, 512);
     } else if (warp < 4) {
-        regs_inc<kRegsScore>();
-        // ------------------------------------------------------------------ score warpgroup
-        const int tq = threadIdx.x;                       // 0..127: key lane
-        const int quarter = warp;
-        const int key = k0 + tq;                          // key index within the head
-        const int kb = tq >> 6;                           // key block of this lane (0/1)
-        const int kblk = min(key, N - 1) >> 6;            // global key block
-        const bool key_ok = key < N;
-        const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
-        const float sk = a.sK[static_cast<size_t>(bh) * nblk + kblk];
-        // per-chunk scalars, fetched one chunk ahead
-        const float *sQh = a.sQ + static_cast<size_t>(bh) * nblk;
-        const float *biash = BIAS ? a.qbias + static_cast<size_t>(bh) * nblk * N + min(key, N - 1) : nullptr;
-        float sq0 = 0.0f, sq1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
-        if (nmine > 0) {
-            sq0 = sQh[min(2 * c_first, nblk - 1)];
-            sq1 = sQh[min(2 * c_first + 1, nblk - 1)];
-            if (BIAS && key_ok) {
-                b0 = biash[static_cast<size_t>(min(2 * c_first, nblk - 1)) * N];
-                b1 = biash[static_cast<size_t>(min(2 * c_first + 1, nblk - 1)) * N];
-            }
-        }
-        for (int it = 0; it < nmine; ++it) {
-            const uint32_t ph = it & 1;
-            const int slot = it & 1;
-            const int ic = c_first + it;
-            const int q0 = 128 * ic;
-            float nsq0 = 0.0f, nsq1 = 0.0f, nb0 = 0.0f, nb1 = 0.0f;
-            if (it + 1 < nmine) {
-                nsq0 = sQh[min(2 * ic + 2, nblk - 1)];
-                nsq1 = sQh[min(2 * ic + 3, nblk - 1)];
-                if (BIAS && key_ok) {
-                    nb0 = biash[static_cast<size_t>(min(2 * ic + 2, nblk - 1)) * N];
-                    nb1 = biash[static_cast<size_t>(min(2 * ic + 3, nblk - 1)) * N];
-                }
-            }
-            const float cq[2] = {__fmul_rn(__fmul_rn(sq0, sk), a.sl2), __fmul_rn(__fmul_rn(sq1, sk), a.sl2)};
-            const float biasv[2] = {b0, b1};
-            // valid query columns for this key: [qlo, qhi) relative to q0
-            const int qhi = min(128, N - q0);
-            const int qlo = a.causal ? max(0, key - q0) : 0;
-            const bool edge = (a.causal && ic == jt) || q0 + 128 > N || k0 + 128 > N;
-            if (!mbar_wait(&s.meta_full[slot], (it >> 1) & 1, abort_flag, &g_bwd_err, 19)) break;
-            if (!mbar_wait(&s.s_full, ph, abort_flag, &g_bwd_err, 20)) break;
-            if (!mbar_wait(&s.dp_full, ph, abort_flag, &g_bwd_err, 21)) break;
-            tc_fence_after();
-            // pass 1: P and dS in place, tile maxima, column sums of dS
-            float mp[2] = {0.0f, 0.0f}, md[2] = {0.0f, 0.0f}, cs[2] = {0.0f, 0.0f};
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll 1
-            for (int cc = 64 * h; cc < 64 * h + 64; cc += 8) {
-                uint32_t sr[8], dr[8];
-                tmem_ld8(lane_base + R_S + cc, sr);
-                tmem_ld8(lane_base + R_DP + cc, dr);
-                float l2v[8], dvv[8];
-#pragma unroll
-                for (int k = 0; k < 8; k += 4) {
-                    *reinterpret_cast<float4 *>(&l2v[k]) = *reinterpret_cast<const float4 *>(&s.L2s[slot][cc + k]);
-                    *reinterpret_cast<float4 *>(&dvv[k]) = *reinterpret_cast<const float4 *>(&s.Ds[slot][cc + k]);
-                }
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int col = cc + k;
-                    const float acc = __uint_as_float(sr[k]);
-                    float x;
-                    if (BIAS) x = __fsub_rn(__fmaf_rn(acc, cq[h], biasv[h]), l2v[k]);
-                    else x = __fmaf_rn(acc, cq[h], -l2v[k]);
-                    float p = ex2_approx(x);
-                    float ds = __fmul_rn(p, __fsub_rn(__uint_as_float(dr[k]), dvv[k]));
-                    if (edge) {
-                        const bool ok = key_ok && col >= qlo && col < qhi;
-                        p = ok ? p : 0.0f;
-                        ds = ok ? ds : 0.0f;
-                        if (DUMP) {
-                            if (ok) a.dump_s[(bhN + q0 + col) * N + key] = static_cast<int32_t>(acc);
-                        }
-                    } else if (DUMP) {
-                        a.dump_s[(bhN + q0 + col) * N + key] = static_cast<int32_t>(acc);
-                    }
-                    mp[h] = fmaxf(mp[h], p);
-                    md[h] = fmaxf(md[h], fabsf(ds));
-                    if (BIAS) cs[h] += ds;
-                    sr[k] = __float_as_uint(p);
-                    dr[k] = __float_as_uint(ds);
-                }
-                tmem_st8(lane_base + R_S + cc, sr);
-                tmem_st8(lane_base + R_DP + cc, dr);
-            }
-            tmem_wait_st();
-            // per 64x64 tile maxima: over the 32 lanes, then over the two warps of this key block
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    mp[h] = fmaxf(mp[h], __shfl_xor_sync(0xffffffffu, mp[h], o));
-                    md[h] = fmaxf(md[h], __shfl_xor_sync(0xffffffffu, md[h], o));
-                }
-            }
-            if (lane_id() == 0) {
-                s.red[warp][slot][0] = mp[0];
-                s.red[warp][slot][1] = mp[1];
-                s.red[warp][slot][2] = md[0];
-                s.red[warp][slot][3] = md[1];
-            }
-            if (BIAS) {
-                s.colsum[0][tq] = cs[0];
-                s.colsum[1][tq] = cs[1];
-            }
-            named_bar_sync(1, 128);
-            const int w0 = warp & ~1;
-            float sp[2], sd[2], ip[2], id[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float mxp = fmaxf(s.red[w0][slot][h], s.red[w0 + 1][slot][h]);
-                const float mxd = fmaxf(s.red[w0][slot][2 + h], s.red[w0 + 1][slot][2 + h]);
-                sp[h] = mxp < kTileZero ? 0.0f : __fdiv_rn(mxp, 127.0f);
-                ip[h] = mxp < kTileZero ? 0.0f : __frcp_rn(sp[h]);
-                sd[h] = mxd < kTileZero ? 0.0f : __fdiv_rn(mxd, 127.0f);
-                id[h] = mxd < kTileZero ? 0.0f : __frcp_rn(sd[h]);
-            }
-            if ((tq & 63) == 0) {
-                s.sds[slot][kb][0] = sd[0];
-                s.sds[slot][kb][1] = sd[1];
-                s.sps[slot][kb][0] = sp[0];
-                s.sps[slot][kb][1] = sp[1];
-                if (DUMP) {
-                    for (int h = 0; h < 2; ++h) {
-                        if (key_ok && q0 + 64 * h < N) {
-                            const size_t ti = (static_cast<size_t>(bh) * nblk + 2 * ic + h) * nblk + kblk;
-                            a.dump_sp[ti] = sp[h];
-                            a.dump_sds[ti] = sd[h];
-                        }
-                    }
-                }
-            }
-            // the dQ MMAs of the previous chunk must be done with the dS^ shared tile
-            if (it > 0 && !mbar_wait(&s.dss_free, (it - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
-            // pass 2: codes -> TMEM (P^T over R_S, dS^T over R_DP) and dS^ -> shared (MN-major A)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll 1
-            for (int cc = 64 * h; cc < 64 * h + 64; cc += 16) {
-                uint32_t pr[16], dr[16];
-                tmem_ld16(lane_base + R_S + cc, pr);
-                tmem_ld16(lane_base + R_DP + cc, dr);
-                tmem_wait_ld();
-                uint32_t pk[8], dk[8];
-#pragma unroll
-                for (int k = 0; k < 16; k += 2) {
-                    pk[k / 2] = codes2(__uint_as_float(pr[k]), __uint_as_float(pr[k + 1]), ip[h]);
-                    dk[k / 2] = codes2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1]), id[h]);
-                    if (DUMP) {
-                        const int col = cc + k;
-                        if (key_ok && q0 + col < N) {
-                            a.dump_p[(bhN + q0 + col) * N + key] = code_lo(pk[k / 2]);
-                            a.dump_ds[(bhN + q0 + col) * N + key] = code_lo(dk[k / 2]);
-                        }
-                        if (key_ok && q0 + col + 1 < N) {
-                            a.dump_p[(bhN + q0 + col + 1) * N + key] = code_hi(pk[k / 2]);
-                            a.dump_ds[(bhN + q0 + col + 1) * N + key] = code_hi(dk[k / 2]);
-                        }
-                    }
-                }
-                tmem_st8(lane_base + R_S + cc / 2, pk);
-                tmem_st8(lane_base + R_DP + cc / 2, dk);
-                // dS^ row of this key, q columns [cc, cc+16) -> two 16-byte chunks of the 128-byte
-                // row (q % 64) of block h, swizzled: chunk index ^= key % 8
-                uint8_t *row = s.dss[h] + tq * 128;
-                const int c16 = (cc & 63) >> 3;                    // first 16-byte chunk (8 q each)
-                *reinterpret_cast<uint4 *>(row + (((c16) ^ (tq & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-                *reinterpret_cast<uint4 *>(row + (((c16 + 1) ^ (tq & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
-            }
-            tmem_wait_st();
-            fence_view_async_shared();
-            tc_fence_before();
-            __syncwarp();
-            if (lane_id() == 0) mbar_arrive(&s.codes_ready);
-            sq0 = nsq0;
-            sq1 = nsq1;
-            b0 = nb0;
-            b1 = nb1;
-        }
+        score_role<D, BF16, BIAS, DUMP>(s, a);
+        tc_fence_before();
+        __syncthreads();
     } else if (warp < 8) {
-        regs_inc<kRegsDV>();
-        // ------------------------------------------------------------------ dV warpgroup
-        // dV rows in registers (thread = key); the two dQ products of each chunk (d = 128:
-        // thread = d column) scaled, summed and added to global dQ with float32 atomics
-        const int tq = threadIdx.x - 128;
-        const int quarter = warp & 3;
-        const int key = k0 + tq;
-        const int kb = tq >> 6;
-        const bool key_ok = key < N;
-        const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
-        float dv[D];
-#pragma unroll
-        for (int c = 0; c < D; ++c) dv[c] = 0.0f;
-        float skb[2];
-#pragma unroll
-        for (int g = 0; g < 2; ++g)
-            skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
-        float sdo[2], nsdo[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) sdo[h] = nmine > 0 ? a.sdO[static_cast<size_t>(bh) * nblk + min(2 * c_first + h, nblk - 1)] : 0.0f;
-        for (int it = 0; it < nmine; ++it) {
-            const int ic = c_first + it;
-            const int q0 = 128 * ic;
-            const int slot = it & 1;
-            if (it + 1 < nmine) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) nsdo[h] = a.sdO[static_cast<size_t>(bh) * nblk + min(2 * ic + 2 + h, nblk - 1)];
-            }
-            // dV += s_P s_dO (P^T dO^)_h: product h in slot A (h = 0) or B (h = 1); this
-            // warpgroup's barrier of a slot completes twice a chunk: dV (parity 0), then dQ (1)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (!mbar_wait(h == 0 ? &s.a_full_v : &s.b_full_v, 0, abort_flag, &g_bwd_err, 23)) break;
-                tc_fence_after();
-                const float sc = __fmul_rn(s.sps[slot][kb][h], sdo[h]);
-                const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 8) {
-                    uint32_t r[8];
-                    tmem_ld8(src + cc, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane_id() == 0) mbar_arrive(h == 0 ? &s.a_free : &s.b_free);
-            }
-            // dQ: both key blocks' products, each scaled by its own s_dS s_K / sqrt(d) and summed
-            if (!mbar_wait(&s.a_full_v, 1, abort_flag, &g_bwd_err, 31)) break;
-            if (!mbar_wait(&s.b_full_v, 1, abort_flag, &g_bwd_err, 32)) break;
-            tc_fence_after();
-            if (D == 128) {
-                // transposed products: thread = d column c, TMEM columns = the chunk's query rows.
-                // The scaled sum goes to shared memory (the dS^ tile, which the dQ MMAs have
-                // finished reading) as 64 query rows x 128 floats at a time, and one TMA bulk
-                // reduction adds each 32 KB block of rows to global dQ.
-                const int c = tq;
-                float sg0[2], sg1[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    sg0[h] = __fmul_rn(__fmul_rn(s.sds[slot][0][h], skb[0]), a.inv_sqrt_d);
-                    sg1[h] = __fmul_rn(__fmul_rn(s.sds[slot][1][h], skb[1]), a.inv_sqrt_d);
-                }
-                const int nrow = min(128, N - q0);
-                float *stage = reinterpret_cast<float *>(s.dss[0]);        // [64 rows][128 floats]
-                const bool leader = tq == 0;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int rows = min(64, nrow - 64 * h);
-                    if (rows <= 0) break;
-                    if (h == 1) {
-                        // the first block's reduction must have read the staging tile
-                        if (leader) bulk_wait_read_all();
-                        named_bar_sync(2, 128);
-                    }
-#pragma unroll 1
-                    for (int cc = 64 * h; cc < 64 * h + 64; cc += 8) {
-                        uint32_t r0[8], r1[8];
-                        tmem_ld8(lane_base + R_A + cc, r0);
-                        tmem_ld8(lane_base + R_B + cc, r1);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            stage[(cc - 64 * h + k) * 128 + c] =
-                                __fmaf_rn(sg1[h], __uint_as_float(r1[k]), __fmul_rn(sg0[h], __uint_as_float(r0[k])));
-                    }
-                    fence_view_async_shared();
-                    named_bar_sync(2, 128);
-                    if (leader) {
-                        bulk_reduce_add_f32(a.dQ + (bhN + q0 + 64 * h) * D, stage, static_cast<uint32_t>(rows) * 128u * 4u);
-                        bulk_commit();
-                    }
-                }
-                // the products have been read out of TMEM: release both slots
-                tc_fence_before();
-                __syncwarp();
-                if (lane_id() == 0) {
-                    mbar_arrive(&s.a_free);
-                    mbar_arrive(&s.b_free);
-                }
-                // the staging tile goes back to the score warpgroup once the last reduction read it
-                if (leader) {
-                    bulk_wait_read_all();
-                    mbar_arrive(&s.dss_free);
-                }
-            } else {
-                // d = 64: thread = query row of the chunk, vector atomics along the row
-                const int qrow = q0 + tq;
-                const int h_row = tq >> 6;
-                const float s0 = __fmul_rn(__fmul_rn(s.sds[slot][0][h_row], skb[0]), a.inv_sqrt_d);
-                const float s1 = __fmul_rn(__fmul_rn(s.sds[slot][1][h_row], skb[1]), a.inv_sqrt_d);
-                const bool live = qrow < N;
-                float *dst = a.dQ + (bhN + min(qrow, N - 1)) * D;
-#pragma unroll 1
-                for (int cc = 0; cc < D; cc += 8) {
-                    uint32_t r0[8], r1[8];
-                    tmem_ld8(lane_base + R_A + cc, r0);
-                    tmem_ld8(lane_base + R_B + cc, r1);
-                    tmem_wait_ld();
-                    if (live) {
-#pragma unroll
-                        for (int k = 0; k < 8; k += 4) {
-                            float v[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                v[e] = __fmaf_rn(s1, __uint_as_float(r1[k + e]), __fmul_rn(s0, __uint_as_float(r0[k + e])));
-                            red_add_v4(dst + cc + k, v[0], v[1], v[2], v[3]);
-                        }
-                    }
-                }
-            }
-            if (D != 128) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane_id() == 0) {
-                    mbar_arrive(&s.a_free);
-                    mbar_arrive(&s.b_free);
-                }
-            }
-            if (it + 1 < nmine) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) sdo[h] = nsdo[h];
-            }
-        }
-        if (D == 128 && tq == 0) bulk_wait_all();
-        if (key_ok && !*abort_flag) {
-            float *dst = a.dV + (bhN + key) * D;
-#pragma unroll
-            for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(dv[c], dv[c + 1], dv[c + 2], dv[c + 3]);
-        }
+        dv_role<D, BF16, BIAS, DUMP>(s, a);
+        tc_fence_before();
+        __syncthreads();
     } else {
-        regs_inc<kRegsDK>();
-        // ------------------------------------------------------------------ dK warpgroup
-        const int tq = threadIdx.x - 256;                 // key lane
-        const int quarter = warp & 3;
-        const int key = k0 + tq;
-        const int kb = tq >> 6;
-        const bool key_ok = key < N;
-        const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
-        float dk[D];
-#pragma unroll
-        for (int c = 0; c < D; ++c) dk[c] = 0.0f;
-        float skb[2];
-#pragma unroll
-        for (int g = 0; g < 2; ++g)
-            skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
-        float sq[2], nsq[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) sq[h] = nmine > 0 ? a.sQ[static_cast<size_t>(bh) * nblk + min(2 * c_first + h, nblk - 1)] : 0.0f;
-        for (int it = 0; it < nmine; ++it) {
-            const int ic = c_first + it;
-            const int q0 = 128 * ic;
-            const int slot = it & 1;
-            if (it + 1 < nmine) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) nsq[h] = a.sQ[static_cast<size_t>(bh) * nblk + min(2 * ic + 2 + h, nblk - 1)];
-            }
-            // dK += s_dS s_Q / sqrt(d) (dS^T Q^)_h   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d));
-            // this warpgroup's barrier of a slot completes once a chunk
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (!mbar_wait(h == 0 ? &s.a_full_k : &s.b_full_k, it & 1, abort_flag, &g_bwd_err, 30)) break;
-                tc_fence_after();
-                const float sc = __fmul_rn(__fmul_rn(s.sds[slot][kb][h], sq[h]), a.inv_sqrt_d);
-                const uint32_t src = lane_base + (h == 0 ? R_A : R_B);
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 8) {
-                    uint32_t r[8];
-                    tmem_ld8(src + cc, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
-                }
-                if (BIAS && q0 + 64 * h < N) {
-                    const float w = __fmul_rn(s.colsum[h][tq], a.inv_sqrt_d);
-                    const float *mu = a.muQ + (static_cast<size_t>(bh) * nblk + min(2 * ic + h, nblk - 1)) * D;
-#pragma unroll
-                    for (int c = 0; c < D; ++c) dk[c] = __fmaf_rn(w, mu[c], dk[c]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane_id() == 0) mbar_arrive(h == 0 ? &s.a_free : &s.b_free);
-            }
-            if (it + 1 < nmine) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) sq[h] = nsq[h];
-            }
-        }
-        if (key_ok && !*abort_flag) {
-            float *dst = a.dK + (bhN + key) * D;
-#pragma unroll
-            for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(dk[c], dk[c + 1], dk[c + 2], dk[c + 3]);
-        }
+        dk_role<D, BF16, BIAS, DUMP>(s, a);
+        tc_fence_before();
+        __syncthreads();
     }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace bwd
@@ -780,11 +847,12 @@ static cudaError_t launch_bwd_d(const sage_params &p, const CUtensorMap *maps, c
 cudaError_t launch_bwd(const sage_params &p, const __half *Q16, const __half *K16,
                        const void *V, const void *dO, const __half *dO16, BwdArgs a,
                        cudaStream_t st) {
+    // K^ and V: 128-row key tiles; Q^, dO and dO^: 64-row query blocks
     CUtensorMap maps[5];
     const uint64_t bh = static_cast<uint64_t>(p.B) * p.H;
-    if (!make_tmap_3d(&maps[0], K16, p.d, p.N, bh) || !make_tmap_3d(&maps[1], V, p.d, p.N, bh) ||
-        !make_tmap_3d(&maps[2], Q16, p.d, p.N, bh) || !make_tmap_3d(&maps[3], dO, p.d, p.N, bh) ||
-        !make_tmap_3d(&maps[4], dO16, p.d, p.N, bh))
+    if (!make_tmap_3d(&maps[0], K16, p.d, p.N, bh, 128) || !make_tmap_3d(&maps[1], V, p.d, p.N, bh, 128) ||
+        !make_tmap_3d(&maps[2], Q16, p.d, p.N, bh, 64) || !make_tmap_3d(&maps[3], dO, p.d, p.N, bh, 64) ||
+        !make_tmap_3d(&maps[4], dO16, p.d, p.N, bh, 64))
         return cudaErrorInvalidValue;
     const bool bf = p.dtype == SAGE_BF16;
     if (p.d == 128) return bf ? launch_bwd_d<128, true>(p, maps, a, st) : launch_bwd_d<128, false>(p, maps, a, st);

@@ -24,13 +24,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // (d, N, B*H) fp16 tensor, boxes of 64 x 128 x 1 with the 128-byte swizzle: rows past N of a
 // head read as zeros.
-bool make_tmap_3d(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh) {
+bool make_tmap_3d(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), bh};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -38,13 +38,13 @@ bool make_tmap_3d(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh) 
     return r == CUDA_SUCCESS;
 }
 
-bool make_tmap_3d_bf16(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh) {
+bool make_tmap_3d_bf16(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), bh};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

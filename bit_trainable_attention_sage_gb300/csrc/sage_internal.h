@@ -86,8 +86,8 @@ cudaError_t launch_bwd(const sage_params &p, const __half *Q16, const __half *K1
 unsigned int take_bwd_error();
 
 // tensor maps (sage_capi.cu)
-// (d, N, B*H) 16-bit tensor maps with 64 x 128 boxes and the 128-byte swizzle
-bool make_tmap_3d(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh);
-bool make_tmap_3d_bf16(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh);
+// (d, N, B*H) 16-bit tensor maps with 64 x box_rows boxes and the 128-byte swizzle
+bool make_tmap_3d(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh, uint32_t box_rows = 128);
+bool make_tmap_3d_bf16(CUtensorMap *map, const void *ptr, int d, int N, uint64_t bh, uint32_t box_rows = 128);
 
 }  // namespace sage
