@@ -241,8 +241,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, &g_fwd_err, 10)) break;
             tc_fence_after();
             const bool has_b = 128 * j + 64 < kv_end;
-            float r_h[2] = {-INFINITY, -INFINITY}, sum_h[2] = {0.0f, 0.0f};
-#pragma unroll
+            float r_h0 = -INFINITY, r_h1 = -INFINITY, sum_h0 = 0.0f, sum_h1 = 0.0f;
+#pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 if (h == 1 && !has_b) break;
                 const int kb = 2 * j + h;                     // key block index
@@ -253,8 +253,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (grow >= N) nvalid = 0;
                 const float *bias = BIAS ? a.qbias + (static_cast<size_t>(bh) * nblk + qblk) * N + key0 : nullptr;
                 // pass 1: row maximum over the block (of the integer products, or of the biased logits)
+                // (loops kept rolled: unrolled bodies of both softmax warpgroups and the control
+                // warps overflow the instruction cache)
                 float r = -INFINITY;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < 64; cc += 16) {
                     uint32_t raw[16];
                     tmem_ld16(lane_base + 64 * h + cc, raw);
@@ -271,10 +273,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 }
                 if (!BIAS && nvalid > 0) r = __fmul_rn(r, c);
                 const float rs = (r == -INFINITY) ? 0.0f : r;
-                r_h[h] = r;
+                if (h == 0) r_h0 = r; else r_h1 = r;
                 // pass 2: codes, row sum; codes go to TMEM cols [32h, 32h+32) over consumed S columns
                 float sum = 0.0f;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < 64; cc += 16) {
                     uint32_t raw[16];
                     tmem_ld16(lane_base + 64 * h + cc, raw);
@@ -307,8 +309,9 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     }
                     tmem_st8(lane_base + 32 * h + cc / 2, pk);
                 }
-                sum_h[h] = sum;
+                if (h == 0) sum_h0 = sum; else sum_h1 = sum;
             }
+            const float r_h[2] = {r_h0, r_h1}, sum_h[2] = {sum_h0, sum_h1};
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
