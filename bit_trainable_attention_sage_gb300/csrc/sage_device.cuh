@@ -351,6 +351,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (two new values per instruction in a running maximum).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Two floats rounded to fp16 and packed, `lo` in the lower half.
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     uint32_t r;

@@ -90,6 +90,74 @@ __device__ __forceinline__ int tile_kv_end(int q0, int N, int causal) {
     return causal ? min(N, q0 + 128) : N;
 }
 
+// Row maximum of a 64-key block held in registers (of the integer products, or with Q-smoothing
+// of the biased logits acc c + bias, which then replace the products in `raw`), masked to the
+// first `nvalid` keys when MASKED.
+template <bool BIAS, bool MASKED>
+__device__ __forceinline__ float fwd_row_max(uint32_t (&raw)[64], float c, const float *bias,
+                                             int nvalid) {
+    float rp[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int k = 0; k < 64; k += 4) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float acc = __uint_as_float(raw[k + e]);
+            v[e] = BIAS ? __fmaf_rn(acc, c, bias[k + e]) : acc;
+            if (BIAS) raw[k + e] = __float_as_uint(v[e]);
+            if (MASKED) v[e] = (k + e < nvalid) ? v[e] : -INFINITY;
+        }
+        rp[0] = max3f(rp[0], v[0], v[1]);
+        rp[1] = max3f(rp[1], v[2], v[3]);
+    }
+    return fmaxf(rp[0], rp[1]);
+}
+
+// Codes of a 64-key block: P^ = rint(fl32(127 ex2(x))), x = fl32(acc c - r) (or with Q-smoothing
+// fl32(t - r), t = fl32(acc c + bias) left in `raw` by the row maximum), packed as fp16 pairs into
+// the 32 TMEM columns at `code_col`;
+// returns the row sum of ex2(x) (four partial sums).  rint is done with the float32 add of
+// 1.5 * 2^23 and its subtraction (exact for the values 0..127 here, and a full-rate instruction,
+// unlike the conversion unit's round-to-integer).
+template <bool BIAS, bool MASKED, bool DUMP>
+__device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, float rs,
+                                           int nvalid, uint32_t code_col, int16_t *dump_row) {
+    constexpr float kRound = 12582912.0f;          // 1.5 * 2^23
+    float sp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 16) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            float x0, x1;
+            const float a0 = __uint_as_float(raw[cc + k]), a1 = __uint_as_float(raw[cc + k + 1]);
+            if (BIAS) {
+                x0 = __fsub_rn(a0, rs);
+                x1 = __fsub_rn(a1, rs);
+            } else {
+                x0 = __fmaf_rn(a0, c, -rs);
+                x1 = __fmaf_rn(a1, c, -rs);
+            }
+            if (MASKED) {
+                x0 = (cc + k < nvalid) ? x0 : -INFINITY;
+                x1 = (cc + k + 1 < nvalid) ? x1 : -INFINITY;
+            }
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            sp[k & 3] += e0;
+            sp[(k + 1) & 3] += e1;
+            const float p0 = __fsub_rn(__fadd_rn(__fmul_rn(127.0f, e0), kRound), kRound);
+            const float p1 = __fsub_rn(__fadd_rn(__fmul_rn(127.0f, e1), kRound), kRound);
+            pk[k / 2] = pack_half2(p0, p1);
+            if (DUMP && dump_row) {
+                dump_row[cc + k] = static_cast<int16_t>(p0);
+                dump_row[cc + k + 1] = static_cast<int16_t>(p1);
+            }
+        }
+        tmem_st8(code_col + cc / 2, pk);
+    }
+    return (sp[0] + sp[1]) + (sp[2] + sp[3]);
+}
+
 template <int D, typename OutT, bool BIAS, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
@@ -252,63 +320,32 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 int nvalid = a.causal ? min(64, grow - key0 + 1) : 64;
                 if (grow >= N) nvalid = 0;
                 const float *bias = BIAS ? a.qbias + (static_cast<size_t>(bh) * nblk + qblk) * N + key0 : nullptr;
-                // pass 1: row maximum over the block (of the integer products, or of the biased logits)
-                // (loops kept rolled: unrolled bodies of both softmax warpgroups and the control
-                // warps overflow the instruction cache)
-                float r = -INFINITY;
-#pragma unroll 1
-                for (int cc = 0; cc < 64; cc += 16) {
-                    uint32_t raw[16];
-                    tmem_ld16(lane_base + 64 * h + cc, raw);
-                    tmem_wait_ld();
+                // The 64 products of the block are read from TMEM once (four loads in flight, one
+                // wait) and kept in registers for both passes.
+                uint32_t raw[64];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const float acc = __uint_as_float(raw[k]);
-                        const float v = BIAS ? __fmaf_rn(acc, c, bias[cc + k]) : acc;
-                        if (cc + k < nvalid) r = fmaxf(r, v);
-                        if (DUMP) {
-                            if (grow < N) a.dump_s[(bhN + grow) * N + key0 + cc + k] = static_cast<int32_t>(acc);
-                        }
-                    }
+                for (int q4 = 0; q4 < 4; ++q4)
+                    tmem_ld16(lane_base + 64 * h + 16 * q4, *reinterpret_cast<uint32_t(*)[16]>(&raw[16 * q4]));
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[16 * q4]));
+                // pass 1: row maximum over the block (of the integer products, or of the biased
+                // logits); three-input maxima take two columns per instruction
+                if (DUMP) {
+                    if (grow < N)
+                        for (int k = 0; k < 64; ++k) a.dump_s[(bhN + grow) * N + key0 + k] = static_cast<int32_t>(__uint_as_float(raw[k]));
                 }
+                float r;
+                if (nvalid == 64) r = fwd_row_max<BIAS, false>(raw, c, bias, 64);
+                else r = fwd_row_max<BIAS, true>(raw, c, bias, nvalid);
                 if (!BIAS && nvalid > 0) r = __fmul_rn(r, c);
                 const float rs = (r == -INFINITY) ? 0.0f : r;
                 if (h == 0) r_h0 = r; else r_h1 = r;
-                // pass 2: codes, row sum; codes go to TMEM cols [32h, 32h+32) over consumed S columns
-                float sum = 0.0f;
-#pragma unroll 1
-                for (int cc = 0; cc < 64; cc += 16) {
-                    uint32_t raw[16];
-                    tmem_ld16(lane_base + 64 * h + cc, raw);
-                    tmem_wait_ld();
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int k = 0; k < 16; k += 2) {
-                        float x0, x1;
-                        const float a0 = __uint_as_float(raw[k]), a1 = __uint_as_float(raw[k + 1]);
-                        if (BIAS) {
-                            x0 = __fsub_rn(__fmaf_rn(a0, c, bias[cc + k]), rs);
-                            x1 = __fsub_rn(__fmaf_rn(a1, c, bias[cc + k + 1]), rs);
-                        } else {
-                            x0 = __fmaf_rn(a0, c, -rs);
-                            x1 = __fmaf_rn(a1, c, -rs);
-                        }
-                        x0 = (cc + k < nvalid) ? x0 : -INFINITY;
-                        x1 = (cc + k + 1 < nvalid) ? x1 : -INFINITY;
-                        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-                        sum += e0;
-                        sum += e1;
-                        const float p0 = rintf(__fmul_rn(127.0f, e0)), p1 = rintf(__fmul_rn(127.0f, e1));
-                        pk[k / 2] = pack_half2(p0, p1);
-                        if (DUMP) {
-                            if (grow < N) {
-                                a.dump_p[(bhN + grow) * N + key0 + cc + k] = static_cast<int16_t>(p0);
-                                a.dump_p[(bhN + grow) * N + key0 + cc + k + 1] = static_cast<int16_t>(p1);
-                            }
-                        }
-                    }
-                    tmem_st8(lane_base + 32 * h + cc / 2, pk);
-                }
+                // pass 2: codes and the row sum; codes go to TMEM cols [32h, 32h+32) over consumed
+                // S columns.  A warp with a masked column in any lane takes the masked variant.
+                int16_t *dump_row = DUMP && grow < N ? a.dump_p + (bhN + grow) * N + key0 : nullptr;
+                const float sum = __any_sync(0xffffffffu, nvalid < 64)
+                    ? fwd_codes<BIAS, true, DUMP>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
+                    : fwd_codes<BIAS, false, DUMP>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
                 if (h == 0) sum_h0 = sum; else sum_h1 = sum;
             }
             const float r_h[2] = {r_h0, r_h1}, sum_h[2] = {sum_h0, sum_h1};
@@ -336,12 +373,15 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!mbar_wait(&s.pv_full[t], pv_uses & 1, abort_flag, &g_fwd_err, 11)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 16) {
-                    uint32_t raw[16];
-                    tmem_ld16(lane_base + 128 + cc, raw);
-                    tmem_wait_ld();
+                for (int cc = 0; cc < D; cc += 32) {
+                    // 32 columns a wait: two loads in flight
+                    uint32_t raw[32];
+                    tmem_ld16(lane_base + 128 + cc, *reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
+                    tmem_ld16(lane_base + 128 + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
+                    tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
+                    tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
+                    for (int k = 0; k < 32; ++k) {
                         const float pv = __uint_as_float(raw[k]);
                         o[cc + k] = (h == 0) ? __fmaf_rn(alpha, o[cc + k], cpv[0] * pv)
                                              : __fmaf_rn(cpv[1], pv, o[cc + k]);
