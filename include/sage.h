@@ -129,10 +129,10 @@ SAGE_API int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t 
  *      V, O, dO                (B,H,N,d) fp16/bf16: unquantised V, the stored forward output, dO.
  *      L                       (B,H,N) float32 from sage_attn_fwd.
  * Out: dQ, dK, dV              (B,H,N,d) float32, fully overwritten (the library zeroes them).
- * P and dS are quantised per 64x64 tile: s = fl32(max|x| / 127), codes round-half-even of
- * fl32(x * fl32(1 / s)); a tile whose max|x| is below 2^-120 is a zero tile.  dO is quantised
- * per 64-token block like Q.  dQ sums tiles with float32 atomic adds, so its last bits vary
- * from run to run.
+ * P and dS are quantised per 64x64 tile: s = fl32(max|x| / 127), code = the nearest integer
+ * (ties to even) of fl32(x * fl32(1 / s) + 1536), minus 1536; a tile whose max|x| is below
+ * 2^-120 is a zero tile.  dO is quantised per 64-token block like Q.  dQ sums the tiles with
+ * float32 reductions into global memory, so its last bits vary from run to run.
  * ------------------------------------------------------------------------------------------ */
 SAGE_API size_t sage_bwd_workspace_bytes(const sage_params *p);
 SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, const float *sQ,
