@@ -85,6 +85,18 @@ def step_ops(w: workloads.Workload) -> float:
     return ops / 2 if w.causal else ops
 
 
+def quant_bytes(w: workloads.Workload) -> int:
+    """Algorithmic HBM bytes of one sage_quantize_smooth call: Q, K, V read (2 B an element; K twice
+    with K-smoothing, once for its mean and once to quantise it; Q twice with Q-smoothing), int8
+    codes written (1 B), plus the float32 block scales and means."""
+    n = w.B * w.H * w.N * w.d
+    reads = 2 * n * (3 + 1 + (1 if w.smooth_q else 0))
+    writes = 3 * n
+    small = 4 * (3 * w.B * w.H * (w.N // 64) + w.B * w.H * w.d
+                 + (w.B * w.H * (w.N // 64) * w.d if w.smooth_q else 0))
+    return reads + writes + small
+
+
 def bwd_ops(w: workloads.Workload) -> float:
     ops = 10.0 * w.B * w.H * w.N * w.N * w.d
     return ops / 2 if w.causal else ops
@@ -199,15 +211,17 @@ def run_gpu(args, w: workloads.Workload):
     grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=device) for _ in range(3))
 
     def step(ev=None):
-        q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q)
         if ev is not None:
             ev[0].record(stream)
-        sg.sage_attn_fwd(q, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
+        q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q)
         if ev is not None:
             ev[1].record(stream)
-        sg.sage_attn_bwd(q, dev["V"], O, Lse, dev["dO"], causal=w.causal, grads=grads, workspace=ws_b)
+        sg.sage_attn_fwd(q, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
         if ev is not None:
             ev[2].record(stream)
+        sg.sage_attn_bwd(q, dev["V"], O, Lse, dev["dO"], causal=w.causal, grads=grads, workspace=ws_b)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -220,7 +234,7 @@ def run_gpu(args, w: workloads.Workload):
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     clocks.start(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize(device)
@@ -235,8 +249,9 @@ def run_gpu(args, w: workloads.Workload):
     st = sg.sage_device_status()
     if st != 0:
         raise RuntimeError(f"device status after timing: {sg.sage_status_string(st)}")
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    quant_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     ms_max = max_over_ranks(dist, ms, device)
 
     # ---- end to end through the public API with host buffers ------------------------------
@@ -278,6 +293,8 @@ def run_gpu(args, w: workloads.Workload):
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
     peak_src = "measured (bf16_tflops_sustained; fp16 runs at the bf16 rate)" if peaks else "fallback"
     bwd_tflops = bwd_ops(w) / (bwd_ms * 1e-3) / 1e12
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    quant_gbs = quant_bytes(w) / (quant_ms * 1e-3) / 1e9
     fwd_tflops = fwd_ops(w) / (fwd_ms * 1e-3) / 1e12
     if dist is not None:
         dist.destroy_process_group()
@@ -297,6 +314,9 @@ def run_gpu(args, w: workloads.Workload):
                      "traffic": profiled_traffic(w), "flops_per_launch": bwd_ops(w)},
         "fwd_call": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 1), "frac": round(fwd_tflops / peak, 4)},
         "bwd_call": {"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 1), "frac": round(bwd_tflops / peak, 4)},
+        "quantise_call": {"ms": round(quant_ms, 4), "bound": "hbm", "bytes": quant_bytes(w),
+                          "gbs": round(quant_gbs, 1), "peak_gbs": hbm_peak,
+                          "frac": round(quant_gbs / hbm_peak, 4)},
         "step_frac_of_fp16_peak": round(value / world / peak, 4),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

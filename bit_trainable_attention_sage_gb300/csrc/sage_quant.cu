@@ -82,37 +82,79 @@ __device__ __forceinline__ float block_max_256(float v, float *red) {
     return m;
 }
 
+// fp16 value as an exact integer multiple of 2^-24 (the smallest fp16 subnormal): every finite
+// fp16 is m 2^-24 (subnormal) or (1024 + m) 2^(e - 25), so the multiple is m or
+// (1024 + m) << (e - 1), below 2^40 in magnitude.
+__device__ __forceinline__ long long half_fixed24(uint32_t h) {
+    const uint32_t e = (h >> 10) & 31u, m = h & 1023u;
+    const long long mag = e == 0 ? static_cast<long long>(m) : static_cast<long long>(1024u | m) << (e - 1);
+    return (h & 0x8000u) ? -mag : mag;
+}
+
 // ---------------------------------------------------------------------------------------------
-// a1: partial sums of K over token ranges, float64, one (head, split) per CTA.
+// a1: partial sums of K over token ranges, exact, one (head, split) per CTA.
 // partial[(bh * S + s) * d + c] = sum_{n in split s} K[bh, n, c]
+// fp16 input: int64 multiples of 2^-24 (integer adds, far faster than float64 ones here and just
+// as exact: a sum of 32768 values stays below 2^55, and any sum below 2^53 is exact in both);
+// bf16 input (exponent range of float32): float64.  Both occupy 8 bytes per entry.
 // ---------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict__ K,
                                                             double *__restrict__ partial, int N,
                                                             int d, int S, int rows_per_split) {
-    __shared__ double red[256 * 8];
-    const int bh = blockIdx.x, s = blockIdx.y;
-    const int vec_per_row = d / 8;                    // threads per row
-    const int rows_in_flight = 256 / vec_per_row;
-    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
-    const int n0 = s * rows_per_split;
-    const int n1 = min(N, n0 + rows_per_split);
-    double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    const T *base = K + static_cast<size_t>(bh) * N * d;
-    for (int n = n0 + rg; n < n1; n += rows_in_flight) {
-        float v[8];
-        load8(base + static_cast<size_t>(n) * d + cv * 8, v);
+    if constexpr (std::is_same<T, __half>::value) {
+        __shared__ long long redi[256 * 8];
+        const int bh = blockIdx.x, s = blockIdx.y;
+        const int vec_per_row = d / 8;
+        const int rows_in_flight = 256 / vec_per_row;
+        const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+        const int n0 = s * rows_per_split;
+        const int n1 = min(N, n0 + rows_per_split);
+        long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const T *base = K + static_cast<size_t>(bh) * N * d;
+        for (int n = n0 + rg; n < n1; n += rows_in_flight) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(base + static_cast<size_t>(n) * d + cv * 8);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += static_cast<double>(v[i]);
-    }
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += half_fixed24(u[i] & 0xFFFFu);
+                acc[2 * i + 1] += half_fixed24(u[i] >> 16);
+            }
+        }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) red[threadIdx.x * 8 + i] = acc[i];
-    __syncthreads();
-    if (threadIdx.x < d) {
-        const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
-        double sum = 0.0;
-        for (int g = 0; g < rows_in_flight; ++g) sum += red[(g * vec_per_row + cvv) * 8 + ci];
-        partial[(static_cast<size_t>(bh) * S + s) * d + c] = sum;
+        for (int i = 0; i < 8; ++i) redi[threadIdx.x * 8 + i] = acc[i];
+        __syncthreads();
+        if (threadIdx.x < d) {
+            const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
+            long long sum = 0;
+            for (int g = 0; g < rows_in_flight; ++g) sum += redi[(g * vec_per_row + cvv) * 8 + ci];
+            reinterpret_cast<long long *>(partial)[(static_cast<size_t>(bh) * S + s) * d + c] = sum;
+        }
+    } else {
+        __shared__ double red[256 * 8];
+        const int bh = blockIdx.x, s = blockIdx.y;
+        const int vec_per_row = d / 8;                    // threads per row
+        const int rows_in_flight = 256 / vec_per_row;
+        const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+        const int n0 = s * rows_per_split;
+        const int n1 = min(N, n0 + rows_per_split);
+        double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const T *base = K + static_cast<size_t>(bh) * N * d;
+        for (int n = n0 + rg; n < n1; n += rows_in_flight) {
+            float v[8];
+            load8(base + static_cast<size_t>(n) * d + cv * 8, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += static_cast<double>(v[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red[threadIdx.x * 8 + i] = acc[i];
+        __syncthreads();
+        if (threadIdx.x < d) {
+            const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
+            double sum = 0.0;
+            for (int g = 0; g < rows_in_flight; ++g) sum += red[(g * vec_per_row + cvv) * 8 + ci];
+            partial[(static_cast<size_t>(bh) * S + s) * d + c] = sum;
+        }
     }
 }
 
@@ -142,7 +184,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
         if (threadIdx.x < d) {
             const double *p = a.kpartial + static_cast<size_t>(bh) * a.ksplits * d + threadIdx.x;
             double sum = 0.0;
-            for (int s = 0; s < a.ksplits; ++s) sum += p[static_cast<size_t>(s) * d];
+            if constexpr (std::is_same<T, __half>::value) {
+                // exact int64 multiples of 2^-24 (see kmean_partial_kernel)
+                long long si = 0;
+                for (int s = 0; s < a.ksplits; ++s) si += reinterpret_cast<const long long *>(p)[static_cast<size_t>(s) * d];
+                sum = static_cast<double>(si) * 0x1p-24;
+            } else {
+                for (int s = 0; s < a.ksplits; ++s) sum += p[static_cast<size_t>(s) * d];
+            }
             const float mu = static_cast<float>(sum / static_cast<double>(N));
             mu_s[threadIdx.x] = mu;
             if (blk == 0 && a.muK) a.muK[static_cast<size_t>(bh) * d + threadIdx.x] = mu;
