@@ -19,6 +19,7 @@ SAGE_OK, SAGE_ERR_ARG, SAGE_ERR_UNSUPPORTED, SAGE_ERR_ALIGN = 0, 1, 2, 3
 SAGE_ERR_CUDA, SAGE_ERR_TIMEOUT, SAGE_ERR_WORKSPACE = 4, 5, 6
 SAGE_FP16, SAGE_BF16 = 0, 1
 SAGE_FLAG_DUMP = 1
+SAGE_FLAG_DP_INT8 = 2
 
 EXPORTED = (
     "sage_quantize_workspace_bytes", "sage_quantize_smooth", "sage_fwd_workspace_bytes",
@@ -187,12 +188,16 @@ def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,
 
 def sage_attn_bwd(q: Quantized, V: torch.Tensor, O: torch.Tensor, L: torch.Tensor, dO: torch.Tensor, *,
                   causal: bool, K: torch.Tensor | None = None, grads=None,
-                  workspace: torch.Tensor | None = None, dump: torch.Tensor | None = None, stream=None):
-    """SageBwd backward.  Returns (dQ, dK, dV), float32 (B,H,N,d)."""
+                  workspace: torch.Tensor | None = None, dump: torch.Tensor | None = None, stream=None,
+                  dp_int8: bool = False):
+    """SageBwd backward.  Returns (dQ, dK, dV), float32 (B,H,N,d).  ``dp_int8`` selects the
+    INT8-dP ablation (SAGE_FLAG_DP_INT8)."""
     _require_cuda(V, O, L, dO, K)
     B, H, N, d = q.Qh.shape
     dev = q.Qh.device
     p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump)
+    if dp_int8:
+        p.flags |= SAGE_FLAG_DP_INT8
     if grads is None:
         grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3))
     dQ, dK, dV = grads

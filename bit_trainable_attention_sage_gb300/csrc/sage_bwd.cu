@@ -77,6 +77,9 @@ __device__ __forceinline__ void regs_to() {
 constexpr uint32_t R_A = 256;                         // dV product (d columns); d = 128: dQ^T
 constexpr uint32_t R_Q = 384;                         // d = 64: the two dQ products
 constexpr int kScaleSlots = 8;                        // tile scales kept for 8 steps
+// operands of the dP MMA: the unquantised fp16 or bf16 dO and V (the method), or their INT8 codes
+// as integer-valued fp16 (the ablation of "SageAttention3 ..." (review), Table 1c)
+constexpr int kDpFp16 = 0, kDpBf16 = 1, kDpInt8 = 2;
 constexpr float kTileZero = 7.52316384526264e-37f;   // 2^-120
 
 template <int D>
@@ -170,10 +173,11 @@ struct RowData8 {
 // P and dS of 8 query columns [col0, col0 + 8) from S^T and dP^T: P = ex2(acc c - L2) (masked to
 // 0 where EDGE says the pair is not live), dS = P (dP - D).  Pass 1 and pass 2 both call this, so
 // the two passes see bit-identical values.
-template <bool EDGE, bool BIAS>
+template <bool EDGE, bool BIAS, bool DP8>
 __device__ __forceinline__ void score_p_ds_8(const uint32_t (&sr)[8], const uint32_t (&dr)[8],
                                              const RowData8 &rd, int col0, float cq, float bias,
-                                             int qlo, bool key_ok, float (&pv)[8], float (&ds)[8]) {
+                                             int qlo, bool key_ok, float dps, float (&pv)[8],
+                                             float (&ds)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const float acc = __uint_as_float(sr[k]);
@@ -182,7 +186,9 @@ __device__ __forceinline__ void score_p_ds_8(const uint32_t (&sr)[8], const uint
         else x = __fmaf_rn(acc, cq, -rd.l2[k]);
         if (EDGE) x = (key_ok && col0 + k >= qlo) ? x : -INFINITY;   // ex2(-inf) = +0: P = 0, dS = +-0
         pv[k] = ex2_approx(x);
-        ds[k] = __fmul_rn(pv[k], __fsub_rn(__uint_as_float(dr[k]), rd.dd[k]));
+        // DP8: dP = fl32(integer product * fl32(s_dO s_V))
+        const float dp = DP8 ? __fmul_rn(__uint_as_float(dr[k]), dps) : __uint_as_float(dr[k]);
+        ds[k] = __fmul_rn(pv[k], __fsub_rn(dp, rd.dd[k]));
     }
 }
 
@@ -216,14 +222,14 @@ __device__ __forceinline__ void score_walk(uint32_t s_col, uint32_t dp_col, cons
 }
 
 // Pass 1 over the 64 query columns of a block: tile maxima of P and |dS| and the dS column sum.
-template <bool EDGE, bool BIAS, bool DUMP>
+template <bool EDGE, bool BIAS, bool DUMP, bool DP8>
 __device__ __forceinline__ void score_pass1(uint32_t s_col, uint32_t dp_col, const float *L2s,
                                             const float *Ds, float cq, float bias, int qlo,
-                                            bool key_ok, float &mp, float &md, float &cs,
+                                            bool key_ok, float dps, float &mp, float &md, float &cs,
                                             int32_t *dump_col0, int N) {
     score_walk(s_col, dp_col, L2s, Ds, [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8 &rd, int col0) {
         float pv[8], ds[8];
-        score_p_ds_8<EDGE, BIAS>(sr, dr, rd, col0, cq, bias, qlo, key_ok, pv, ds);
+        score_p_ds_8<EDGE, BIAS, DP8>(sr, dr, rd, col0, cq, bias, qlo, key_ok, dps, pv, ds);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             mp = fmaxf(mp, pv[k]);
@@ -239,14 +245,15 @@ __device__ __forceinline__ void score_pass1(uint32_t s_col, uint32_t dp_col, con
 // columns already read (4 packed columns at col0 / 2), dS codes -> this key's 128-byte row of the
 // shared dS^ tile (16-byte chunk j stored at j ^ (key % 8), the 128-byte swizzle the MMA
 // descriptors expect).
-template <bool EDGE, bool BIAS, bool DUMP>
+template <bool EDGE, bool BIAS, bool DUMP, bool DP8>
 __device__ __forceinline__ void score_pass2(uint32_t s_col, uint32_t dp_col, const float *L2s,
                                             const float *Ds, float cq, float bias, int qlo,
-                                            bool key_ok, float ip, float id, uint8_t *dss_row,
-                                            int swz, int16_t *dump_p0, int16_t *dump_ds0, int N) {
+                                            bool key_ok, float dps, float ip, float id,
+                                            uint8_t *dss_row, int swz, int16_t *dump_p0,
+                                            int16_t *dump_ds0, int N) {
     score_walk(s_col, dp_col, L2s, Ds, [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8 &rd, int col0) {
         float pv[8], ds[8];
-        score_p_ds_8<EDGE, BIAS>(sr, dr, rd, col0, cq, bias, qlo, key_ok, pv, ds);
+        score_p_ds_8<EDGE, BIAS, DP8>(sr, dr, rd, col0, cq, bias, qlo, key_ok, dps, pv, ds);
         uint32_t pk[4], dk[4];
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
@@ -289,7 +296,7 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
     }
 }
 
-template <int D, bool BF16, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP>
 __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const CUtensorMap *mapK, const CUtensorMap *mapV,
                                       const CUtensorMap *mapQ, const CUtensorMap *mapdO,
                                       const CUtensorMap *mapdOh) {
@@ -371,7 +378,7 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
         // dS^ tile.
         if (elect_one()) {
             constexpr uint32_t idS = idesc_f16(128, 64, false, false, false);      // S^T
-            constexpr uint32_t idDP = idesc_f16(128, 64, BF16, false, false);      // dP^T
+            constexpr uint32_t idDP = idesc_f16(128, 64, DPK == kDpBf16, false, false);   // dP^T
             constexpr uint32_t idKV = idesc_f16(128, D, false, false, true);       // dK, dV
             constexpr uint32_t idQ = idesc_f16(128, 64, false, true, true);        // dQ(^T)
             // base descriptors; a byte offset `off` inside an operand adds off >> 4
@@ -472,7 +479,7 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
 }
 
 // Score warpgroup (warps 0-3).
-template <int D, bool BF16, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP>
 __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -500,15 +507,21 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const float *biash = BIAS ? a.qbias + static_cast<size_t>(bh) * nblk * N + min(key, N - 1) : nullptr;
     float sq_next = sQh[c_first];
     float b_next = (BIAS && key_ok) ? biash[static_cast<size_t>(c_first) * N] : 0.0f;
+    // INT8 dP (ablation): the tile scale fl32(s_dO s_V) of the integer dP product
+    const float *sdOh = a.sdO + static_cast<size_t>(bh) * nblk;
+    const float sv = (DPK == kDpInt8 && key_ok) ? a.sV[static_cast<size_t>(bh) * nblk + kblk] : 0.0f;
+    float sdo_next = DPK == kDpInt8 ? sdOh[c_first] : 0.0f;
     for (int c = 0; c < n; ++c) {
         const int qb = c_first + c;
         const int q0 = 64 * qb;
         const int b = c & 1, m3 = c % 3, z = c & (kScaleSlots - 1);
         const float cq = __fmul_rn(__fmul_rn(sq_next, sk), a.sl2);
         const float bias = b_next;
+        const float dps = DPK == kDpInt8 ? __fmul_rn(sdo_next, sv) : 1.0f;
         if (c + 1 < n) {
             sq_next = sQh[qb + 1];
             if (BIAS && key_ok) b_next = biash[static_cast<size_t>(qb + 1) * N];
+            if (DPK == kDpInt8) sdo_next = sdOh[qb + 1];
         }
         const int qlo = a.causal ? max(0, key - q0) : 0;
         const bool edge = (a.causal && q0 < k0 + 128) || k0 + 128 > N;
@@ -519,11 +532,11 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         float mp = 0.0f, md = 0.0f, cs = 0.0f;
         int32_t *dump_s0 = DUMP ? a.dump_s + (bhN + q0) * N + key : nullptr;
         if (edge)
-            score_pass1<true, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
-                                          key_ok, mp, md, cs, dump_s0, N);
+            score_pass1<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                                          key_ok, dps, mp, md, cs, dump_s0, N);
         else
-            score_pass1<false, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
-                                           key_ok, mp, md, cs, dump_s0, N);
+            score_pass1<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                                           key_ok, dps, mp, md, cs, dump_s0, N);
         // tile maxima of (this query block, this key block): over the 32 lanes, then over the
         // two warps of the key block
 #pragma unroll
@@ -561,11 +574,11 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         int16_t *dump_ds0 = DUMP ? a.dump_ds + (bhN + q0) * N + key : nullptr;
         uint8_t *dss_row = s.dss[b] + tq * 128;
         if (edge)
-            score_pass2<true, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
-                                          ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
+            score_pass2<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
+                                                          dps, ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
         else
-            score_pass2<false, BIAS, DUMP>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
-                                           ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
+            score_pass2<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
+                                                           dps, ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
         tmem_wait_st();
         fence_view_async_shared();
         tc_fence_before();
@@ -578,7 +591,7 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
 }
 
 // dV warpgroup (warps 4-7).
-template <int D, bool BF16, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP>
 __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -682,7 +695,7 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
 }
 
 // dK warpgroup (warps 8-11).
-template <int D, bool BF16, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP>
 __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -759,7 +772,7 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
     }
 }
 
-template <int D, bool BF16, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                 const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapdO,
@@ -794,20 +807,20 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     // each role computes its own CTA geometry: a value computed here and used by several roles
     // would have to sit in the same register in all of them, the 24-register control one included
     if (warp >= 12) {
-        control_role<D, BF16, BIAS, DUMP>(s, a, &mapK, &mapV, &mapQ, &mapdO, &mapdOh);
+        control_role<D, DPK, BIAS, DUMP>(s, a, &mapK, &mapV, &mapQ, &mapdO, &mapdOh);
         tc_fence_before();
         __syncthreads();
         if (warp == kMmaWarp) tmem_dealloc(s.tmem_base, 512);
     } else if (warp < 4) {
-        score_role<D, BF16, BIAS, DUMP>(s, a);
+        score_role<D, DPK, BIAS, DUMP>(s, a);
         tc_fence_before();
         __syncthreads();
     } else if (warp < 8) {
-        dv_role<D, BF16, BIAS, DUMP>(s, a);
+        dv_role<D, DPK, BIAS, DUMP>(s, a);
         tc_fence_before();
         __syncthreads();
     } else {
-        dk_role<D, BF16, BIAS, DUMP>(s, a);
+        dk_role<D, DPK, BIAS, DUMP>(s, a);
         tc_fence_before();
         __syncthreads();
     }
@@ -815,10 +828,10 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 
 }  // namespace bwd
 
-template <int D, bool BF16, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP>
 static cudaError_t launch_bwd_t(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
                                 cudaStream_t st) {
-    auto kern = bwd::sage_bwd_kernel<D, BF16, BIAS, DUMP>;
+    auto kern = bwd::sage_bwd_kernel<D, DPK, BIAS, DUMP>;
     const int smem = static_cast<int>(sizeof(bwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -834,29 +847,37 @@ static cudaError_t launch_bwd_t(const sage_params &p, const CUtensorMap *maps, c
     return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, int DPK>
 static cudaError_t launch_bwd_d(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
                                 cudaStream_t st) {
     const bool bias = a.qbias != nullptr, dump = a.dump_s != nullptr;
-    if (dump) return bias ? launch_bwd_t<D, BF16, true, true>(p, maps, a, st)
-                          : launch_bwd_t<D, BF16, false, true>(p, maps, a, st);
-    return bias ? launch_bwd_t<D, BF16, true, false>(p, maps, a, st)
-                : launch_bwd_t<D, BF16, false, false>(p, maps, a, st);
+    if (dump) return bias ? launch_bwd_t<D, DPK, true, true>(p, maps, a, st)
+                          : launch_bwd_t<D, DPK, false, true>(p, maps, a, st);
+    return bias ? launch_bwd_t<D, DPK, true, false>(p, maps, a, st)
+                : launch_bwd_t<D, DPK, false, false>(p, maps, a, st);
+}
+
+template <int D>
+static cudaError_t launch_bwd_k(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
+                                cudaStream_t st) {
+    if (p.flags & SAGE_FLAG_DP_INT8) return launch_bwd_d<D, bwd::kDpInt8>(p, maps, a, st);
+    return p.dtype == SAGE_BF16 ? launch_bwd_d<D, bwd::kDpBf16>(p, maps, a, st)
+                                : launch_bwd_d<D, bwd::kDpFp16>(p, maps, a, st);
 }
 
 cudaError_t launch_bwd(const sage_params &p, const __half *Q16, const __half *K16,
                        const void *V, const void *dO, const __half *dO16, BwdArgs a,
                        cudaStream_t st) {
-    // K^ and V: 128-row key tiles; Q^, dO and dO^: 64-row query blocks
+    // K^ and V: 128-row key tiles; Q^, dO and dO^: 64-row query blocks.  With SAGE_FLAG_DP_INT8
+    // the caller passes the fp16 copies of the V and dO codes as V and dO.
     CUtensorMap maps[5];
     const uint64_t bh = static_cast<uint64_t>(p.B) * p.H;
     if (!make_tmap_3d(&maps[0], K16, p.d, p.N, bh, 128) || !make_tmap_3d(&maps[1], V, p.d, p.N, bh, 128) ||
         !make_tmap_3d(&maps[2], Q16, p.d, p.N, bh, 64) || !make_tmap_3d(&maps[3], dO, p.d, p.N, bh, 64) ||
         !make_tmap_3d(&maps[4], dO16, p.d, p.N, bh, 64))
         return cudaErrorInvalidValue;
-    const bool bf = p.dtype == SAGE_BF16;
-    if (p.d == 128) return bf ? launch_bwd_d<128, true>(p, maps, a, st) : launch_bwd_d<128, false>(p, maps, a, st);
-    return bf ? launch_bwd_d<64, true>(p, maps, a, st) : launch_bwd_d<64, false>(p, maps, a, st);
+    if (p.d == 128) return launch_bwd_k<128>(p, maps, a, st);
+    return launch_bwd_k<64>(p, maps, a, st);
 }
 
 unsigned int take_bwd_error() {

@@ -103,6 +103,9 @@ static FwdWs fwd_ws(const sage_params &p, void *w, size_t *bytes) {
 struct BwdWs {
     __half *q16, *k16, *do16;
     float *D, *L2, *sdO, *qbias;
+    int8_t *v8;      // SAGE_FLAG_DP_INT8: V codes, their fp16 copy and the block scales
+    __half *v16;
+    float *sV;
 };
 static BwdWs bwd_ws(const sage_params &p, void *w, size_t *bytes) {
     Carve c(w);
@@ -114,6 +117,10 @@ static BwdWs bwd_ws(const sage_params &p, void *w, size_t *bytes) {
     r.L2 = c.take<float>(rows(p));
     r.sdO = c.take<float>(nblocks(p));
     r.qbias = p.smooth_q ? c.take<float>(nblocks(p) * p.N) : nullptr;
+    const bool dp8 = (p.flags & SAGE_FLAG_DP_INT8) != 0;
+    r.v8 = dp8 ? c.take<int8_t>(elems(p)) : nullptr;
+    r.v16 = dp8 ? c.take<__half>(elems(p)) : nullptr;
+    r.sV = dp8 ? c.take<float>(nblocks(p)) : nullptr;
     if (bytes) *bytes = c.off;
     return r;
 }
@@ -168,7 +175,7 @@ static int check_params(const sage_params *p) {
     if (p->causal != 0 && p->causal != 1) return SAGE_ERR_ARG;
     if (p->smooth_k != 0 && p->smooth_k != 1) return SAGE_ERR_ARG;
     if (p->smooth_q != 0 && p->smooth_q != 1) return SAGE_ERR_ARG;
-    if (p->flags & ~SAGE_FLAG_DUMP) return SAGE_ERR_ARG;
+    if (p->flags & ~(SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8)) return SAGE_ERR_ARG;
     if (p->dtype != SAGE_FP16 && p->dtype != SAGE_BF16) return SAGE_ERR_UNSUPPORTED;
     if (p->d != 64 && p->d != 128) return SAGE_ERR_UNSUPPORTED;
     if (p->N % 64 != 0) return SAGE_ERR_UNSUPPORTED;
@@ -311,6 +318,16 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     if (p->flags & SAGE_FLAG_DUMP) dd = bwd_dump(*p, p->dump, nullptr);
     SAGE_CUDA(launch_widen(Qh, w.q16, n, st));
     SAGE_CUDA(launch_widen(Kh, w.k16, n, st));
+    const bool dp8 = (p->flags & SAGE_FLAG_DP_INT8) != 0;
+    if (dp8) {
+        // V codes for dP (the ablation): the same per-block quantiser as sage_quantize_smooth
+        QuantArgs qa;
+        memset(&qa, 0, sizeof(qa));
+        qa.V = V; qa.Vh = w.v8; qa.sV = w.sV;
+        qa.N = p->N; qa.d = p->d;
+        SAGE_CUDA(launch_quantize_v(*p, qa, st));
+        SAGE_CUDA(launch_widen(w.v8, w.v16, n, st));
+    }
     BwdPrologueArgs pa;
     pa.dO = dO; pa.O = O; pa.L = L; pa.L2 = w.L2; pa.D = w.D; pa.dO16 = w.do16; pa.dOh = dd.doh; pa.sdO = w.sdO;
     pa.N = p->N; pa.d = p->d;
@@ -320,7 +337,7 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     SAGE_CUDA(cudaMemsetAsync(dQ, 0, n * sizeof(float), st));
     BwdArgs a;
     memset(&a, 0, sizeof(a));
-    a.sQ = sQ; a.sK = sK; a.sdO = w.sdO; a.D = w.D; a.L2 = w.L2;
+    a.sQ = sQ; a.sK = sK; a.sdO = w.sdO; a.D = w.D; a.L2 = w.L2; a.sV = w.sV;
     a.qbias = w.qbias; a.muQ = p->smooth_q ? muQ : nullptr;
     a.dQ = dQ; a.dK = dK; a.dV = dV;
     if (p->flags & SAGE_FLAG_DUMP) {
@@ -331,7 +348,9 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     a.N = p->N; a.H = p->H; a.causal = p->causal; a.dtype = p->dtype;
     a.sl2 = sl2;
     a.inv_sqrt_d = static_cast<float>(1.0 / __builtin_sqrt(static_cast<double>(p->d)));
-    SAGE_CUDA(launch_bwd(*p, w.q16, w.k16, V, dO, w.do16, a, st));
+    // the ablation feeds dP from the codes: V^ instead of V, dO^ instead of dO
+    SAGE_CUDA(launch_bwd(*p, w.q16, w.k16, dp8 ? static_cast<const void *>(w.v16) : V,
+                         dp8 ? static_cast<const void *>(w.do16) : dO, w.do16, a, st));
     return SAGE_OK;
 }
 

@@ -26,6 +26,7 @@ struct QuantArgs {
     const double *kpartial;   // (B*H, ksplits, d) float64 partial sums of K (workspace)
     int ksplits;
     int N, d, smooth_k, smooth_q;
+    int z_base;               // first tensor of the launch: 0 = Q, 1 = K, 2 = V
 };
 
 struct BwdPrologueArgs {
@@ -54,6 +55,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     const float *sQ, *sK, *sdO, *D, *L2;   // D and L2 = fl32(L log2 e): (B,H,N), from the prologue
+    const float *sV;      // (B,H,N/64) V block scales (SAGE_FLAG_DP_INT8 only), else NULL
     const float *qbias;   // (B,H,N/64,N) or NULL
     const float *muQ;     // (B,H,N/64,d) or NULL (Q-smoothing dK bias term)
     float *dQ, *dK, *dV;  // (B,H,N,d) float32
@@ -69,6 +71,7 @@ struct BwdArgs {
 // sage_quant.cu
 int kmean_splits(const sage_params &p);
 cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st);
+cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st);   // V only
 cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, cudaStream_t st);
 cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStream_t st);
 cudaError_t launch_qbias(const sage_params &p, const void *K, const float *muK, const float *muQ,

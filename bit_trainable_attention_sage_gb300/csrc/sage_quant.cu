@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     __shared__ float red[8];
     __shared__ float mu_s[128];
     __shared__ double colsum[256 * 8];
-    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z;
+    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z + a.z_base;
     const int d = a.d, N = a.N;
     const T *src = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
     int8_t *dst = z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh);
@@ -380,6 +380,17 @@ cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st) 
             kmean_partial_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.K), const_cast<double *>(a.kpartial), p.N, p.d, S, rows);
     }
     dim3 g(p.N / 64, bh, 3);
+    if (p.dtype == SAGE_FP16)
+        quantize_kernel<__half><<<g, 256, 0, st>>>(a);
+    else
+        quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// V alone (no smoothing applies to V): codes to a.Vh, scales to a.sV
+cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st) {
+    a.z_base = 2;
+    dim3 g(p.N / 64, p.B * p.H, 1);
     if (p.dtype == SAGE_FP16)
         quantize_kernel<__half><<<g, 256, 0, st>>>(a);
     else

@@ -49,6 +49,12 @@ extern "C" {
 /* Flags. */
 #define SAGE_FLAG_DUMP 1u       /* debug: write the integer block products and the in-kernel
                                    codes to `dump` (small problems only; see sage_dump_bytes) */
+#define SAGE_FLAG_DP_INT8 2u    /* sage_attn_bwd only: form dP from the INT8 codes of dO and V,
+                                   dP = fl32(MM(dO^, V^T) * fl32(s_dO s_V)), instead of the 16-bit
+                                   product the method keeps -- the ablation of "SageAttention3 ..."
+                                   (review), Table 1c.  V is quantised per 64-token block inside
+                                   the call (same codes as sage_quantize_smooth); the workspace
+                                   grows by 3 bytes per element plus the scales. */
 
 typedef struct CUstream_st *sage_stream_t;   /* identical to cudaStream_t */
 

@@ -261,8 +261,13 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
 
 
 def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUANTISED,
-                  q_blocks=None, kv_blocks=None, heads=None, record: dict | None = None):
+                  q_blocks=None, kv_blocks=None, heads=None, record: dict | None = None,
+                  dp_int8: bool = False):
     """SageBwd backward (steps a7-a13).  Returns dict(dQ, dK, dV float64 (B,H,N,d), D, dOh, sdO).
+
+    ``dp_int8`` selects the ablation of "SageAttention3 ..." (review), Table 1c: dP from the INT8
+    codes of dO and V, dP_ij = fl32(MM(dO^_i, V^_j^T) * fl32(s_dO,i * s_V,j)), instead of the 16-bit
+    product the method keeps.
 
     ``O_stored`` is the forward output as stored (16-bit values), ``L`` the stored float32 LSE.
     ``q_blocks`` / ``kv_blocks`` restrict which dQ rows / dK, dV rows are completed (for sampled
@@ -305,8 +310,13 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
         s_p, p_hat = arith.tile_quant(P)
         if want_dkv:
             dV[b, h, cols] += (float(s_p) * float(sdO[b, h, i])) * arith.int_mm(p_hat.T, dOh[b, h, rows])
-        # (4) dP_ij = dO_i V_j^T, 16-bit operands, float32 result
-        dP = arith.r32(dO[b, h, rows].astype(np.float64) @ V64[b, h, cols].T)
+        # (4) dP_ij = dO_i V_j^T, 16-bit operands, float32 result (ablation: INT8 codes, exact
+        # integer product times the float32 product of the two block scales)
+        if dp_int8:
+            sc = arith.r32(np.float64(arith.r32(float(sdO[b, h, i]) * float(prep["sV"][b, h, j]))))
+            dP = arith.r32(arith.int_mm(dOh[b, h, rows], np.swapaxes(prep["Vh"][b, h, cols], 0, 1)) * float(sc))
+        else:
+            dP = arith.r32(dO[b, h, rows].astype(np.float64) @ V64[b, h, cols].T)
         # (5) dS_ij = P_ij o (dP_ij - D_i), then per-tile quantisation
         dS = arith.r32(P * arith.r32(dP - D32[b, h, rows][:, None]))
         s_ds, ds_hat = arith.tile_quant(dS)
@@ -350,7 +360,7 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
 
 
 def run(Q, K, V, dO, causal: bool, dtype_round, smooth_k: bool = True, smooth_q: bool = False,
-        arith: Arith = QUANTISED, record: dict | None = None):
+        arith: Arith = QUANTISED, record: dict | None = None, dp_int8: bool = False):
     """Whole path on full tensors: quantise, forward, backward.  ``dtype_round`` rounds O to the
     stored 16-bit type (identity in the dequantised limit)."""
     prep = prepare(Q, K, V, smooth_k=smooth_k, smooth_q=smooth_q, arith=arith)
@@ -358,5 +368,5 @@ def run(Q, K, V, dO, causal: bool, dtype_round, smooth_k: bool = True, smooth_q:
     O, L = sage_forward(prep, causal, arith=arith, record=record)
     O_stored = dtype_round(O.astype(np.float32)) if arith.quantised else O
     L_stored = L.astype(np.float32) if arith.quantised else L
-    g = sage_backward(prep, O_stored, L_stored, dO, causal, arith=arith, record=record)
+    g = sage_backward(prep, O_stored, L_stored, dO, causal, arith=arith, record=record, dp_int8=dp_int8)
     return dict(prep=prep, O=O, L=L, O_stored=O_stored, L_stored=L_stored, **g)

@@ -52,10 +52,11 @@ def make_case(N, d, dtype, causal, B=1, H=2, seed=0, qk="normal", sigma=1.0, k_o
     return w, workloads.make_inputs(w, seed=seed)
 
 
-def oracle_run(w, x, record=True):
+def oracle_run(w, x, record=True, dp_int8=False):
     rec = {} if record else None
     out = osage.run(x["Q"], x["K"], x["V"], x["dO"], w.causal,
-                    lambda a: workloads.round_to(a, w.dtype), smooth_q=w.smooth_q, record=rec)
+                    lambda a: workloads.round_to(a, w.dtype), smooth_q=w.smooth_q, record=rec,
+                    dp_int8=dp_int8)
     out["record"] = rec
     return out
 
@@ -97,7 +98,7 @@ def gpu_fwd(w, x, dump=False):
     return dict(q=q, O=O, L=L, dump=buf, dev=dict(Q=Q, K=K, V=V))
 
 
-def gpu_run(w, x, dump=False):
+def gpu_run(w, x, dump=False, dp_int8=False):
     """quantise -> forward -> backward on the GPU; returns numpy results (+ backward dump views)."""
     import bit_trainable_attention_sage_gb300 as sg
     Q, K, V, dO = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V", "dO"))
@@ -108,7 +109,7 @@ def gpu_run(w, x, dump=False):
     if dump:
         nbytes = sg.sage_dump_bytes(w.B, w.H, w.N, w.d, 1)
         buf = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-    dQ, dK, dV = sg.sage_attn_bwd(q, V, O, L, dO, causal=w.causal, K=Kb, dump=buf)
+    dQ, dK, dV = sg.sage_attn_bwd(q, V, O, L, dO, causal=w.causal, K=Kb, dump=buf, dp_int8=dp_int8)
     st = sg.sage_device_status()
     assert st == 0, sg.sage_status_string(st)
     out = dict(O=O.float().cpu().numpy(), L=L.cpu().numpy(), dQ=dQ.cpu().numpy(),

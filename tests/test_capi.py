@@ -47,6 +47,11 @@ def test_workspace_sizes(sg):
     assert L.sage_fwd_workspace_bytes(ctypes.byref(pq)) >= fwd + 4 * 2 * 16 * 128 * 8192
     bad = sg.make_params(1, 1, 100, 128, 0, False)
     assert L.sage_fwd_workspace_bytes(ctypes.byref(bad)) == 0
+    # the INT8-dP ablation adds the V codes (1 B), their fp16 copy (2 B) and the block scales
+    p8 = sg.make_params(2, 16, 8192, 128, 0, False)
+    p8.flags = sg.binding.SAGE_FLAG_DP_INT8
+    extra = L.sage_bwd_workspace_bytes(ctypes.byref(p8)) - bwd
+    assert 3 * n + 4 * 2 * 16 * 128 <= extra <= 3 * n + 4 * 2 * 16 * 128 + 3 * 256
 
 
 def _fake(i):

@@ -216,3 +216,44 @@ def test_sweep_trend_matches_table1():
     last = rows[2]
     assert last["dQ"] > 3 * last["O"] and last["dK"] > 3 * last["dV"]
     assert 0.4 < last["dQ"] < 0.9 and 0.6 < last["cos_dQ"] < 0.95
+
+
+def _exact_code_tensor(rng, shape, log2_step):
+    """Integer codes in [-127, 127] with a 127 in every 64-token block, times 2^log2_step: the
+    per-block quantiser returns exactly these codes with the scale 2^log2_step."""
+    codes = rng.integers(-127, 128, size=shape).astype(np.float64)
+    codes[..., ::64, 0] = 127.0
+    return (codes * 2.0 ** log2_step).astype(np.float32)
+
+
+def test_dp_int8_equals_16bit_dp_when_codes_are_exact():
+    """INT8-dP ablation ("SageAttention3 ..." (review), Table 1c): when V and dO are exactly their
+    codes times power-of-two block scales, dP = fl32(MM(dO^, V^T) fl32(s_dO s_V)) equals the 16-bit
+    product, so every gradient must come out bit for bit the same as the method's path.  A dropped
+    scale, a transposed operand or a wrong block index breaks the equality."""
+    rng = np.random.default_rng(21)
+    B, H, N, d = 1, 2, 192, 64
+    Q, K = (workloads.round_fp16(rng.standard_normal((B, H, N, d)).astype(np.float32)) for _ in range(2))
+    V = _exact_code_tensor(rng, (B, H, N, d), -3)
+    dO = _exact_code_tensor(rng, (B, H, N, d), -9)
+    for causal in (False, True):
+        a = sage.run(Q, K, V, dO, causal, workloads.round_fp16)
+        b = sage.run(Q, K, V, dO, causal, workloads.round_fp16, dp_int8=True)
+        for k in ("dQ", "dK", "dV"):
+            assert np.array_equal(a[k], b[k]), (causal, k)
+
+
+def test_dp_int8_ablation_is_less_accurate():
+    """Table 1c of "SageAttention3 ..." (review): forming dO V^T from INT8 codes (cos 97.47 %) is
+    worse than keeping it in 16 bits (cos 99.77 %).  On Gaussian inputs the oracle's INT8-dP dP
+    and dQ, dK must be further from FPA than the method's."""
+    Q, K, V, dO = _inputs(256, 64, seed=33)
+    g = fpa.fpa_backward(Q, K, V, dO, False)
+    errs = {}
+    for flag in (False, True):
+        rec = {}
+        out = sage.run(Q, K, V, dO, False, workloads.round_fp16, record=rec, dp_int8=flag)
+        errs[flag] = dict(dP=metrics.rel_l2(rec[(0, 0)]["dP"], g["dP"][0, 0]),
+                          dQ=metrics.rel_l2(out["dQ"], g["dQ"]), dK=metrics.rel_l2(out["dK"], g["dK"]))
+    assert errs[False]["dP"] < 1e-5 < errs[True]["dP"]
+    assert errs[True]["dQ"] > errs[False]["dQ"] and errs[True]["dK"] > errs[False]["dK"]
