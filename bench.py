@@ -205,7 +205,10 @@ def run_gpu(args, w: workloads.Workload):
     import ctypes
     L = sg.lib()
     ws_f = torch.empty(L.sage_fwd_workspace_bytes(ctypes.byref(p)), dtype=torch.uint8, device=device)
-    ws_b = torch.empty(L.sage_bwd_workspace_bytes(ctypes.byref(p)), dtype=torch.uint8, device=device)
+    pb = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal, smooth_q=w.smooth_q)
+    if args.dp_int8:
+        pb.flags = sg.binding.SAGE_FLAG_DP_INT8
+    ws_b = torch.empty(L.sage_bwd_workspace_bytes(ctypes.byref(pb)), dtype=torch.uint8, device=device)
     O = torch.empty((B, H, N, d), dtype=dt, device=device)
     Lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=device) for _ in range(3))
@@ -219,7 +222,8 @@ def run_gpu(args, w: workloads.Workload):
         sg.sage_attn_fwd(q, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
         if ev is not None:
             ev[2].record(stream)
-        sg.sage_attn_bwd(q, dev["V"], O, Lse, dev["dO"], causal=w.causal, grads=grads, workspace=ws_b)
+        sg.sage_attn_bwd(q, dev["V"], O, Lse, dev["dO"], causal=w.causal, grads=grads, workspace=ws_b,
+                         dp_int8=args.dp_int8)
         if ev is not None:
             ev[3].record(stream)
 
@@ -304,7 +308,8 @@ def run_gpu(args, w: workloads.Workload):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "s8 codes as f16 (f32 accumulate); dP f16", "data": "synthetic",
+        "dtype": "s8 codes as f16 (f32 accumulate); dP " + ("s8 codes (ablation)" if args.dp_int8 else "f16"),
+        "data": "synthetic",
         "config": {"workload": f"headline {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "smooth_k": True, "smooth_q": w.smooth_q,
                    "per_rank": "own batch", "l2": "inputs larger than L2 (Q,K,V,dO = 268 MB per step)"},
@@ -406,6 +411,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--dp-int8", action="store_true",
+                    help="backward with the INT8-dP ablation (dP from the dO and V codes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")

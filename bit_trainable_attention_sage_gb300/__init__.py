@@ -2,10 +2,12 @@
 
 The compute path is the C-ABI library libsage_gb300.so (include/sage.h); this package holds its
 CUDA sources (csrc/), the in-tree build (build.py) and a thin ctypes binding (binding.py) whose
-functions carry the C entry points' names.
+functions carry the C entry points' names.  ``autograd.sage_attention`` wraps the calls as a
+differentiable PyTorch operation.
 """
 from .binding import (  # noqa: F401
     Quantized, SageError, SageParams, lib, make_params, sage_attn_bwd, sage_attn_fwd,
     sage_device_status, sage_dump_bytes, sage_quantize_smooth, sage_quantize_smooth_noalloc,
     sage_status_string, sage_version,
 )
+from .autograd import SageAttentionFunction, sage_attention  # noqa: F401,E402
