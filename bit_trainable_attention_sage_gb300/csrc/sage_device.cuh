@@ -351,6 +351,42 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Packed float32 pairs (sm_100 family): one instruction rounds each lane exactly as the scalar
+// .rn instruction would, so results are bit-identical to two scalar operations.
+struct f2 {
+    float x, y;
+};
+__device__ __forceinline__ unsigned long long f2_bits(f2 a) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+__device__ __forceinline__ f2 f2_from(unsigned long long r) {
+    f2 a;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+    return a;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+    return f2_from(r);
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_from(r);
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_from(r);
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_from(r);
+}
+
 // max(a, b, c) in one instruction (two new values per instruction in a running maximum).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;

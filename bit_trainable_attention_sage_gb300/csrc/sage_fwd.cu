@@ -123,30 +123,25 @@ template <bool BIAS, bool MASKED, bool DUMP>
 __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, float rs,
                                            int nvalid, uint32_t code_col, int16_t *dump_row) {
     constexpr float kRound = 12582912.0f;          // 1.5 * 2^23
-    float sp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const f2 c2{c, c}, nrs2{-rs, -rs}, rs2{rs, rs}, k127{127.0f, 127.0f}, kr2{kRound, kRound};
+    f2 sp[2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 16) {
         uint32_t pk[8];
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
-            float x0, x1;
-            const float a0 = __uint_as_float(raw[cc + k]), a1 = __uint_as_float(raw[cc + k + 1]);
-            if (BIAS) {
-                x0 = __fsub_rn(a0, rs);
-                x1 = __fsub_rn(a1, rs);
-            } else {
-                x0 = __fmaf_rn(a0, c, -rs);
-                x1 = __fmaf_rn(a1, c, -rs);
-            }
+            // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
+            const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
+            f2 x2 = BIAS ? sub2(a2, rs2) : fma2(a2, c2, nrs2);
             if (MASKED) {
-                x0 = (cc + k < nvalid) ? x0 : -INFINITY;
-                x1 = (cc + k + 1 < nvalid) ? x1 : -INFINITY;
+                x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
+                x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
             }
-            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-            sp[k & 3] += e0;
-            sp[(k + 1) & 3] += e1;
-            const float p0 = __fsub_rn(__fadd_rn(__fmul_rn(127.0f, e0), kRound), kRound);
-            const float p1 = __fsub_rn(__fadd_rn(__fmul_rn(127.0f, e1), kRound), kRound);
+            const f2 e2{ex2_approx(x2.x), ex2_approx(x2.y)};
+            sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e2);
+            const f2 p2 = sub2(add2(mul2(k127, e2), kr2), kr2);
+            const float e0 = e2.x, e1 = e2.y, p0 = p2.x, p1 = p2.y;
+            (void)e0; (void)e1;
             pk[k / 2] = pack_half2(p0, p1);
             if (DUMP && dump_row) {
                 dump_row[cc + k] = static_cast<int16_t>(p0);
@@ -155,7 +150,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
         }
         tmem_st8(code_col + cc / 2, pk);
     }
-    return (sp[0] + sp[1]) + (sp[2] + sp[3]);
+    return (sp[0].x + sp[1].x) + (sp[0].y + sp[1].y);
 }
 
 template <int D, typename OutT, bool BIAS, bool DUMP>
