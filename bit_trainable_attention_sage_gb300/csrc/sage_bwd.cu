@@ -139,7 +139,8 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
 // Values x * inv lie in [-127, 127], so x * inv + 1536 lies in [1024, 2048) where fp16 spacing is
 // 1: the fp16 conversion rounds to an integer and the subtraction is exact.
 __device__ __forceinline__ uint32_t codes2(float x0, float x1, float inv) {
-    const float y0 = __fmaf_rn(x0, inv, 1536.0f), y1 = __fmaf_rn(x1, inv, 1536.0f);
+    const f2 y = fma2(f2{x0, x1}, f2{inv, inv}, f2{1536.0f, 1536.0f});
+    const float y0 = y.x, y1 = y.y;
     uint32_t r;
     // cvt packs its first source into the upper half; 0x6600 is 1536 in fp16
     asm("{\n\t.reg .b32 t;\n\t"
@@ -178,17 +179,26 @@ __device__ __forceinline__ void score_p_ds_8(const uint32_t (&sr)[8], const uint
                                              const RowData8 &rd, int col0, float cq, float bias,
                                              int qlo, bool key_ok, float dps, float (&pv)[8],
                                              float (&ds)[8]) {
+    // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
+    const f2 cq2{cq, cq}, b2{bias, bias}, dps2{dps, dps};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float acc = __uint_as_float(sr[k]);
-        float x;
-        if (BIAS) x = __fsub_rn(__fmaf_rn(acc, cq, bias), rd.l2[k]);
-        else x = __fmaf_rn(acc, cq, -rd.l2[k]);
-        if (EDGE) x = (key_ok && col0 + k >= qlo) ? x : -INFINITY;   // ex2(-inf) = +0: P = 0, dS = +-0
-        pv[k] = ex2_approx(x);
+    for (int k = 0; k < 8; k += 2) {
+        const f2 acc{__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])};
+        const f2 l2{rd.l2[k], rd.l2[k + 1]};
+        f2 x = BIAS ? sub2(fma2(acc, cq2, b2), l2) : fma2(acc, cq2, f2{-l2.x, -l2.y});
+        if (EDGE) {                                    // ex2(-inf) = +0: P = 0, dS = +-0
+            x.x = (key_ok && col0 + k >= qlo) ? x.x : -INFINITY;
+            x.y = (key_ok && col0 + k + 1 >= qlo) ? x.y : -INFINITY;
+        }
+        const f2 p{ex2_approx(x.x), ex2_approx(x.y)};
         // DP8: dP = fl32(integer product * fl32(s_dO s_V))
-        const float dp = DP8 ? __fmul_rn(__uint_as_float(dr[k]), dps) : __uint_as_float(dr[k]);
-        ds[k] = __fmul_rn(pv[k], __fsub_rn(dp, rd.dd[k]));
+        f2 dp{__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])};
+        if (DP8) dp = mul2(dp, dps2);
+        const f2 d = mul2(p, sub2(dp, f2{rd.dd[k], rd.dd[k + 1]}));
+        pv[k] = p.x;
+        pv[k + 1] = p.y;
+        ds[k] = d.x;
+        ds[k + 1] = d.y;
     }
 }
 
@@ -284,6 +294,14 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
         tmem_ld8(lane_base + R_A + 32 * half + r0, v0);
         tmem_ld8(lane_base + R_A + 64 + 32 * half + r0, v1);
         tmem_wait_ld_regs(v0, v1);
+        float dq[8];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const f2 t = fma2(f2{sg1, sg1}, f2{__uint_as_float(v1[k]), __uint_as_float(v1[k + 1])},
+                              mul2(f2{sg0, sg0}, f2{__uint_as_float(v0[k]), __uint_as_float(v0[k + 1])}));
+            dq[k] = t.x;
+            dq[k + 1] = t.y;
+        }
         if (r0 + 8 == 32) {
             // every TMEM read of this warpgroup is done: R_A may be refilled
             tc_fence_before();
@@ -292,7 +310,7 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            red_add(dst + (r0 + k) * 128, __fmaf_rn(sg1, __uint_as_float(v1[k]), __fmul_rn(sg0, __uint_as_float(v0[k]))));
+            red_add(dst + (r0 + k) * 128, dq[k]);
     }
 }
 
@@ -639,7 +657,12 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
                 tmem_ld8(lane_base + R_A + cc, r);
                 tmem_wait_ld_regs(r);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) dv[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dv[cc + k]);
+                for (int k = 0; k < 8; k += 2) {
+                    const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(r[k]), __uint_as_float(r[k + 1])},
+                                      f2{dv[cc + k], dv[cc + k + 1]});
+                    dv[cc + k] = t.x;
+                    dv[cc + k + 1] = t.y;
+                }
             }
         }
         tc_fence_before();
@@ -744,7 +767,12 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
                 tmem_ld8(lane_base + R_B + cc, r);
                 tmem_wait_ld_regs(r);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) dk[cc + k] = __fmaf_rn(sc, __uint_as_float(r[k]), dk[cc + k]);
+                for (int k = 0; k < 8; k += 2) {
+                    const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(r[k]), __uint_as_float(r[k + 1])},
+                                      f2{dk[cc + k], dk[cc + k + 1]});
+                    dk[cc + k] = t.x;
+                    dk[cc + k + 1] = t.y;
+                }
             }
         }
         if (BIAS) {
