@@ -90,7 +90,7 @@ struct Smem {
     alignas(1024) uint8_t doc[2][D / 64][64 * 128];    // dO blocks (16-bit input type)
     alignas(1024) uint8_t dohc[D / 64][64 * 128];      // dO^ codes block
     alignas(1024) uint8_t dss[2][128 * 128];           // dS^ codes [step % 2][key][64 q], 128-byte rows
-    alignas(16) float L2s[3][64];                      // [stage][q]: fl32(L log2 e)
+    alignas(16) float L2s[3][64];                      // [stage][q]: -fl32(L log2 e), negated
     alignas(16) float Ds[3][64];                       // [stage][q]: D
     float red[4][2][2];                                // [warp][step parity][P max, |dS| max]
     float sps[kScaleSlots][2];                         // [step % 8][key block] P tile scales
@@ -158,7 +158,7 @@ __device__ __forceinline__ int16_t code_hi(uint32_t w) {
     return static_cast<int16_t>(__half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
 }
 
-// Row data of 8 query columns (L2 = fl32(L log2 e) and D), loaded ahead of use: the MMAs read
+// Row data of 8 query columns (-L2 = -fl32(L log2 e) and D), loaded ahead of use: the MMAs read
 // their operands from shared memory at a high rate, so a shared-memory load waited for at once
 // would stall the score warps.
 struct RowData8 {
@@ -185,7 +185,9 @@ __device__ __forceinline__ void score_p_ds_8(const uint32_t (&sr)[8], const uint
     for (int k = 0; k < 8; k += 2) {
         const f2 acc{__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])};
         const f2 l2{rd.l2[k], rd.l2[k + 1]};
-        f2 x = BIAS ? sub2(fma2(acc, cq2, b2), l2) : fma2(acc, cq2, f2{-l2.x, -l2.y});
+        // the row data holds -L2: x = fl32(acc c - L2) is one fused multiply-add, and
+        // fl32(t - L2) = fl32(t + (-L2)) exactly
+        f2 x = BIAS ? add2(fma2(acc, cq2, b2), l2) : fma2(acc, cq2, l2);
         if (EDGE) {                                    // ex2(-inf) = +0: P = 0, dS = +-0
             x.x = (key_ok && col0 + k >= qlo) ? x.x : -INFINITY;
             x.y = (key_ok && col0 + k + 1 >= qlo) ? x.y : -INFINITY;

@@ -375,11 +375,19 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     tmem_ld16(lane_base + 128 + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
                     tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
                     tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
+                    // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const f2 pv2{__uint_as_float(raw[k]), __uint_as_float(raw[k + 1])};
+                        const f2 o2{o[cc + k], o[cc + k + 1]};
+                        const f2 r2 = (h == 0) ? fma2(f2{alpha, alpha}, o2, mul2(f2{cpv[0], cpv[0]}, pv2))
+                                               : fma2(f2{cpv[1], cpv[1]}, pv2, o2);
+                        o[cc + k] = r2.x;
+                        o[cc + k + 1] = r2.y;
+                    }
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const float pv = __uint_as_float(raw[k]);
-                        o[cc + k] = (h == 0) ? __fmaf_rn(alpha, o[cc + k], cpv[0] * pv)
-                                             : __fmaf_rn(cpv[1], pv, o[cc + k]);
                         if (DUMP) {
                             if (grow < N)
                                 a.dump_pv[(((static_cast<size_t>(bh) * nblk + qblk) * nblk + 2 * j + h) * 64 + (grow & 63)) * D + cc + k] =

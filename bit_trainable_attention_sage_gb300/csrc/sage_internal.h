@@ -32,7 +32,7 @@ struct QuantArgs {
 struct BwdPrologueArgs {
     const void *dO, *O;
     const float *L;    // (B,H,N) log-sum-exp from the forward
-    float *L2;         // (B,H,N) fl32(L * log2 e), read by the backward kernel
+    float *L2;         // (B,H,N) -fl32(L * log2 e) (negated), read by the backward kernel
     float *D;          // (B,H,N)
     __half *dO16;      // (B,H,N,d) integer-valued fp16 codes of dO
     int8_t *dOh;       // optional int8 codes of dO (debug dump), may be NULL
@@ -54,7 +54,7 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-    const float *sQ, *sK, *sdO, *D, *L2;   // D and L2 = fl32(L log2 e): (B,H,N), from the prologue
+    const float *sQ, *sK, *sdO, *D, *L2;   // D and -fl32(L log2 e) (negated): (B,H,N), from the prologue
     const float *sV;      // (B,H,N/64) V block scales (SAGE_FLAG_DP_INT8 only), else NULL
     const float *qbias;   // (B,H,N/64,N) or NULL
     const float *muQ;     // (B,H,N/64,d) or NULL (Q-smoothing dK bias term)

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(BwdPrologueArgs a) {
         if (cv == 0) {
             const size_t row = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r;
             a.D[row] = part;
-            a.L2[row] = __fmul_rn(a.L[row], kLog2e);
+            a.L2[row] = -__fmul_rn(a.L[row], kLog2e);     // stored negated: -fl32(L log2 e)
         }
     }
     mx = block_max_256(mx, red);
