@@ -38,6 +38,14 @@ Readings where the pages are silent, garbled or at odds (listed again in DESIGN.
 Where float decides an integer code (P^, dS^), the decision is taken in float32 as the kernel
 does; everything that only accumulates (m, l, O, dV, dQ, dK, D) is float64.
 
+FP8 variant (``QUANTISED_FP8``; "SageAttention3 ..." (review), "INT8 vs FP8 training"): every
+INT8 code becomes an E4M3 code with 448 in place of 127 (see oracle.quant): block scales
+fl32(max|x|/448); forward P^_k = e4m3_round(fl32(448 * fl32(2^x_k))), s_P = 2^(r - m)/448;
+backward tile codes e4m3_round(fl32(x * fl32(1/s))), s = fl32(max|x|/448), a tile whose max|x|
+is below 2^-110 being a zero tile (1/s stays finite).  Block products of E4M3 values are exact in
+float64: each product is a multiple of 2^-18 below 2^18, a sum of at most 128 of them stays
+below 2^25, so 43 bits suffice.
+
 The ``DEQUANTISED`` arithmetic replaces every quantiser by the identity and drops every float32
 rounding; the very same tiled code must then equal float64 full-precision attention, which pins
 the tiling, the online-softmax bookkeeping, L and the backward structure (tests/test_oracle_sage.py).
@@ -48,7 +56,7 @@ import math
 
 import numpy as np
 
-from .quant import BLOCK, quantize_per_block, quantize_smooth, k_mean, q_block_mean
+from .quant import BLOCK, QMAX, e4m3_round, quantize_per_block, quantize_smooth, k_mean, q_block_mean
 
 LOG2E = 1.4426950408889634      # log2(e), the double nearest 1/ln(2)
 LN2 = 0.6931471805599453
@@ -56,13 +64,16 @@ F32 = np.float32
 # R8b: a backward P / dS tile whose max|x| is below 2^-120 is a zero tile (s = 0, q = 0); below
 # that bound the float32 reciprocal 1/s of its scale would overflow.
 TILE_ZERO_BELOW = np.float32(2.0 ** -120)
+TILE_ZERO_BELOW_FP8 = np.float32(2.0 ** -110)     # the same bound for s = max|x| / 448
 
 
 class Arith:
     """The arithmetic of the quantisation steps: SageBwd's (quantised) or the identity limit."""
 
-    def __init__(self, quantised: bool):
+    def __init__(self, quantised: bool, fmt: str = "int8"):
         self.quantised = quantised
+        self.fmt = fmt                  # code format: "int8" or "e4m3"
+        self.qmax = QMAX[fmt]           # 127 or 448
 
     # -- plain float helpers --------------------------------------------------------------
     def r32(self, x):
@@ -79,9 +90,13 @@ class Arith:
 
     # -- exact integer block products ------------------------------------------------------
     def int_mm(self, a, b):
-        """MM(A^, B^): exact for integer codes (every partial sum is far below 2^53)."""
+        """MM(A^, B^): exact for integer codes (every partial sum is far below 2^53) and for E4M3
+        codes (multiples of 2^-18 below 2^25: checked)."""
         p = np.asarray(a, np.float64) @ np.asarray(b, np.float64)
         if not self.quantised:
+            return p
+        if self.fmt == "e4m3":
+            assert np.array_equal(np.rint(p * 2.0 ** 18), p * 2.0 ** 18), "E4M3 block product not exact"
             return p
         r = np.rint(p)
         assert np.array_equal(r, p), "integer block product is not integral"
@@ -126,7 +141,7 @@ class Arith:
     def block_quant(self, x):
         """Per-64-token-block quantiser of Q, K, V, dO (see oracle.quant)."""
         if self.quantised:
-            return quantize_per_block(x)
+            return quantize_per_block(x, fmt=self.fmt)
         x = np.asarray(x, np.float64)
         return x, np.ones(x.shape[:-2] + (x.shape[-2] // BLOCK,))
 
@@ -137,6 +152,8 @@ class Arith:
         if not self.quantised:
             return e64, 127.0 * e64
         e32 = e64.astype(np.float32)
+        if self.fmt == "e4m3":
+            return e64, e4m3_round(F32(448) * e32)
         return e64, np.clip(np.rint(F32(127) * e32), 0, 127).astype(np.int64)
 
     def tile_quant(self, x):
@@ -145,6 +162,12 @@ class Arith:
             return 1.0, np.asarray(x, np.float64)
         x = np.asarray(x, np.float32)
         mx = np.max(np.abs(x)) if x.size else F32(0)
+        if self.fmt == "e4m3":
+            if mx < TILE_ZERO_BELOW_FP8:
+                return F32(0), np.zeros(x.shape)
+            s = F32(mx) / F32(448)
+            inv = F32(1) / s
+            return s, e4m3_round(x * inv)          # float32 product, one rounding, then E4M3
         if mx < TILE_ZERO_BELOW:
             return F32(0), np.zeros(x.shape, np.int64)
         s = F32(mx) / F32(127)
@@ -162,13 +185,14 @@ class Arith:
 
 
 QUANTISED = Arith(True)
+QUANTISED_FP8 = Arith(True, fmt="e4m3")
 DEQUANTISED = Arith(False)
 
 
 def prepare(Q, K, V, smooth_k: bool = True, smooth_q: bool = False, arith: Arith = QUANTISED) -> dict:
     """Steps a1 + a2 in the chosen arithmetic: K-mean, smoothing and the per-block quantisers."""
     if arith.quantised:
-        return quantize_smooth(Q, K, V, smooth_k=smooth_k, smooth_q=smooth_q)
+        return quantize_smooth(Q, K, V, smooth_k=smooth_k, smooth_q=smooth_q, fmt=arith.fmt)
     Q = np.asarray(Q, np.float64)
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
@@ -204,8 +228,8 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
     """SageBwd forward (steps a3-a6).  Returns (O float64 (B,H,N,d), L float64 (B,H,N)).
 
     ``q_blocks`` limits the query blocks computed (others stay zero), ``heads`` the (b, h) pairs.
-    ``record`` (small N only) receives, per head, the integer S products, the P^ codes and the
-    integer P^ V^ products of every tile.
+    ``record`` (small N only) receives, per head, the S block products, the P^ codes and the
+    P^ V^ block products of every tile (integers for INT8 codes, float64 for E4M3).
     """
     Qh, Kh, Vh = prep["Qh"], prep["Kh"], prep["Vh"]
     sQ, sK, sV = prep["sQ"], prep["sK"], prep["sV"]
@@ -219,8 +243,9 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
     for (b, h) in heads:
         if record is not None:
             rec = record.setdefault((b, h), {})
-            rec["S_int"] = np.zeros((N, N), np.int64)
-            rec["P_hat"] = np.zeros((N, N), np.int64)
+            rtype = np.int64 if arith.fmt == "int8" else np.float64
+            rec["S_int"] = np.zeros((N, N), rtype)
+            rec["P_hat"] = np.zeros((N, N), rtype)
             rec["PV_int"] = {}
         for i in (range(T) if q_blocks is None else q_blocks):
             rows = slice(i * BLOCK, (i + 1) * BLOCK)
@@ -245,7 +270,7 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
                 e64, p_hat = arith.token_quant(x)
                 alpha = np.exp2(m - m_new)
                 grow = np.exp2(r.astype(np.float64) - m_new)
-                s_p = grow / 127.0
+                s_p = grow / arith.qmax
                 l = alpha * l + grow * e64.sum(axis=1)
                 # (5) O_ij = diag(e^{m_old - m_new}) O + MM(P^_ij, V^_j) * s_P * s_V
                 pv = arith.int_mm(p_hat, Vh[b, h, cols])
@@ -274,6 +299,8 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
     checks at large N); by default everything is computed, looping over key/value blocks and,
     inside, query blocks.  ``record`` receives the per-tile dequantised P, dP, dequantised dS.
     """
+    if dp_int8 and arith.fmt != "int8":
+        raise ValueError("the INT8-dP ablation applies to INT8 codes only")
     Qh, Kh = prep["Qh"], prep["Kh"]
     sQ, sK = prep["sQ"], prep["sK"]
     B, H, N, d = Qh.shape

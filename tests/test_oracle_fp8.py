@@ -1,0 +1,196 @@
+"""Pins of the oracle's FP8 (E4M3) SageBwd variant, independent of the oracle's own arithmetic.
+
+"SageAttention3 ..." (review), "INT8 vs FP8 training": SageBwd with FP8 codes instead of INT8
+(dQ L1 error 0.0696 against 0.0290 for INT8).  The code format is E4M3 of the OCP 8-bit
+floating-point format: sign bit, 4 exponent bits with bias 7, 3 mantissa bits, subnormals below
+2^-6, largest finite value 448, the all-ones exponent-and-mantissa patterns NaN.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction as Fr
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import fpa, metrics, quant, sage
+from tests.exact import fl32
+
+
+def _grid():
+    """(values, patterns) of the 127 non-negative finite E4M3 values, by pattern 0x00..0x7E."""
+    pats = np.arange(0x7F, dtype=np.uint8)
+    return quant.e4m3_decode(pats), pats
+
+
+def _nearest_brute(y):
+    """Nearest finite E4M3 value to each float by search over the grid, ties to the even pattern
+    (even mantissa); values beyond the grid land on its last point, 448."""
+    vals, pats = _grid()
+    y = np.asarray(y, np.float64).ravel()
+    dist = np.abs(np.abs(y)[:, None] - vals[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    tie = dist == best
+    # among the (at most two) nearest points prefer the even pattern
+    score = np.where(tie, 2 - (pats[None, :] % 2 == 0), 9)
+    pick = vals[np.argmin(score, axis=1)]
+    return np.copysign(pick, y)
+
+
+def test_decode_known_patterns():
+    d = quant.e4m3_decode(np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0x39, 0x7E, 0x80, 0xB8, 0xFE], np.uint8))
+    assert d.tolist() == [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 1.125, 448.0, -0.0, -1.0, -448.0]
+    assert np.isnan(quant.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    vals, _ = _grid()
+    assert (np.diff(vals) > 0).all()                  # patterns 0x00..0x7E increase strictly
+    # every step inside a binade is that binade's quantum 2^(e-3); subnormals step by 2^-9
+    steps = np.diff(vals)
+    assert set(steps[:8].tolist()) == {2.0 ** -9}
+    assert steps[-1] == 32.0                          # 416 -> 448
+
+
+def test_encode_round_trips_every_finite_pattern():
+    pats = np.array([p for p in range(256) if p not in (0x7F, 0xFF)], np.uint8)
+    assert np.array_equal(quant.e4m3_encode(quant.e4m3_decode(pats)), pats)
+
+
+def test_rounding_against_brute_force_nearest():
+    vals, _ = _grid()
+    mids = (vals[1:] + vals[:-1]) / 2                 # every tie point
+    rng = np.random.default_rng(7)
+    y = np.concatenate([
+        vals, mids, np.nextafter(mids, 0), np.nextafter(mids, 1000),
+        np.exp2(rng.uniform(-12, 9.5, 20000)),         # across the whole range, and beyond 448
+        [448.0, 460.0, 464.0, 470.0, 1e6, 2.0 ** -10, 2.0 ** -11],
+    ])
+    y = np.concatenate([y, -y]).astype(np.float32).astype(np.float64)
+    assert np.array_equal(quant.e4m3_round(y), _nearest_brute(y))
+
+
+def test_rounding_hand_worked():
+    """1.0625 lies halfway between 1 (mantissa 0) and 1.125 (mantissa 1): even -> 1.
+    1.1875 between 1.125 (1) and 1.25 (2): -> 1.25.  2^-10 between 0 and 2^-9: -> 0.
+    3 2^-10 between 2^-9 (1) and 2^-8 (2): -> 2^-8.  15.9 rounds up into the next binade: 16.
+    500 saturates to 448."""
+    y = [1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 15.9, 500.0, -0.3]
+    assert quant.e4m3_round(y).tolist() == [1.0, 1.25, 0.0, 2.0 ** -8, 16.0, 448.0, -0.3125]
+
+
+def test_block_quantiser_hand_worked():
+    """delta = fl32(1/448); 0.3 * 448 = 134.4 -> 128 (quantum 16 in [128, 256)),
+    -0.7 * 448 = -313.6 -> -320 (quantum 32), 0.05 * 448 = 22.4 -> 22 (quantum 2), 1 -> 448."""
+    x = np.array([[1.0, 0.3, -0.7, 0.05]], np.float32)
+    q, delta = quant.quantize_block(x, "e4m3")
+    assert Fr(float(delta)) == fl32(Fr(1) / 448)
+    assert q.tolist() == [[448.0, 128.0, -320.0, 22.0]]
+    q0, d0 = quant.quantize_block(np.zeros((4, 4), np.float32), "e4m3")
+    assert d0 == 0 and not q0.any()
+
+
+def test_block_quantiser_against_exact_rationals():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((64, 16)) * 3.0).astype(np.float32)
+    q, delta = quant.quantize_block(x, "e4m3")
+    mx = max(abs(Fr(float(v))) for v in x.ravel())
+    de = fl32(mx / 448)
+    assert Fr(float(delta)) == de
+    want = _nearest_brute([float(fl32(Fr(float(v)) / de)) for v in x.ravel()])
+    assert np.array_equal(q.ravel().astype(np.float64), want)
+
+
+def test_block_products_exact():
+    """Float64 block products of E4M3 values equal the exact rational sums."""
+    rng = np.random.default_rng(8)
+    vals, _ = _grid()
+    a = rng.choice(np.concatenate([vals, -vals]), size=(4, 128))
+    b = rng.choice(np.concatenate([vals, -vals]), size=(128, 3))
+    p = sage.QUANTISED_FP8.int_mm(a, b)
+    for i in range(4):
+        for j in range(3):
+            assert Fr(float(p[i, j])) == sum(Fr(float(a[i, k])) * Fr(float(b[k, j])) for k in range(128))
+    # the extreme: 448^2 over a 128-long contraction
+    big = np.full((2, 128), 448.0)
+    assert sage.QUANTISED_FP8.int_mm(big, big.T)[0, 0] == 128 * 448 * 448
+
+
+def test_tile_quantiser_fp8():
+    rng = np.random.default_rng(9)
+    for scale in (1.0, 1e-6, 1e-33):
+        x = (rng.standard_normal((64, 64)) * scale).astype(np.float32)
+        s, q = sage.QUANTISED_FP8.tile_quant(x)
+        mx = max(abs(Fr(float(v))) for v in x.ravel())
+        if mx < Fr(2) ** -110:
+            assert s == 0 and not q.any()
+            continue
+        se = fl32(mx / 448)
+        inv = fl32(1 / se)
+        assert Fr(float(s)) == se
+        want = _nearest_brute([float(fl32(Fr(float(v)) * inv)) for v in x.ravel()])
+        assert np.array_equal(np.asarray(q, np.float64).ravel(), want)
+        assert np.abs(q).max() == 448.0
+
+
+def test_token_quantiser_fp8():
+    """P^ = e4m3(fl32(448 2^x)): 448; 224; 448/sqrt(2) = 316.8 -> 320; 0 for -inf."""
+    x = np.array([[0.0, -1.0, -0.5, -np.inf]], np.float32)
+    _, q = sage.QUANTISED_FP8.token_quant(x)
+    assert q.tolist() == [[448.0, 224.0, 320.0, 0.0]]
+
+
+def _inputs(N, d, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    Q, K, V, dO = (rng.standard_normal((1, 1, N, d)).astype(np.float32) * s
+                   for s in (scale, scale, 1.0, 1.0))
+    r = workloads.round_fp16
+    return r(Q), r(K), r(V), r(dO)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_closed_form(causal):
+    """O_i = sum_j 2^(r_ij - M_i) (s_V,j / 448) P^_ij V^_j / sum_j 2^(r_ij - M_i) sum_k 2^(x_ijk),
+    with P^ the nearest E4M3 value to fl32(448 fl32(2^x)) (brute-force search here), evaluated
+    row by row without tiling."""
+    N, d = 256, 64
+    Q, K, V, _ = _inputs(N, d, seed=12, scale=2.0)
+    prep = sage.prepare(Q, K, V, arith=sage.QUANTISED_FP8)
+    O, _ = sage.sage_forward(prep, causal, arith=sage.QUANTISED_FP8)
+    Qh, Kh, Vh, sQ, sK, sV = (prep[k][0, 0] for k in ("Qh", "Kh", "Vh", "sQ", "sK", "sV"))
+    T = N // 64
+    sl2 = np.float32(sage.LOG2E / math.sqrt(d))
+    acc = Qh.astype(np.float64) @ Kh.astype(np.float64).T
+    c = ((np.repeat(sQ, 64)[:, None] * np.repeat(sK, 64)[None, :]).astype(np.float32) * sl2).astype(np.float64)
+    valid = ~np.triu(np.ones((N, N), bool), 1) if causal else np.ones((N, N), bool)
+    accj, cj, vj = acc.reshape(N, T, 64), c.reshape(N, T, 64)[:, :, 0], valid.reshape(N, T, 64)
+    live = vj.any(axis=2)
+    amax = np.where(vj, accj, -np.inf).max(axis=2)
+    r = np.where(live, (np.where(live, amax, 0) * cj).astype(np.float32), -np.inf)
+    x = np.where(vj, (accj * cj[:, :, None] - np.where(live, r, 0)[:, :, None]).astype(np.float32), -np.inf)
+    e64 = np.exp2(x.astype(np.float64))
+    p_hat = _nearest_brute(np.float32(448) * e64.astype(np.float32)).reshape(N, T, 64)
+    r64 = r.astype(np.float64)
+    w = np.where(live, np.exp2(np.where(live, r64, 0.0) - r64.max(axis=1)[:, None]), 0.0)
+    num = sum((w[:, j] / 448.0 * sV[j])[:, None] * (p_hat[:, j, :] @ Vh[64 * j:64 * j + 64].astype(np.float64))
+              for j in range(T))
+    den = (w * e64.sum(axis=2)).sum(axis=1)
+    assert metrics.rel_l2(O[0, 0], num / den[:, None]) < 1e-12
+
+
+def test_fp8_is_less_accurate_than_int8():
+    """The pages' comparison: INT8 SageBwd gradients are closer to full precision than FP8 ones
+    (dQ L1 0.0290 vs 0.0696, dK 0.0317 vs 0.0999, dV 0.0423 vs 0.0873).  On Gaussian inputs the
+    oracle's FP8 variant must be further from FPA in O, dQ, dK and dV."""
+    Q, K, V, dO = _inputs(256, 64, seed=34)
+    O_ref, _, _ = fpa.fpa_forward(Q, K, V, False)
+    g = fpa.fpa_backward(Q, K, V, dO, False)
+    errs = {}
+    for ar in (sage.QUANTISED, sage.QUANTISED_FP8):
+        out = sage.run(Q, K, V, dO, False, workloads.round_fp16, arith=ar)
+        errs[ar.fmt] = [metrics.rel_l2(out["O"], O_ref)] + [metrics.rel_l2(out[k], g[k]) for k in ("dQ", "dK", "dV")]
+    assert all(f > i for f, i in zip(errs["e4m3"], errs["int8"])), errs
+
+
+def test_dp_int8_with_fp8_codes_is_refused():
+    Q, K, V, dO = _inputs(64, 64, seed=1)
+    with pytest.raises(ValueError):
+        sage.run(Q, K, V, dO, False, workloads.round_fp16, arith=sage.QUANTISED_FP8, dp_int8=True)
