@@ -201,13 +201,14 @@ def run_gpu(args, w: workloads.Workload):
     B, H, N, d = w.B, w.H, w.N, w.d
 
     # outputs and workspaces allocated once (the library allocates nothing)
-    p = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal)
+    p = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal, fp8=args.fp8)
     import ctypes
     L = sg.lib()
     ws_f = torch.empty(L.sage_fwd_workspace_bytes(ctypes.byref(p)), dtype=torch.uint8, device=device)
-    pb = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal, smooth_q=w.smooth_q)
+    pb = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal, smooth_q=w.smooth_q,
+                        fp8=args.fp8)
     if args.dp_int8:
-        pb.flags = sg.binding.SAGE_FLAG_DP_INT8
+        pb.flags |= sg.binding.SAGE_FLAG_DP_INT8
     ws_b = torch.empty(L.sage_bwd_workspace_bytes(ctypes.byref(pb)), dtype=torch.uint8, device=device)
     O = torch.empty((B, H, N, d), dtype=dt, device=device)
     Lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
@@ -216,7 +217,7 @@ def run_gpu(args, w: workloads.Workload):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q)
+        q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q, fp8=args.fp8)
         if ev is not None:
             ev[1].record(stream)
         sg.sage_attn_fwd(q, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
@@ -308,7 +309,8 @@ def run_gpu(args, w: workloads.Workload):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "s8 codes as f16 (f32 accumulate); dP " + ("s8 codes (ablation)" if args.dp_int8 else "f16"),
+        "dtype": ("e4m3" if args.fp8 else "s8") + " codes as f16 (f32 accumulate); dP "
+                 + ("s8 codes (ablation)" if args.dp_int8 else "f16"),
         "data": "synthetic",
         "config": {"workload": f"headline {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "smooth_k": True, "smooth_q": w.smooth_q,
@@ -413,6 +415,8 @@ def main():
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--dp-int8", action="store_true",
                     help="backward with the INT8-dP ablation (dP from the dO and V codes)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="the FP8 SageBwd variant (E4M3 codes in place of INT8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")

@@ -20,6 +20,7 @@ SAGE_ERR_CUDA, SAGE_ERR_TIMEOUT, SAGE_ERR_WORKSPACE = 4, 5, 6
 SAGE_FP16, SAGE_BF16 = 0, 1
 SAGE_FLAG_DUMP = 1
 SAGE_FLAG_DP_INT8 = 2
+SAGE_FLAG_FP8 = 4
 
 EXPORTED = (
     "sage_quantize_workspace_bytes", "sage_quantize_smooth", "sage_fwd_workspace_bytes",
@@ -103,10 +104,12 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_params(B: int, H: int, N: int, d: int, dtype: int, causal: bool, smooth_k: bool = True,
-                smooth_q: bool = False, dump: torch.Tensor | None = None) -> SageParams:
+                smooth_q: bool = False, dump: torch.Tensor | None = None, fp8: bool = False) -> SageParams:
     p = SageParams(B, H, N, d, dtype, int(causal), int(smooth_k), int(smooth_q), 0, None, 0)
+    if fp8:
+        p.flags |= SAGE_FLAG_FP8
     if dump is not None:
-        p.flags = SAGE_FLAG_DUMP
+        p.flags |= SAGE_FLAG_DUMP
         p.dump = dump.data_ptr()
         p.dump_bytes = dump.numel() * dump.element_size()
     return p
@@ -126,7 +129,9 @@ def _workspace(nbytes: int, device) -> torch.Tensor | None:
 
 @dataclass
 class Quantized:
-    """The quantised forward inputs (codes, scales, means) and the problem description."""
+    """The quantised forward inputs (codes, scales, means) and the problem description.
+    With ``fp8`` the int8 code tensors hold FP8 E4M3 bit patterns (SAGE_FLAG_FP8), and the
+    forward and backward calls on this object run the FP8 variant."""
     Qh: torch.Tensor
     Kh: torch.Tensor
     Vh: torch.Tensor
@@ -138,16 +143,18 @@ class Quantized:
     dtype: int
     smooth_k: bool
     smooth_q: bool
+    fp8: bool = False
 
 
 def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, smooth_k: bool = True,
-                         smooth_q: bool = False, stream=None) -> Quantized:
-    """K-smoothing (+ optional Q-smoothing) and per-block INT8 quantisation of (B,H,N,d) Q, K, V."""
+                         smooth_q: bool = False, fp8: bool = False, stream=None) -> Quantized:
+    """K-smoothing (+ optional Q-smoothing) and per-block INT8 (``fp8``: E4M3) quantisation of
+    (B,H,N,d) Q, K, V."""
     _require_cuda(Q, K, V)
     B, H, N, d = Q.shape
     dt = _dtype_code(Q)
     dev = Q.device
-    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q)
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
     Qh = torch.empty((B, H, N, d), dtype=torch.int8, device=dev)
     Kh, Vh = torch.empty_like(Qh), torch.empty_like(Qh)
     sQ = torch.empty((B, H, N // 64), dtype=torch.float32, device=dev)
@@ -161,7 +168,7 @@ def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, s
                                 _ptr(sQ), _ptr(sK), _ptr(sV), _ptr(muK), _ptr(muQ), _ptr(ws), nws,
                                 _stream(stream))
     _check("sage_quantize_smooth", st)
-    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q)
+    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8)
 
 
 def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,
@@ -171,7 +178,7 @@ def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,
     """SageBwd forward.  Returns (O (B,H,N,d) in the input dtype, L (B,H,N) float32)."""
     B, H, N, d = q.Qh.shape
     dev = q.Qh.device
-    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump)
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump, q.fp8)
     odt = torch.float16 if q.dtype == SAGE_FP16 else torch.bfloat16
     O = torch.empty((B, H, N, d), dtype=odt, device=dev) if out is None else out
     Lse = torch.empty((B, H, N), dtype=torch.float32, device=dev) if lse is None else lse
@@ -195,7 +202,7 @@ def sage_attn_bwd(q: Quantized, V: torch.Tensor, O: torch.Tensor, L: torch.Tenso
     _require_cuda(V, O, L, dO, K)
     B, H, N, d = q.Qh.shape
     dev = q.Qh.device
-    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump)
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump, q.fp8)
     if dp_int8:
         p.flags |= SAGE_FLAG_DP_INT8
     if grads is None:
@@ -231,8 +238,8 @@ def sage_status_string(status: int) -> str:
 
 
 def sage_quantize_smooth_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *,
-                                 smooth_k: bool = True, smooth_q: bool = False, out=None,
-                                 stream=None) -> Quantized:
+                                 smooth_k: bool = True, smooth_q: bool = False, fp8: bool = False,
+                                 out=None, stream=None) -> Quantized:
     """sage_quantize_smooth for callers that cannot allocate device memory while they run: the
     K-mean scratch lives in a fixed array inside the library.  ``out`` (a Quantized whose tensors
     the caller allocated beforehand) receives the results; without it they are allocated here."""
@@ -246,12 +253,12 @@ def sage_quantize_smooth_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
         out = Quantized(Qh, torch.empty_like(Qh), torch.empty_like(Qh), sQ, torch.empty_like(sQ),
                         torch.empty_like(sQ), torch.empty((B, H, d), dtype=torch.float32, device=dev),
                         torch.empty((B, H, N // 64, d), dtype=torch.float32, device=dev) if smooth_q else None,
-                        dt, smooth_k, smooth_q)
+                        dt, smooth_k, smooth_q, fp8)
     L = lib()
     fn = L.sage_quantize_smooth_noalloc
     fn.argtypes = [ctypes.POINTER(SageParams)] + [ctypes.c_void_p] * 12
     fn.restype = ctypes.c_int
-    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q)
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
     st = fn(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(out.Qh), _ptr(out.Kh), _ptr(out.Vh),
             _ptr(out.sQ), _ptr(out.sK), _ptr(out.sV), _ptr(out.muK), _ptr(out.muQ), _stream(stream))
     _check("sage_quantize_smooth_noalloc", st)

@@ -80,7 +80,8 @@ constexpr int kScaleSlots = 8;                        // tile scales kept for 8 
 // operands of the dP MMA: the unquantised fp16 or bf16 dO and V (the method), or their INT8 codes
 // as integer-valued fp16 (the ablation of "SageAttention3 ..." (review), Table 1c)
 constexpr int kDpFp16 = 0, kDpBf16 = 1, kDpInt8 = 2;
-constexpr float kTileZero = 7.52316384526264e-37f;   // 2^-120
+constexpr float kTileZero = 0x1p-120f;              // tile max below which s = max / 127 is zero
+constexpr float kTileZeroFp8 = 0x1p-110f;          // the same for s = max / 448 (1 / s stays finite)
 
 template <int D>
 struct Smem {
@@ -149,6 +150,12 @@ __device__ __forceinline__ uint32_t codes2(float x0, float x1, float inv) {
         : "=r"(r)
         : "f"(y0), "f"(y1), "r"(0x66006600u));
     return r;
+}
+
+// FP8 variant: two E4M3 tile codes e4m3(fl32(x * inv)) as fp16 values (inv = 0 for a zero tile)
+__device__ __forceinline__ uint32_t codes2_e4m3(float x0, float x1, float inv) {
+    const f2 y = mul2(f2{x0, x1}, f2{inv, inv});
+    return e4m3x2_f16x2(y.x, y.y);
 }
 
 __device__ __forceinline__ int16_t code_lo(uint32_t w) {
@@ -257,7 +264,7 @@ __device__ __forceinline__ void score_pass1(uint32_t s_col, uint32_t dp_col, con
 // columns already read (4 packed columns at col0 / 2), dS codes -> this key's 128-byte row of the
 // shared dS^ tile (16-byte chunk j stored at j ^ (key % 8), the 128-byte swizzle the MMA
 // descriptors expect).
-template <bool EDGE, bool BIAS, bool DUMP, bool DP8>
+template <bool EDGE, bool BIAS, bool DUMP, bool DP8, bool FP8>
 __device__ __forceinline__ void score_pass2(uint32_t s_col, uint32_t dp_col, const float *L2s,
                                             const float *Ds, float cq, float bias, int qlo,
                                             bool key_ok, float dps, float ip, float id,
@@ -269,8 +276,8 @@ __device__ __forceinline__ void score_pass2(uint32_t s_col, uint32_t dp_col, con
         uint32_t pk[4], dk[4];
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
-            pk[k / 2] = codes2(pv[k], pv[k + 1], ip);
-            dk[k / 2] = codes2(ds[k], ds[k + 1], id);
+            pk[k / 2] = FP8 ? codes2_e4m3(pv[k], pv[k + 1], ip) : codes2(pv[k], pv[k + 1], ip);
+            dk[k / 2] = FP8 ? codes2_e4m3(ds[k], ds[k + 1], id) : codes2(ds[k], ds[k + 1], id);
             if (DUMP && key_ok) {
                 dump_p0[static_cast<size_t>(col0 + k) * N] = code_lo(pk[k / 2]);
                 dump_p0[static_cast<size_t>(col0 + k + 1) * N] = code_hi(pk[k / 2]);
@@ -499,7 +506,7 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
 }
 
 // Score warpgroup (warps 0-3).
-template <int D, int DPK, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP, bool FP8>
 __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -573,10 +580,13 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         const int w0 = warp & ~1;
         const float mxp = fmaxf(s.red[w0][c & 1][0], s.red[w0 + 1][c & 1][0]);
         const float mxd = fmaxf(s.red[w0][c & 1][1], s.red[w0 + 1][c & 1][1]);
-        const float sp = mxp < kTileZero ? 0.0f : __fdiv_rn(mxp, 127.0f);
-        const float ip = mxp < kTileZero ? 0.0f : __frcp_rn(sp);
-        const float sd = mxd < kTileZero ? 0.0f : __fdiv_rn(mxd, 127.0f);
-        const float id = mxd < kTileZero ? 0.0f : __frcp_rn(sd);
+        // FP8: s = max/448, and a tile below 2^-110 is zero so that 1/s stays finite
+        constexpr float kZero = FP8 ? kTileZeroFp8 : kTileZero;
+        constexpr float kQmax = FP8 ? 448.0f : 127.0f;
+        const float sp = mxp < kZero ? 0.0f : __fdiv_rn(mxp, kQmax);
+        const float ip = mxp < kZero ? 0.0f : __frcp_rn(sp);
+        const float sd = mxd < kZero ? 0.0f : __fdiv_rn(mxd, kQmax);
+        const float id = mxd < kZero ? 0.0f : __frcp_rn(sd);
         if ((tq & 63) == 0) {
             s.sps[z][kb] = sp;
             s.sds[z][kb] = sd;
@@ -594,10 +604,10 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         int16_t *dump_ds0 = DUMP ? a.dump_ds + (bhN + q0) * N + key : nullptr;
         uint8_t *dss_row = s.dss[b] + tq * 128;
         if (edge)
-            score_pass2<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
+            score_pass2<true, BIAS, DUMP, DPK == kDpInt8, FP8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
                                                           dps, ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
         else
-            score_pass2<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
+            score_pass2<false, BIAS, DUMP, DPK == kDpInt8, FP8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo, key_ok,
                                                            dps, ip, id, dss_row, tq & 7, dump_p0, dump_ds0, N);
         tmem_wait_st();
         fence_view_async_shared();
@@ -802,7 +812,7 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
     }
 }
 
-template <int D, int DPK, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                 const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapdO,
@@ -842,7 +852,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
         __syncthreads();
         if (warp == kMmaWarp) tmem_dealloc(s.tmem_base, 512);
     } else if (warp < 4) {
-        score_role<D, DPK, BIAS, DUMP>(s, a);
+        score_role<D, DPK, BIAS, DUMP, FP8>(s, a);
         tc_fence_before();
         __syncthreads();
     } else if (warp < 8) {
@@ -858,10 +868,10 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 
 }  // namespace bwd
 
-template <int D, int DPK, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP, bool FP8>
 static cudaError_t launch_bwd_t(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
                                 cudaStream_t st) {
-    auto kern = bwd::sage_bwd_kernel<D, DPK, BIAS, DUMP>;
+    auto kern = bwd::sage_bwd_kernel<D, DPK, BIAS, DUMP, FP8>;
     const int smem = static_cast<int>(sizeof(bwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -881,15 +891,26 @@ template <int D, int DPK>
 static cudaError_t launch_bwd_d(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
                                 cudaStream_t st) {
     const bool bias = a.qbias != nullptr, dump = a.dump_s != nullptr;
-    if (dump) return bias ? launch_bwd_t<D, DPK, true, true>(p, maps, a, st)
-                          : launch_bwd_t<D, DPK, false, true>(p, maps, a, st);
-    return bias ? launch_bwd_t<D, DPK, true, false>(p, maps, a, st)
-                : launch_bwd_t<D, DPK, false, false>(p, maps, a, st);
+    if (dump) return bias ? launch_bwd_t<D, DPK, true, true, false>(p, maps, a, st)
+                          : launch_bwd_t<D, DPK, false, true, false>(p, maps, a, st);
+    return bias ? launch_bwd_t<D, DPK, true, false, false>(p, maps, a, st)
+                : launch_bwd_t<D, DPK, false, false, false>(p, maps, a, st);
+}
+
+// FP8 codes (the C ABI refuses them with the dump and with INT8 dP)
+template <int D, int DPK>
+static cudaError_t launch_bwd_fp8(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
+                                  cudaStream_t st) {
+    return a.qbias != nullptr ? launch_bwd_t<D, DPK, true, false, true>(p, maps, a, st)
+                              : launch_bwd_t<D, DPK, false, false, true>(p, maps, a, st);
 }
 
 template <int D>
 static cudaError_t launch_bwd_k(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
                                 cudaStream_t st) {
+    if (p.flags & SAGE_FLAG_FP8)
+        return p.dtype == SAGE_BF16 ? launch_bwd_fp8<D, bwd::kDpBf16>(p, maps, a, st)
+                                    : launch_bwd_fp8<D, bwd::kDpFp16>(p, maps, a, st);
     if (p.flags & SAGE_FLAG_DP_INT8) return launch_bwd_d<D, bwd::kDpInt8>(p, maps, a, st);
     return p.dtype == SAGE_BF16 ? launch_bwd_d<D, bwd::kDpBf16>(p, maps, a, st)
                                 : launch_bwd_d<D, bwd::kDpFp16>(p, maps, a, st);

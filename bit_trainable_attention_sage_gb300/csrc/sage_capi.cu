@@ -175,7 +175,8 @@ static int check_params(const sage_params *p) {
     if (p->causal != 0 && p->causal != 1) return SAGE_ERR_ARG;
     if (p->smooth_k != 0 && p->smooth_k != 1) return SAGE_ERR_ARG;
     if (p->smooth_q != 0 && p->smooth_q != 1) return SAGE_ERR_ARG;
-    if (p->flags & ~(SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8)) return SAGE_ERR_ARG;
+    if (p->flags & ~(SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8 | SAGE_FLAG_FP8)) return SAGE_ERR_ARG;
+    if ((p->flags & SAGE_FLAG_FP8) && (p->flags & (SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8))) return SAGE_ERR_UNSUPPORTED;
     if (p->dtype != SAGE_FP16 && p->dtype != SAGE_BF16) return SAGE_ERR_UNSUPPORTED;
     if (p->d != 64 && p->d != 128) return SAGE_ERR_UNSUPPORTED;
     if (p->N % 64 != 0) return SAGE_ERR_UNSUPPORTED;
@@ -250,6 +251,7 @@ int sage_quantize_smooth(const sage_params *p, const void *Q, const void *K, con
     QuantWs w = quant_ws(*p, p->smooth_k ? workspace : nullptr, nullptr);
     a.kpartial = w.kpartial;
     a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
+    a.fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
     SAGE_CUDA(launch_quantize(*p, a, reinterpret_cast<cudaStream_t>(stream)));
     return SAGE_OK;
 }
@@ -273,9 +275,10 @@ int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     FwdWs w = fwd_ws(*p, workspace, nullptr);
     const size_t n = elems(*p);
-    SAGE_CUDA(launch_widen(Qh, w.q16, n, st));
-    SAGE_CUDA(launch_widen(Kh, w.k16, n, st));
-    SAGE_CUDA(launch_widen(Vh, w.v16, n, st));
+    const bool fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
+    SAGE_CUDA(launch_widen(Qh, w.q16, n, fp8, st));
+    SAGE_CUDA(launch_widen(Kh, w.k16, n, fp8, st));
+    SAGE_CUDA(launch_widen(Vh, w.v16, n, fp8, st));
     const float sl2 = scale_log2(p->d);
     if (p->smooth_q) SAGE_CUDA(launch_qbias(*p, K, muK, muQ, w.qbias, sl2, st));
     FwdArgs a;
@@ -316,8 +319,9 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     BwdDump dd;
     memset(&dd, 0, sizeof(dd));
     if (p->flags & SAGE_FLAG_DUMP) dd = bwd_dump(*p, p->dump, nullptr);
-    SAGE_CUDA(launch_widen(Qh, w.q16, n, st));
-    SAGE_CUDA(launch_widen(Kh, w.k16, n, st));
+    const bool fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
+    SAGE_CUDA(launch_widen(Qh, w.q16, n, fp8, st));
+    SAGE_CUDA(launch_widen(Kh, w.k16, n, fp8, st));
     const bool dp8 = (p->flags & SAGE_FLAG_DP_INT8) != 0;
     if (dp8) {
         // V codes for dP (the ablation): the same per-block quantiser as sage_quantize_smooth
@@ -326,11 +330,11 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
         qa.V = V; qa.Vh = w.v8; qa.sV = w.sV;
         qa.N = p->N; qa.d = p->d;
         SAGE_CUDA(launch_quantize_v(*p, qa, st));
-        SAGE_CUDA(launch_widen(w.v8, w.v16, n, st));
+        SAGE_CUDA(launch_widen(w.v8, w.v16, n, false, st));
     }
     BwdPrologueArgs pa;
     pa.dO = dO; pa.O = O; pa.L = L; pa.L2 = w.L2; pa.D = w.D; pa.dO16 = w.do16; pa.dOh = dd.doh; pa.sdO = w.sdO;
-    pa.N = p->N; pa.d = p->d;
+    pa.N = p->N; pa.d = p->d; pa.fp8 = fp8;
     SAGE_CUDA(launch_bwd_prologue(*p, pa, st));
     const float sl2 = scale_log2(p->d);
     if (p->smooth_q) SAGE_CUDA(launch_qbias(*p, K, muK, muQ, w.qbias, sl2, st));

@@ -401,6 +401,30 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return r;
 }
 
+// FP8 E4M3 codes (OCP 8-bit floating point: 4 exponent bits, bias 7, 3 mantissa bits, largest
+// finite 448).  The float32 -> E4M3 conversion rounds to nearest, ties to even, and saturates
+// to +-448; every E4M3 value is exact in fp16.  In each pair `lo` is the low byte / half.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+// two float32 values rounded to E4M3 and returned as an fp16 pair (the MMA operand format)
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(lo), "f"(hi));
+    return r;
+}
+
 // Warpgroup register reallocation (all four warps of a warpgroup execute the same one).
 template <uint32_t R>
 __device__ __forceinline__ void regs_inc() {

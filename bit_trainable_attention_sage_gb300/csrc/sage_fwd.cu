@@ -33,6 +33,10 @@
 //   with Q-smoothing: t_k = fl32(acc_k * c + bias_k), r = max t_k, x_k = fl32(t_k - r)
 //   l <- 2^(m - m') l + 2^(r - m') sum_k ex2(x_k);  O <- 2^(m - m') O + (2^(r - m') / 127) s_V PV
 //   O_out = O / l;  L = (m + log2 l) ln 2
+// FP8 variant (SAGE_FLAG_FP8, "SageAttention3 ..." (review), INT8 vs FP8 training): the codes are
+// E4M3 values, P^_k = e4m3(fl32(448 * ex2(x_k))) and the PV scale is (2^(r - m') / 448) s_V.
+// E4M3 values are exact fp16 operands; their products are exact in the fp32 accumulator, the
+// sums rounded as any fp32 accumulation.
 #include "sage_device.cuh"
 #include "sage_internal.h"
 
@@ -119,11 +123,13 @@ __device__ __forceinline__ float fwd_row_max(uint32_t (&raw)[64], float c, const
 // returns the row sum of ex2(x) (four partial sums).  rint is done with the float32 add of
 // 1.5 * 2^23 and its subtraction (exact for the values 0..127 here, and a full-rate instruction,
 // unlike the conversion unit's round-to-integer).
-template <bool BIAS, bool MASKED, bool DUMP>
+// FP8: P^ = e4m3(fl32(448 ex2(x))) instead, converted to fp16 in two instructions per pair.
+template <bool BIAS, bool MASKED, bool DUMP, bool FP8>
 __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, float rs,
                                            int nvalid, uint32_t code_col, int16_t *dump_row) {
     constexpr float kRound = 12582912.0f;          // 1.5 * 2^23
     const f2 c2{c, c}, nrs2{-rs, -rs}, rs2{rs, rs}, k127{127.0f, 127.0f}, kr2{kRound, kRound};
+    const f2 k448{448.0f, 448.0f};
     f2 sp[2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 16) {
@@ -139,13 +145,17 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
             }
             const f2 e2{ex2_approx(x2.x), ex2_approx(x2.y)};
             sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e2);
-            const f2 p2 = sub2(add2(mul2(k127, e2), kr2), kr2);
-            const float e0 = e2.x, e1 = e2.y, p0 = p2.x, p1 = p2.y;
-            (void)e0; (void)e1;
-            pk[k / 2] = pack_half2(p0, p1);
-            if (DUMP && dump_row) {
-                dump_row[cc + k] = static_cast<int16_t>(p0);
-                dump_row[cc + k + 1] = static_cast<int16_t>(p1);
+            if (FP8) {
+                const f2 v2 = mul2(k448, e2);
+                pk[k / 2] = e4m3x2_f16x2(v2.x, v2.y);
+            } else {
+                const f2 p2 = sub2(add2(mul2(k127, e2), kr2), kr2);
+                const float p0 = p2.x, p1 = p2.y;
+                pk[k / 2] = pack_half2(p0, p1);
+                if (DUMP && dump_row) {
+                    dump_row[cc + k] = static_cast<int16_t>(p0);
+                    dump_row[cc + k + 1] = static_cast<int16_t>(p1);
+                }
             }
         }
         tmem_st8(code_col + cc / 2, pk);
@@ -153,7 +163,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
     return (sp[0].x + sp[1].x) + (sp[0].y + sp[1].y);
 }
 
-template <int D, typename OutT, bool BIAS, bool DUMP>
+template <int D, typename OutT, bool BIAS, bool DUMP, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, const FwdArgs a) {
@@ -339,8 +349,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 // S columns.  A warp with a masked column in any lane takes the masked variant.
                 int16_t *dump_row = DUMP && grow < N ? a.dump_p + (bhN + grow) * N + key0 : nullptr;
                 const float sum = __any_sync(0xffffffffu, nvalid < 64)
-                    ? fwd_codes<BIAS, true, DUMP>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
-                    : fwd_codes<BIAS, false, DUMP>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
+                    ? fwd_codes<BIAS, true, DUMP, FP8>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
+                    : fwd_codes<BIAS, false, DUMP, FP8>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
                 if (h == 0) sum_h0 = sum; else sum_h1 = sum;
             }
             const float r_h[2] = {r_h0, r_h1}, sum_h[2] = {sum_h0, sum_h1};
@@ -358,7 +368,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const float g = live ? ex2_approx(__fsub_rn(r_h[h], m_new)) : 0.0f;
                 l = (h == 0) ? __fmaf_rn(alpha, l, g * sum_h[h]) : __fmaf_rn(g, sum_h[h], l);
                 const int kb = min(2 * j + h, nblk - 1);
-                cpv[h] = (g * (1.0f / 127.0f)) * a.sV[static_cast<size_t>(bh) * nblk + kb];
+                cpv[h] = (g * (FP8 ? 1.0f / 448.0f : 1.0f / 127.0f)) * a.sV[static_cast<size_t>(bh) * nblk + kb];
             }
             m = m_new;
             // O = alpha O + c_h PV_h
@@ -424,10 +434,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
 }  // namespace fwd
 
-template <int D, typename OutT, bool BIAS, bool DUMP>
+template <int D, typename OutT, bool BIAS, bool DUMP, bool FP8>
 static cudaError_t launch_fwd_t(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
-    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP>;
+    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP, FP8>;
     const int smem = static_cast<int>(sizeof(fwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -447,10 +457,13 @@ template <int D, typename OutT>
 static cudaError_t launch_fwd_d(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
     const bool bias = a.qbias != nullptr, dump = a.dump_s != nullptr;
-    if (dump) return bias ? launch_fwd_t<D, OutT, true, true>(p, mq, mk, mv, a, st)
-                          : launch_fwd_t<D, OutT, false, true>(p, mq, mk, mv, a, st);
-    return bias ? launch_fwd_t<D, OutT, true, false>(p, mq, mk, mv, a, st)
-                : launch_fwd_t<D, OutT, false, false>(p, mq, mk, mv, a, st);
+    // the debug dump exists for the INT8 codes only (the C ABI refuses FP8 with it)
+    if (p.flags & SAGE_FLAG_FP8) return bias ? launch_fwd_t<D, OutT, true, false, true>(p, mq, mk, mv, a, st)
+                                             : launch_fwd_t<D, OutT, false, false, true>(p, mq, mk, mv, a, st);
+    if (dump) return bias ? launch_fwd_t<D, OutT, true, true, false>(p, mq, mk, mv, a, st)
+                          : launch_fwd_t<D, OutT, false, true, false>(p, mq, mk, mv, a, st);
+    return bias ? launch_fwd_t<D, OutT, true, false, false>(p, mq, mk, mv, a, st)
+                : launch_fwd_t<D, OutT, false, false, false>(p, mq, mk, mv, a, st);
 }
 
 cudaError_t launch_fwd(const sage_params &p, const __half *Q16, const __half *K16,

@@ -27,6 +27,7 @@ struct QuantArgs {
     int ksplits;
     int N, d, smooth_k, smooth_q;
     int z_base;               // first tensor of the launch: 0 = Q, 1 = K, 2 = V
+    int fp8;                  // 1: E4M3 codes, delta = max|x| / 448 (SAGE_FLAG_FP8)
 };
 
 struct BwdPrologueArgs {
@@ -38,6 +39,7 @@ struct BwdPrologueArgs {
     int8_t *dOh;       // optional int8 codes of dO (debug dump), may be NULL
     float *sdO;        // (B,H,N/64)
     int N, d;
+    int fp8;           // 1: the dO codes are E4M3 values (SAGE_FLAG_FP8)
 };
 
 // Forward kernel arguments (device pointers; tensor maps are separate __grid_constant__ params)
@@ -72,7 +74,8 @@ struct BwdArgs {
 int kmean_splits(const sage_params &p);
 cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st);
 cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st);   // V only
-cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, cudaStream_t st);
+// int8 codes (or E4M3 bit patterns when fp8) -> their exact fp16 values
+cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, bool fp8, cudaStream_t st);
 cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStream_t st);
 cudaError_t launch_qbias(const sage_params &p, const void *K, const float *muK, const float *muQ,
                          float *bias, float sl2, cudaStream_t st);

@@ -49,7 +49,7 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
     if (!p) return SAGE_ERR_ARG;
     if (p->B <= 0 || p->H <= 0 || p->N <= 0 || p->d <= 0) return SAGE_ERR_ARG;
     if ((p->causal | p->smooth_k | p->smooth_q) & ~1) return SAGE_ERR_ARG;
-    if (p->flags != 0) return SAGE_ERR_ARG;
+    if (p->flags & ~SAGE_FLAG_FP8) return SAGE_ERR_ARG;
     if (p->dtype != SAGE_FP16 && p->dtype != SAGE_BF16) return SAGE_ERR_UNSUPPORTED;
     if ((p->d != 64 && p->d != 128) || p->N % 64 != 0) return SAGE_ERR_UNSUPPORTED;
     if (static_cast<long long>(p->B) * p->H > 65535) return SAGE_ERR_UNSUPPORTED;
@@ -81,6 +81,7 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
     // array needs no clearing; calls that overlap on the GPU share it and race
     a.kpartial = p->smooth_k ? scratch : nullptr;
     a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
+    a.fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
     if (launch_quantize(*p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SAGE_ERR_CUDA;
     return SAGE_OK;
 }

@@ -12,8 +12,11 @@
 //   x            = fl32(v - mu)
 //   delta        = fl32(max|x| / 127)        (IEEE division, __fdiv_rn)
 //   code         = clamp(rint_half_even(fl32(x / delta)), -127, 127), zero block -> delta 0, code 0
+// FP8 variant ("SageAttention3 ..." (review), INT8 vs FP8 training): delta = fl32(max|x| / 448)
+// and code = E4M3(fl32(x / delta)), round to nearest even, saturating at +-448.
 //
 // All kernels here stream through HBM once; they are bound by memory bandwidth.
+#include "sage_device.cuh"
 #include "sage_internal.h"
 
 namespace sage {
@@ -54,6 +57,24 @@ __device__ __forceinline__ uint2 pack_codes8(const float (&x)[8], float delta) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) hi |= (static_cast<uint32_t>(quant_code(x[4 + i], delta)) & 0xFFu) << (8 * i);
     return make_uint2(lo, hi);
+}
+
+// E4M3 codes of 8 values (bit patterns, 8 bytes); delta = 0 gives all-zero codes
+__device__ __forceinline__ uint2 pack_codes8_e4m3(const float (&x)[8], float delta) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = delta == 0.0f ? 0u : e4m3x2(__fdiv_rn(x[2 * i], delta), __fdiv_rn(x[2 * i + 1], delta));
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+// fp16 copies of the E4M3 codes of 8 values
+__device__ __forceinline__ uint4 pack_codes8_e4m3_f16(const float (&x)[8], float delta) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = delta == 0.0f ? 0u : e4m3x2_f16x2(__fdiv_rn(x[2 * i], delta), __fdiv_rn(x[2 * i + 1], delta));
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // integer-valued fp16 copies of the codes (the tensor-core operand format on sm_103a)
@@ -236,20 +257,40 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
         }
     }
     mx = block_max_256(mx, red);
-    const float delta = __fdiv_rn(mx, 127.0f);
+    const float delta = __fdiv_rn(mx, a.fp8 ? 448.0f : 127.0f);
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         if (it >= iters) break;
         const int r = rg + it * rows_in_flight;
         *reinterpret_cast<uint2 *>(dst + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-            pack_codes8(x[it], delta);
+            a.fp8 ? pack_codes8_e4m3(x[it], delta) : pack_codes8(x[it], delta);
     }
     if (threadIdx.x == 0) scale[static_cast<size_t>(bh) * (N / 64) + blk] = delta;
 }
 
 // ---------------------------------------------------------------------------------------------
-// widen: int8 codes -> integer-valued fp16 (exact), 16 codes per thread per step
+// widen: int8 codes -> integer-valued fp16, or E4M3 codes -> their fp16 values (both exact),
+// 16 codes per thread per step
 // ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const int8_t *__restrict__ src,
+                                                         __half *__restrict__ dst, size_t n16) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int4 u = reinterpret_cast<const int4 *>(src)[i];
+        const uint32_t w[4] = {static_cast<uint32_t>(u.x), static_cast<uint32_t>(u.y),
+                               static_cast<uint32_t>(u.z), static_cast<uint32_t>(u.w)};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            o[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+            o[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
+        }
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst) + 2 * i;
+        d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
 __global__ void __launch_bounds__(256) widen_kernel(const int8_t *__restrict__ src,
                                                     __half *__restrict__ dst, size_t n16) {
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
@@ -313,13 +354,13 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(BwdPrologueArgs a) {
         }
     }
     mx = block_max_256(mx, red);
-    const float delta = __fdiv_rn(mx, 127.0f);
+    const float delta = __fdiv_rn(mx, a.fp8 ? 448.0f : 127.0f);
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         if (it >= iters) break;
         const int r = rg + it * rows_in_flight;
         *reinterpret_cast<uint4 *>(a.dO16 + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-            pack_codes8_f16(x[it], delta);
+            a.fp8 ? pack_codes8_e4m3_f16(x[it], delta) : pack_codes8_f16(x[it], delta);
         if (a.dOh)
             *reinterpret_cast<uint2 *>(a.dOh + blk_off + static_cast<size_t>(r) * d + cv * 8) =
                 pack_codes8(x[it], delta);
@@ -398,12 +439,15 @@ cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st
     return cudaGetLastError();
 }
 
-cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, cudaStream_t st) {
+cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, bool fp8, cudaStream_t st) {
     const size_t n16 = n / 16;
     int blocks = static_cast<int>((n16 + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    widen_kernel<<<blocks, 256, 0, st>>>(src, dst, n16);
+    if (fp8)
+        widen_e4m3_kernel<<<blocks, 256, 0, st>>>(src, dst, n16);
+    else
+        widen_kernel<<<blocks, 256, 0, st>>>(src, dst, n16);
     return cudaGetLastError();
 }
 

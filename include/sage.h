@@ -55,6 +55,17 @@ extern "C" {
                                    (review), Table 1c.  V is quantised per 64-token block inside
                                    the call (same codes as sage_quantize_smooth); the workspace
                                    grows by 3 bytes per element plus the scales. */
+#define SAGE_FLAG_FP8 4u        /* FP8 SageBwd ("SageAttention3 ..." (review), INT8 vs FP8
+                                   training): every INT8 code becomes an FP8 E4M3 code (OCP
+                                   format: bias 7, 3 mantissa bits, largest finite 448), with 448
+                                   in place of 127 -- block scales fl32(max|x| / 448) and codes
+                                   e4m3(fl32(x / delta)) (round to nearest even, saturating);
+                                   forward P codes e4m3(fl32(448 ex2(x))); backward tile codes
+                                   e4m3(fl32(x fl32(1 / s))), s = fl32(max|x| / 448), tiles with
+                                   max|x| < 2^-110 zero.  The int8_t code buffers then hold E4M3
+                                   bit patterns.  Pass it to all three calls of one pass; it
+                                   cannot be combined with SAGE_FLAG_DUMP or SAGE_FLAG_DP_INT8
+                                   (SAGE_ERR_UNSUPPORTED). */
 
 typedef struct CUstream_st *sage_stream_t;   /* identical to cudaStream_t */
 
@@ -164,7 +175,7 @@ SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t 
  *   - Every call shares the one array, which keeps the last call's partial sums.  Nothing has to
  *     start at zero (each call writes every entry it reads first), but calls that overlap on the
  *     GPU -- on different streams, or from different host threads -- race on it.
- *   - `flags` must be 0 (no debug dump).
+ *   - `flags` must be 0 or SAGE_FLAG_FP8 (no debug dump).
  * ------------------------------------------------------------------------------------------ */
 SAGE_API size_t sage_quantize_noalloc_max_partials(void);
 SAGE_API int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, const void *K,

@@ -52,11 +52,11 @@ def make_case(N, d, dtype, causal, B=1, H=2, seed=0, qk="normal", sigma=1.0, k_o
     return w, workloads.make_inputs(w, seed=seed)
 
 
-def oracle_run(w, x, record=True, dp_int8=False):
+def oracle_run(w, x, record=True, dp_int8=False, fp8=False):
     rec = {} if record else None
     out = osage.run(x["Q"], x["K"], x["V"], x["dO"], w.causal,
                     lambda a: workloads.round_to(a, w.dtype), smooth_q=w.smooth_q, record=rec,
-                    dp_int8=dp_int8)
+                    dp_int8=dp_int8, arith=osage.QUANTISED_FP8 if fp8 else osage.QUANTISED)
     out["record"] = rec
     return out
 
@@ -98,11 +98,12 @@ def gpu_fwd(w, x, dump=False):
     return dict(q=q, O=O, L=L, dump=buf, dev=dict(Q=Q, K=K, V=V))
 
 
-def gpu_run(w, x, dump=False, dp_int8=False):
-    """quantise -> forward -> backward on the GPU; returns numpy results (+ backward dump views)."""
+def gpu_run(w, x, dump=False, dp_int8=False, fp8=False):
+    """quantise -> forward -> backward on the GPU; returns numpy results (+ backward dump views,
+    + the quantiser's outputs when fp8)."""
     import bit_trainable_attention_sage_gb300 as sg
     Q, K, V, dO = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V", "dO"))
-    q = sg.sage_quantize_smooth(Q, K, V, smooth_q=w.smooth_q)
+    q = sg.sage_quantize_smooth(Q, K, V, smooth_q=w.smooth_q, fp8=fp8)
     Kb = K if w.smooth_q else None
     O, L = sg.sage_attn_fwd(q, causal=w.causal, K=Kb)
     buf = None
@@ -116,4 +117,6 @@ def gpu_run(w, x, dump=False, dp_int8=False):
                dK=dK.cpu().numpy(), dV=dV.cpu().numpy())
     if dump:
         out["dump"] = {k: v.cpu().numpy() for k, v in bwd_dump_views(buf, w.B, w.H, w.N, w.d).items()}
+    if fp8:
+        out["q"] = {k: getattr(q, k).cpu().numpy() for k in ("Qh", "Kh", "Vh", "sQ", "sK", "sV", "muK")}
     return out

@@ -54,6 +54,22 @@ def test_workspace_sizes(sg):
     assert 3 * n + 4 * 2 * 16 * 128 <= extra <= 3 * n + 4 * 2 * 16 * 128 + 3 * 256
 
 
+def test_fp8_flag_checks(sg):
+    """SAGE_FLAG_FP8 is accepted alone (same workspaces as INT8) and refused with the dump or with
+    INT8 dP (SAGE_ERR_UNSUPPORTED) before any launch."""
+    L = sg.lib()
+    p = sg.make_params(1, 2, 256, 128, 0, False)
+    pf = sg.make_params(1, 2, 256, 128, 0, False, fp8=True)
+    assert pf.flags == sg.binding.SAGE_FLAG_FP8
+    for q in ("sage_quantize_workspace_bytes", "sage_fwd_workspace_bytes", "sage_bwd_workspace_bytes"):
+        assert getattr(L, q)(ctypes.byref(pf)) == getattr(L, q)(ctypes.byref(p)) > 0 or q == "sage_quantize_workspace_bytes"
+    for extra in (sg.binding.SAGE_FLAG_DUMP, sg.binding.SAGE_FLAG_DP_INT8):
+        bad = sg.make_params(1, 2, 256, 128, 0, False, fp8=True)
+        bad.flags |= extra
+        assert L.sage_attn_fwd(ctypes.byref(bad), *[_fake(i) for i in range(12)], 1 << 30, None) == 2
+        assert L.sage_attn_bwd(ctypes.byref(bad), *[_fake(i) for i in range(15)], 1 << 30, None) == 2
+
+
 def _fake(i):
     return 0x10000 * (i + 1)    # aligned non-null addresses; never dereferenced (calls fail first)
 
