@@ -85,6 +85,13 @@ def step_ops(w: workloads.Workload) -> float:
     return ops / 2 if w.causal else ops
 
 
+def qknorm_bwd_bytes(w: workloads.Workload) -> int:
+    """Algorithmic HBM bytes of one sage_qknorm_bwd call: X read (2 B an element), dY read and dX
+    written (4 B each), the row factors read (4 B a row)."""
+    n = w.B * w.H * w.N * w.d
+    return 10 * n + 4 * w.B * w.H * w.N
+
+
 def quant_bytes(w: workloads.Workload) -> int:
     """Algorithmic HBM bytes of one sage_quantize_smooth call: Q, K, V read (2 B an element; K twice
     with K-smoothing, once for its mean and once to quantise it; Q twice with Q-smoothing), int8
@@ -214,10 +221,19 @@ def run_gpu(args, w: workloads.Workload):
     Lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=device) for _ in range(3))
 
+    gam = None
+    if args.qk_norm:
+        gen = torch.Generator(device="cpu").manual_seed(rank)
+        gam = [(0.5 + torch.rand(d, generator=gen)).to(device) for _ in range(2)]
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q, fp8=args.fp8)
+        if args.qk_norm:
+            q = sg.sage_quantize_smooth_qknorm(dev["Q"], dev["K"], dev["V"], gamma_q=gam[0], gamma_k=gam[1],
+                                               smooth_q=w.smooth_q, fp8=args.fp8)
+        else:
+            q = sg.sage_quantize_smooth(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q, fp8=args.fp8)
         if ev is not None:
             ev[1].record(stream)
         sg.sage_attn_fwd(q, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
@@ -227,6 +243,12 @@ def run_gpu(args, w: workloads.Workload):
                          dp_int8=args.dp_int8)
         if ev is not None:
             ev[3].record(stream)
+        if args.qk_norm:
+            # the attention gradients are those of the normalised Q and K: chain them through the norm
+            sg.sage_qknorm_bwd(dev["Q"], q.rQ, grads[0], gamma=gam[0])
+            sg.sage_qknorm_bwd(dev["K"], q.rK, grads[1], gamma=gam[1])
+        if ev is not None:
+            ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -239,7 +261,7 @@ def run_gpu(args, w: workloads.Workload):
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     clocks.start(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize(device)
@@ -257,6 +279,7 @@ def run_gpu(args, w: workloads.Workload):
     quant_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    qkn_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs) if args.qk_norm else 0.0
     ms_max = max_over_ranks(dist, ms, device)
 
     # ---- end to end through the public API with host buffers ------------------------------
@@ -327,9 +350,15 @@ def run_gpu(args, w: workloads.Workload):
         "step_frac_of_fp16_peak": round(value / world / peak, 4),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (2 if args.qk_norm else 0)) * args.steps,
         "clocks": clk,
     }
+    if args.qk_norm:
+        # two gradient calls (Q and K) per step; the prologue's cost is inside quantise_call
+        gbs = 2 * qknorm_bwd_bytes(w) / (qkn_ms * 1e-3) / 1e9
+        line["qknorm_bwd_calls"] = {"ms": round(qkn_ms, 4), "bound": "hbm", "bytes": 2 * qknorm_bwd_bytes(w),
+                                    "gbs": round(gbs, 1), "peak_gbs": hbm_peak, "frac": round(gbs / hbm_peak, 4)}
+        line["config"]["qk_norm"] = True
     return line
 
 
@@ -417,6 +446,8 @@ def main():
                     help="backward with the INT8-dP ablation (dP from the dO and V codes)")
     ap.add_argument("--fp8", action="store_true",
                     help="the FP8 SageBwd variant (E4M3 codes in place of INT8)")
+    ap.add_argument("--qk-norm", action="store_true",
+                    help="QK-norm fused into the quantise call, and its gradient after the backward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")

@@ -7,7 +7,7 @@ differentiable PyTorch operation.
 """
 from .binding import (  # noqa: F401
     Quantized, SageError, SageParams, lib, make_params, sage_attn_bwd, sage_attn_fwd,
-    sage_device_status, sage_dump_bytes, sage_quantize_smooth, sage_quantize_smooth_noalloc,
-    sage_status_string, sage_version,
+    sage_device_status, sage_dump_bytes, sage_qknorm_bwd, sage_quantize_smooth,
+    sage_quantize_smooth_noalloc, sage_quantize_smooth_qknorm, sage_status_string, sage_version,
 )
 from .autograd import SageAttentionFunction, sage_attention  # noqa: F401,E402

@@ -25,7 +25,8 @@ SAGE_FLAG_FP8 = 4
 EXPORTED = (
     "sage_quantize_workspace_bytes", "sage_quantize_smooth", "sage_fwd_workspace_bytes",
     "sage_attn_fwd", "sage_bwd_workspace_bytes", "sage_attn_bwd", "sage_dump_bytes",
-    "sage_device_status", "sage_status_string", "sage_version",
+    "sage_device_status", "sage_status_string", "sage_version", "sage_quantize_smooth_qknorm",
+    "sage_qknorm_bwd",
 )
 
 
@@ -35,6 +36,15 @@ class SageParams(ctypes.Structure):
         ("dtype", ctypes.c_int), ("causal", ctypes.c_int), ("smooth_k", ctypes.c_int),
         ("smooth_q", ctypes.c_int), ("flags", ctypes.c_uint), ("dump", ctypes.c_void_p),
         ("dump_bytes", ctypes.c_size_t),
+    ]
+
+
+class SageQkNorm(ctypes.Structure):
+    """struct sage_qknorm (include/sage.h)."""
+    _fields_ = [
+        ("gQ", ctypes.c_void_p), ("gK", ctypes.c_void_p), ("eps", ctypes.c_float),
+        ("rQ", ctypes.c_void_p), ("rK", ctypes.c_void_p), ("Qn", ctypes.c_void_p),
+        ("Kn", ctypes.c_void_p),
     ]
 
 
@@ -66,6 +76,10 @@ def lib() -> ctypes.CDLL:
     L.sage_dump_bytes.restype = sz
     L.sage_quantize_smooth.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sage_quantize_smooth.restype = ci
+    L.sage_quantize_smooth_qknorm.argtypes = [P, ctypes.POINTER(SageQkNorm)] + [vp] * 12 + [sz, vp]
+    L.sage_quantize_smooth_qknorm.restype = ci
+    L.sage_qknorm_bwd.argtypes = [P] + [vp] * 6 + [vp]
+    L.sage_qknorm_bwd.restype = ci
     L.sage_attn_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sage_attn_fwd.restype = ci
     L.sage_attn_bwd.argtypes = [P] + [vp] * 15 + [sz, vp]
@@ -144,6 +158,11 @@ class Quantized:
     smooth_k: bool
     smooth_q: bool
     fp8: bool = False
+    # QK-norm prologue (sage_quantize_smooth_qknorm): row factors and, when kept, normalised Q, K
+    rQ: torch.Tensor | None = None
+    rK: torch.Tensor | None = None
+    Qn: torch.Tensor | None = None
+    Kn: torch.Tensor | None = None
 
 
 def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, smooth_k: bool = True,
@@ -169,6 +188,58 @@ def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, s
                                 _stream(stream))
     _check("sage_quantize_smooth", st)
     return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8)
+
+
+def sage_quantize_smooth_qknorm(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *,
+                                gamma_q: torch.Tensor | None = None, gamma_k: torch.Tensor | None = None,
+                                eps: float = 1e-6, smooth_k: bool = True, smooth_q: bool = False,
+                                fp8: bool = False, keep_normed: bool = False, stream=None) -> Quantized:
+    """QK-norm (per-token RMSNorm of Q and K, float32 gammas of d entries or None) fused into
+    sage_quantize_smooth.  The result carries the row factors rQ, rK and, with ``keep_normed``
+    (forced when ``smooth_q``), the normalised Q and K; pass ``q.Kn`` as K to the forward and
+    backward calls when ``smooth_q``."""
+    _require_cuda(Q, K, V, gamma_q, gamma_k)
+    B, H, N, d = Q.shape
+    dt = _dtype_code(Q)
+    dev = Q.device
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
+    Qh = torch.empty((B, H, N, d), dtype=torch.int8, device=dev)
+    Kh, Vh = torch.empty_like(Qh), torch.empty_like(Qh)
+    sQ = torch.empty((B, H, N // 64), dtype=torch.float32, device=dev)
+    sK, sV = torch.empty_like(sQ), torch.empty_like(sQ)
+    muK = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    muQ = torch.empty((B, H, N // 64, d), dtype=torch.float32, device=dev) if smooth_q else None
+    rQ = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    rK = torch.empty_like(rQ)
+    keep = keep_normed or smooth_q
+    Qn = torch.empty_like(Q) if keep else None
+    Kn = torch.empty_like(K) if keep else None
+    qn = SageQkNorm(_ptr(gamma_q), _ptr(gamma_k), float(eps), _ptr(rQ), _ptr(rK), _ptr(Qn), _ptr(Kn))
+    L = lib()
+    nws = L.sage_quantize_workspace_bytes(ctypes.byref(p))
+    ws = _workspace(nws, dev)
+    st = L.sage_quantize_smooth_qknorm(ctypes.byref(p), ctypes.byref(qn), _ptr(Q), _ptr(K), _ptr(V),
+                                       _ptr(Qh), _ptr(Kh), _ptr(Vh), _ptr(sQ), _ptr(sK), _ptr(sV),
+                                       _ptr(muK), _ptr(muQ), _ptr(ws), nws, _stream(stream))
+    _check("sage_quantize_smooth_qknorm", st)
+    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8, rQ, rK, Qn, Kn)
+
+
+def sage_qknorm_bwd(X: torch.Tensor, r: torch.Tensor, dY: torch.Tensor, *, gamma: torch.Tensor | None = None,
+                    want_dgamma: bool = True, stream=None):
+    """Gradient of the QK-norm for the raw tensor X (Q or K) given the row factors r of the
+    forward call and dY (float32), the gradient for the normalised tensor.  Returns (dX float32,
+    dgamma float32 (d) or None)."""
+    _require_cuda(X, r, dY, gamma)
+    B, H, N, d = X.shape
+    dev = X.device
+    p = make_params(B, H, N, d, _dtype_code(X), False)
+    dX = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    dg = torch.empty(d, dtype=torch.float32, device=dev) if want_dgamma else None
+    st = lib().sage_qknorm_bwd(ctypes.byref(p), _ptr(X), _ptr(gamma), _ptr(r), _ptr(dY), _ptr(dX),
+                               _ptr(dg), _stream(stream))
+    _check("sage_qknorm_bwd", st)
+    return dX, dg
 
 
 def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,

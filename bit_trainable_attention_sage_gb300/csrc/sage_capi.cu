@@ -233,11 +233,22 @@ size_t sage_quantize_workspace_bytes(const sage_params *p) {
     return b;
 }
 
-int sage_quantize_smooth(const sage_params *p, const void *Q, const void *K, const void *V,
-                         int8_t *Qh, int8_t *Kh, int8_t *Vh, float *sQ, float *sK, float *sV,
-                         float *muK, float *muQ, void *workspace, size_t workspace_bytes,
+}  // extern "C"
+
+// sage_quantize_smooth and its QK-norm form (qn != NULL)
+static int quantize_call(const sage_params *p, const sage_qknorm *qn, const void *Q, const void *K,
+                         const void *V, int8_t *Qh, int8_t *Kh, int8_t *Vh, float *sQ, float *sK,
+                         float *sV, float *muK, float *muQ, void *workspace, size_t workspace_bytes,
                          sage_stream_t stream) {
     SAGE_TRY(check_params(p));
+    if (qn) {
+        if (!(qn->eps >= 0.0f) || !(qn->eps <= 3.0e38f)) return SAGE_ERR_ARG;   // NaN, < 0 or inf
+        SAGE_TRY(check_ptrs({qn->rQ, qn->rK}));
+        const void *opt[] = {qn->gQ, qn->gK, qn->Qn, qn->Kn};
+        for (const void *q : opt)
+            if (q && !aligned16(q)) return SAGE_ERR_ALIGN;
+        if (p->smooth_q && !qn->Kn) return SAGE_ERR_ARG;
+    }
     SAGE_TRY(check_ptrs({Q, K, V, Qh, Kh, Vh, sQ, sK, sV, muK}));
     if (p->smooth_q) SAGE_TRY(check_ptrs({muQ}));
     SAGE_TRY(check_ws(workspace, workspace_bytes, sage_quantize_workspace_bytes(p)));
@@ -252,7 +263,46 @@ int sage_quantize_smooth(const sage_params *p, const void *Q, const void *K, con
     a.kpartial = w.kpartial;
     a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
     a.fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
-    SAGE_CUDA(launch_quantize(*p, a, reinterpret_cast<cudaStream_t>(stream)));
+    QkNormArgs na{};
+    if (qn) {
+        a.qk_norm = 1;
+        na.eps = qn->eps;
+        na.gamma[0] = qn->gQ; na.gamma[1] = qn->gK;
+        na.rnorm[0] = qn->rQ; na.rnorm[1] = qn->rK;
+        na.xnorm[0] = qn->Qn; na.xnorm[1] = qn->Kn;
+    }
+    SAGE_CUDA(launch_quantize(*p, a, reinterpret_cast<cudaStream_t>(stream), qn ? &na : nullptr));
+    return SAGE_OK;
+}
+
+extern "C" {
+
+int sage_quantize_smooth(const sage_params *p, const void *Q, const void *K, const void *V,
+                         int8_t *Qh, int8_t *Kh, int8_t *Vh, float *sQ, float *sK, float *sV,
+                         float *muK, float *muQ, void *workspace, size_t workspace_bytes,
+                         sage_stream_t stream) {
+    return quantize_call(p, nullptr, Q, K, V, Qh, Kh, Vh, sQ, sK, sV, muK, muQ, workspace,
+                         workspace_bytes, stream);
+}
+
+int sage_quantize_smooth_qknorm(const sage_params *p, const sage_qknorm *qn, const void *Q,
+                                const void *K, const void *V, int8_t *Qh, int8_t *Kh, int8_t *Vh,
+                                float *sQ, float *sK, float *sV, float *muK, float *muQ,
+                                void *workspace, size_t workspace_bytes, sage_stream_t stream) {
+    if (!qn) return SAGE_ERR_ARG;
+    return quantize_call(p, qn, Q, K, V, Qh, Kh, Vh, sQ, sK, sV, muK, muQ, workspace,
+                         workspace_bytes, stream);
+}
+
+int sage_qknorm_bwd(const sage_params *p, const void *X, const float *g, const float *r,
+                    const float *dY, float *dX, float *dg, sage_stream_t stream) {
+    SAGE_TRY(check_params(p));
+    SAGE_TRY(check_ptrs({X, r, dY, dX}));
+    if ((g && !aligned16(g)) || (dg && !aligned16(dg))) return SAGE_ERR_ALIGN;
+    if (static_cast<const void *>(dX) == static_cast<const void *>(dY)) return SAGE_ERR_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dg) SAGE_CUDA(cudaMemsetAsync(dg, 0, static_cast<size_t>(p->d) * sizeof(float), st));
+    SAGE_CUDA(launch_qknorm_bwd(*p, X, g, r, dY, dX, dg, st));
     return SAGE_OK;
 }
 

@@ -28,6 +28,16 @@ struct QuantArgs {
     int N, d, smooth_k, smooth_q;
     int z_base;               // first tensor of the launch: 0 = Q, 1 = K, 2 = V
     int fp8;                  // 1: E4M3 codes, delta = max|x| / 448 (SAGE_FLAG_FP8)
+    int qk_norm;              // 1: QK-norm prologue (arguments in QkNormArgs)
+};
+
+// QK-norm prologue: Q (index 0) and K (index 1) are RMS-normalised per token.  A kernel parameter
+// of its own: folding these fields into QuantArgs raised the plain quantiser's register count.
+struct QkNormArgs {
+    float eps;
+    const float *gamma[2];    // (d) scales or NULL (ones)
+    float *rnorm[2];          // (B,H,N) row factors (written)
+    void *xnorm[2];           // (B,H,N,d) normalised 16-bit tensors or NULL
 };
 
 struct BwdPrologueArgs {
@@ -72,11 +82,16 @@ struct BwdArgs {
 
 // sage_quant.cu
 int kmean_splits(const sage_params &p);
-cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st);
+cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st,
+                            const QkNormArgs *qn = nullptr);
 cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st);   // V only
 // int8 codes (or E4M3 bit patterns when fp8) -> their exact fp16 values
 cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, bool fp8, cudaStream_t st);
 cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStream_t st);
+// gradient of the QK-norm: dX = r (g dY - xh mean(g dY xh)), xh = x r; dg (nullable, zeroed by
+// the caller) += sum over rows of dY xh
+cudaError_t launch_qknorm_bwd(const sage_params &p, const void *X, const float *g, const float *r,
+                              const float *dY, float *dX, float *dg, cudaStream_t st);
 cudaError_t launch_qbias(const sage_params &p, const void *K, const float *muK, const float *muQ,
                          float *bias, float sl2, cudaStream_t st);
 

@@ -14,6 +14,9 @@
 //   code         = clamp(rint_half_even(fl32(x / delta)), -127, 127), zero block -> delta 0, code 0
 // FP8 variant ("SageAttention3 ..." (review), INT8 vs FP8 training): delta = fl32(max|x| / 448)
 // and code = E4M3(fl32(x / delta)), round to nearest even, saturating at +-448.
+// QK-norm prologue ("SageBwd ..." (structured summary), QK-norm; norm epsilon 1e-6): Q and K rows
+// become y = rnd16(fl32(fl32(x r) gamma_c)), r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))) with
+// S = fl32(exact sum of x^2), before the K-mean, the smoothing and the quantiser see them.
 //
 // All kernels here stream through HBM once; they are bound by memory bandwidth.
 #include "sage_device.cuh"
@@ -89,6 +92,99 @@ __device__ __forceinline__ uint4 pack_codes8_f16(const float (&x)[8], float delt
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+template <typename T>
+__device__ __forceinline__ float round_to(float y);
+template <>
+__device__ __forceinline__ float round_to<__half>(float y) { return __half2float(__float2half_rn(y)); }
+template <>
+__device__ __forceinline__ float round_to<__nv_bfloat16>(float y) { return __bfloat162float(__float2bfloat16_rn(y)); }
+
+// s + e = a + b exactly (Knuth's two-sum; the error term does not depend on the operand order)
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// QK-norm of this lane's 8 values of a row whose d / 8 slices sit in `lanes` consecutive lanes
+// (every lane of the warp takes part).  The squares of 16-bit values are exact in float32 (bf16:
+// for 2^-63 <= |x| < 2^63).  They are summed as an unevaluated float32 triple h + l + t with
+// two-sums, whose only rounding is in t (relative 2^-65 over a row); a butterfly of the same
+// exact steps leaves the same triple in every lane of the row.  h then becomes fl32(h + l + t),
+// the exact sum rounded once (a tie in h + l is settled by the sign of t).
+// Returns r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))) and replaces v by rnd_T(fl32(fl32(v r) g_c)).
+template <typename T>
+__device__ __forceinline__ float qk_norm8(float (&v)[8], const float *gamma, int c0, int lanes,
+                                          int d, float eps) {
+    float h = 0.0f, l = 0.0f, t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float e1, e2;
+        two_sum(h, __fmul_rn(v[i], v[i]), h, e1);
+        two_sum(l, e1, l, e2);
+        t = __fadd_rn(t, e2);
+    }
+    for (int o = 1; o < lanes; o <<= 1) {
+        const float ho = __shfl_xor_sync(0xffffffffu, h, o);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+        const float to = __shfl_xor_sync(0xffffffffu, t, o);
+        float e1, e2, e3;
+        two_sum(h, ho, h, e1);
+        two_sum(l, lo, l, e2);
+        two_sum(l, e1, l, e3);
+        t = __fadd_rn(__fadd_rn(__fadd_rn(t, to), e2), e3);
+    }
+    // S = h + l + t exactly (up to t's own roundings): round it once to float32
+    {
+        float e;
+        two_sum(l, t, l, t);                      // l = fl32(l + t), t = its error
+        two_sum(h, l, h, e);                      // h = fl32(h + l), e = h + l - h (exact)
+        // h + e on a midpoint between floats: the sign of t decides (S >= 0, h >= 0).  The
+        // midpoint above h lies half an ulp of h's binade away; below a power of two, half that.
+        float half_ulp = __uint_as_float((__float_as_uint(h) & 0x7F800000u)) * 0x1p-24f;
+        if (e < 0.0f && (__float_as_uint(h) & 0x7FFFFFu) == 0u) half_ulp *= 0.5f;
+        if (t != 0.0f && h > 0.0f && fabsf(e) == half_ulp && ((e > 0.0f) == (t > 0.0f)))
+            h = __fadd_rn(h, __fmul_rn(2.0f, e));
+    }
+    const float ms = __fmul_rn(h, 1.0f / static_cast<float>(d));         // exact: d = 64 or 128
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+    float g[8] = {1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f};
+    if (gamma) {
+        *reinterpret_cast<float4 *>(&g[0]) = *reinterpret_cast<const float4 *>(gamma + c0);
+        *reinterpret_cast<float4 *>(&g[4]) = *reinterpret_cast<const float4 *>(gamma + c0 + 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float y = __fmul_rn(v[i], r);
+        if (gamma) y = __fmul_rn(y, g[i]);
+        v[i] = round_to<T>(y);
+    }
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]);
+template <>
+__device__ __forceinline__ uint4 pack8<__half>(const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ uint4 pack8<__nv_bfloat16>(const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Block-wide max of non-negative floats (256 threads).
 __device__ __forceinline__ float block_max_256(float v, float *red) {
 #pragma unroll
@@ -119,11 +215,62 @@ __device__ __forceinline__ long long half_fixed24(uint32_t h) {
 // as exact: a sum of 32768 values stays below 2^55, and any sum below 2^53 is exact in both);
 // bf16 input (exponent range of float32): float64.  Both occupy 8 bytes per entry.
 // ---------------------------------------------------------------------------------------------
-template <typename T>
+// With QK-norm (NORM) the rows are normalised first; the loop then runs warp-uniform trip counts
+// (rows past the split are zeros and not added) because the norm's shuffles need every lane.
+template <typename T, bool NORM>
 __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict__ K,
                                                             double *__restrict__ partial, int N,
-                                                            int d, int S, int rows_per_split) {
-    if constexpr (std::is_same<T, __half>::value) {
+                                                            int d, int S, int rows_per_split,
+                                                            const float *__restrict__ gamma, float eps) {
+    if constexpr (NORM) {
+        __shared__ double redn[256 * 8];
+        const int bh = blockIdx.x, s = blockIdx.y;
+        const int vec_per_row = d / 8;
+        const int rows_in_flight = 256 / vec_per_row;
+        const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+        const int n0 = s * rows_per_split;
+        const int n1 = min(N, n0 + rows_per_split);
+        long long acci[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        double accd[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const T *base = K + static_cast<size_t>(bh) * N * d;
+        // unrolled: the norm's two-sum chains of several rows overlap
+#pragma unroll 4
+        for (int b0 = n0; b0 < n1; b0 += rows_in_flight) {
+            const int n = b0 + rg;
+            float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (n < n1) load8(base + static_cast<size_t>(n) * d + cv * 8, v);
+            qk_norm8<T>(v, gamma, cv * 8, vec_per_row, d, eps);
+            if (n < n1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if constexpr (std::is_same<T, __half>::value)
+                        acci[i] += half_fixed24(__half_as_ushort(__float2half_rn(v[i])));
+                    else
+                        accd[i] += static_cast<double>(v[i]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (std::is_same<T, __half>::value)
+                reinterpret_cast<long long *>(redn)[threadIdx.x * 8 + i] = acci[i];
+            else
+                redn[threadIdx.x * 8 + i] = accd[i];
+        }
+        __syncthreads();
+        if (threadIdx.x < d) {
+            const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
+            if constexpr (std::is_same<T, __half>::value) {
+                long long sum = 0;
+                for (int g = 0; g < rows_in_flight; ++g) sum += reinterpret_cast<long long *>(redn)[(g * vec_per_row + cvv) * 8 + ci];
+                reinterpret_cast<long long *>(partial)[(static_cast<size_t>(bh) * S + s) * d + c] = sum;
+            } else {
+                double sum = 0.0;
+                for (int g = 0; g < rows_in_flight; ++g) sum += redn[(g * vec_per_row + cvv) * 8 + ci];
+                partial[(static_cast<size_t>(bh) * S + s) * d + c] = sum;
+            }
+        }
+    } else if constexpr (std::is_same<T, __half>::value) {
         __shared__ long long redi[256 * 8];
         const int bh = blockIdx.x, s = blockIdx.y;
         const int vec_per_row = d / 8;
@@ -182,8 +329,8 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
 // ---------------------------------------------------------------------------------------------
 // a2: smoothing + per-block quantisation of Q (z=0), K (z=1), V (z=2).  One 64 x d block per CTA.
 // ---------------------------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
+template <typename T, bool NORM, bool FP8>
+__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs qn) {
     __shared__ float red[8];
     __shared__ float mu_s[128];
     __shared__ double colsum[256 * 8];
@@ -191,6 +338,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     const int d = a.d, N = a.N;
     const T *src = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
     int8_t *dst = z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh);
+    const bool norm = NORM && z < 2;                   // uniform over the CTA
+    const float *gamma = norm ? qn.gamma[z] : nullptr;
     float *scale = z == 0 ? a.sQ : (z == 1 ? a.sK : a.sV);
     const int vec_per_row = d / 8;
     const int rows_in_flight = 256 / vec_per_row;
@@ -224,6 +373,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
             const int r = rg + it * rows_in_flight;
             float v[8];
             load8(src + blk_off + static_cast<size_t>(r) * d + cv * 8, v);
+            if (norm) qk_norm8<T>(v, gamma, cv * 8, vec_per_row, d, qn.eps);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] += static_cast<double>(v[i]);
         }
@@ -250,6 +400,13 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
         if (it >= iters) break;
         const int r = rg + it * rows_in_flight;
         load8(src + blk_off + static_cast<size_t>(r) * d + cv * 8, x[it]);
+        if (norm) {
+            const float rf = qk_norm8<T>(x[it], gamma, cv * 8, vec_per_row, d, qn.eps);
+            if (cv == 0) qn.rnorm[z][static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r] = rf;
+            if (qn.xnorm[z])
+                *reinterpret_cast<uint4 *>(static_cast<T *>(qn.xnorm[z]) + blk_off + static_cast<size_t>(r) * d + cv * 8) =
+                    pack8<T>(x[it]);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (smooth) x[it][i] = __fsub_rn(x[it][i], mu_s[cv * 8 + i]);
@@ -257,13 +414,13 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
         }
     }
     mx = block_max_256(mx, red);
-    const float delta = __fdiv_rn(mx, a.fp8 ? 448.0f : 127.0f);
+    const float delta = __fdiv_rn(mx, FP8 ? 448.0f : 127.0f);
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         if (it >= iters) break;
         const int r = rg + it * rows_in_flight;
         *reinterpret_cast<uint2 *>(dst + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-            a.fp8 ? pack_codes8_e4m3(x[it], delta) : pack_codes8(x[it], delta);
+            FP8 ? pack_codes8_e4m3(x[it], delta) : pack_codes8(x[it], delta);
     }
     if (threadIdx.x == 0) scale[static_cast<size_t>(bh) * (N / 64) + blk] = delta;
 }
@@ -402,6 +559,23 @@ __global__ void __launch_bounds__(256) qbias_kernel(const T *__restrict__ K,
 // ---------------------------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------------------------
+template <typename T>
+static void launch_quantize_t(const QuantArgs &a, const QkNormArgs &qn, dim3 g, cudaStream_t st) {
+    if (a.qk_norm) {
+        if (a.fp8) quantize_kernel<T, true, true><<<g, 256, 0, st>>>(a, qn);
+        else quantize_kernel<T, true, false><<<g, 256, 0, st>>>(a, qn);
+    } else {
+        if (a.fp8) quantize_kernel<T, false, true><<<g, 256, 0, st>>>(a, qn);
+        else quantize_kernel<T, false, false><<<g, 256, 0, st>>>(a, qn);
+    }
+}
+
+static void launch_quantize_grid(const sage_params &p, const QuantArgs &a, const QkNormArgs &qn,
+                                 dim3 g, cudaStream_t st) {
+    if (p.dtype == SAGE_FP16) launch_quantize_t<__half>(a, qn, g, st);
+    else launch_quantize_t<__nv_bfloat16>(a, qn, g, st);
+}
+
 int kmean_splits(const sage_params &p) {
     const int bh = p.B * p.H;
     int s = (2 * 152 + bh - 1) / bh;
@@ -409,22 +583,27 @@ int kmean_splits(const sage_params &p) {
     return s < 1 ? 1 : (s > max_s ? max_s : s);
 }
 
-cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st) {
+cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st, const QkNormArgs *qn) {
+    QkNormArgs nq{};
+    if (qn) nq = *qn;
     const int bh = p.B * p.H;
     if (p.smooth_k) {
         const int S = a.ksplits;
         const int rows = (p.N + S - 1) / S;
         dim3 g(bh, S);
-        if (p.dtype == SAGE_FP16)
-            kmean_partial_kernel<__half><<<g, 256, 0, st>>>(static_cast<const __half *>(a.K), const_cast<double *>(a.kpartial), p.N, p.d, S, rows);
-        else
-            kmean_partial_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.K), const_cast<double *>(a.kpartial), p.N, p.d, S, rows);
+        double *part = const_cast<double *>(a.kpartial);
+        if (p.dtype == SAGE_FP16) {
+            const __half *K = static_cast<const __half *>(a.K);
+            if (a.qk_norm) kmean_partial_kernel<__half, true><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nq.gamma[1], nq.eps);
+            else kmean_partial_kernel<__half, false><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nullptr, 0.0f);
+        } else {
+            const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.K);
+            if (a.qk_norm) kmean_partial_kernel<__nv_bfloat16, true><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nq.gamma[1], nq.eps);
+            else kmean_partial_kernel<__nv_bfloat16, false><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nullptr, 0.0f);
+        }
     }
     dim3 g(p.N / 64, bh, 3);
-    if (p.dtype == SAGE_FP16)
-        quantize_kernel<__half><<<g, 256, 0, st>>>(a);
-    else
-        quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(a);
+    launch_quantize_grid(p, a, nq, g, st);
     return cudaGetLastError();
 }
 
@@ -432,10 +611,7 @@ cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st) 
 cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st) {
     a.z_base = 2;
     dim3 g(p.N / 64, p.B * p.H, 1);
-    if (p.dtype == SAGE_FP16)
-        quantize_kernel<__half><<<g, 256, 0, st>>>(a);
-    else
-        quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(a);
+    launch_quantize_grid(p, a, QkNormArgs{}, g, st);
     return cudaGetLastError();
 }
 
@@ -457,6 +633,82 @@ cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStr
         bwd_prologue_kernel<__half><<<g, 256, 0, st>>>(a);
     else
         bwd_prologue_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// QK-norm gradient.  Rows of d / 8 lanes (as in the quantiser), warp-uniform grid-stride loop;
+// dg partials per thread, reduced over the CTA's row groups, one float32 reduction per channel.
+// ---------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) qknorm_bwd_kernel(const T *__restrict__ X,
+                                                         const float *__restrict__ g,
+                                                         const float *__restrict__ r,
+                                                         const float *__restrict__ dY,
+                                                         float *__restrict__ dX,
+                                                         float *__restrict__ dg, size_t rows, int d) {
+    __shared__ float red[256 * 8];
+    const int vec_per_row = d / 8;
+    const int rows_in_flight = 256 / vec_per_row;
+    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+    float gg[8] = {1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f};
+    if (g) {
+        *reinterpret_cast<float4 *>(&gg[0]) = *reinterpret_cast<const float4 *>(g + cv * 8);
+        *reinterpret_cast<float4 *>(&gg[4]) = *reinterpret_cast<const float4 *>(g + cv * 8 + 4);
+    }
+    float dga[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const float inv_d = 1.0f / static_cast<float>(d);
+    for (size_t b0 = static_cast<size_t>(blockIdx.x) * rows_in_flight; b0 < rows;
+         b0 += static_cast<size_t>(gridDim.x) * rows_in_flight) {
+        const size_t row = b0 + rg;
+        const bool ok = row < rows;
+        float x[8] = {0, 0, 0, 0, 0, 0, 0, 0}, dy[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        float rr = 0.0f;
+        if (ok) {
+            load8(X + row * d + cv * 8, x);
+            *reinterpret_cast<float4 *>(&dy[0]) = *reinterpret_cast<const float4 *>(dY + row * d + cv * 8);
+            *reinterpret_cast<float4 *>(&dy[4]) = *reinterpret_cast<const float4 *>(dY + row * d + cv * 8 + 4);
+            rr = r[row];
+        }
+        float xh[8], gdy[8], part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            xh[i] = x[i] * rr;
+            gdy[i] = gg[i] * dy[i];
+            part = fmaf(gdy[i], xh[i], part);
+            dga[i] = fmaf(dy[i], xh[i], dga[i]);
+        }
+        for (int o = 1; o < vec_per_row; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        const float m = part * inv_d;
+        if (ok) {
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = rr * fmaf(-xh[i], m, gdy[i]);
+            *reinterpret_cast<float4 *>(dX + row * d + cv * 8) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4 *>(dX + row * d + cv * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        }
+    }
+    if (!dg) return;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[threadIdx.x * 8 + i] = dga[i];
+    __syncthreads();
+    if (threadIdx.x < d) {
+        const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
+        float sum = 0.0f;
+        for (int q = 0; q < rows_in_flight; ++q) sum += red[(q * vec_per_row + cvv) * 8 + ci];
+        atomicAdd(dg + c, sum);
+    }
+}
+
+cudaError_t launch_qknorm_bwd(const sage_params &p, const void *X, const float *g, const float *r,
+                              const float *dY, float *dX, float *dg, cudaStream_t st) {
+    const size_t rows = static_cast<size_t>(p.B) * p.H * p.N;
+    const size_t groups = (rows + (2048 / p.d) - 1) / (2048 / p.d);
+    const int blocks = static_cast<int>(groups < 152 * 8 ? groups : 152 * 8);
+    if (p.dtype == SAGE_FP16)
+        qknorm_bwd_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const __half *>(X), g, r, dY, dX, dg, rows, p.d);
+    else
+        qknorm_bwd_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(X), g, r, dY, dX, dg, rows, p.d);
     return cudaGetLastError();
 }
 

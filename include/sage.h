@@ -113,6 +113,48 @@ SAGE_API int sage_quantize_smooth(const sage_params *p, const void *Q, const voi
                          sage_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------ *
+ * Step 1 with the QK-norm prologue fused in, and the QK-norm gradient.
+ * "SageBwd: A Trainable Low-bit Attention" (structured summary), QK-norm: each token's query and
+ * key vector is RMS-normalised, RMSNorm(x) = x / sqrt((1/d) sum_c x_c^2) * gamma, gamma a learnable
+ * scale vector; the reproduction paragraph gives the norm epsilon 1e-6 (added to the mean square).
+ *
+ * sage_quantize_smooth_qknorm: as sage_quantize_smooth, on the normalised Q and K:
+ *   r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))) per token, S = fl32(sum_c x_c^2), the exact sum
+ *       rounded once (every step a correctly rounded float32 operation, independent of any
+ *       summation order; bf16 inputs need 2^-63 <= |x| < 2^63 or x = 0 for exact squares);
+ *   y = rnd(fl32(fl32(x r) * gamma_c)) rounded to the input dtype, so the call equals a separate
+ *       norm writing a 16-bit tensor followed by sage_quantize_smooth.  V is not normalised.
+ *   Same workspace as sage_quantize_smooth.  With smooth_q = 1, Kn is required and is the K to
+ *   pass to sage_attn_fwd / sage_attn_bwd (the Q-smoothing bias reads the normalised K).
+ *   Errors: SAGE_ERR_ARG for a NULL qn, rQ or rK, a negative or non-finite eps, or smooth_q = 1
+ *   without Kn; the rules of sage_quantize_smooth otherwise.
+ * sage_qknorm_bwd: the gradient of y = gamma * x * r(x) for one of the two tensors (the rounding
+ *   to 16 bits is taken as the identity), in float32:
+ *   dX = r (gamma dY - xh * mean_c(gamma_c dY_c xh_c)), xh = x r;
+ *   dg (nullable, (d) float32, overwritten) = sum over all B*H*N tokens of dY * xh, by float32
+ *   reductions (not bit-reproducible).
+ *   In: X (B,H,N,d) the raw Q or K (input dtype), g (nullable) its gamma, r the row factors the
+ *   forward call wrote, dY (B,H,N,d) float32 (the gradient sage_attn_bwd wrote for the normalised
+ *   tensor).  Out: dX (B,H,N,d) float32.  dX may not alias dY.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct sage_qknorm {
+    const float *gQ;   /* (d) float32 gamma of Q, or NULL for ones (device)                    */
+    const float *gK;   /* (d) float32 gamma of K, or NULL for ones (device)                    */
+    float eps;         /* added to the mean square; the pages' setup uses 1e-6                  */
+    float *rQ;         /* out: (B,H,N) float32 row factors r of Q                               */
+    float *rK;         /* out: (B,H,N) float32 row factors r of K                               */
+    void *Qn;          /* out, nullable: (B,H,N,d) normalised Q in the input dtype              */
+    void *Kn;          /* out, nullable (required when smooth_q = 1): normalised K              */
+} sage_qknorm;
+
+SAGE_API int sage_quantize_smooth_qknorm(const sage_params *p, const sage_qknorm *qn,
+                         const void *Q, const void *K, const void *V, int8_t *Qh, int8_t *Kh,
+                         int8_t *Vh, float *sQ, float *sK, float *sV, float *muK, float *muQ,
+                         void *workspace, size_t workspace_bytes, sage_stream_t stream);
+SAGE_API int sage_qknorm_bwd(const sage_params *p, const void *X, const float *g, const float *r,
+                         const float *dY, float *dX, float *dg, sage_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ *
  * Step 2 -- forward.
  * "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps, forward (3)-(5);
  * "SageAttention3 ..." (review) eq. (1) online softmax and eq. (8): S_ij = MM(Q^_i, K^_j) s_Q s_K,

@@ -6,9 +6,11 @@ key vector is RMS-normalised, RMSNorm(x) = x / sqrt((1/d) sum_i x_i^2) * gamma w
 scale vector gamma; reproduction paragraph: norm epsilon 1e-6 (read as added to the mean square).
 
 Readings where the pages leave a step open (listed again in the design doc, R18):
-  * the mean square is the exact sum of the squares rounded once to float64 (math.fsum), divided
-    by d (a power of two, exact); r = fl32(1 / sqrt(ms + eps)) with each step an IEEE float64
-    operation and one final rounding to float32;
+  * the sum of squares is the exact sum rounded once to float32, S = fl32(sum_c x_c^2); then, in
+    IEEE float32 operations, ms = S / d (exact, d a power of two), v = fl32(ms + eps),
+    s = fl32(sqrt(v)), r = fl32(1 / s); eps is a float32 value (1e-6 rounded to float32 in the
+    pages' setup).  Every step is a correctly rounded float32 operation on a uniquely defined
+    value, so the result does not depend on any summation order;
   * the normalised value is y = round_dtype(fl32(fl32(x * r) * gamma_c)): the fused prologue
     produces exactly what a separate norm writing a 16-bit tensor would, and everything after it
     (K-mean, smoothing, quantisation) runs on those 16-bit values;
@@ -23,21 +25,40 @@ scaling, a hand-worked row).
 """
 from __future__ import annotations
 
-import math
+from fractions import Fraction
 
 import numpy as np
 
 F32 = np.float32
 
 
+def round_f32(q: Fraction) -> np.float32:
+    """The float32 nearest to a non-negative rational (ties to even); normal range only."""
+    if q == 0:
+        return F32(0)
+    e = q.numerator.bit_length() - q.denominator.bit_length()     # 2^e <= q < 2^(e+2)
+    if Fraction(2) ** e > q:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= q:
+        e += 1
+    scaled = q / Fraction(2) ** (e - 23)                             # in [2^23, 2^24)
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return F32(n * 2.0 ** (e - 23))
+
+
 def row_factor(x, eps: float) -> np.ndarray:
-    """r = fl32(1 / sqrt(fl64(fsum(x^2)) / d + eps)) per row of (..., d) float values."""
-    x = np.asarray(x, np.float64)
+    """r = fl32(1 / fl32(sqrt(fl32(fl32(sum x^2) / d + eps)))) per row of (..., d) 16-bit values,
+    the sum exact before its one rounding."""
+    x = np.asarray(x, np.float32)
     d = x.shape[-1]
     flat = x.reshape(-1, d)
-    ss = np.array([math.fsum(v * v for v in row) for row in flat])    # exact sum, one rounding
-    ms = ss / d
-    r = 1.0 / np.sqrt(ms + np.float64(eps))
+    S = np.array([round_f32(sum(Fraction(float(v)) ** 2 for v in row)) for row in flat], np.float32)
+    ms = S / F32(d)
+    v = ms + F32(eps)
+    r = F32(1) / np.sqrt(v)
     return r.astype(np.float32).reshape(x.shape[:-1])
 
 

@@ -103,3 +103,33 @@ def test_null_misaligned_and_workspace(sg):
     qargs = [_fake(i) for i in range(12)]
     qargs[9] = None   # muK
     assert L.sage_quantize_smooth(ctypes.byref(p), *qargs, 1 << 30, None) == 1
+
+
+def test_qknorm_argument_checks(sg):
+    """The QK-norm calls refuse bad arguments before any launch (fake device pointers are never
+    dereferenced)."""
+    L = sg.lib()
+    p = sg.make_params(1, 1, 128, 64, 0, False)
+    args = [_fake(i) for i in range(12)]
+    QN = sg.binding.SageQkNorm
+
+    def call(qn, params=p):
+        return L.sage_quantize_smooth_qknorm(ctypes.byref(params), None if qn is None else ctypes.byref(qn),
+                                             *args, 1 << 30, None)
+
+    assert call(None) == 1
+    assert call(QN(None, None, -1.0, _fake(20), _fake(21), None, None)) == 1
+    assert call(QN(None, None, float("nan"), _fake(20), _fake(21), None, None)) == 1
+    assert call(QN(None, None, float("inf"), _fake(20), _fake(21), None, None)) == 1
+    assert call(QN(None, None, 1e-6, None, _fake(21), None, None)) == 1
+    assert call(QN(None, None, 1e-6, _fake(20) + 4, _fake(21), None, None)) == 3
+    assert call(QN(_fake(22) + 8, None, 1e-6, _fake(20), _fake(21), None, None)) == 3
+    psq = sg.make_params(1, 1, 128, 64, 0, False, smooth_q=True)
+    assert call(QN(None, None, 1e-6, _fake(20), _fake(21), None, None), psq) == 1    # smooth_q needs Kn
+    bad = sg.make_params(1, 1, 100, 64, 0, False)
+    assert call(QN(None, None, 1e-6, _fake(20), _fake(21), None, None), bad) == 2
+    # the gradient call: null input, dX aliasing dY, misaligned gamma
+    f = [_fake(i) for i in range(6)]
+    assert L.sage_qknorm_bwd(ctypes.byref(p), None, None, f[2], f[3], f[4], None, None) == 1
+    assert L.sage_qknorm_bwd(ctypes.byref(p), f[1], None, f[2], f[3], f[3], None, None) == 1
+    assert L.sage_qknorm_bwd(ctypes.byref(p), f[1], f[0] + 4, f[2], f[3], f[4], None, None) == 3
