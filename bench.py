@@ -226,9 +226,23 @@ def run_gpu(args, w: workloads.Workload):
         gen = torch.Generator(device="cpu").manual_seed(rank)
         gam = [(0.5 + torch.rand(d, generator=gen)).to(device) for _ in range(2)]
 
+    if args.fp4:
+        # the FP4 leg is an inference forward: no dO
+        host.pop("dO")
+        dev.pop("dO")
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
+        if args.fp4:
+            q4 = sg.sage_quantize_fp4(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q)
+            if ev is not None:
+                ev[1].record(stream)
+            sg.sage_attn_fwd_fp4(q4, causal=w.causal, out=O, lse=Lse, workspace=ws_f)
+            if ev is not None:
+                for e in ev[2:]:
+                    e.record(stream)
+            return
         if args.qk_norm:
             q = sg.sage_quantize_smooth_qknorm(dev["Q"], dev["K"], dev["V"], gamma_q=gam[0], gamma_k=gam[1],
                                                smooth_q=w.smooth_q, fp8=args.fp8)
@@ -283,10 +297,11 @@ def run_gpu(args, w: workloads.Workload):
     ms_max = max_over_ranks(dist, ms, device)
 
     # ---- end to end through the public API with host buffers ------------------------------
-    host_out = {"O": torch.empty_like(O, device="cpu").pin_memory(),
-                "dQ": torch.empty_like(grads[0], device="cpu").pin_memory(),
-                "dK": torch.empty_like(grads[1], device="cpu").pin_memory(),
-                "dV": torch.empty_like(grads[2], device="cpu").pin_memory()}
+    host_out = {"O": torch.empty_like(O, device="cpu").pin_memory()}
+    if not args.fp4:
+        host_out.update({"dQ": torch.empty_like(grads[0], device="cpu").pin_memory(),
+                         "dK": torch.empty_like(grads[1], device="cpu").pin_memory(),
+                         "dV": torch.empty_like(grads[2], device="cpu").pin_memory()})
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
@@ -295,8 +310,9 @@ def run_gpu(args, w: workloads.Workload):
             dev[k].copy_(host[k], non_blocking=True)
         step()
         host_out["O"].copy_(O, non_blocking=True)
-        for name, g in zip(("dQ", "dK", "dV"), grads):
-            host_out[name].copy_(g, non_blocking=True)
+        if not args.fp4:
+            for name, g in zip(("dQ", "dK", "dV"), grads):
+                host_out[name].copy_(g, non_blocking=True)
 
     for _ in range(max(1, args.warmup // 2)):
         e2e_step()
@@ -310,9 +326,9 @@ def run_gpu(args, w: workloads.Workload):
     torch.cuda.synchronize(device)
     barrier(dist, device)
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
-    assert np.isfinite(host_out["dQ"].float().numpy()).all()
+    assert np.isfinite(host_out["O" if args.fp4 else "dQ"].float().numpy()).all()
 
-    ops = step_ops(w)
+    ops = fwd_ops(w) if args.fp4 else step_ops(w)
     value = world * ops * args.steps / (ms_max * 1e-3) / 1e12
     e2e_value = world * ops * args.steps / (e2e_ms * 1e-3) / 1e12
 
@@ -320,7 +336,7 @@ def run_gpu(args, w: workloads.Workload):
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
     peak_src = "measured (bf16_tflops_sustained; fp16 runs at the bf16 rate)" if peaks else "fallback"
-    bwd_tflops = bwd_ops(w) / (bwd_ms * 1e-3) / 1e12
+    bwd_tflops = bwd_ops(w) / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else 0.0
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     quant_gbs = quant_bytes(w) / (quant_ms * 1e-3) / 1e9
     fwd_tflops = fwd_ops(w) / (fwd_ms * 1e-3) / 1e12
@@ -359,6 +375,17 @@ def run_gpu(args, w: workloads.Workload):
         line["qknorm_bwd_calls"] = {"ms": round(qkn_ms, 4), "bound": "hbm", "bytes": 2 * qknorm_bwd_bytes(w),
                                     "gbs": round(gbs, 1), "peak_gbs": hbm_peak, "frac": round(gbs / hbm_peak, 4)}
         line["config"]["qk_norm"] = True
+    if args.fp4:
+        # the FP4 leg times quantise + forward only: its value is forward TOPS
+        line["metric"] = "SageAttention3 FP4 inference forward TOPS (N=8192,d=128)"
+        line["dtype"] = "NVFP4 (e2m1 codes, e4m3 scales per 16) dequantised to f16 (f32 accumulate)"
+        line["config"]["fp4_forward"] = True
+        line["roofline"] = {"kernel": "sage_attn_fwd_fp4 call (widen + tcgen05 forward kernel)",
+                            "bound": "tensor", "achieved": round(fwd_tflops, 1), "peak": peak,
+                            "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(fwd_tflops / peak, 4),
+                            "traffic": None, "flops_per_launch": fwd_ops(w)}
+        line.pop("bwd_call", None)
+        line["gpu_launches"] = 6 * args.steps        # K-mean, FP4 quantise, 3 widen, forward
     return line
 
 
@@ -448,6 +475,8 @@ def main():
                     help="the FP8 SageBwd variant (E4M3 codes in place of INT8)")
     ap.add_argument("--qk-norm", action="store_true",
                     help="QK-norm fused into the quantise call, and its gradient after the backward")
+    ap.add_argument("--fp4", action="store_true",
+                    help="the SageAttention3 FP4 inference forward (quantise + forward only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")

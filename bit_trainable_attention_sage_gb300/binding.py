@@ -26,7 +26,7 @@ EXPORTED = (
     "sage_quantize_workspace_bytes", "sage_quantize_smooth", "sage_fwd_workspace_bytes",
     "sage_attn_fwd", "sage_bwd_workspace_bytes", "sage_attn_bwd", "sage_dump_bytes",
     "sage_device_status", "sage_status_string", "sage_version", "sage_quantize_smooth_qknorm",
-    "sage_qknorm_bwd",
+    "sage_qknorm_bwd", "sage_quantize_fp4", "sage_attn_fwd_fp4",
 )
 
 
@@ -80,6 +80,10 @@ def lib() -> ctypes.CDLL:
     L.sage_quantize_smooth_qknorm.restype = ci
     L.sage_qknorm_bwd.argtypes = [P] + [vp] * 6 + [vp]
     L.sage_qknorm_bwd.restype = ci
+    L.sage_quantize_fp4.argtypes = [P] + [vp] * 12 + [sz, vp]
+    L.sage_quantize_fp4.restype = ci
+    L.sage_attn_fwd_fp4.argtypes = [P] + [vp] * 12 + [sz, vp]
+    L.sage_attn_fwd_fp4.restype = ci
     L.sage_attn_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sage_attn_fwd.restype = ci
     L.sage_attn_bwd.argtypes = [P] + [vp] * 15 + [sz, vp]
@@ -240,6 +244,67 @@ def sage_qknorm_bwd(X: torch.Tensor, r: torch.Tensor, dY: torch.Tensor, *, gamma
                                _ptr(dg), _stream(stream))
     _check("sage_qknorm_bwd", st)
     return dX, dg
+
+
+@dataclass
+class Fp4Quantized:
+    """NVFP4 inputs of the FP4 inference forward: packed E2M1 codes (uint8, two a byte) and E4M3
+    scale bytes -- sQ, sK (B,H,N,d/16) along d, sV (B,H,N/16,d) along the tokens -- plus means."""
+    Qc: torch.Tensor
+    Kc: torch.Tensor
+    Vc: torch.Tensor
+    sQ: torch.Tensor
+    sK: torch.Tensor
+    sV: torch.Tensor
+    muK: torch.Tensor
+    muQ: torch.Tensor | None
+    dtype: int
+    smooth_k: bool
+    smooth_q: bool
+
+
+def sage_quantize_fp4(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, smooth_k: bool = True,
+                      smooth_q: bool = False, stream=None) -> Fp4Quantized:
+    """Smoothing and NVFP4 quantisation (1 x 16 blocks, E4M3 scales) of (B,H,N,d) Q, K, V."""
+    _require_cuda(Q, K, V)
+    B, H, N, d = Q.shape
+    dt = _dtype_code(Q)
+    dev = Q.device
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    Qc, Kc, Vc = (torch.empty((B, H, N, d // 2), **u8) for _ in range(3))
+    sQ, sK = (torch.empty((B, H, N, d // 16), **u8) for _ in range(2))
+    sV = torch.empty((B, H, N // 16, d), **u8)
+    muK = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    muQ = torch.empty((B, H, N // 64, d), dtype=torch.float32, device=dev) if smooth_q else None
+    L = lib()
+    nws = L.sage_quantize_workspace_bytes(ctypes.byref(p))
+    ws = _workspace(nws, dev)
+    st = L.sage_quantize_fp4(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(Qc), _ptr(Kc), _ptr(Vc),
+                             _ptr(sQ), _ptr(sK), _ptr(sV), _ptr(muK), _ptr(muQ), _ptr(ws), nws, _stream(stream))
+    _check("sage_quantize_fp4", st)
+    return Fp4Quantized(Qc, Kc, Vc, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q)
+
+
+def sage_attn_fwd_fp4(q: Fp4Quantized, *, causal: bool, K: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None):
+    """SageAttention3 FP4 inference forward.  Returns (O in the input dtype, L float32)."""
+    B, H, N, d = q.Qc.shape[0], q.Qc.shape[1], q.Qc.shape[2], 2 * q.Qc.shape[3]
+    dev = q.Qc.device
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q)
+    odt = torch.float16 if q.dtype == SAGE_FP16 else torch.bfloat16
+    O = torch.empty((B, H, N, d), dtype=odt, device=dev) if out is None else out
+    Lse = torch.empty((B, H, N), dtype=torch.float32, device=dev) if lse is None else lse
+    _require_cuda(O, Lse, K)
+    L = lib()
+    nws = L.sage_fwd_workspace_bytes(ctypes.byref(p))
+    ws = workspace if workspace is not None else _workspace(nws, dev)
+    st = L.sage_attn_fwd_fp4(ctypes.byref(p), _ptr(q.Qc), _ptr(q.Kc), _ptr(q.Vc), _ptr(q.sQ), _ptr(q.sK),
+                             _ptr(q.sV), _ptr(K), _ptr(q.muK), _ptr(q.muQ), _ptr(O), _ptr(Lse), _ptr(ws),
+                             nws if ws is None else ws.numel(), _stream(stream))
+    _check("sage_attn_fwd_fp4", st)
+    return O, Lse
 
 
 def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,

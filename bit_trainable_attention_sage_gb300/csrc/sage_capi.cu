@@ -346,6 +346,54 @@ int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     return SAGE_OK;
 }
 
+int sage_quantize_fp4(const sage_params *p, const void *Q, const void *K, const void *V,
+                      uint8_t *Qc, uint8_t *Kc, uint8_t *Vc, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
+                      float *muK, float *muQ, void *workspace, size_t workspace_bytes,
+                      sage_stream_t stream) {
+    SAGE_TRY(check_params(p));
+    if (p->flags) return SAGE_ERR_UNSUPPORTED;
+    SAGE_TRY(check_ptrs({Q, K, V, Qc, Kc, Vc, sQ, sK, sV, muK}));
+    if (p->smooth_q) SAGE_TRY(check_ptrs({muQ}));
+    SAGE_TRY(check_ws(workspace, workspace_bytes, sage_quantize_workspace_bytes(p)));
+    QuantArgs a;
+    memset(&a, 0, sizeof(a));
+    a.Q = Q; a.K = K; a.V = V;
+    a.muK = muK; a.muQ = p->smooth_q ? muQ : nullptr;
+    a.ksplits = kmean_splits(*p);
+    a.kpartial = quant_ws(*p, p->smooth_k ? workspace : nullptr, nullptr).kpartial;
+    a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
+    Fp4Out o{Qc, Kc, Vc, sQ, sK, sV};
+    SAGE_CUDA(launch_quantize_fp4(*p, a, o, reinterpret_cast<cudaStream_t>(stream)));
+    return SAGE_OK;
+}
+
+int sage_attn_fwd_fp4(const sage_params *p, const uint8_t *Qc, const uint8_t *Kc, const uint8_t *Vc,
+                      const uint8_t *sQ, const uint8_t *sK, const uint8_t *sV, const void *K,
+                      const float *muK, const float *muQ, void *O, float *L, void *workspace,
+                      size_t workspace_bytes, sage_stream_t stream) {
+    SAGE_TRY(check_params(p));
+    if (p->flags) return SAGE_ERR_UNSUPPORTED;
+    SAGE_TRY(check_ptrs({Qc, Kc, Vc, sQ, sK, sV, O, L}));
+    if (p->smooth_q) SAGE_TRY(check_ptrs({K, muK, muQ}));
+    SAGE_TRY(check_ws(workspace, workspace_bytes, sage_fwd_workspace_bytes(p)));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    FwdWs w = fwd_ws(*p, workspace, nullptr);
+    SAGE_CUDA(launch_widen_fp4(Qc, sQ, w.q16, *p, false, st));
+    SAGE_CUDA(launch_widen_fp4(Kc, sK, w.k16, *p, false, st));
+    SAGE_CUDA(launch_widen_fp4(Vc, sV, w.v16, *p, true, st));
+    const float sl2 = scale_log2(p->d);
+    if (p->smooth_q) SAGE_CUDA(launch_qbias(*p, K, muK, muQ, w.qbias, sl2, st));
+    FwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.qbias = w.qbias;
+    a.O = O; a.L = L;
+    a.N = p->N; a.H = p->H; a.causal = p->causal; a.dtype = p->dtype;
+    a.sl2 = sl2;
+    a.fp4 = 1;
+    SAGE_CUDA(launch_fwd(*p, w.q16, w.k16, w.v16, a, st));
+    return SAGE_OK;
+}
+
 size_t sage_bwd_workspace_bytes(const sage_params *p) {
     if (check_params(p) != SAGE_OK) return 0;
     size_t b = 0;

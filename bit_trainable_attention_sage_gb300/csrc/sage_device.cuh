@@ -414,6 +414,38 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
     return r;
 }
+// FP4 E2M1 codes (1 sign, 2 exponent bits with bias 1, 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4,
+// 6).  The float32 -> E2M1 conversion rounds to nearest, ties to even, and saturates to +-6.
+// One byte holds two codes, `lo` in the low nibble; every E2M1 value is exact in fp16.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.u8.u32 t, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(r)
+        : "r"(byte));
+    return r;
+}
+// the E4M3 value nearest to s (ties even, saturating), as float
+__device__ __forceinline__ float e4m3_round_f(float s) {
+    const uint32_t h = e4m3x2_to_f16x2(e4m3x2(s, 0.0f));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // two float32 values rounded to E4M3 and returned as an fp16 pair (the MMA operand format)
 __device__ __forceinline__ uint32_t e4m3x2_f16x2(float lo, float hi) {
     uint32_t r;

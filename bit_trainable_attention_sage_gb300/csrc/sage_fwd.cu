@@ -37,6 +37,11 @@
 // E4M3 values, P^_k = e4m3(fl32(448 * ex2(x_k))) and the PV scale is (2^(r - m') / 448) s_V.
 // E4M3 values are exact fp16 operands; their products are exact in the fp32 accumulator, the
 // sums rounded as any fp32 accumulation.
+// FP4 inference forward ("SageAttention3 ..." (review), eq. (4)-(6)): Q, K, V arrive as their
+// dequantised NVFP4 values s * code (exact fp16, at most 5 significant bits), so c = fl32(log2(e) /
+// sqrt(d)) alone; P~2 = fl32(2688 ex2(x)) is quantised per 16 keys, s_P2 = e4m3(fl32(max / 6)),
+// code = e2m1(fl32(v fl32(1 / s_P2))), and the PV operand is s_P2 * code; the PV scale is
+// s_P1 = 2^(r - m') / 2688 (eq. (6) with the tile row max r).
 #include "sage_device.cuh"
 #include "sage_internal.h"
 
@@ -124,16 +129,48 @@ __device__ __forceinline__ float fwd_row_max(uint32_t (&raw)[64], float c, const
 // 1.5 * 2^23 and its subtraction (exact for the values 0..127 here, and a full-rate instruction,
 // unlike the conversion unit's round-to-integer).
 // FP8: P^ = e4m3(fl32(448 ex2(x))) instead, converted to fp16 in two instructions per pair.
-template <bool BIAS, bool MASKED, bool DUMP, bool FP8>
+// FP4: each 16-key group is an NVFP4 block of v = fl32(2688 ex2(x)) (two passes over the group:
+// its maximum, then the codes), written as the dequantised fp16 values.
+constexpr int kFmtInt8 = 0, kFmtFp8 = 1, kFmtFp4 = 2;
+
+template <bool BIAS, bool MASKED, bool DUMP, int FMT>
 __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, float rs,
                                            int nvalid, uint32_t code_col, int16_t *dump_row) {
     constexpr float kRound = 12582912.0f;          // 1.5 * 2^23
     const f2 c2{c, c}, nrs2{-rs, -rs}, rs2{rs, rs}, k127{127.0f, 127.0f}, kr2{kRound, kRound};
-    const f2 k448{448.0f, 448.0f};
+    const f2 k448{448.0f, 448.0f}, k2688{2688.0f, 2688.0f};
     f2 sp[2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 16) {
         uint32_t pk[8];
+        if (FMT == kFmtFp4) {
+            f2 e[8];
+            float emax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
+                f2 x2 = BIAS ? sub2(a2, rs2) : fma2(a2, c2, nrs2);
+                if (MASKED) {
+                    x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
+                    x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
+                }
+                e[k / 2] = f2{ex2_approx(x2.x), ex2_approx(x2.y)};
+                sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e[k / 2]);
+                emax = max3f(emax, e[k / 2].x, e[k / 2].y);
+            }
+            // max v = fl32(2688 max e): the rounding is monotonic
+            const float s2 = e4m3_round_f(__fdiv_rn(__fmul_rn(2688.0f, emax), 6.0f));
+            const float inv = s2 > 0.0f ? __frcp_rn(s2) : 0.0f;
+            const f2 inv2{inv, inv};
+            const uint32_t s2h = pack_half2(s2, s2);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const f2 y = mul2(mul2(k2688, e[k]), inv2);
+                pk[k] = hmul2(e2m1x2_to_f16x2(e2m1x2(y.x, y.y)), s2h);
+            }
+            tmem_st8(code_col + cc / 2, pk);
+            continue;
+        }
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
             // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
@@ -145,7 +182,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
             }
             const f2 e2{ex2_approx(x2.x), ex2_approx(x2.y)};
             sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e2);
-            if (FP8) {
+            if (FMT == kFmtFp8) {
                 const f2 v2 = mul2(k448, e2);
                 pk[k / 2] = e4m3x2_f16x2(v2.x, v2.y);
             } else {
@@ -163,7 +200,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
     return (sp[0].x + sp[1].x) + (sp[0].y + sp[1].y);
 }
 
-template <int D, typename OutT, bool BIAS, bool DUMP, bool FP8>
+template <int D, typename OutT, bool BIAS, bool DUMP, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, const FwdArgs a) {
@@ -303,7 +340,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int nblk = N >> 6;
         const int kv_end = kv_end_t[t];
         const int my_steps = nsteps_t[t];
-        const float sq = a.sQ[static_cast<size_t>(bh) * nblk + qblk];
+        // FP4: the block scales live inside the dequantised operands
+        const float sq = FMT == kFmtFp4 ? 1.0f : a.sQ[static_cast<size_t>(bh) * nblk + qblk];
         const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 256 * t);
         float o[D];
 #pragma unroll
@@ -320,7 +358,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (h == 1 && !has_b) break;
                 const int kb = 2 * j + h;                     // key block index
                 const int key0 = 64 * kb;
-                const float c = __fmul_rn(__fmul_rn(sq, a.sK[static_cast<size_t>(bh) * nblk + kb]), a.sl2);
+                const float c = FMT == kFmtFp4 ? a.sl2
+                                               : __fmul_rn(__fmul_rn(sq, a.sK[static_cast<size_t>(bh) * nblk + kb]), a.sl2);
                 // keys allowed for this row inside the block: [key0, key0 + nvalid)
                 int nvalid = a.causal ? min(64, grow - key0 + 1) : 64;
                 if (grow >= N) nvalid = 0;
@@ -349,8 +388,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 // S columns.  A warp with a masked column in any lane takes the masked variant.
                 int16_t *dump_row = DUMP && grow < N ? a.dump_p + (bhN + grow) * N + key0 : nullptr;
                 const float sum = __any_sync(0xffffffffu, nvalid < 64)
-                    ? fwd_codes<BIAS, true, DUMP, FP8>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
-                    : fwd_codes<BIAS, false, DUMP, FP8>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
+                    ? fwd_codes<BIAS, true, DUMP, FMT>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
+                    : fwd_codes<BIAS, false, DUMP, FMT>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
                 if (h == 0) sum_h0 = sum; else sum_h1 = sum;
             }
             const float r_h[2] = {r_h0, r_h1}, sum_h[2] = {sum_h0, sum_h1};
@@ -368,7 +407,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const float g = live ? ex2_approx(__fsub_rn(r_h[h], m_new)) : 0.0f;
                 l = (h == 0) ? __fmaf_rn(alpha, l, g * sum_h[h]) : __fmaf_rn(g, sum_h[h], l);
                 const int kb = min(2 * j + h, nblk - 1);
-                cpv[h] = (g * (FP8 ? 1.0f / 448.0f : 1.0f / 127.0f)) * a.sV[static_cast<size_t>(bh) * nblk + kb];
+                if (FMT == kFmtFp4)
+                    cpv[h] = g * (1.0f / 2688.0f);
+                else
+                    cpv[h] = (g * (FMT == kFmtFp8 ? 1.0f / 448.0f : 1.0f / 127.0f)) * a.sV[static_cast<size_t>(bh) * nblk + kb];
             }
             m = m_new;
             // O = alpha O + c_h PV_h
@@ -434,10 +476,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
 }  // namespace fwd
 
-template <int D, typename OutT, bool BIAS, bool DUMP, bool FP8>
+template <int D, typename OutT, bool BIAS, bool DUMP, int FMT>
 static cudaError_t launch_fwd_t(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
-    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP, FP8>;
+    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP, FMT>;
     const int smem = static_cast<int>(sizeof(fwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -456,14 +498,19 @@ static cudaError_t launch_fwd_t(const sage_params &p, const CUtensorMap &mq, con
 template <int D, typename OutT>
 static cudaError_t launch_fwd_d(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
+    using fwd::kFmtFp4;
+    using fwd::kFmtFp8;
+    using fwd::kFmtInt8;
     const bool bias = a.qbias != nullptr, dump = a.dump_s != nullptr;
-    // the debug dump exists for the INT8 codes only (the C ABI refuses FP8 with it)
-    if (p.flags & SAGE_FLAG_FP8) return bias ? launch_fwd_t<D, OutT, true, false, true>(p, mq, mk, mv, a, st)
-                                             : launch_fwd_t<D, OutT, false, false, true>(p, mq, mk, mv, a, st);
-    if (dump) return bias ? launch_fwd_t<D, OutT, true, true, false>(p, mq, mk, mv, a, st)
-                          : launch_fwd_t<D, OutT, false, true, false>(p, mq, mk, mv, a, st);
-    return bias ? launch_fwd_t<D, OutT, true, false, false>(p, mq, mk, mv, a, st)
-                : launch_fwd_t<D, OutT, false, false, false>(p, mq, mk, mv, a, st);
+    // the debug dump exists for the INT8 codes only (the C ABI refuses the other formats with it)
+    if (a.fp4) return bias ? launch_fwd_t<D, OutT, true, false, kFmtFp4>(p, mq, mk, mv, a, st)
+                           : launch_fwd_t<D, OutT, false, false, kFmtFp4>(p, mq, mk, mv, a, st);
+    if (p.flags & SAGE_FLAG_FP8) return bias ? launch_fwd_t<D, OutT, true, false, kFmtFp8>(p, mq, mk, mv, a, st)
+                                             : launch_fwd_t<D, OutT, false, false, kFmtFp8>(p, mq, mk, mv, a, st);
+    if (dump) return bias ? launch_fwd_t<D, OutT, true, true, kFmtInt8>(p, mq, mk, mv, a, st)
+                          : launch_fwd_t<D, OutT, false, true, kFmtInt8>(p, mq, mk, mv, a, st);
+    return bias ? launch_fwd_t<D, OutT, true, false, kFmtInt8>(p, mq, mk, mv, a, st)
+                : launch_fwd_t<D, OutT, false, false, kFmtInt8>(p, mq, mk, mv, a, st);
 }
 
 cudaError_t launch_fwd(const sage_params &p, const __half *Q16, const __half *K16,

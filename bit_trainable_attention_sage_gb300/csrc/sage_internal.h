@@ -40,6 +40,14 @@ struct QkNormArgs {
     void *xnorm[2];           // (B,H,N,d) normalised 16-bit tensors or NULL
 };
 
+// NVFP4 outputs of the FP4 quantiser: packed E2M1 codes (two per byte, the even element in the
+// low nibble) and E4M3 block scales (one byte each)
+struct Fp4Out {
+    uint8_t *Qc, *Kc, *Vc;    // (B,H,N,d/2)
+    uint8_t *sQ, *sK;         // (B,H,N,d/16): blocks of 16 channels
+    uint8_t *sV;              // (B,H,N/16,d): blocks of 16 tokens per channel
+};
+
 struct BwdPrologueArgs {
     const void *dO, *O;
     const float *L;    // (B,H,N) log-sum-exp from the forward
@@ -63,6 +71,7 @@ struct FwdArgs {
     int32_t *dump_pv;     // debug: (B,H,N/64,N/64,64,d) integer P V products, or NULL
     int N, H, causal, dtype;
     float sl2;            // log2(e)/sqrt(d)
+    int fp4;              // 1: FP4 inference forward (dequantised NVFP4 operands, two-level P)
 };
 
 struct BwdArgs {
@@ -85,6 +94,11 @@ int kmean_splits(const sage_params &p);
 cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st,
                             const QkNormArgs *qn = nullptr);
 cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st);   // V only
+// NVFP4 quantisation of Q, K (along d) and V (along the tokens), smoothed as for INT8
+cudaError_t launch_quantize_fp4(const sage_params &p, QuantArgs a, Fp4Out o, cudaStream_t st);
+// NVFP4 codes and scales -> the exact fp16 values s * code (along_tokens: V's scale layout)
+cudaError_t launch_widen_fp4(const uint8_t *codes, const uint8_t *scales, __half *dst,
+                             const sage_params &p, bool along_tokens, cudaStream_t st);
 // int8 codes (or E4M3 bit patterns when fp8) -> their exact fp16 values
 cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, bool fp8, cudaStream_t st);
 cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStream_t st);

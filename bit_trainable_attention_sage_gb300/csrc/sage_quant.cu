@@ -326,27 +326,26 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
     }
 }
 
-// ---------------------------------------------------------------------------------------------
-// a2: smoothing + per-block quantisation of Q (z=0), K (z=1), V (z=2).  One 64 x d block per CTA.
-// ---------------------------------------------------------------------------------------------
-template <typename T, bool NORM, bool FP8>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs qn) {
-    __shared__ float red[8];
-    __shared__ float mu_s[128];
-    __shared__ double colsum[256 * 8];
-    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z + a.z_base;
-    const int d = a.d, N = a.N;
-    const T *src = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
-    int8_t *dst = z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh);
-    const bool norm = NORM && z < 2;                   // uniform over the CTA
-    const float *gamma = norm ? qn.gamma[z] : nullptr;
-    float *scale = z == 0 ? a.sQ : (z == 1 ? a.sK : a.sV);
-    const int vec_per_row = d / 8;
-    const int rows_in_flight = 256 / vec_per_row;
-    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
-    const int iters = 64 / rows_in_flight;            // 4 for d = 128, 2 for d = 64
-    const size_t blk_off = (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * d;
+// Per-channel mean that tensor z of 64-row block blk has subtracted before quantisation, into
+// mu_s: mu_K from the K-mean partial sums (z = 1 with smooth_k), or the block's own mean of Q
+// (z = 0 with smooth_q; with NORM the rows pass through the QK-norm first).  Writes muK / muQ and
+// returns whether the tensor is smoothed.  Ends with a CTA barrier.
+// The fields of the kernel parameter the helper reads, by value (a reference to the parameter
+// itself would copy it to local memory).
+struct SmoothIn {
+    const double *kpartial;
+    float *muK, *muQ;
+    int ksplits, N, d, smooth_k, smooth_q;
+};
 
+template <typename T, bool NORM>
+__device__ __forceinline__ bool smoothing_mean(const SmoothIn a, const T *src, int z, int blk,
+                                               int bh, size_t blk_off, int cv, int rg,
+                                               int vec_per_row, int rows_in_flight, int iters,
+                                               const float *gamma, float eps, float *mu_s,
+                                               double *colsum) {
+    const int d = a.d, N = a.N;
+    const bool norm = NORM && z < 2;
     // per-channel mean to subtract (zero when this tensor is not smoothed)
     bool smooth = false;
     if (z == 1 && a.smooth_k) {
@@ -373,7 +372,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs q
             const int r = rg + it * rows_in_flight;
             float v[8];
             load8(src + blk_off + static_cast<size_t>(r) * d + cv * 8, v);
-            if (norm) qk_norm8<T>(v, gamma, cv * 8, vec_per_row, d, qn.eps);
+            if (norm) qk_norm8<T>(v, gamma, cv * 8, vec_per_row, d, eps);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] += static_cast<double>(v[i]);
         }
@@ -393,6 +392,35 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs q
     }
     __syncthreads();
 
+    return smooth;
+}
+
+// ---------------------------------------------------------------------------------------------
+// a2: smoothing + per-block quantisation of Q (z=0), K (z=1), V (z=2).  One 64 x d block per CTA.
+// ---------------------------------------------------------------------------------------------
+template <typename T, bool NORM, bool FP8>
+__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs qn) {
+    __shared__ float red[8];
+    __shared__ float mu_s[128];
+    __shared__ double colsum[256 * 8];
+    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z + a.z_base;
+    const int d = a.d, N = a.N;
+    const T *src = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
+    int8_t *dst = z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh);
+    const bool norm = NORM && z < 2;                   // uniform over the CTA
+    // selected by value: indexing the parameter's arrays with z would copy them to local memory
+    const float *gamma = norm ? (z == 0 ? qn.gamma[0] : qn.gamma[1]) : nullptr;
+    float *scale = z == 0 ? a.sQ : (z == 1 ? a.sK : a.sV);
+    const int vec_per_row = d / 8;
+    const int rows_in_flight = 256 / vec_per_row;
+    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+    const int iters = 64 / rows_in_flight;            // 4 for d = 128, 2 for d = 64
+    const size_t blk_off = (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * d;
+
+    const SmoothIn si{a.kpartial, a.muK, a.muQ, a.ksplits, N, d, a.smooth_k, a.smooth_q};
+    const bool smooth = smoothing_mean<T, NORM>(si, src, z, blk, bh, blk_off, cv, rg, vec_per_row,
+                                                 rows_in_flight, iters, gamma, qn.eps, mu_s, colsum);
+
     float x[4][8];
     float mx = 0.0f;
 #pragma unroll
@@ -402,9 +430,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs q
         load8(src + blk_off + static_cast<size_t>(r) * d + cv * 8, x[it]);
         if (norm) {
             const float rf = qk_norm8<T>(x[it], gamma, cv * 8, vec_per_row, d, qn.eps);
-            if (cv == 0) qn.rnorm[z][static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r] = rf;
-            if (qn.xnorm[z])
-                *reinterpret_cast<uint4 *>(static_cast<T *>(qn.xnorm[z]) + blk_off + static_cast<size_t>(r) * d + cv * 8) =
+            float *rnorm = z == 0 ? qn.rnorm[0] : qn.rnorm[1];
+            void *xnorm = z == 0 ? qn.xnorm[0] : qn.xnorm[1];
+            if (cv == 0) rnorm[static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r] = rf;
+            if (xnorm)
+                *reinterpret_cast<uint4 *>(static_cast<T *>(xnorm) + blk_off + static_cast<size_t>(r) * d + cv * 8) =
                     pack8<T>(x[it]);
         }
 #pragma unroll
@@ -423,6 +453,146 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs q
             FP8 ? pack_codes8_e4m3(x[it], delta) : pack_codes8(x[it], delta);
     }
     if (threadIdx.x == 0) scale[static_cast<size_t>(bh) * (N / 64) + blk] = delta;
+}
+
+// ---------------------------------------------------------------------------------------------
+// NVFP4 ("SageAttention3 ..." (review), eq. (2)-(3) and the NVFP4 row of its format table):
+// 1 x 16 blocks, s = e4m3(fl32(max|x| / 6)), codes e2m1(fl32(x / s)), all-zero codes where s = 0.
+// Q (z = 0) and K (z = 1), smoothed as for INT8, are blocked along d (a block is the 8 channels
+// of two neighbouring lanes); V (z = 2) along the tokens, 16 rows per channel (the block maximum
+// through shared-memory atomics on the float bits, which order like the values when >= 0).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_e2m1x8(const float (&x)[8], const float (&s)[8]) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = s[2 * i] == 0.0f ? 0.0f : __fdiv_rn(x[2 * i], s[2 * i]);
+        const float hi = s[2 * i + 1] == 0.0f ? 0.0f : __fdiv_rn(x[2 * i + 1], s[2 * i + 1]);
+        w |= e2m1x2(lo, hi) << (8 * i);
+    }
+    return w;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_fp4_kernel(QuantArgs a, Fp4Out o) {
+    __shared__ float mu_s[128];
+    __shared__ double colsum[256 * 8];
+    __shared__ unsigned int vmax[4][128];
+    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z;
+    const int d = a.d, N = a.N;
+    const T *src = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
+    const int vec_per_row = d / 8;
+    const int rows_in_flight = 256 / vec_per_row;
+    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+    const int iters = 64 / rows_in_flight;
+    const size_t blk_off = (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * d;
+    if (z == 2) {
+        for (int i = threadIdx.x; i < 4 * 128; i += 256) (&vmax[0][0])[i] = 0u;
+    }
+    const SmoothIn si{a.kpartial, a.muK, a.muQ, a.ksplits, N, d, a.smooth_k, a.smooth_q};
+    const bool smooth = smoothing_mean<T, false>(si, src, z, blk, bh, blk_off, cv, rg, vec_per_row,
+                                                  rows_in_flight, iters, nullptr, 0.0f, mu_s, colsum);
+    float x[4][8];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        if (it >= iters) break;
+        load8(src + blk_off + static_cast<size_t>(rg + it * rows_in_flight) * d + cv * 8, x[it]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (smooth) x[it][i] = __fsub_rn(x[it][i], mu_s[cv * 8 + i]);
+    }
+    uint8_t *codes = z == 0 ? o.Qc : (z == 1 ? o.Kc : o.Vc);
+    if (z < 2) {
+        uint8_t *scales = z == 0 ? o.sQ : o.sK;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            if (it >= iters) break;
+            const int r = rg + it * rows_in_flight;
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[it][i]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));       // the block's other lane
+            const float sb = e4m3_round_f(__fdiv_rn(m, 6.0f));
+            float s8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s8[i] = sb;
+            const size_t row = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r;
+            reinterpret_cast<uint32_t *>(codes + row * (d / 2))[cv] = pack_e2m1x8(x[it], s8);
+            if ((cv & 1) == 0) scales[row * (d / 16) + (cv >> 1)] = static_cast<uint8_t>(e4m3x2(sb, 0.0f) & 0xFFu);
+        }
+        return;
+    }
+    // V: 16-token blocks per channel
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        if (it >= iters) break;
+        const int g = (rg + it * rows_in_flight) >> 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) atomicMax(&vmax[g][cv * 8 + i], __float_as_uint(fabsf(x[it][i])));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        if (it >= iters) break;
+        const int r = rg + it * rows_in_flight;
+        const int g = r >> 4;
+        float s8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s8[i] = e4m3_round_f(__fdiv_rn(__uint_as_float(vmax[g][cv * 8 + i]), 6.0f));
+        const size_t row = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r;
+        reinterpret_cast<uint32_t *>(codes + row * (d / 2))[cv] = pack_e2m1x8(x[it], s8);
+        if ((r & 15) == 0) {
+            uint8_t *sv = o.sV + (static_cast<size_t>(bh) * (N / 16) + static_cast<size_t>(blk) * 4 + g) * d + cv * 8;
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w0 |= (e4m3x2(s8[i], 0.0f) & 0xFFu) << (8 * i);
+                w1 |= (e4m3x2(s8[4 + i], 0.0f) & 0xFFu) << (8 * i);
+            }
+            *reinterpret_cast<uint2 *>(sv) = make_uint2(w0, w1);
+        }
+    }
+}
+
+// 16 codes (8 bytes) of one scale block -> 16 fp16 values s * code (exact: at most 5 bits)
+__global__ void __launch_bounds__(256) widen_fp4_kernel(const uint8_t *__restrict__ codes,
+                                                        const uint8_t *__restrict__ scales,
+                                                        __half *__restrict__ dst, size_t n16,
+                                                        int d, int N, int along_tokens) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const uint2 c = reinterpret_cast<const uint2 *>(codes)[i];
+        const uint32_t cw[2] = {c.x, c.y};
+        uint32_t sc[8];                                   // 8 fp16 pairs of scales
+        if (!along_tokens) {
+            const uint32_t b = scales[i];
+            const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(b | (b << 8)));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sc[k] = h;
+        } else {
+            // element i*16 .. i*16+15 of row n = (i*16) / d, channels c0 .. c0+15
+            const size_t e0 = i * 16;
+            const size_t row = e0 / d;                    // (bh * N + n)
+            const int c0 = static_cast<int>(e0 % d);
+            const size_t bhh = row / N, n = row % N;
+            const uint4 sv = *reinterpret_cast<const uint4 *>(scales + (bhh * (N / 16) + n / 16) * d + c0);
+            const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sc[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(sw[k] & 0xFFFFu));
+                sc[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(sw[k] >> 16));
+            }
+        }
+        uint32_t out[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t byte = (cw[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+            out[k] = hmul2(e2m1x2_to_f16x2(byte), sc[k]);
+        }
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst) + 2 * i;
+        d4[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        d4[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -612,6 +782,36 @@ cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st
     a.z_base = 2;
     dim3 g(p.N / 64, p.B * p.H, 1);
     launch_quantize_grid(p, a, QkNormArgs{}, g, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp4(const sage_params &p, QuantArgs a, Fp4Out o, cudaStream_t st) {
+    const int bh = p.B * p.H;
+    if (p.smooth_k) {
+        const int S = a.ksplits;
+        const int rows = (p.N + S - 1) / S;
+        dim3 g(bh, S);
+        double *part = const_cast<double *>(a.kpartial);
+        if (p.dtype == SAGE_FP16)
+            kmean_partial_kernel<__half, false><<<g, 256, 0, st>>>(static_cast<const __half *>(a.K), part, p.N, p.d, S, rows, nullptr, 0.0f);
+        else
+            kmean_partial_kernel<__nv_bfloat16, false><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.K), part, p.N, p.d, S, rows, nullptr, 0.0f);
+    }
+    dim3 g(p.N / 64, bh, 3);
+    if (p.dtype == SAGE_FP16)
+        quantize_fp4_kernel<__half><<<g, 256, 0, st>>>(a, o);
+    else
+        quantize_fp4_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(a, o);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_fp4(const uint8_t *codes, const uint8_t *scales, __half *dst,
+                             const sage_params &p, bool along_tokens, cudaStream_t st) {
+    const size_t n16 = static_cast<size_t>(p.B) * p.H * p.N * p.d / 16;
+    int blocks = static_cast<int>((n16 + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    widen_fp4_kernel<<<blocks, 256, 0, st>>>(codes, scales, dst, n16, p.d, p.N, along_tokens ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -155,6 +155,39 @@ SAGE_API int sage_qknorm_bwd(const sage_params *p, const void *X, const float *g
                          const float *dY, float *dX, float *dg, sage_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------ *
+ * FP4 inference forward (SageAttention3): sage_quantize_fp4 then sage_attn_fwd_fp4.
+ * "SageAttention3: Microscaling FP4 Attention for Inference and An Exploration of 8-Bit
+ * Training" (review): FP4 microscaling, eq. (2)-(3); the NVFP4 row of its format table (E2M1
+ * values, 1 x 16 blocks, E4M3 scales); eq. (4)-(5) (S and O as FP4 products); two-level P
+ * scaling, eq. (6); Q- and K-smoothing.
+ *
+ * sage_quantize_fp4: smoothing as sage_quantize_smooth (mu_K, and mu_Q when smooth_q), then per
+ *   1 x 16 block s = e4m3(fl32(max|x| / 6)) (nearest E4M3, ties even) and codes
+ *   e2m1(fl32(x / s)) (nearest E2M1: 0, 0.5, 1, 1.5, 2, 3, 4, 6; ties even; saturating; all zero
+ *   where s = 0).
+ *   Out: Qc, Kc, Vc (B,H,N,d/2) uint8, two codes a byte (the even element in the low nibble);
+ *        sQ, sK (B,H,N,d/16) E4M3 bytes: Q and K blocked along d;
+ *        sV (B,H,N/16,d) E4M3 bytes: V blocked along the tokens, 16 per channel;
+ *        muK, muQ as sage_quantize_smooth.  Workspace: sage_quantize_workspace_bytes.
+ * sage_attn_fwd_fp4: S = (s_Q Q^)(s_K K^)^T / sqrt(d) (+ the Q-smoothing bias, K required then),
+ *   online softmax per 64-key tile; P~2 = fl32(2688 ex2(x)), x = logits - tile row max r, is
+ *   quantised per 16 keys as above with codes e2m1(fl32(v fl32(1 / s))), and
+ *   O += 2^(r - m) / 2688 * (s_P2 P^2)(s_V V^).  Writes O and L like sage_attn_fwd.  Workspace:
+ *   sage_fwd_workspace_bytes.
+ * Both calls refuse every flag (SAGE_ERR_UNSUPPORTED).  The tensor cores run the dequantised
+ * values s * code, exact in fp16, through the same kind::f16 MMAs as the INT8 path.
+ * ------------------------------------------------------------------------------------------ */
+SAGE_API int sage_quantize_fp4(const sage_params *p, const void *Q, const void *K, const void *V,
+                         uint8_t *Qc, uint8_t *Kc, uint8_t *Vc, uint8_t *sQ, uint8_t *sK,
+                         uint8_t *sV, float *muK, float *muQ, void *workspace,
+                         size_t workspace_bytes, sage_stream_t stream);
+SAGE_API int sage_attn_fwd_fp4(const sage_params *p, const uint8_t *Qc, const uint8_t *Kc,
+                         const uint8_t *Vc, const uint8_t *sQ, const uint8_t *sK,
+                         const uint8_t *sV, const void *K, const float *muK, const float *muQ,
+                         void *O, float *L, void *workspace, size_t workspace_bytes,
+                         sage_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ *
  * Step 2 -- forward.
  * "SageBwd: A Trainable Low-bit Attention" (structured summary), method steps, forward (3)-(5);
  * "SageAttention3 ..." (review) eq. (1) online softmax and eq. (8): S_ij = MM(Q^_i, K^_j) s_Q s_K,
