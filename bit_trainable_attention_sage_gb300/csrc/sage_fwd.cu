@@ -143,7 +143,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 16) {
         uint32_t pk[8];
-        if (FMT == kFmtFp4) {
+        if constexpr (FMT == kFmtFp4) {
             f2 e[8];
             float emax = 0.0f;
 #pragma unroll
@@ -168,30 +168,29 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
                 const f2 y = mul2(mul2(k2688, e[k]), inv2);
                 pk[k] = hmul2(e2m1x2_to_f16x2(e2m1x2(y.x, y.y)), s2h);
             }
-            tmem_st8(code_col + cc / 2, pk);
-            continue;
-        }
+        } else {
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-            // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
-            const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
-            f2 x2 = BIAS ? sub2(a2, rs2) : fma2(a2, c2, nrs2);
-            if (MASKED) {
-                x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
-                x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
-            }
-            const f2 e2{ex2_approx(x2.x), ex2_approx(x2.y)};
-            sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e2);
-            if (FMT == kFmtFp8) {
-                const f2 v2 = mul2(k448, e2);
-                pk[k / 2] = e4m3x2_f16x2(v2.x, v2.y);
-            } else {
-                const f2 p2 = sub2(add2(mul2(k127, e2), kr2), kr2);
-                const float p0 = p2.x, p1 = p2.y;
-                pk[k / 2] = pack_half2(p0, p1);
-                if (DUMP && dump_row) {
-                    dump_row[cc + k] = static_cast<int16_t>(p0);
-                    dump_row[cc + k + 1] = static_cast<int16_t>(p1);
+            for (int k = 0; k < 16; k += 2) {
+                // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
+                const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
+                f2 x2 = BIAS ? sub2(a2, rs2) : fma2(a2, c2, nrs2);
+                if (MASKED) {
+                    x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
+                    x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
+                }
+                const f2 e2{ex2_approx(x2.x), ex2_approx(x2.y)};
+                sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e2);
+                if (FMT == kFmtFp8) {
+                    const f2 v2 = mul2(k448, e2);
+                    pk[k / 2] = e4m3x2_f16x2(v2.x, v2.y);
+                } else {
+                    const f2 p2 = sub2(add2(mul2(k127, e2), kr2), kr2);
+                    const float p0 = p2.x, p1 = p2.y;
+                    pk[k / 2] = pack_half2(p0, p1);
+                    if (DUMP && dump_row) {
+                        dump_row[cc + k] = static_cast<int16_t>(p0);
+                        dump_row[cc + k + 1] = static_cast<int16_t>(p1);
+                    }
                 }
             }
         }
