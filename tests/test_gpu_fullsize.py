@@ -84,3 +84,59 @@ def test_full_size_sampled_parity(case):
         assert np.all(np.isfinite(gv)), nm
         err = rel_l2(gv, want[b, h][r])
         assert err <= 1e-3, (nm, err)
+
+
+def test_full_size_fp8_headline():
+    """The FP8 variant on the headline workload: E4M3 codes and scales byte for byte, sampled
+    rows of head (0, 9) within rel-l2 1e-3 of the oracle's FP8 arithmetic."""
+    import bit_trainable_attention_sage_gb300 as sg
+    from oracle import quant
+    w = workloads.get("headline")
+    x = workloads.make_inputs(w, seed=1)
+    Q, K, V, dO = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V", "dO"))
+    q = sg.sage_quantize_smooth(Q, K, V, fp8=True)
+    O, L = sg.sage_attn_fwd(q, causal=False)
+    dQ, dK, dV = sg.sage_attn_bwd(q, V, O, L, dO, causal=False)
+    assert sg.sage_device_status() == 0
+    ar = osage.QUANTISED_FP8
+    prep = osage.prepare(x["Q"], x["K"], x["V"], arith=ar)
+    for k in ("Qh", "Kh", "Vh"):
+        assert np.array_equal(getattr(q, k).cpu().numpy().view(np.uint8), quant.e4m3_encode(prep[k])), k
+    for k in ("sQ", "sK", "sV"):
+        assert np.array_equal(getattr(q, k).cpu().numpy().view(np.uint32), prep[k].view(np.uint32)), k
+    b, h = 0, 9
+    Oref, Lref = osage.sage_forward(prep, False, arith=ar, heads=[(b, h)])
+    O_stored = workloads.round_to(Oref.astype(np.float32), w.dtype)
+    assert rel_l2(O.float().cpu().numpy()[b, h], O_stored[b, h]) <= 1e-3
+    prep["V16"] = np.asarray(x["V"], np.float64)
+    g = osage.sage_backward(prep, O_stored, Lref.astype(np.float32), x["dO"], False, arith=ar,
+                            q_blocks=[3, 120], kv_blocks=[0, 64], heads=[(b, h)])
+    qrows = np.r_[192:256, 7680:7744]
+    krows = np.r_[0:64, 4096:4160]
+    for nm, got, want, r in (("dQ", dQ, g["dQ"], qrows), ("dK", dK, g["dK"], krows), ("dV", dV, g["dV"], krows)):
+        err = rel_l2(got.cpu().numpy()[b, h][r], want[b, h][r])
+        assert err <= 1e-3, (nm, err)
+
+
+def test_full_size_fp4_headline():
+    """The FP4 inference forward on the headline workload: NVFP4 codes and scales of the whole
+    tensors as values, O and L of head (1, 2) within rel-l2 1e-3 of the oracle's FP4 forward."""
+    import bit_trainable_attention_sage_gb300 as sg
+    from oracle import fp4, quant
+    w = workloads.get("headline")
+    x = workloads.make_inputs(w, seed=2)
+    Q, K, V = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V"))
+    q = sg.sage_quantize_fp4(Q, K, V)
+    O, L = sg.sage_attn_fwd_fp4(q, causal=False)
+    assert sg.sage_device_status() == 0
+    prep = fp4.quantize_fp4(x["Q"], x["K"], x["V"])
+    for nm in ("Q", "K", "V"):
+        c = getattr(q, nm + "c").cpu().numpy()
+        vals = fp4.e2m1_decode(np.stack([c & 15, c >> 4], axis=-1).reshape(*c.shape[:-1], c.shape[-1] * 2))
+        assert np.array_equal(vals, prep[nm + "c"]), nm
+        assert np.array_equal(quant.e4m3_decode(getattr(q, "s" + nm).cpu().numpy()), prep["s" + nm]), nm
+    b, h = 1, 2
+    Oref, Lref = fp4.sage_fp4_forward(prep, False, heads=[(b, h)])
+    O_stored = workloads.round_to(Oref.astype(np.float32), w.dtype)
+    assert rel_l2(O.float().cpu().numpy()[b, h], O_stored[b, h]) <= 1e-3
+    assert np.max(np.abs(L.cpu().numpy()[b, h] - Lref[b, h])) <= 1e-3 * max(1.0, float(np.max(np.abs(Lref[b, h]))))
