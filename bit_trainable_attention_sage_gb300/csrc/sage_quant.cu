@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
         const int n1 = min(N, n0 + rows_per_split);
         long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         const T *base = K + static_cast<size_t>(bh) * N * d;
+        // unrolled so that several rows' loads are in flight at once
+#pragma unroll 4
         for (int n = n0 + rg; n < n1; n += rows_in_flight) {
             const uint4 w = *reinterpret_cast<const uint4 *>(base + static_cast<size_t>(n) * d + cv * 8);
             const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -308,6 +310,8 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
         const int n1 = min(N, n0 + rows_per_split);
         double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         const T *base = K + static_cast<size_t>(bh) * N * d;
+        // unrolled so that several rows' loads are in flight at once
+#pragma unroll 4
         for (int n = n0 + rg; n < n1; n += rows_in_flight) {
             float v[8];
             load8(base + static_cast<size_t>(n) * d + cv * 8, v);
@@ -748,7 +752,7 @@ static void launch_quantize_grid(const sage_params &p, const QuantArgs &a, const
 
 int kmean_splits(const sage_params &p) {
     const int bh = p.B * p.H;
-    int s = (2 * 152 + bh - 1) / bh;
+    int s = (4 * 152 + bh - 1) / bh;                   // about four CTAs per SM
     const int max_s = p.N / 64;
     return s < 1 ? 1 : (s > max_s ? max_s : s);
 }
