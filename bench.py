@@ -381,9 +381,9 @@ def run_gpu(args, w: workloads.Workload):
         "dtype": ("e4m3" if args.fp8 else "s8") + " codes as f16 (f32 accumulate); dP "
                  + ("s8 codes (ablation)" if args.dp_int8 else "f16"),
         "data": "synthetic",
-        "config": {"workload": f"headline {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+        "config": {"workload": f"{w.name} {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "smooth_k": True, "smooth_q": w.smooth_q,
-                   "per_rank": "own batch", "l2": "inputs larger than L2 (Q,K,V,dO = 268 MB per step)"},
+                   "per_rank": "own batch", "l2": f"inputs larger than L2 (Q,K,V,dO = {8 * w.B * w.H * w.N * w.d // 2**20} MiB per step)"},
         "roofline": {"kernel": "sage_attn_bwd call (bwd prologue + tcgen05 backward kernel)",
                      "bound": "tensor", "achieved": round(bwd_tflops, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
@@ -487,7 +487,7 @@ def run_reference(args, w: workloads.Workload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (f32 codes)",
         "data": "synthetic",
-        "config": {"workload": f"headline {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "config": {"workload": f"{w.name} {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
         "cpu_baseline": {"value": round(value, 8), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label},
         "e2e": {"value": round(value, 8), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -508,18 +508,21 @@ def main():
                     help="QK-norm fused into the quantise call, and its gradient after the backward")
     ap.add_argument("--fp4", action="store_true",
                     help="the SageAttention3 FP4 inference forward (quantise + forward only)")
+    ap.add_argument("--workload", default="headline", choices=["headline", "qknorm", "outlier", "longseq"],
+                    help="the workload (default: the headline B2 H16 N8192 d128 fp16); the others are the "
+                         "parity workloads of workloads.py, timed the same way")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    over = {"causal": args.causal}
+    over = {"causal": True} if args.causal else {}
     if args.batch:
         over["B"] = args.batch
     if args.heads:
         over["H"] = args.heads
-    w = workloads.get("headline", **over)
+    w = workloads.get(args.workload, **over)
     if args.impl == "reference":
         line = run_reference(args, w)
         if line is not None:
