@@ -106,6 +106,23 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// A sum of float32 values kept as an unevaluated triple h + l + t: two-sums make every step exact
+// but the additions into t (relative 2^-65 over thousands of terms).  bf16 inputs are exact in
+// float32, so this replaces per-element float64 additions (slow on GB300) at no loss of accuracy;
+// the sum must stay below the float32 range.
+struct Sum3 {
+    float h = 0.0f, l = 0.0f, t = 0.0f;
+    __device__ __forceinline__ void add(float v) {
+        float e1, e2;
+        two_sum(h, v, h, e1);
+        two_sum(l, e1, l, e2);
+        t = __fadd_rn(t, e2);
+    }
+    __device__ __forceinline__ double value() const {
+        return (static_cast<double>(h) + static_cast<double>(l)) + static_cast<double>(t);
+    }
+};
+
 // QK-norm of this lane's 8 values of a row whose d / 8 slices sit in `lanes` consecutive lanes
 // (every lane of the warp takes part).  The squares of 16-bit values are exact in float32 (bf16:
 // for 2^-63 <= |x| < 2^63).  They are summed as an unevaluated float32 triple h + l + t with
@@ -213,7 +230,8 @@ __device__ __forceinline__ long long half_fixed24(uint32_t h) {
 // partial[(bh * S + s) * d + c] = sum_{n in split s} K[bh, n, c]
 // fp16 input: int64 multiples of 2^-24 (integer adds, far faster than float64 ones here and just
 // as exact: a sum of 32768 values stays below 2^55, and any sum below 2^53 is exact in both);
-// bf16 input (exponent range of float32): float64.  Both occupy 8 bytes per entry.
+// bf16 input (exponent range of float32): float32 two-sum triples per thread, turned into float64
+// once (see Sum3).  Both occupy 8 bytes per entry.
 // ---------------------------------------------------------------------------------------------
 // With QK-norm (NORM) the rows are normalised first; the loop then runs warp-uniform trip counts
 // (rows past the split are zeros and not added) because the norm's shuffles need every lane.
@@ -231,7 +249,7 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
         const int n0 = s * rows_per_split;
         const int n1 = min(N, n0 + rows_per_split);
         long long acci[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        double accd[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        Sum3 accd[8];
         const T *base = K + static_cast<size_t>(bh) * N * d;
         // unrolled: the norm's two-sum chains of several rows overlap
 #pragma unroll 4
@@ -246,7 +264,7 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
                     if constexpr (std::is_same<T, __half>::value)
                         acci[i] += half_fixed24(__half_as_ushort(__float2half_rn(v[i])));
                     else
-                        accd[i] += static_cast<double>(v[i]);
+                        accd[i].add(v[i]);
                 }
             }
         }
@@ -255,7 +273,7 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
             if constexpr (std::is_same<T, __half>::value)
                 reinterpret_cast<long long *>(redn)[threadIdx.x * 8 + i] = acci[i];
             else
-                redn[threadIdx.x * 8 + i] = accd[i];
+                redn[threadIdx.x * 8 + i] = accd[i].value();
         }
         __syncthreads();
         if (threadIdx.x < d) {
@@ -308,7 +326,7 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
         const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
         const int n0 = s * rows_per_split;
         const int n1 = min(N, n0 + rows_per_split);
-        double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        Sum3 acc[8];
         const T *base = K + static_cast<size_t>(bh) * N * d;
         // unrolled so that several rows' loads are in flight at once
 #pragma unroll 4
@@ -316,10 +334,10 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
             float v[8];
             load8(base + static_cast<size_t>(n) * d + cv * 8, v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] += static_cast<double>(v[i]);
+            for (int i = 0; i < 8; ++i) acc[i].add(v[i]);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) red[threadIdx.x * 8 + i] = acc[i];
+        for (int i = 0; i < 8; ++i) red[threadIdx.x * 8 + i] = acc[i].value();
         __syncthreads();
         if (threadIdx.x < d) {
             const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
