@@ -389,17 +389,30 @@ __device__ __forceinline__ bool smoothing_mean(const SmoothIn a, const T *src, i
         }
     } else if (z == 0 && a.smooth_q) {
         smooth = true;
-        double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        // per thread: fp16 values as exact int64 multiples of 2^-24 (no float64 adds, slow on
+        // GB300); bf16 in float64 (a float32 triple here would cost the plain kernel registers)
+        long long acci[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        double accd[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int it = 0; it < iters; ++it) {
             const int r = rg + it * rows_in_flight;
             float v[8];
             load8(src + blk_off + static_cast<size_t>(r) * d + cv * 8, v);
             if (norm) qk_norm8<T>(v, gamma, cv * 8, vec_per_row, d, eps);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] += static_cast<double>(v[i]);
+            for (int i = 0; i < 8; ++i) {
+                if constexpr (std::is_same<T, __half>::value)
+                    acci[i] += half_fixed24(__half_as_ushort(__float2half_rn(v[i])));
+                else
+                    accd[i] += static_cast<double>(v[i]);
+            }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) colsum[threadIdx.x * 8 + i] = acc[i];
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (std::is_same<T, __half>::value)
+                colsum[threadIdx.x * 8 + i] = static_cast<double>(acci[i]) * 0x1p-24;
+            else
+                colsum[threadIdx.x * 8 + i] = accd[i];
+        }
         __syncthreads();
         if (threadIdx.x < d) {
             const int c = threadIdx.x, cvv = c / 8, ci = c % 8;
