@@ -281,29 +281,36 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             constexpr uint32_t idPV = idesc_f16(128, D, false, false, true);
             const uint32_t k_addr = smem_u32(s.k[0]), v_addr = smem_u32(s.v[0]);
             int pv_count[2] = {0, 0};
-            mbar_wait(&s.q_full, 0, abort_flag, &g_fwd_err, 5);
-            for (int j = 0; j < nsteps; ++j) {
-                if (!mbar_wait(&s.k_full, j & 1, abort_flag, &g_fwd_err, 6)) break;
-                tc_fence_after();
+            // S_t = Q^_t K^(j)^T into the tile's S columns
+            auto issue_s = [&](int t) {
+                const uint32_t q_addr = smem_u32(s.q[t][0]);
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= nsteps_t[t]) continue;
-                    const uint32_t q_addr = smem_u32(s.q[t][0]);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                        umma_ss(tmem + 256 * t, sdesc_sw128(q_addr + off, 16, 1024),
-                                sdesc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
-                    }
-                    umma_commit(&s.s_full[t]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    umma_ss(tmem + 256 * t, sdesc_sw128(q_addr + off, 16, 1024),
+                            sdesc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
                 }
+                umma_commit(&s.s_full[t]);
+            };
+            bool ok = mbar_wait(&s.q_full, 0, abort_flag, &g_fwd_err, 5) &&
+                      mbar_wait(&s.k_full, 0, abort_flag, &g_fwd_err, 6);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (0 < nsteps_t[t]) issue_s(t);
                 umma_commit(&s.k_free);
-                if (!mbar_wait(&s.v_full, j & 1, abort_flag, &g_fwd_err, 8)) break;
-                bool ok = true;
+            }
+            // Per step j: the PV MMAs of both tiles, half by half; a tile's S of step j + 1 goes in
+            // right after its last PV of step j (the PV MMAs have then taken its P codes: the pipe
+            // runs in issue order), so its next softmax need not wait for the other tile's PVs.
+            for (int j = 0; j < nsteps && ok; ++j) {
+                if (!(ok = mbar_wait(&s.v_full, j & 1, abort_flag, &g_fwd_err, 8))) break;
+                bool k_next = false;                              // K of step j + 1 has landed
+                int s_left = (j + 1 < nsteps_t[0]) + (j + 1 < nsteps_t[1]);
                 for (int h = 0; h < 2 && ok; ++h) {
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= nsteps_t[t]) continue;
-                        if (h == 1 && 128 * j + 64 >= kv_end_t[t]) continue;
+                        if (h == 1 && 128 * j + 64 >= kv_end_t[t]) continue;   // (then j is its last step)
                         if (h == 0 && !mbar_wait(&s.p_full[t], j & 1, abort_flag, &g_fwd_err, 7)) { ok = false; break; }
                         // the tile's PV accumulator must have been read out
                         if (pv_count[t] > 0 &&
@@ -317,10 +324,18 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         }
                         umma_commit(&s.pv_full[t]);
                         ++pv_count[t];
+                        if (h == 1 && j + 1 < nsteps_t[t]) {
+                            if (!k_next) {
+                                if (!(ok = mbar_wait(&s.k_full, (j + 1) & 1, abort_flag, &g_fwd_err, 6))) break;
+                                tc_fence_after();
+                                k_next = true;
+                            }
+                            issue_s(t);
+                            if (--s_left == 0) umma_commit(&s.k_free);
+                        }
                     }
                 }
                 umma_commit(&s.v_free);
-                if (!ok) break;
             }
             // every MMA must have finished before the tensor memory is released
             umma_commit(&s.mma_done);
