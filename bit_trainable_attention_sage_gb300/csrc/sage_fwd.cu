@@ -66,7 +66,7 @@ struct Smem {
     alignas(1024) uint8_t k[D / 64][128 * 128];
     alignas(1024) uint8_t v[D / 64][128 * 128];
     uint64_t q_full, k_full, k_free, v_full, v_free, mma_done;
-    uint64_t s_full[2], p_full[2], pv_full[2], pv_free[2];
+    uint64_t s_full[2], p_full[2][2], pv_full[2], pv_free[2];   // p_full[tile][64-key half]
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -236,7 +236,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         mbar_init(&s.mma_done, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s.s_full[t], 1);
-            mbar_init(&s.p_full[t], 4);
+            mbar_init(&s.p_full[t][0], 4);
+            mbar_init(&s.p_full[t][1], 4);
             mbar_init(&s.pv_full[t], 1);
             mbar_init(&s.pv_free[t], 4);
         }
@@ -311,7 +312,9 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= nsteps_t[t]) continue;
                         if (h == 1 && 128 * j + 64 >= kv_end_t[t]) continue;   // (then j is its last step)
-                        if (h == 0 && !mbar_wait(&s.p_full[t], j & 1, abort_flag, &g_fwd_err, 7)) { ok = false; break; }
+                        // this half's P codes are in place (each half has its own barrier, so the
+                        // first half's PV runs while the second half is being coded)
+                        if (!mbar_wait(&s.p_full[t][h], j & 1, abort_flag, &g_fwd_err, 7)) { ok = false; break; }
                         // the tile's PV accumulator must have been read out
                         if (pv_count[t] > 0 &&
                             !mbar_wait(&s.pv_free[t], (pv_count[t] - 1) & 1, abort_flag, &g_fwd_err, 9)) { ok = false; break; }
@@ -405,12 +408,13 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     ? fwd_codes<BIAS, true, DUMP, FMT>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
                     : fwd_codes<BIAS, false, DUMP, FMT>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
                 if (h == 0) sum_h0 = sum; else sum_h1 = sum;
+                // this half's codes are stored: its PV MMA may start
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane_id() == 0) mbar_arrive(&s.p_full[t][h]);
             }
             const float r_h[2] = {r_h0, r_h1}, sum_h[2] = {sum_h0, sum_h1};
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane_id() == 0) mbar_arrive(&s.p_full[t]);
             // online softmax statistics
             const float m_new = fmaxf(m, fmaxf(r_h[0], r_h[1]));
             const float alpha = (m == -INFINITY) ? 0.0f : ex2_approx(__fsub_rn(m, m_new));
