@@ -24,6 +24,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -134,7 +135,7 @@ class ClockSampler:
             self.fh = open(path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -276,8 +277,13 @@ def run_gpu(args, w: workloads.Workload):
 
     # ---- device-timed region -------------------------------------------------------------
     clocks = ClockSampler(local)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks.start(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    if args.clock_log:
+        clock_path = f"{args.clock_log}.rank{rank}.csv"
+        os.makedirs(os.path.dirname(os.path.abspath(clock_path)), exist_ok=True)
+    else:
+        fd, clock_path = tempfile.mkstemp(prefix="sage_clocks_", suffix=".csv")
+        os.close(fd)
+    clocks.start(clock_path)
     time.sleep(0.3)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -511,6 +517,9 @@ def main():
     ap.add_argument("--workload", default="headline", choices=["headline", "qknorm", "outlier", "longseq"],
                     help="the workload (default: the headline B2 H16 N8192 d128 fp16); the others are the "
                          "parity workloads of workloads.py, timed the same way")
+    ap.add_argument("--clock-log", default=None,
+                    help="keep the nvidia-smi clock samples of the timed region in PATH.rank<r>.csv "
+                         "(default: a temporary file)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling of a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling of a smaller case)")

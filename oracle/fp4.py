@@ -11,7 +11,7 @@
     (s_P2, P^2) = phi(P~2), O = FP4MM(P^2, s_P2, V^, s_V) x s_P1;
   * with Q- and K-smoothing (the review's "smoothing Q+K" row).
 
-Readings where the pages leave a step open (listed again in the design doc, R19):
+Readings where the pages leave a step open:
   * E2M1 is 1 sign, 2 exponent bits (bias 1), 1 mantissa bit: values 0, 0.5, 1, 1.5, 2, 3, 4, 6;
     FP4 rounding is round to nearest, ties to the even mantissa, saturating at +-6;
   * a block scale is s = e4m3(fl32(max|x| / 6)) (the E4M3 value nearest, ties even); codes are

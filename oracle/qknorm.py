@@ -5,7 +5,7 @@ product code).
 key vector is RMS-normalised, RMSNorm(x) = x / sqrt((1/d) sum_i x_i^2) * gamma with a learnable
 scale vector gamma; reproduction paragraph: norm epsilon 1e-6 (read as added to the mean square).
 
-Readings where the pages leave a step open (listed again in the design doc, R18):
+Readings where the pages leave a step open:
   * the sum of squares is the exact sum rounded once to float32, S = fl32(sum_c x_c^2); then, in
     IEEE float32 operations, ms = S / d (exact, d a power of two), v = fl32(ms + eps),
     s = fl32(sqrt(v)), r = fl32(1 / s); eps is a float32 value (1e-6 rounded to float32 in the

@@ -11,7 +11,7 @@ Backward -- "SageBwd: A Trainable Low-bit Attention" (structured summary), metho
 backward (1)-(7); "SageAttention3 ..." (review), INT8 backward (Algorithm 3 equations): dV, dP kept
 16-bit, dS = P o (dP - D), dQ, dK with per-block INT8 products; section summary A.2.
 
-Readings where the pages are silent, garbled or at odds (listed again in the design doc):
+Readings where the pages are silent, garbled or at odds:
   R1  the softmax scale 1/sqrt(d) is applied after dequantisation, in float32, folded with
       log2(e) into c = fl32(fl32(s_Q s_K) * fl32(log2(e)/sqrt(d))): the logits in log2 units are
       acc * c; dQ and dK carry 1/sqrt(d) by the chain rule.
