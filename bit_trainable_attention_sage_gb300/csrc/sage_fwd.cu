@@ -38,7 +38,7 @@
 // E4M3 values are exact fp16 operands; their products are exact in the fp32 accumulator, the
 // sums rounded as any fp32 accumulation.
 // FP4 inference forward ("SageAttention3 ..." (review), eq. (4)-(6)): Q, K, V arrive as their
-// dequantised NVFP4 values s * code (exact fp16, at most 5 significant bits), so c = fl32(log2(e) /
+// dequantised NVFP4 values s * code (exact fp16, at most 6 significant bits), so c = fl32(log2(e) /
 // sqrt(d)) alone; P~2 = fl32(2688 ex2(x)) is quantised per 16 keys, s_P2 = e4m3(fl32(max / 6)),
 // code = e2m1(fl32(v fl32(1 / s_P2))), and the PV operand is s_P2 * code; the PV scale is
 // s_P1 = 2^(r - m') / 2688 (eq. (6) with the tile row max r).

@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(QuantArgs a, Fp4Out o
     }
 }
 
-// 16 codes (8 bytes) of one scale block -> 16 fp16 values s * code (exact: at most 5 bits)
+// 16 codes (8 bytes) of one scale block -> 16 fp16 values s * code (exact: at most 6 significant bits)
 __global__ void __launch_bounds__(256) widen_fp4_kernel(const uint8_t *__restrict__ codes,
                                                         const uint8_t *__restrict__ scales,
                                                         __half *__restrict__ dst, size_t n16,

@@ -11,6 +11,7 @@ Modules
   qknorm   QK-norm (per-token RMSNorm of Q and K) and its gradient           (the prologue)
   sage     SageBwd forward (tiled online softmax, per-token P) and backward   (steps a3-a13)
   fp4      SageAttention3 FP4 (NVFP4) inference forward with two-level P scaling
+  qat      Attn-QAT: NVFP4 fake-quantised forward with a high-precision O', 16-bit backward
   fpa      float64 full-precision attention and its gradients (the FPA baseline)
   metrics  cosine similarity and relative l2 error
 
@@ -19,7 +20,7 @@ than itself (hand-worked values, exact rational re-derivation, finite difference
 invariants).  One reported quantity is "parity unpinned": the exact Table-1 numbers of the pages'
 random-QKV sweep (their N, d and block sizes are not printed), which is checked for its trend only.
 """
-from . import quant, qknorm, sage, fp4, fpa, metrics  # noqa: F401
+from . import quant, qknorm, sage, fp4, qat, fpa, metrics  # noqa: F401
 from .quant import quantize_block, quantize_per_block, k_mean, quantize_smooth  # noqa: F401
 from .sage import sage_forward, sage_backward, Arith, QUANTISED, QUANTISED_FP8, DEQUANTISED  # noqa: F401
 from .fpa import fpa_forward, fpa_backward  # noqa: F401

@@ -26,7 +26,8 @@ Readings where the pages leave a step open:
   * l accumulates the unquantised P~ as in eq. (1); Q-smoothing adds the same bias as R5.
 
 The block products of dequantised FP4 operands are computed in float64 (each operand has at most
-5 significant bits; the sums are exact unless a row spans more than 2^36 in magnitude).
+6 significant bits, an E2M1 value 1.1b times an E4M3 scale 1.xxxb, so each product at most 12; a
+sum of 128 of them is exact unless its products span more than 2^34 in magnitude).
 
 Parity: pinned by tests/test_oracle_fp4.py (E2M1 rounding against the nearest point of the
 decoded 16-pattern grid, a hand-worked block with scale rounding and saturation, the forward
@@ -84,7 +85,7 @@ def nvfp4_quant(x, axis: int = -1) -> tuple[np.ndarray, np.ndarray]:
 
 
 def dequant(codes, scales, axis: int = -1) -> np.ndarray:
-    """X' = s X^ (exact: at most 5 significant bits)."""
+    """X' = s X^ (exact: at most 6 significant bits)."""
     c = np.moveaxis(np.asarray(codes, np.float64), axis, -1)
     s = np.moveaxis(np.asarray(scales, np.float64), axis, -1)
     return np.moveaxis(c * np.repeat(s, 16, axis=-1), -1, axis)

@@ -20,6 +20,8 @@ CASES = [
     (512, 128, "bf16", False, dict(qk="qknorm", k_offset_var=4.0, do_var=1e-4)),
     (256, 128, "fp16", False, dict(sigma=5.0)),
     (192, 64, "fp16", True, dict(qk="outlier", smooth_q=True)),
+    (64, 128, "fp16", True, {}),                      # one block: diagonal only
+    (64, 64, "bf16", False, dict(smooth_q=True)),     # one block, Q-smoothing
 ]
 
 

@@ -23,6 +23,8 @@ CASES = [
     (512, 128, "bf16", False, dict(qk="qknorm", k_offset_var=4.0)),  # QK-norm + K channel offsets
     (256, 128, "fp16", False, dict(sigma=5.0)),                      # large logits (sweep sigma 5)
     (192, 64, "fp16", False, dict(qk="outlier", smooth_q=True)),     # outlier channels
+    (64, 128, "fp16", True, {}),                                     # one block: diagonal only
+    (64, 64, "bf16", False, dict(smooth_q=True)),                    # one block, Q-smoothing
 ]
 
 
