@@ -22,16 +22,21 @@ Readings where the pages leave a step open (the plainest ones the rest supports)
   Q3  phi, the P fake quantiser, is one-level NVFP4 along the keys: per 16 keys of a row,
       s = e4m3(fl32(max e / 6)), codes e2m1(fl32(e * fl32(1/s))), P^ = codes * s (a zero scale
       gives zero codes).  The forward applies it to e (each 64-key block normalised by its own
-      row max r, so the block's largest entry is 1), the backward to the normalised
-      P = fl32(2^(fl32(acc c - L2))).  The two inputs differ by a per-row factor, so the codes
-      agree up to the E4M3 rounding of the scales, which is not scale invariant.
+      row max r, so the block's largest entry is 1) and keeps r (float32, one per row and key
+      block).  "The same quantisation as the forward" in the backward is read as rebuilding the
+      forward's quantised P exactly: e from the stored r, phi(e), then normalised,
+      P^ = rnd16(fl32(phi(e) * fl32(2^(fl32(r - L2))))), so that dV is the gradient of the
+      forward's own O with respect to V'.  (phi of the normalised P itself would not do: in a
+      diffuse row of 8192 keys P is near 1.2e-4 and max / 6 lies far below the smallest E4M3
+      scale 2^-9, so whole blocks would quantise to zero.)
   Q4  O = sum_j 2^(r_j - m) P^_j V'_j / l in the input dtype; O' = sum_j 2^(r_j - m) rnd16(e_j) V'_j
       / l kept in float32: the unquantised P~ enters its product as a 16-bit operand (BF16 is the
       pages' "high precision"), exactly as the backward's products do.
-  Q5  backward: D = rowsum(dO o O'); dP = fl32(dO V'^T); dS = fl32(P fl32(dP - D)) rounded to the
-      input dtype for the two products it feeds; dV = P^^T dO, dQ = dS K' / sqrt(d),
-      dK = dS^T Q' / sqrt(d) (the fake quantisers pass the gradient straight through, so these
-      are also the gradients of Q, K and V).
+  Q5  backward: P = fl32(2^(fl32(acc c - L2))) with L2 = fl32(L log2(e)); D = rowsum(dO o O');
+      dP = fl32(dO V'^T); dS = fl32(P fl32(dP - D)) rounded to the input dtype for the two
+      products it feeds; dV = P^^T dO (P^ of Q3), dQ = dS K' / sqrt(d), dK = dS^T Q' / sqrt(d)
+      (the fake quantisers pass the gradient straight through, so these are also the gradients
+      of Q, K and V).
 
 Exactness: every float32 rounding the kernels take is taken here at the same step (fl32 below);
 products of fake-quantised operands are exact in float64 (at most 12 significant bits each, a
@@ -42,9 +47,9 @@ attention and its gradients (oracle.fpa), which pins the tiling, O', D and the b
 
 Parity: pinned by tests/test_oracle_qat.py (the identity limit against oracle.fpa, the P fake
 quantiser against a brute-force grid search, a hand-worked block, the forward against its
-untiled closed form, the rowsum identity behind O', dV against its closed form, and the pages'
-ablation ordering: D from the FP4 output O is further from the straight-through gradient than D
-from O').
+untiled closed form, the rowsum identity behind O', dV as the exact gradient of the forward's O
+with respect to V', the straight-through gradient, and the pages' ablation ordering: D from the
+FP4 output O is further from the straight-through gradient than D from O').
 """
 from __future__ import annotations
 
@@ -94,7 +99,9 @@ def _mask(causal: bool, i: int, j: int):
 
 
 def qat_forward(fq: dict, causal: bool, dtype_round, exact: bool = False, heads=None, q_blocks=None):
-    """Q2-Q4.  Returns (O, O', L) float64; O before its rounding to the stored dtype."""
+    """Q2-Q4.  Returns (O, O', L, R): O, O', L float64 (O before its rounding to the stored
+    dtype), R (B, H, N/64, N) the row maxima r of each (key block, row), float32 values (-inf
+    where the row sees no key of the block; NaN where the forward never visits the pair)."""
     Qf, Kf, Vf = fq["Qf"], fq["Kf"], fq["Vf"]
     B, H, N, d = Qf.shape
     T = N // BLOCK
@@ -102,6 +109,7 @@ def qat_forward(fq: dict, causal: bool, dtype_round, exact: bool = False, heads=
     O = np.zeros((B, H, N, d))
     Op = np.zeros((B, H, N, d))
     L = np.zeros((B, H, N))
+    R = np.full((B, H, T, N), np.nan)
     heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for (b, h) in heads:
         for i in (q_blocks if q_blocks is not None else range(T)):
@@ -118,6 +126,7 @@ def qat_forward(fq: dict, causal: bool, dtype_round, exact: bool = False, heads=
                 acc = Qf[b, h, rows] @ Kf[b, h, cols].T
                 amax = np.where(valid, acc, -np.inf).max(axis=1)
                 r = _fl32(amax * c, exact)
+                R[b, h, j, rows] = r
                 x = np.where(valid, _fl32(acc * c - r[:, None], exact), -np.inf)
                 e = _fl32(np.exp2(x), exact)
                 p_hat = e if exact else p_fake_quant(e)
@@ -132,13 +141,13 @@ def qat_forward(fq: dict, causal: bool, dtype_round, exact: bool = False, heads=
             O[b, h, rows] = acc_o / l[:, None]
             Op[b, h, rows] = acc_p / l[:, None]
             L[b, h, rows] = (m + np.log2(l)) * LN2
-    return O, Op, L
+    return O, Op, L, R
 
 
-def qat_backward(fq: dict, Op_stored, L_stored, dO, causal: bool, dtype_round, exact: bool = False,
+def qat_backward(fq: dict, Op_stored, L_stored, R, dO, causal: bool, dtype_round, exact: bool = False,
                  heads=None, q_blocks=None, kv_blocks=None, D_from=None, bwd_p_quant: bool = True):
-    """Q5.  ``Op_stored``: O' as stored (float32), ``L_stored``: the stored float32 L, ``dO`` the
-    16-bit upstream gradient.  ``q_blocks`` / ``kv_blocks`` restrict which dQ / dK, dV rows are
+    """Q5.  ``Op_stored``: O' as stored (float32), ``L_stored``: the stored float32 L, ``R`` the
+    forward's row maxima, ``dO`` the 16-bit upstream gradient.  ``q_blocks`` / ``kv_blocks`` restrict which dQ / dK, dV rows are
     completed.  The two ablations of section 2.2 / the results: ``D_from`` replaces O' in D (D
     from the FP4 output O), ``bwd_p_quant=False`` feeds dV the unquantised P.
     Returns dict(dQ, dK, dV, D) float64."""
@@ -171,7 +180,17 @@ def qat_backward(fq: dict, Op_stored, L_stored, dO, causal: bool, dtype_round, e
         dS = _fl32(P * _fl32(dP - D32[b, h, rows][:, None], exact), exact)
         dS16 = dS if exact else np.asarray(dtype_round(dS.astype(np.float32)), np.float64)
         if want_dkv:
-            p_hat = P if (exact or not bwd_p_quant) else p_fake_quant(P)
+            if exact or not bwd_p_quant:
+                p_hat = P
+            else:
+                # Q3: the forward's quantised P, rebuilt from its row maxima and normalised
+                r = np.asarray(R[b, h, j, rows], np.float64)
+                live = valid.any(axis=1)
+                r0 = np.where(live, r, 0.0)
+                e = np.where(valid, _fl32(np.exp2(_fl32(acc * c - r0[:, None], False)), False), 0.0)
+                g = _fl32(np.exp2(_fl32(r0 - L2[b, h, rows], False)), False)
+                p_hat = np.where(live[:, None], _fl32(p_fake_quant(e) * g[:, None], False), 0.0)
+                p_hat = np.asarray(dtype_round(p_hat.astype(np.float32)), np.float64)
             dV[b, h, cols] += p_hat.T @ dO[b, h, rows]
             dK[b, h, cols] += inv_sqrt_d * (dS16.T @ Qf[b, h, rows])
         if want_dq:
@@ -195,9 +214,9 @@ def qat_backward(fq: dict, Op_stored, L_stored, dO, causal: bool, dtype_round, e
 def run(Q, K, V, dO, causal: bool, dtype_round, exact: bool = False) -> dict:
     """Whole Attn-QAT path on full tensors: fake quantisation, forward, backward."""
     fq = fake_quant(Q, K, V, exact=exact)
-    O, Op, L = qat_forward(fq, causal, dtype_round, exact=exact)
+    O, Op, L, R = qat_forward(fq, causal, dtype_round, exact=exact)
     Op_stored = Op if exact else Op.astype(np.float32)
     L_stored = L if exact else L.astype(np.float32)
     O_stored = O if exact else dtype_round(O.astype(np.float32))
-    g = qat_backward(fq, Op_stored, L_stored, dO, causal, dtype_round, exact=exact)
-    return dict(fq=fq, O=O, Op=Op, L=L, O_stored=O_stored, Op_stored=Op_stored, L_stored=L_stored, **g)
+    g = qat_backward(fq, Op_stored, L_stored, R, dO, causal, dtype_round, exact=exact)
+    return dict(fq=fq, O=O, Op=Op, L=L, R=R, O_stored=O_stored, Op_stored=Op_stored, L_stored=L_stored, **g)

@@ -133,7 +133,7 @@ def test_forward_closed_form(causal, dtype):
     N, d = 128, 64
     Q, K, V, _ = _inputs(N, d, seed=3, dtype=dtype)
     fq = qat.fake_quant(Q[:, :1], K[:, :1], V[:, :1])
-    O, Op, _ = qat.qat_forward(fq, causal, lambda a: workloads.round_to(a, dtype))
+    O, Op, _, _ = qat.qat_forward(fq, causal, lambda a: workloads.round_to(a, dtype))
     O_cf, Op_cf = _closed_form_forward(fq, N, d, causal, dtype)
     assert metrics.rel_l2(O[0, 0], O_cf) < 1e-12
     assert metrics.rel_l2(Op[0, 0], Op_cf) < 1e-12
@@ -157,7 +157,7 @@ def test_rowsum_identity_behind_o_prime():
     output O does not."""
     Q, K, V, dO = _inputs(192, 64, seed=6)
     fq = qat.fake_quant(Q, K, V)
-    O, Op, L = qat.qat_forward(fq, False, lambda a: a)
+    O, Op, L, _ = qat.qat_forward(fq, False, lambda a: a)
     _, _, P = fpa.fpa_forward(fq["Qf"], fq["Kf"], fq["Vf"], False)
     dP = np.asarray(dO, np.float64) @ np.swapaxes(fq["Vf"], -1, -2)
     want = (P * dP).sum(-1)
@@ -167,20 +167,39 @@ def test_rowsum_identity_behind_o_prime():
     assert metrics.rel_l2(D_o, want) > 1e-2
 
 
-def test_dv_closed_form():
-    """dV = phi(P)^T dO with P = fl32(2^fl32(acc c - L2)) row by row, phi by grid search."""
-    N, d = 128, 64
+@pytest.mark.parametrize("causal", [False, True])
+def test_dv_is_the_gradient_of_the_forward_output(causal):
+    """The forward's O is linear in V': O = W V' with W_ik = 2^(r_j(i) - M_i) phi(e_i, block j)_k /
+    l_i (untiled, phi by grid search, j the key block of k).  The backward's dV must be W^T dO:
+    the exact gradient of the fake-quantised forward (16-bit rounding of P^ switched off; the
+    float32 roundings of L2 and of 2^(r - L2) leave ~1e-7)."""
+    N, d = 192, 64
     Q, K, V, dO = _inputs(N, d, seed=7)
     Q, K, V, dO = Q[:, :1], K[:, :1], V[:, :1], dO[:, :1]
-    out = qat.run(Q, K, V, dO, True, workloads.round_fp16)
-    fq = out["fq"]
+    ident = lambda a: a
+    fq = qat.fake_quant(Q, K, V)
+    O, Op, L, R = qat.qat_forward(fq, causal, ident)
+    g = qat.qat_backward(fq, Op.astype(np.float32), L.astype(np.float32), R, dO, causal, ident)
+    Qf, Kf, Vf = (fq[k][0, 0] for k in ("Qf", "Kf", "Vf"))
     c = float(np.float32(qat.LOG2E / math.sqrt(d)))
-    L2 = (out["L_stored"][0, 0] * np.float32(qat.LOG2E)).astype(np.float32).astype(np.float64)
-    acc = fq["Qf"][0, 0] @ fq["Kf"][0, 0].T
-    x = np.where(np.triu(np.ones((N, N), bool), 1), -np.inf, (acc * c - L2[:, None]).astype(np.float32))
-    P = np.exp2(x.astype(np.float64)).astype(np.float32)
-    Ph = np.stack([_phi_brute(P[i]) for i in range(N)])
-    assert metrics.rel_l2(out["dV"][0, 0], Ph.T @ np.asarray(dO[0, 0], np.float64)) < 1e-12
+    W = np.zeros((N, N))
+    for i in range(N):
+        rs, ph, sums = {}, {}, {}
+        for j in range(N // 64):
+            keys = np.arange(64 * j, 64 * j + 64)
+            valid = keys <= i if causal else np.ones(64, bool)
+            if not valid.any():
+                continue
+            acc = Kf[keys] @ Qf[i]
+            r = float(np.float32(np.where(valid, acc, -np.inf).max() * c))
+            e = np.exp2(np.where(valid, (acc * c - r).astype(np.float32), -np.inf).astype(np.float64)).astype(np.float32)
+            rs[j], ph[j], sums[j] = r, _phi_brute(e), e.astype(np.float64).sum()
+        M = max(rs.values())
+        den = sum(2.0 ** (rs[j] - M) * sums[j] for j in rs)
+        for j in rs:
+            W[i, 64 * j:64 * j + 64] = 2.0 ** (rs[j] - M) * ph[j] / den
+    assert metrics.rel_l2(O[0, 0], W @ Vf) < 1e-12
+    assert metrics.rel_l2(g["dV"][0, 0], W.T @ np.asarray(dO[0, 0], np.float64)) < 1e-6
 
 
 def test_straight_through_gradient_of_fake_quantised_operands():
@@ -189,13 +208,13 @@ def test_straight_through_gradient_of_fake_quantised_operands():
     Q, K, V, dO = _inputs(192, 64, seed=8)
     fq = qat.fake_quant(Q, K, V)
     ident = lambda a: a
-    O, Op, L = qat.qat_forward(fq, True, ident)
-    g = qat.qat_backward(fq, Op, L.astype(np.float32), dO, True, ident, bwd_p_quant=False)
+    O, Op, L, R = qat.qat_forward(fq, True, ident)
+    g = qat.qat_backward(fq, Op, L.astype(np.float32), R, dO, True, ident, bwd_p_quant=False)
     ref = fpa.fpa_backward(fq["Qf"], fq["Kf"], fq["Vf"], dO, True)
     for k in ("dQ", "dK", "dV"):
         assert metrics.rel_l2(g[k], ref[k]) < 1e-5, (k, metrics.rel_l2(g[k], ref[k]))
     # the method's dV carries the FP4 P and differs
-    g_q = qat.qat_backward(fq, Op, L.astype(np.float32), dO, True, ident)
+    g_q = qat.qat_backward(fq, Op, L.astype(np.float32), R, dO, True, ident)
     assert metrics.rel_l2(g_q["dV"], ref["dV"]) > 1e-3
 
 
@@ -206,7 +225,7 @@ def test_ablation_d_from_fp4_output_is_worse():
     out = qat.run(Q, K, V, dO, False, workloads.round_fp16)
     fq = out["fq"]
     ref = fpa.fpa_backward(fq["Qf"], fq["Kf"], fq["Vf"], dO, False)
-    bad = qat.qat_backward(fq, out["Op_stored"], out["L_stored"], dO, False, workloads.round_fp16,
+    bad = qat.qat_backward(fq, out["Op_stored"], out["L_stored"], out["R"], dO, False, workloads.round_fp16,
                            D_from=out["O_stored"])
     for k in ("dQ", "dK"):
         good_err = metrics.rel_l2(out[k], ref[k])
