@@ -7,7 +7,7 @@ differentiable PyTorch operation.
 """
 from .binding import (  # noqa: F401
     Fp4Quantized, Quantized, SageError, SageParams, lib, make_params, sage_attn_bwd, sage_attn_fwd,
-    sage_attn_fwd_fp4, sage_quantize_fp4,
+    sage_attn_fwd_fp4, sage_quantize_fp4, sage_qat_bwd, sage_qat_fwd, sage_qat_quantize,
     sage_device_status, sage_dump_bytes, sage_qknorm_bwd, sage_quantize_smooth,
     sage_quantize_smooth_noalloc, sage_quantize_smooth_qknorm, sage_status_string, sage_version,
 )

@@ -69,7 +69,8 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER(SageParams)
     vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
-    for name in ("sage_quantize_workspace_bytes", "sage_fwd_workspace_bytes", "sage_bwd_workspace_bytes"):
+    for name in ("sage_quantize_workspace_bytes", "sage_fwd_workspace_bytes", "sage_bwd_workspace_bytes",
+                 "sage_qat_bwd_workspace_bytes"):
         getattr(L, name).argtypes = [P]
         getattr(L, name).restype = sz
     L.sage_dump_bytes.argtypes = [P, ci]
@@ -88,6 +89,12 @@ def lib() -> ctypes.CDLL:
     L.sage_attn_fwd.restype = ci
     L.sage_attn_bwd.argtypes = [P] + [vp] * 15 + [sz, vp]
     L.sage_attn_bwd.restype = ci
+    L.sage_qat_quantize.argtypes = [P] + [vp] * 6 + [vp]
+    L.sage_qat_quantize.restype = ci
+    L.sage_qat_fwd.argtypes = [P] + [vp] * 7 + [vp]
+    L.sage_qat_fwd.restype = ci
+    L.sage_qat_bwd.argtypes = [P] + [vp] * 11 + [sz, vp]
+    L.sage_qat_bwd.restype = ci
     L.sage_device_status.argtypes = [vp]
     L.sage_device_status.restype = ci
     L.sage_status_string.argtypes = [ci]
@@ -352,6 +359,61 @@ def sage_attn_bwd(q: Quantized, V: torch.Tensor, O: torch.Tensor, L: torch.Tenso
                           _ptr(dK), _ptr(dV), _ptr(ws), nws if ws is None else ws.numel(),
                           _stream(stream))
     _check("sage_attn_bwd", st)
+    return dQ, dK, dV
+
+
+def _qat_params(t: torch.Tensor, causal: bool) -> SageParams:
+    B, H, N, d = t.shape
+    return make_params(B, H, N, d, _dtype_code(t), causal, smooth_k=False, smooth_q=False)
+
+
+def sage_qat_quantize(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, out=None, stream=None):
+    """Attn-QAT NVFP4 fake quantisation (no smoothing).  Returns (Qf, Kf, Vf) in the input dtype."""
+    _require_cuda(Q, K, V)
+    Qf, Kf, Vf = out if out is not None else (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V))
+    p = _qat_params(Q, False)
+    st = lib().sage_qat_quantize(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(Qf), _ptr(Kf), _ptr(Vf),
+                                 _stream(stream))
+    _check("sage_qat_quantize", st)
+    return Qf, Kf, Vf
+
+
+def sage_qat_fwd(Qf: torch.Tensor, Kf: torch.Tensor, Vf: torch.Tensor, *, causal: bool, out=None, stream=None):
+    """Attn-QAT forward.  Returns (O input dtype, O' float32, L float32 (B,H,N),
+    R float32 (B,H,N/64,N) the row maxima the backward needs)."""
+    _require_cuda(Qf, Kf, Vf)
+    B, H, N, d = Qf.shape
+    dev = Qf.device
+    if out is None:
+        out = (torch.empty_like(Qf), torch.empty((B, H, N, d), dtype=torch.float32, device=dev),
+               torch.empty((B, H, N), dtype=torch.float32, device=dev),
+               torch.empty((B, H, N // 64, N), dtype=torch.float32, device=dev))
+    O, Op, Lse, R = out
+    _require_cuda(O, Op, Lse, R)
+    p = _qat_params(Qf, causal)
+    st = lib().sage_qat_fwd(ctypes.byref(p), _ptr(Qf), _ptr(Kf), _ptr(Vf), _ptr(O), _ptr(Op), _ptr(Lse), _ptr(R),
+                            _stream(stream))
+    _check("sage_qat_fwd", st)
+    return O, Op, Lse, R
+
+
+def sage_qat_bwd(Qf: torch.Tensor, Kf: torch.Tensor, Vf: torch.Tensor, Op: torch.Tensor, L: torch.Tensor,
+                 R: torch.Tensor, dO: torch.Tensor, *, causal: bool, grads=None,
+                 workspace: torch.Tensor | None = None, stream=None):
+    """Attn-QAT backward.  Returns (dQ, dK, dV) float32 (B,H,N,d)."""
+    _require_cuda(Qf, Kf, Vf, Op, L, R, dO)
+    B, H, N, d = Qf.shape
+    dev = Qf.device
+    if grads is None:
+        grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3))
+    dQ, dK, dV = grads
+    p = _qat_params(Qf, causal)
+    lb = lib()
+    nws = lb.sage_qat_bwd_workspace_bytes(ctypes.byref(p))
+    ws = workspace if workspace is not None else _workspace(nws, dev)
+    st = lb.sage_qat_bwd(ctypes.byref(p), _ptr(Qf), _ptr(Kf), _ptr(Vf), _ptr(Op), _ptr(L), _ptr(R), _ptr(dO),
+                         _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), nws if ws is None else ws.numel(), _stream(stream))
+    _check("sage_qat_bwd", st)
     return dQ, dK, dV
 
 

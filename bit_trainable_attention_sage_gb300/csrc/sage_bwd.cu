@@ -45,6 +45,15 @@
 //   dS = fl32(P * fl32(dP - D))
 //   per 64x64 tile: s = fl32(max|x| / 127), code = rne16(fl32(x * fl32(1/s) + 1536)) - 1536;
 //   max|x| < 2^-120 -> zero tile
+// Attn-QAT variant ("Attn-QAT: 4-Bit Attention With Quantization-Aware Training", technical
+// summary, sections 2.2-2.3): every operand is a 16-bit value of the input type -- the
+// fake-quantised Q', K', V' and the plain dO (also the B operand of dV) -- and the scales are 1:
+//   P  = fl32(ex2(fl32(acc c - L2))), D from the high-precision O', dS = fl32(P fl32(dP - D))
+//        rounded to the input type (A operand of dK, B operand of dQ);
+//   P^ = the forward's quantised P rebuilt: e = ex2(fl32(acc c - r)) with the forward's row
+//        maximum r of this (key block, query), phi(e) one-level NVFP4 over the 16 keys of a block
+//        (16 lanes of a warp: shuffles), P^ = rnd16(fl32(phi(e) fl32(ex2(fl32(r - L2))))) (A of dV).
+// One pass over S^T and dP^T suffices: nothing waits for a tile maximum.
 #include "sage_device.cuh"
 #include "sage_internal.h"
 
@@ -93,6 +102,7 @@ struct Smem {
     alignas(1024) uint8_t dss[2][128 * 128];           // dS^ codes [step % 2][key][64 q], 128-byte rows
     alignas(16) float L2s[3][64];                      // [stage][q]: -fl32(L log2 e), negated
     alignas(16) float Ds[3][64];                       // [stage][q]: D
+    alignas(16) float Rs[3][2][64];                    // Attn-QAT: [stage][key block][q] forward row maxima
     float red[4][2][2];                                // [warp][step parity][P max, |dS| max]
     float sps[kScaleSlots][2];                         // [step % 8][key block] P tile scales
     float sds[kScaleSlots][2];                         // [step % 8][key block] dS tile scales
@@ -290,6 +300,88 @@ __device__ __forceinline__ void score_pass2(uint32_t s_col, uint32_t dp_col, con
     });
 }
 
+// Attn-QAT row data of 8 query columns: -L2, D and the forward's row maxima r of this key block
+struct RowData8Q : RowData8 {
+    float rr[8];
+    __device__ __forceinline__ void load(const float *L2s, const float *Ds, const float *Rs, int col0) {
+        RowData8::load(L2s, Ds, col0);
+        *reinterpret_cast<float4 *>(&rr[0]) = *reinterpret_cast<const float4 *>(&Rs[col0]);
+        *reinterpret_cast<float4 *>(&rr[4]) = *reinterpret_cast<const float4 *>(&Rs[col0 + 4]);
+    }
+};
+
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Attn-QAT: the single score pass over the 64 query columns of a block (same staging as
+// score_walk).  Per column: P and dS as score_p_ds_8; e = ex2(fl32(acc c - r)) (masked to 0 where
+// EDGE says the pair is not live); the NVFP4 block maximum over the 16 keys = 16 lanes; s, 1/s and
+// the E2M1 codes as the forward forms them; P^ = rnd16(fl32(phi(e) g)), g = ex2(fl32(r - L2)),
+// zero where phi(e) is zero (r may be undefined for a pair the forward never visited, all of
+// whose entries are masked).  P^ goes to TMEM over read S^T columns, dS to this key's dS row.
+template <bool EDGE, bool BF16>
+__device__ __forceinline__ void score_pass_qat(uint32_t s_col, uint32_t dp_col, const float *L2s,
+                                               const float *Ds, const float *Rs, float cq, int qlo,
+                                               bool key_ok, uint8_t *dss_row, int swz) {
+    auto half = [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8Q &rd, int col0) {
+        float pv[8], ds[8];
+        score_p_ds_8<EDGE, false, false>(sr, dr, rd, col0, cq, 0.0f, qlo, key_ok, 1.0f, pv, ds);
+        uint32_t pk[4], dk[4];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            float e[2], sc[2], g[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                float x = __fmaf_rn(__uint_as_float(sr[k + u]), cq, -rd.rr[k + u]);
+                if (EDGE) x = (key_ok && col0 + k + u >= qlo) ? x : -INFINITY;
+                e[u] = ex2_approx(x);
+                float m = e[u];
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                sc[u] = e4m3_round_f(__fdiv_rn(m, 6.0f));
+                g[u] = ex2_approx(__fadd_rn(rd.rr[k + u], rd.l2[k + u]));
+            }
+            const float i0 = sc[0] > 0.0f ? __frcp_rn(sc[0]) : 0.0f;
+            const float i1 = sc[1] > 0.0f ? __frcp_rn(sc[1]) : 0.0f;
+            const f2 y = mul2(f2{e[0], e[1]}, f2{i0, i1});
+            const uint32_t h = hmul2(e2m1x2_to_f16x2(e2m1x2(y.x, y.y)), pack_half2(sc[0], sc[1]));
+            const float2 ph = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+            const float p0 = ph.x != 0.0f ? __fmul_rn(ph.x, g[0]) : 0.0f;
+            const float p1 = ph.y != 0.0f ? __fmul_rn(ph.y, g[1]) : 0.0f;
+            pk[k / 2] = pack16x2(p0, p1, BF16);
+            dk[k / 2] = pack16x2(ds[k], ds[k + 1], BF16);
+        }
+        tmem_st4(s_col + col0 / 2, pk);
+        *reinterpret_cast<uint4 *>(dss_row + (((col0 >> 3) ^ swz) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+    };
+    uint32_t sA[8], dA[8], sB[8], dB[8];
+    RowData8Q rA, rB;
+    tmem_ld8(s_col, sA);
+    tmem_ld8(dp_col, dA);
+    rA.load(L2s, Ds, Rs, 0);
+#pragma unroll 1
+    for (int col0 = 0; col0 < 64; col0 += 16) {
+        tmem_wait_ld_regs(sA, dA);
+        tmem_ld8(s_col + col0 + 8, sB);
+        tmem_ld8(dp_col + col0 + 8, dB);
+        rB.load(L2s, Ds, Rs, col0 + 8);
+        half(sA, dA, rA, col0);
+        tmem_wait_ld_regs(sB, dB);
+        if (col0 + 16 < 64) {
+            tmem_ld8(s_col + col0 + 16, sA);
+            tmem_ld8(dp_col + col0 + 16, dA);
+            rA.load(L2s, Ds, Rs, col0 + 16);
+        }
+        half(sB, dB, rB, col0 + 8);
+    }
+}
+
 // d = 128: this warpgroup's 32 query rows [32 half, 32 half + 32) of the step's two transposed dQ
 // products in R_A (thread = d column, TMEM columns = query rows): the scaled sum is added to
 // global dQ by float32 reductions, one row at a time, so a warp's 32 lanes cover 32 consecutive
@@ -323,7 +415,7 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
     }
 }
 
-template <int D, int DPK, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP, bool QAT>
 __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const CUtensorMap *mapK, const CUtensorMap *mapV,
                                       const CUtensorMap *mapQ, const CUtensorMap *mapdO,
                                       const CUtensorMap *mapdOh) {
@@ -364,9 +456,13 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
                 for (int dc = 0; dc < D / 64; ++dc) tma_load_3d(s.doc[s2][dc], mapdO, &s.do_full[s2], 64 * dc, q0, bh);
                 last_do[s2] = c;
                 if (c >= 3 && !mbar_wait(&s.meta_free[s3], (c / 3 - 1) & 1, abort_flag, &g_bwd_err, 2)) break;
-                mbar_arrive_expect_tx(&s.meta_full[s3], 2 * 64 * 4);
+                mbar_arrive_expect_tx(&s.meta_full[s3], (QAT ? 4 : 2) * 64 * 4);
                 bulk_load(s.L2s[s3], a.L2 + bhN + q0, 64 * 4, &s.meta_full[s3]);
                 bulk_load(s.Ds[s3], a.D + bhN + q0, 64 * 4, &s.meta_full[s3]);
+                if (QAT)
+                    for (int g = 0; g < 2; ++g)
+                        bulk_load(s.Rs[s3][g], a.R + (static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)) * N + q0,
+                                  64 * 4, &s.meta_full[s3]);
                 last_meta[s3] = c;
                 if (c >= 3 && !mbar_wait(&s.q_free[s3], (c / 3 - 1) & 1, abort_flag, &g_bwd_err, 3)) break;
                 mbar_arrive_expect_tx(&s.q_full[s3], kBlkBytes);
@@ -404,10 +500,12 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
         // first because the score warpgroup's pass 2 of step c + 1 waits for it to release the
         // dS^ tile.
         if (elect_one()) {
-            constexpr uint32_t idS = idesc_f16(128, 64, false, false, false);      // S^T
+            // Attn-QAT: every operand in the input type; otherwise codes as fp16, dP per dtype
+            constexpr bool kOpsBf16 = QAT && DPK == kDpBf16;
+            constexpr uint32_t idS = idesc_f16(128, 64, kOpsBf16, false, false);   // S^T
             constexpr uint32_t idDP = idesc_f16(128, 64, DPK == kDpBf16, false, false);   // dP^T
-            constexpr uint32_t idKV = idesc_f16(128, D, false, false, true);       // dK, dV
-            constexpr uint32_t idQ = idesc_f16(128, 64, false, true, true);        // dQ(^T)
+            constexpr uint32_t idKV = idesc_f16(128, D, kOpsBf16, false, true);    // dK, dV
+            constexpr uint32_t idQ = idesc_f16(128, 64, kOpsBf16, true, true);     // dQ(^T)
             // base descriptors; a byte offset `off` inside an operand adds off >> 4
             const uint64_t dKt = sdesc_sw128(smem_u32(s.kt[0]), 16, 1024);         // K-major A
             const uint64_t dVt = sdesc_sw128(smem_u32(s.vt[0]), 16, 1024);
@@ -506,7 +604,7 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
 }
 
 // Score warpgroup (warps 0-3).
-template <int D, int DPK, bool BIAS, bool DUMP, bool FP8>
+template <int D, int DPK, bool BIAS, bool DUMP, bool FP8, bool QAT>
 __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -529,6 +627,35 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const bool key_ok = key < N;
     const int kblk = min(2 * jt + kb, nblk - 1);
     const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 0);
+    if constexpr (QAT) {
+        for (int c = 0; c < n; ++c) {
+            const int q0 = 64 * (c_first + c);
+            const int b = c & 1, m3 = c % 3;
+            const int qlo = a.causal ? max(0, key - q0) : 0;
+            const bool edge = (a.causal && q0 < k0 + 128) || k0 + 128 > N;
+            if (!mbar_wait(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19)) break;
+            if (!mbar_wait(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20)) break;
+            tc_fence_after();
+            if (D != 128 && c >= 2 && !mbar_wait(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
+            const uint32_t s_col = lane_base + 128 * b;
+            uint8_t *dss_row = s.dss[b] + tq * 128;
+            if (edge)
+                score_pass_qat<true, DPK == kDpBf16>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], s.Rs[m3][kb], a.sl2, qlo,
+                                                     key_ok, dss_row, tq & 7);
+            else
+                score_pass_qat<false, DPK == kDpBf16>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], s.Rs[m3][kb], a.sl2, qlo,
+                                                      key_ok, dss_row, tq & 7);
+            tmem_wait_st();
+            fence_view_async_shared();
+            tc_fence_before();
+            __syncwarp();
+            if (lane_id() == 0) {
+                mbar_arrive(&s.codes_ready[b]);
+                mbar_arrive(&s.meta_free[m3]);
+            }
+        }
+        return;
+    }
     const float sk = key_ok ? a.sK[static_cast<size_t>(bh) * nblk + kblk] : 0.0f;
     const float *sQh = a.sQ + static_cast<size_t>(bh) * nblk;
     const float *biash = BIAS ? a.qbias + static_cast<size_t>(bh) * nblk * N + min(key, N - 1) : nullptr;
@@ -621,7 +748,7 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
 }
 
 // dV warpgroup (warps 4-7).
-template <int D, int DPK, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP, bool QAT>
 __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -649,20 +776,20 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
     float skb[2];
 #pragma unroll
     for (int g = 0; g < 2; ++g)
-        skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
-    const float *sdOh = a.sdO + static_cast<size_t>(bh) * nblk;
-    float sdo_next = sdOh[c_first];
+        skb[g] = QAT ? 1.0f : (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
+    const float *sdOh = QAT ? nullptr : a.sdO + static_cast<size_t>(bh) * nblk;
+    float sdo_next = QAT ? 1.0f : sdOh[c_first];
     for (int c = 0; c < n; ++c) {
         const int qb = c_first + c;
         const int q0 = 64 * qb;
         const int z = c & (kScaleSlots - 1);
         const float sdo = sdo_next;
-        if (c + 1 < n) sdo_next = sdOh[qb + 1];
+        if (!QAT && c + 1 < n) sdo_next = sdOh[qb + 1];
         // dV += s_P s_dO (P^T dO^)
         if (!mbar_wait(&s.a_full, c & 1, abort_flag, &g_bwd_err, 23)) break;
         tc_fence_after();
         {
-            const float sc = __fmul_rn(s.sps[z][kb], sdo);
+            const float sc = QAT ? 1.0f : __fmul_rn(s.sps[z][kb], sdo);
 #pragma unroll
             for (int cc = 0; cc < D; cc += 8) {
                 uint32_t r[8];
@@ -685,8 +812,8 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
             // s_dS s_K / sqrt(d), summed
             if (!mbar_wait(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 24)) break;
             tc_fence_after();
-            const float sg0 = __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
-            const float sg1 = __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
+            const float sg0 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
+            const float sg1 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
             dq_consume_128(lane_base, 0, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free);
         } else if ((c & 1) || c == n - 1) {
             // d = 64, step pair (c - 1, c) (or the last step alone): thread = query row of the
@@ -696,8 +823,8 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
             tc_fence_after();
             const int zq = (2 * pr + (tq >> 6)) & (kScaleSlots - 1);
             const int qrow = 64 * (c_first + 2 * pr) + tq;
-            const float s0 = __fmul_rn(__fmul_rn(s.sds[zq][0], skb[0]), a.inv_sqrt_d);
-            const float s1 = __fmul_rn(__fmul_rn(s.sds[zq][1], skb[1]), a.inv_sqrt_d);
+            const float s0 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[zq][0], skb[0]), a.inv_sqrt_d);
+            const float s1 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[zq][1], skb[1]), a.inv_sqrt_d);
             const bool live = qrow < N && 2 * pr + (tq >> 6) < n;
             float *dst = a.dQ + (bhN + min(qrow, N - 1)) * D;
 #pragma unroll
@@ -730,7 +857,7 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
 }
 
 // dK warpgroup (warps 8-11).
-template <int D, int DPK, bool BIAS, bool DUMP>
+template <int D, int DPK, bool BIAS, bool DUMP, bool QAT>
 __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
@@ -760,19 +887,19 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
 #pragma unroll
     for (int g = 0; g < 2; ++g)
         skb[g] = (k0 + 64 * g < N) ? a.sK[static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)] : 0.0f;
-    const float *sQh = a.sQ + static_cast<size_t>(bh) * nblk;
-    float sq_next = sQh[c_first];
+    const float *sQh = QAT ? nullptr : a.sQ + static_cast<size_t>(bh) * nblk;
+    float sq_next = QAT ? 1.0f : sQh[c_first];
     for (int c = 0; c < n; ++c) {
         const int qb = c_first + c;
         const int q0 = 64 * qb;
         const int z = c & (kScaleSlots - 1);
         const float sq = sq_next;
-        if (c + 1 < n) sq_next = sQh[qb + 1];
+        if (!QAT && c + 1 < n) sq_next = sQh[qb + 1];
         // dK += s_dS s_Q / sqrt(d) (dS^T Q^)   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d))
         if (!mbar_wait(&s.b_full, c & 1, abort_flag, &g_bwd_err, 30)) break;
         tc_fence_after();
         {
-            const float sc = __fmul_rn(__fmul_rn(s.sds[z][kb], sq), a.inv_sqrt_d);
+            const float sc = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][kb], sq), a.inv_sqrt_d);
 #pragma unroll
             for (int cc = 0; cc < D; cc += 8) {
                 uint32_t r[8];
@@ -800,8 +927,8 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
             // dQ rows 32-63 of this step
             if (!mbar_wait(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 31)) break;
             tc_fence_after();
-            const float sg0 = __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
-            const float sg1 = __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
+            const float sg0 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
+            const float sg1 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
             dq_consume_128(lane_base, 1, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free);
         }
     }
@@ -812,7 +939,7 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
     }
 }
 
-template <int D, int DPK, bool BIAS, bool DUMP, bool FP8>
+template <int D, int DPK, bool BIAS, bool DUMP, bool FP8, bool QAT>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                 const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapdO,
@@ -847,20 +974,20 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
     // each role computes its own CTA geometry: a value computed here and used by several roles
     // would have to sit in the same register in all of them, the 24-register control one included
     if (warp >= 12) {
-        control_role<D, DPK, BIAS, DUMP>(s, a, &mapK, &mapV, &mapQ, &mapdO, &mapdOh);
+        control_role<D, DPK, BIAS, DUMP, QAT>(s, a, &mapK, &mapV, &mapQ, &mapdO, &mapdOh);
         tc_fence_before();
         __syncthreads();
         if (warp == kMmaWarp) tmem_dealloc(s.tmem_base, 512);
     } else if (warp < 4) {
-        score_role<D, DPK, BIAS, DUMP, FP8>(s, a);
+        score_role<D, DPK, BIAS, DUMP, FP8, QAT>(s, a);
         tc_fence_before();
         __syncthreads();
     } else if (warp < 8) {
-        dv_role<D, DPK, BIAS, DUMP>(s, a);
+        dv_role<D, DPK, BIAS, DUMP, QAT>(s, a);
         tc_fence_before();
         __syncthreads();
     } else {
-        dk_role<D, DPK, BIAS, DUMP>(s, a);
+        dk_role<D, DPK, BIAS, DUMP, QAT>(s, a);
         tc_fence_before();
         __syncthreads();
     }
@@ -868,10 +995,10 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
 
 }  // namespace bwd
 
-template <int D, int DPK, bool BIAS, bool DUMP, bool FP8>
+template <int D, int DPK, bool BIAS, bool DUMP, bool FP8, bool QAT = false>
 static cudaError_t launch_bwd_t(const sage_params &p, const CUtensorMap *maps, const BwdArgs &a,
                                 cudaStream_t st) {
-    auto kern = bwd::sage_bwd_kernel<D, DPK, BIAS, DUMP, FP8>;
+    auto kern = bwd::sage_bwd_kernel<D, DPK, BIAS, DUMP, FP8, QAT>;
     const int smem = static_cast<int>(sizeof(bwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -929,6 +1056,24 @@ cudaError_t launch_bwd(const sage_params &p, const __half *Q16, const __half *K1
         return cudaErrorInvalidValue;
     if (p.d == 128) return launch_bwd_k<128>(p, maps, a, st);
     return launch_bwd_k<64>(p, maps, a, st);
+}
+
+cudaError_t launch_bwd_qat(const sage_params &p, const void *Qf, const void *Kf, const void *Vf,
+                           const void *dO, BwdArgs a, cudaStream_t st) {
+    // K' and V': 128-row key tiles; Q', dO (for dP) and dO again (the B operand of dV): 64-row
+    // query blocks
+    CUtensorMap maps[5];
+    const uint64_t bh = static_cast<uint64_t>(p.B) * p.H;
+    if (!make_tmap_3d(&maps[0], Kf, p.d, p.N, bh, 128) || !make_tmap_3d(&maps[1], Vf, p.d, p.N, bh, 128) ||
+        !make_tmap_3d(&maps[2], Qf, p.d, p.N, bh, 64) || !make_tmap_3d(&maps[3], dO, p.d, p.N, bh, 64) ||
+        !make_tmap_3d(&maps[4], dO, p.d, p.N, bh, 64))
+        return cudaErrorInvalidValue;
+    const bool bf = p.dtype == SAGE_BF16;
+    if (p.d == 128)
+        return bf ? launch_bwd_t<128, bwd::kDpBf16, false, false, false, true>(p, maps, a, st)
+                  : launch_bwd_t<128, bwd::kDpFp16, false, false, false, true>(p, maps, a, st);
+    return bf ? launch_bwd_t<64, bwd::kDpBf16, false, false, false, true>(p, maps, a, st)
+              : launch_bwd_t<64, bwd::kDpFp16, false, false, false, true>(p, maps, a, st);
 }
 
 unsigned int take_bwd_error() {

@@ -456,6 +456,62 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     return SAGE_OK;
 }
 
+// Attn-QAT entries: no flags, no smoothing
+static int check_qat(const sage_params *p) {
+    SAGE_TRY(check_params(p));
+    if (p->flags || p->smooth_k || p->smooth_q) return SAGE_ERR_UNSUPPORTED;
+    return SAGE_OK;
+}
+
+int sage_qat_quantize(const sage_params *p, const void *Q, const void *K, const void *V,
+                      void *Qf, void *Kf, void *Vf, sage_stream_t stream) {
+    SAGE_TRY(check_qat(p));
+    SAGE_TRY(check_ptrs({Q, K, V, Qf, Kf, Vf}));
+    SAGE_CUDA(launch_qat_fake_quant(*p, Q, K, V, Qf, Kf, Vf, reinterpret_cast<cudaStream_t>(stream)));
+    return SAGE_OK;
+}
+
+int sage_qat_fwd(const sage_params *p, const void *Qf, const void *Kf, const void *Vf, void *O,
+                 float *Op, float *L, float *R, sage_stream_t stream) {
+    SAGE_TRY(check_qat(p));
+    SAGE_TRY(check_ptrs({Qf, Kf, Vf, O, Op, L, R}));
+    FwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.O = O; a.L = L; a.R = R;
+    a.N = p->N; a.H = p->H; a.causal = p->causal; a.dtype = p->dtype;
+    a.sl2 = scale_log2(p->d);
+    SAGE_CUDA(launch_fwd_qat(*p, Qf, Kf, Vf, a, Op, reinterpret_cast<cudaStream_t>(stream)));
+    return SAGE_OK;
+}
+
+size_t sage_qat_bwd_workspace_bytes(const sage_params *p) {
+    if (check_qat(p) != SAGE_OK) return 0;
+    return 2 * ((rows(*p) * sizeof(float) + 255) & ~static_cast<size_t>(255));
+}
+
+int sage_qat_bwd(const sage_params *p, const void *Qf, const void *Kf, const void *Vf, const float *Op,
+                 const float *L, const float *R, const void *dO, float *dQ, float *dK, float *dV,
+                 void *workspace, size_t workspace_bytes, sage_stream_t stream) {
+    SAGE_TRY(check_qat(p));
+    SAGE_TRY(check_ptrs({Qf, Kf, Vf, Op, L, R, dO, dQ, dK, dV}));
+    SAGE_TRY(check_ws(workspace, workspace_bytes, sage_qat_bwd_workspace_bytes(p)));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Carve c(workspace);
+    float *D = c.take<float>(rows(*p));
+    float *L2 = c.take<float>(rows(*p));
+    SAGE_CUDA(launch_qat_bwd_prologue(*p, dO, Op, L, L2, D, st));
+    SAGE_CUDA(cudaMemsetAsync(dQ, 0, elems(*p) * sizeof(float), st));
+    BwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.D = D; a.L2 = L2; a.R = R;
+    a.dQ = dQ; a.dK = dK; a.dV = dV;
+    a.N = p->N; a.H = p->H; a.causal = p->causal; a.dtype = p->dtype;
+    a.sl2 = scale_log2(p->d);
+    a.inv_sqrt_d = static_cast<float>(1.0 / __builtin_sqrt(static_cast<double>(p->d)));
+    SAGE_CUDA(launch_bwd_qat(*p, Qf, Kf, Vf, dO, a, st));
+    return SAGE_OK;
+}
+
 size_t sage_dump_bytes(const sage_params *p, int which) {
     if (check_params(p) != SAGE_OK) return 0;
     size_t b = 0;

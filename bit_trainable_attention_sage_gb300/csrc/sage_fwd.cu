@@ -42,6 +42,15 @@
 // sqrt(d)) alone; P~2 = fl32(2688 ex2(x)) is quantised per 16 keys, s_P2 = e4m3(fl32(max / 6)),
 // code = e2m1(fl32(v fl32(1 / s_P2))), and the PV operand is s_P2 * code; the PV scale is
 // s_P1 = 2^(r - m') / 2688 (eq. (6) with the tile row max r).
+// Attn-QAT forward ("Attn-QAT: 4-Bit Attention With Quantization-Aware Training", technical
+// summary, section 2.2): Q, K, V arrive fake-quantised in the input 16-bit type, and the MMAs run
+// on that type; c = fl32(log2(e) / sqrt(d)).  Two passes of this kernel: the first (QAT) codes
+// P^ = phi(e), phi one-level NVFP4 per 16 keys (s = e4m3(fl32(max / 6)), code =
+// e2m1(fl32(e fl32(1 / s))), operand s * code), and writes O, L and the row maxima r of every
+// (key block, row), from which the backward rebuilds P^; the second (QAT_HP) feeds the
+// unquantised e rounded to the 16-bit type and writes the high-precision O' in float32.  Both
+// scale their PV products by 2^(r - m') alone.  (A fused pass would need a second O accumulator:
+// 2 d float32 registers a thread do not fit beside the rest at d = 128.)
 #include "sage_device.cuh"
 #include "sage_internal.h"
 
@@ -93,6 +102,8 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) { return pack2<__nv_bfloat16>(lo, hi); }
+
 // number of keys a CTA tile visits: causal tiles stop at their last row
 __device__ __forceinline__ int tile_kv_end(int q0, int N, int causal) {
     if (q0 >= N) return 0;
@@ -131,9 +142,18 @@ __device__ __forceinline__ float fwd_row_max(uint32_t (&raw)[64], float c, const
 // FP8: P^ = e4m3(fl32(448 ex2(x))) instead, converted to fp16 in two instructions per pair.
 // FP4: each 16-key group is an NVFP4 block of v = fl32(2688 ex2(x)) (two passes over the group:
 // its maximum, then the codes), written as the dequantised fp16 values.
-constexpr int kFmtInt8 = 0, kFmtFp8 = 1, kFmtFp4 = 2;
+constexpr int kFmtInt8 = 0, kFmtFp8 = 1, kFmtFp4 = 2, kFmtQat = 3, kFmtQatHp = 4;
+// formats whose block scales live inside the dequantised operands: c = log2(e)/sqrt(d) alone
+__host__ __device__ constexpr bool scales_inside(int fmt) { return fmt == kFmtFp4 || fmt == kFmtQat || fmt == kFmtQatHp; }
 
-template <bool BIAS, bool MASKED, bool DUMP, int FMT>
+// an fp16 pair -> the same values as a bf16 pair (exact for the fake-quantised P values)
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+template <bool BIAS, bool MASKED, bool DUMP, int FMT, bool BF16OPS>
 __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, float rs,
                                            int nvalid, uint32_t code_col, int16_t *dump_row) {
     constexpr float kRound = 12582912.0f;          // 1.5 * 2^23
@@ -143,7 +163,38 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 16) {
         uint32_t pk[8];
-        if constexpr (FMT == kFmtFp4) {
+        if constexpr (FMT == kFmtQat || FMT == kFmtQatHp) {
+            f2 e[8];
+            float emax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
+                f2 x2 = fma2(a2, c2, nrs2);
+                if (MASKED) {
+                    x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
+                    x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
+                }
+                e[k / 2] = f2{ex2_approx(x2.x), ex2_approx(x2.y)};
+                sp[(k >> 1) & 1] = add2(sp[(k >> 1) & 1], e[k / 2]);
+                emax = max3f(emax, e[k / 2].x, e[k / 2].y);
+            }
+            if constexpr (FMT == kFmtQatHp) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) pk[k] = BF16OPS ? pack_bf162(e[k].x, e[k].y) : pack_half2(e[k].x, e[k].y);
+            } else {
+                // phi: one-level NVFP4 of this 16-key group (its largest entry is at most 1)
+                const float s1 = e4m3_round_f(__fdiv_rn(emax, 6.0f));
+                const float inv = s1 > 0.0f ? __frcp_rn(s1) : 0.0f;
+                const f2 inv2{inv, inv};
+                const uint32_t s1h = pack_half2(s1, s1);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const f2 y = mul2(e[k], inv2);
+                    const uint32_t h = hmul2(e2m1x2_to_f16x2(e2m1x2(y.x, y.y)), s1h);
+                    pk[k] = BF16OPS ? f16x2_to_bf16x2(h) : h;
+                }
+            }
+        } else if constexpr (FMT == kFmtFp4) {
             f2 e[8];
             float emax = 0.0f;
 #pragma unroll
@@ -199,7 +250,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
     return (sp[0].x + sp[1].x) + (sp[0].y + sp[1].y);
 }
 
-template <int D, typename OutT, bool BIAS, bool DUMP, int FMT>
+template <int D, typename OutT, bool BIAS, bool DUMP, int FMT, bool BF16OPS>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, const FwdArgs a) {
@@ -278,8 +329,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (elect_one()) {
-            constexpr uint32_t idS = idesc_f16(128, 128, false, false, false);
-            constexpr uint32_t idPV = idesc_f16(128, D, false, false, true);
+            constexpr uint32_t idS = idesc_f16(128, 128, BF16OPS, false, false);
+            constexpr uint32_t idPV = idesc_f16(128, D, BF16OPS, false, true);
             const uint32_t k_addr = smem_u32(s.k[0]), v_addr = smem_u32(s.v[0]);
             int pv_count[2] = {0, 0};
             // S_t = Q^_t K^(j)^T into the tile's S columns
@@ -358,7 +409,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int kv_end = kv_end_t[t];
         const int my_steps = nsteps_t[t];
         // FP4: the block scales live inside the dequantised operands
-        const float sq = FMT == kFmtFp4 ? 1.0f : a.sQ[static_cast<size_t>(bh) * nblk + qblk];
+        const float sq = scales_inside(FMT) ? 1.0f : a.sQ[static_cast<size_t>(bh) * nblk + qblk];
         const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 256 * t);
         float o[D];
 #pragma unroll
@@ -375,8 +426,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (h == 1 && !has_b) break;
                 const int kb = 2 * j + h;                     // key block index
                 const int key0 = 64 * kb;
-                const float c = FMT == kFmtFp4 ? a.sl2
-                                               : __fmul_rn(__fmul_rn(sq, a.sK[static_cast<size_t>(bh) * nblk + kb]), a.sl2);
+                const float c = scales_inside(FMT) ? a.sl2
+                                                   : __fmul_rn(__fmul_rn(sq, a.sK[static_cast<size_t>(bh) * nblk + kb]), a.sl2);
                 // keys allowed for this row inside the block: [key0, key0 + nvalid)
                 int nvalid = a.causal ? min(64, grow - key0 + 1) : 64;
                 if (grow >= N) nvalid = 0;
@@ -399,14 +450,16 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (nvalid == 64) r = fwd_row_max<BIAS, false>(raw, c, bias, 64);
                 else r = fwd_row_max<BIAS, true>(raw, c, bias, nvalid);
                 if (!BIAS && nvalid > 0) r = __fmul_rn(r, c);
+                // Attn-QAT: the backward rebuilds this pass's P^ from r
+                if (FMT == kFmtQat && grow < N) a.R[(static_cast<size_t>(bh) * nblk + kb) * N + grow] = r;
                 const float rs = (r == -INFINITY) ? 0.0f : r;
                 if (h == 0) r_h0 = r; else r_h1 = r;
                 // pass 2: codes and the row sum; codes go to TMEM cols [32h, 32h+32) over consumed
                 // S columns.  A warp with a masked column in any lane takes the masked variant.
                 int16_t *dump_row = DUMP && grow < N ? a.dump_p + (bhN + grow) * N + key0 : nullptr;
                 const float sum = __any_sync(0xffffffffu, nvalid < 64)
-                    ? fwd_codes<BIAS, true, DUMP, FMT>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
-                    : fwd_codes<BIAS, false, DUMP, FMT>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
+                    ? fwd_codes<BIAS, true, DUMP, FMT, BF16OPS>(raw, c, rs, nvalid, lane_base + 32 * h, dump_row)
+                    : fwd_codes<BIAS, false, DUMP, FMT, BF16OPS>(raw, c, rs, 64, lane_base + 32 * h, dump_row);
                 if (h == 0) sum_h0 = sum; else sum_h1 = sum;
                 // this half's codes are stored: its PV MMA may start
                 tmem_wait_st();
@@ -425,7 +478,9 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const float g = live ? ex2_approx(__fsub_rn(r_h[h], m_new)) : 0.0f;
                 l = (h == 0) ? __fmaf_rn(alpha, l, g * sum_h[h]) : __fmaf_rn(g, sum_h[h], l);
                 const int kb = min(2 * j + h, nblk - 1);
-                if (FMT == kFmtFp4)
+                if (FMT == kFmtQat || FMT == kFmtQatHp)
+                    cpv[h] = g;
+                else if (FMT == kFmtFp4)
                     cpv[h] = g * (1.0f / 2688.0f);
                 else
                     cpv[h] = (g * (FMT == kFmtFp8 ? 1.0f / 448.0f : 1.0f / 127.0f)) * a.sV[static_cast<size_t>(bh) * nblk + kb];
@@ -471,10 +526,15 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 ++pv_uses;
             }
         }
-        // epilogue: O / l in the output type, L = (m + log2 l) ln 2
+        // epilogue: O / l in the output type, L = (m + log2 l) ln 2 (the O' pass writes O' alone)
         if (grow < N && !*abort_flag) {
             const float inv_l = 1.0f / l;
             OutT *dst = static_cast<OutT *>(a.O) + (bhN + grow) * D;
+            if constexpr (std::is_same<OutT, float>::value) {
+#pragma unroll
+                for (int c = 0; c < D; c += 4)
+                    *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c] * inv_l, o[c + 1] * inv_l, o[c + 2] * inv_l, o[c + 3] * inv_l);
+            } else {
 #pragma unroll
             for (int c = 0; c < D; c += 8) {
                 uint4 w;
@@ -484,7 +544,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 w.w = pack2<OutT>(o[c + 6] * inv_l, o[c + 7] * inv_l);
                 *reinterpret_cast<uint4 *>(dst + c) = w;
             }
-            a.L[bhN + grow] = (m + __log2f(l)) * 0.69314718055994531f;
+            }
+            if (FMT != kFmtQatHp) a.L[bhN + grow] = (m + __log2f(l)) * 0.69314718055994531f;
         }
     }
     tc_fence_before();
@@ -494,10 +555,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
 }  // namespace fwd
 
-template <int D, typename OutT, bool BIAS, bool DUMP, int FMT>
+template <int D, typename OutT, bool BIAS, bool DUMP, int FMT, bool BF16OPS = false>
 static cudaError_t launch_fwd_t(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const FwdArgs &a, cudaStream_t st) {
-    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP, FMT>;
+    auto kern = fwd::sage_fwd_kernel<D, OutT, BIAS, DUMP, FMT, BF16OPS>;
     const int smem = static_cast<int>(sizeof(fwd::Smem<D>)) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -529,6 +590,32 @@ static cudaError_t launch_fwd_d(const sage_params &p, const CUtensorMap &mq, con
                           : launch_fwd_t<D, OutT, false, true, kFmtInt8>(p, mq, mk, mv, a, st);
     return bias ? launch_fwd_t<D, OutT, true, false, kFmtInt8>(p, mq, mk, mv, a, st)
                 : launch_fwd_t<D, OutT, false, false, kFmtInt8>(p, mq, mk, mv, a, st);
+}
+
+// Attn-QAT forward: both passes over the fake-quantised Q', K', V' (input 16-bit type); O and L,
+// then O' (float32)
+template <int D, typename T>
+static cudaError_t launch_fwd_qat_d(const sage_params &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                                    const CUtensorMap &mv, FwdArgs a, float *Op, cudaStream_t st) {
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    cudaError_t e = launch_fwd_t<D, T, false, false, fwd::kFmtQat, kBf16>(p, mq, mk, mv, a, st);
+    if (e != cudaSuccess) return e;
+    a.O = Op;
+    return launch_fwd_t<D, float, false, false, fwd::kFmtQatHp, kBf16>(p, mq, mk, mv, a, st);
+}
+
+cudaError_t launch_fwd_qat(const sage_params &p, const void *Qf, const void *Kf, const void *Vf, FwdArgs a,
+                           float *Op, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    const uint64_t bh = static_cast<uint64_t>(p.B) * p.H;
+    if (!make_tmap_3d(&mq, Qf, p.d, p.N, bh) || !make_tmap_3d(&mk, Kf, p.d, p.N, bh) ||
+        !make_tmap_3d(&mv, Vf, p.d, p.N, bh))
+        return cudaErrorInvalidValue;
+    if (p.d == 128)
+        return p.dtype == SAGE_FP16 ? launch_fwd_qat_d<128, __half>(p, mq, mk, mv, a, Op, st)
+                                    : launch_fwd_qat_d<128, __nv_bfloat16>(p, mq, mk, mv, a, Op, st);
+    return p.dtype == SAGE_FP16 ? launch_fwd_qat_d<64, __half>(p, mq, mk, mv, a, Op, st)
+                                : launch_fwd_qat_d<64, __nv_bfloat16>(p, mq, mk, mv, a, Op, st);
 }
 
 cudaError_t launch_fwd(const sage_params &p, const __half *Q16, const __half *K16,

@@ -72,6 +72,7 @@ struct FwdArgs {
     int N, H, causal, dtype;
     float sl2;            // log2(e)/sqrt(d)
     int fp4;              // 1: FP4 inference forward (dequantised NVFP4 operands, two-level P)
+    float *R;             // Attn-QAT: (B,H,N/64,N) row maxima r of each (key block, row), or NULL
 };
 
 struct BwdArgs {
@@ -85,6 +86,7 @@ struct BwdArgs {
     int16_t *dump_ds;     // debug: (B,H,N,N) dS codes
     float *dump_sp;       // debug: (B,H,N/64,N/64) P tile scales
     float *dump_sds;      // debug: (B,H,N/64,N/64) dS tile scales
+    const float *R;       // Attn-QAT: the forward's row maxima (B,H,N/64,N), else NULL
     int N, H, causal, dtype;
     float sl2, inv_sqrt_d;
 };
@@ -102,6 +104,12 @@ cudaError_t launch_widen_fp4(const uint8_t *codes, const uint8_t *scales, __half
 // int8 codes (or E4M3 bit patterns when fp8) -> their exact fp16 values
 cudaError_t launch_widen(const int8_t *src, __half *dst, size_t n, bool fp8, cudaStream_t st);
 cudaError_t launch_bwd_prologue(const sage_params &p, BwdPrologueArgs a, cudaStream_t st);
+// Attn-QAT: NVFP4 fake quantisation of Q, K, V into the input 16-bit type (no smoothing), and the
+// backward prologue D = rowsum(dO o O') (O' float32), L2 = -fl32(L log2 e)
+cudaError_t launch_qat_fake_quant(const sage_params &p, const void *Q, const void *K, const void *V,
+                                  void *Qf, void *Kf, void *Vf, cudaStream_t st);
+cudaError_t launch_qat_bwd_prologue(const sage_params &p, const void *dO, const float *Op, const float *L,
+                                    float *L2, float *D, cudaStream_t st);
 // gradient of the QK-norm: dX = r (g dY - xh mean(g dY xh)), xh = x r; dg (nullable, zeroed by
 // the caller) += sum over rows of dY xh
 cudaError_t launch_qknorm_bwd(const sage_params &p, const void *X, const float *g, const float *r,
@@ -112,12 +120,19 @@ cudaError_t launch_qbias(const sage_params &p, const void *K, const float *muK, 
 // sage_fwd.cu
 cudaError_t launch_fwd(const sage_params &p, const __half *Q16, const __half *K16,
                        const __half *V16, FwdArgs a, cudaStream_t st);
+// Attn-QAT: the forward over fake-quantised Q', K', V' in the input type (a.O, a.L), then O' into Op
+cudaError_t launch_fwd_qat(const sage_params &p, const void *Qf, const void *Kf, const void *Vf, FwdArgs a,
+                           float *Op, cudaStream_t st);
 unsigned int take_fwd_error();
 
 // sage_bwd.cu
 cudaError_t launch_bwd(const sage_params &p, const __half *Q16, const __half *K16,
                        const void *V, const void *dO, const __half *dO16, BwdArgs a,
                        cudaStream_t st);
+// Attn-QAT backward: S^T, dP^T, dV, dK, dQ on the fake-quantised Q', K', V' and dO, all in the
+// input 16-bit type (a.R, a.L2, a.D set; the scale pointers unused)
+cudaError_t launch_bwd_qat(const sage_params &p, const void *Qf, const void *Kf, const void *Vf,
+                           const void *dO, BwdArgs a, cudaStream_t st);
 unsigned int take_bwd_error();
 
 // tensor maps (sage_capi.cu)

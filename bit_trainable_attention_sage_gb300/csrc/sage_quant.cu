@@ -631,6 +631,119 @@ __global__ void __launch_bounds__(256) widen_fp4_kernel(const uint8_t *__restric
 }
 
 // ---------------------------------------------------------------------------------------------
+// Attn-QAT fake quantisation ("Attn-QAT: 4-Bit Attention With Quantization-Aware Training",
+// technical summary, section 2.2: no smoothing): the NVFP4 quantiser above, Q and K blocked along
+// d, V along the tokens, but each value leaves as s * code in the input 16-bit type (exact: at
+// most 6 significant bits, magnitudes in [2^-10, 2688]).
+// ---------------------------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ uint4 fake_quant8(const float (&x)[8], const float (&s)[8]) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = s[2 * i] == 0.0f ? 0.0f : __fdiv_rn(x[2 * i], s[2 * i]);
+        const float hi = s[2 * i + 1] == 0.0f ? 0.0f : __fdiv_rn(x[2 * i + 1], s[2 * i + 1]);
+        const uint32_t h = e2m1x2_to_f16x2(e2m1x2(lo, hi));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        v[2 * i] = c.x * s[2 * i];                   // exact products
+        v[2 * i + 1] = c.y * s[2 * i + 1];
+    }
+    return pack8<T>(v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) qat_fake_quant_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                             const T *__restrict__ V, T *__restrict__ Qf,
+                                                             T *__restrict__ Kf, T *__restrict__ Vf, int N,
+                                                             int d) {
+    __shared__ unsigned int vmax[4][128];
+    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z;
+    const T *src = z == 0 ? Q : (z == 1 ? K : V);
+    T *dst = z == 0 ? Qf : (z == 1 ? Kf : Vf);
+    const int vec_per_row = d / 8;
+    const int rows_in_flight = 256 / vec_per_row;
+    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
+    const int iters = 64 / rows_in_flight;
+    const size_t blk_off = (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * d;
+    if (z == 2) {
+        for (int i = threadIdx.x; i < 4 * 128; i += 256) (&vmax[0][0])[i] = 0u;
+        __syncthreads();
+    }
+    float x[4][8];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        if (it >= iters) break;
+        load8(src + blk_off + static_cast<size_t>(rg + it * rows_in_flight) * d + cv * 8, x[it]);
+    }
+    if (z < 2) {
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            if (it >= iters) break;
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[it][i]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));       // the block's other lane
+            const float sb = e4m3_round_f(__fdiv_rn(m, 6.0f));
+            float s8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s8[i] = sb;
+            *reinterpret_cast<uint4 *>(dst + blk_off + static_cast<size_t>(rg + it * rows_in_flight) * d + cv * 8) =
+                fake_quant8<T>(x[it], s8);
+        }
+        return;
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        if (it >= iters) break;
+        const int g = (rg + it * rows_in_flight) >> 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) atomicMax(&vmax[g][cv * 8 + i], __float_as_uint(fabsf(x[it][i])));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        if (it >= iters) break;
+        const int r = rg + it * rows_in_flight;
+        float s8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s8[i] = e4m3_round_f(__fdiv_rn(__uint_as_float(vmax[r >> 4][cv * 8 + i]), 6.0f));
+        *reinterpret_cast<uint4 *>(dst + blk_off + static_cast<size_t>(r) * d + cv * 8) = fake_quant8<T>(x[it], s8);
+    }
+}
+
+// Attn-QAT backward prologue (section 2.2: the scalar term from dO and the high-precision O'
+// alone): D = rowsum(dO o O') with O' in float32, fixed order as in bwd_prologue_kernel, and the
+// negated L2 = -fl32(L log2 e).  Thread = (row, 8 channels).
+template <typename T>
+__global__ void __launch_bounds__(256) qat_bwd_prologue_kernel(const T *__restrict__ dO,
+                                                               const float *__restrict__ Op,
+                                                               const float *__restrict__ L,
+                                                               float *__restrict__ L2,
+                                                               float *__restrict__ D, size_t rows,
+                                                               int d) {
+    const int vec_per_row = d / 8;
+    const size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    const size_t row = t / vec_per_row;
+    const int cv = static_cast<int>(t % vec_per_row);
+    const bool live = row < rows;
+    const size_t r = live ? row : rows - 1;
+    float x[8], o[8];
+    load8(dO + r * d + cv * 8, x);
+    const float4 o0 = *reinterpret_cast<const float4 *>(Op + r * d + cv * 8);
+    const float4 o1 = *reinterpret_cast<const float4 *>(Op + r * d + cv * 8 + 4);
+    o[0] = o0.x; o[1] = o0.y; o[2] = o0.z; o[3] = o0.w;
+    o[4] = o1.x; o[5] = o1.y; o[6] = o1.z; o[7] = o1.w;
+    float part = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part = __fmaf_rn(x[i], o[i], part);
+    for (int o2 = 1; o2 < vec_per_row; o2 <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+    if (live && cv == 0) {
+        D[row] = part;
+        L2[row] = -__fmul_rn(L[row], kLog2e);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // widen: int8 codes -> integer-valued fp16, or E4M3 codes -> their fp16 values (both exact),
 // 16 codes per thread per step
 // ---------------------------------------------------------------------------------------------
@@ -847,6 +960,34 @@ cudaError_t launch_widen_fp4(const uint8_t *codes, const uint8_t *scales, __half
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
     widen_fp4_kernel<<<blocks, 256, 0, st>>>(codes, scales, dst, n16, p.d, p.N, along_tokens ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qat_fake_quant(const sage_params &p, const void *Q, const void *K, const void *V,
+                                  void *Qf, void *Kf, void *Vf, cudaStream_t st) {
+    dim3 g(p.N / 64, p.B * p.H, 3);
+    if (p.dtype == SAGE_FP16)
+        qat_fake_quant_kernel<__half><<<g, 256, 0, st>>>(
+            static_cast<const __half *>(Q), static_cast<const __half *>(K), static_cast<const __half *>(V),
+            static_cast<__half *>(Qf), static_cast<__half *>(Kf), static_cast<__half *>(Vf), p.N, p.d);
+    else
+        qat_fake_quant_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(K),
+            static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Qf),
+            static_cast<__nv_bfloat16 *>(Kf), static_cast<__nv_bfloat16 *>(Vf), p.N, p.d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qat_bwd_prologue(const sage_params &p, const void *dO, const float *Op, const float *L,
+                                    float *L2, float *D, cudaStream_t st) {
+    const size_t rows = static_cast<size_t>(p.B) * p.H * p.N;
+    const size_t threads = rows * (p.d / 8);
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    if (p.dtype == SAGE_FP16)
+        qat_bwd_prologue_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const __half *>(dO), Op, L, L2, D, rows, p.d);
+    else
+        qat_bwd_prologue_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(dO), Op, L,
+                                                                       L2, D, rows, p.d);
     return cudaGetLastError();
 }
 

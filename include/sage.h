@@ -258,6 +258,51 @@ SAGE_API int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, c
                                           float *sQ, float *sK, float *sV, float *muK, float *muQ,
                                           sage_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------ *
+ * Attn-QAT: 4-bit attention trained with fake quantisation.
+ * "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (technical summary), sections
+ * 2.1-2.3: NVFP4 fake quantisation, no Q/K smoothing and no two-level P scaling; the backward
+ * recomputes P with the forward's FP4 quantisation and forms D from a high-precision forward
+ * output O'; the backward runs in 16 bits.
+ * All three calls require flags = 0, smooth_k = 0 and smooth_q = 0 (SAGE_ERR_UNSUPPORTED
+ * otherwise); pointers are device memory of the caller, 16-byte aligned (SAGE_ERR_ALIGN), and
+ * asynchronous on `stream`.
+ *
+ * sage_qat_quantize -- Q' = s * code for Q, K (1 x 16 blocks along d) and V (16 tokens per
+ *   channel), s = e4m3(fl32(max|x| / 6)), code = e2m1(fl32(x / s)) (nearest, ties to even,
+ *   saturating at 6; a zero scale gives zero codes), written in the input type: the values have at
+ *   most 6 significant bits and magnitudes in [2^-10, 2688], so they are exact.
+ *   In: Q, K, V (B,H,N,d) fp16/bf16.  Out: Qf, Kf, Vf (B,H,N,d) same type.
+ *
+ * sage_qat_fwd -- per 64-key block, r = fl32(max acc * c) (c = fl32(log2(e) / sqrt(d)), acc the
+ *   product Q' K'^T), e = ex2(fl32(acc c - r)); P^ = phi(e), phi one-level NVFP4 over 16 keys
+ *   (s = e4m3(fl32(max e / 6)), code = e2m1(fl32(e fl32(1/s)))); O = sum 2^(r - m) P^ V' / l,
+ *   O' = sum 2^(r - m) rnd16(e) V' / l, l the running sum of e.
+ *   In: Qf, Kf, Vf from sage_qat_quantize.
+ *   Out: O (B,H,N,d) input type; Op = O' (B,H,N,d) float32; L (B,H,N) float32 natural-log LSE;
+ *        R (B,H,N/64,N) float32: r of every (key block, query row) the forward visits (-inf when
+ *        the row sees no key of the block); entries of pairs it never visits are left as they were.
+ *
+ * sage_qat_bwd -- P = ex2(fl32(acc c - L2)), L2 = fl32(L log2(e)); D = rowsum(dO o O');
+ *   dP = dO V'^T; dS = fl32(P fl32(dP - D)) rounded to the input type; P^ = the forward's
+ *   phi(ex2(fl32(acc c - r))) times fl32(ex2(fl32(r - L2))), rounded to the input type;
+ *   dV = P^^T dO; dQ = dS K' / sqrt(d); dK = dS^T Q' / sqrt(d) (fake quantisation passes the
+ *   gradient straight through: these are the gradients of Q, K and V).
+ *   In: Qf, Kf, Vf; Op, L, R from sage_qat_fwd; dO (B,H,N,d) input type.
+ *   Out: dQ, dK, dV (B,H,N,d) float32, overwritten (dQ by float32 reductions: last bits vary).
+ *   Workspace: sage_qat_bwd_workspace_bytes(p) bytes (D and L2), 256-byte aligned
+ *   (SAGE_ERR_WORKSPACE when missing or short).
+ * ------------------------------------------------------------------------------------------ */
+SAGE_API int sage_qat_quantize(const sage_params *p, const void *Q, const void *K, const void *V,
+                               void *Qf, void *Kf, void *Vf, sage_stream_t stream);
+SAGE_API int sage_qat_fwd(const sage_params *p, const void *Qf, const void *Kf, const void *Vf,
+                          void *O, float *Op, float *L, float *R, sage_stream_t stream);
+SAGE_API size_t sage_qat_bwd_workspace_bytes(const sage_params *p);
+SAGE_API int sage_qat_bwd(const sage_params *p, const void *Qf, const void *Kf, const void *Vf,
+                          const float *Op, const float *L, const float *R, const void *dO,
+                          float *dQ, float *dK, float *dV, void *workspace, size_t workspace_bytes,
+                          sage_stream_t stream);
+
 /* Bytes the SAGE_FLAG_DUMP buffer needs for a forward (which = 0) or backward (which = 1). */
 SAGE_API size_t sage_dump_bytes(const sage_params *p, int which);
 

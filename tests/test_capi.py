@@ -133,3 +133,24 @@ def test_qknorm_argument_checks(sg):
     assert L.sage_qknorm_bwd(ctypes.byref(p), None, None, f[2], f[3], f[4], None, None) == 1
     assert L.sage_qknorm_bwd(ctypes.byref(p), f[1], None, f[2], f[3], f[3], None, None) == 1
     assert L.sage_qknorm_bwd(ctypes.byref(p), f[1], f[0] + 4, f[2], f[3], f[4], None, None) == 3
+
+
+def test_qat_argument_checks(sg):
+    """The Attn-QAT calls take no flags and no smoothing (SAGE_ERR_UNSUPPORTED), refuse null and
+    misaligned pointers and a short workspace, all before any launch (fake device pointers are
+    never dereferenced).  Their workspace holds D and L2: two 256-byte-aligned float rows."""
+    L = sg.lib()
+    p = sg.make_params(1, 2, 128, 64, 0, False, smooth_k=False)
+    f = [_fake(i) for i in range(12)]
+    assert L.sage_qat_bwd_workspace_bytes(ctypes.byref(p)) == 2 * 1024
+    for bad in (sg.make_params(1, 2, 128, 64, 0, False), sg.make_params(1, 2, 128, 64, 0, False, smooth_k=False, smooth_q=True),
+                sg.make_params(1, 2, 128, 64, 0, False, smooth_k=False, fp8=True)):
+        assert L.sage_qat_quantize(ctypes.byref(bad), *f[:6], None) == 2
+        assert L.sage_qat_fwd(ctypes.byref(bad), *f[:7], None) == 2
+        assert L.sage_qat_bwd(ctypes.byref(bad), *f[:10], f[11], 1 << 20, None) == 2
+        assert L.sage_qat_bwd_workspace_bytes(ctypes.byref(bad)) == 0
+    assert L.sage_qat_quantize(ctypes.byref(p), f[0], None, *f[2:6], None) == 1
+    assert L.sage_qat_fwd(ctypes.byref(p), *f[:6], f[6] + 4, None) == 3
+    assert L.sage_qat_bwd(ctypes.byref(p), *f[:10], f[11], 100, None) == 6
+    assert L.sage_qat_bwd(ctypes.byref(p), *f[:10], None, 1 << 20, None) == 6
+    assert L.sage_qat_bwd(ctypes.byref(p), *f[:9], f[9] + 8, f[11], 1 << 20, None) == 3
