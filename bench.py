@@ -105,6 +105,13 @@ def quant_bytes(w: workloads.Workload) -> int:
     return reads + writes + small
 
 
+def qat_step_ops(w: workloads.Workload) -> float:
+    """Algorithmic tensor ops of one Attn-QAT step: forward S, P^ V' and the high-precision
+    P~ V' (6 B H N^2 d), backward S, dP, dV, dK, dQ (10 B H N^2 d); x 1/2 causal."""
+    ops = 16.0 * w.B * w.H * w.N * w.N * w.d
+    return ops / 2 if w.causal else ops
+
+
 def bwd_ops(w: workloads.Workload) -> float:
     ops = 10.0 * w.B * w.H * w.N * w.N * w.d
     return ops / 2 if w.causal else ops
@@ -231,6 +238,13 @@ def run_gpu(args, w: workloads.Workload):
         # the FP4 leg is an inference forward: no dO
         host.pop("dO")
         dev.pop("dO")
+    if args.qat:
+        # Attn-QAT intermediates, shared by both buffer sets (one compute stream orders the steps)
+        qat_f = tuple(torch.empty((B, H, N, d), dtype=dt, device=device) for _ in range(3))
+        qat_op = torch.empty((B, H, N, d), dtype=torch.float32, device=device)
+        qat_r = torch.empty((B, H, N // 64, N), dtype=torch.float32, device=device)
+        pq = sg.make_params(B, H, N, d, 0 if w.dtype == "fp16" else 1, w.causal, smooth_k=False)
+        ws_q = torch.empty(L.sage_qat_bwd_workspace_bytes(ctypes.byref(pq)), dtype=torch.uint8, device=device)
     # buffer set 0: the device-timed steps; sets 0 and 1 alternate in the pipelined end-to-end loop
     set0 = {"dev": dev, "O": O, "Lse": Lse, "grads": grads}
 
@@ -239,6 +253,18 @@ def run_gpu(args, w: workloads.Workload):
         dev, O, Lse, grads = bs["dev"], bs["O"], bs["Lse"], bs["grads"]
         if ev is not None:
             ev[0].record(stream)
+        if args.qat:
+            sg.sage_qat_quantize(dev["Q"], dev["K"], dev["V"], out=qat_f)
+            if ev is not None:
+                ev[1].record(stream)
+            sg.sage_qat_fwd(*qat_f, causal=w.causal, out=(O, qat_op, Lse, qat_r))
+            if ev is not None:
+                ev[2].record(stream)
+            sg.sage_qat_bwd(*qat_f, qat_op, Lse, qat_r, dev["dO"], causal=w.causal, grads=grads, workspace=ws_q)
+            if ev is not None:
+                ev[3].record(stream)
+                ev[4].record(stream)
+            return
         if args.fp4:
             q4 = sg.sage_quantize_fp4(dev["Q"], dev["K"], dev["V"], smooth_q=w.smooth_q)
             if ev is not None:
@@ -364,7 +390,7 @@ def run_gpu(args, w: workloads.Workload):
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
     assert np.isfinite(host_out["O" if args.fp4 else "dQ"].float().numpy()).all()
 
-    ops = fwd_ops(w) if args.fp4 else step_ops(w)
+    ops = fwd_ops(w) if args.fp4 else (qat_step_ops(w) if args.qat else step_ops(w))
     value = world * ops * args.steps / (ms_max * 1e-3) / 1e12
     e2e_value = world * ops * args.steps / (e2e_ms * 1e-3) / 1e12
 
@@ -375,7 +401,7 @@ def run_gpu(args, w: workloads.Workload):
     bwd_tflops = bwd_ops(w) / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else 0.0
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     quant_gbs = quant_bytes(w) / (quant_ms * 1e-3) / 1e9
-    fwd_tflops = fwd_ops(w) / (fwd_ms * 1e-3) / 1e12
+    fwd_tflops = (1.5 if args.qat else 1.0) * fwd_ops(w) / (fwd_ms * 1e-3) / 1e12
     if dist is not None:
         dist.destroy_process_group()
     if rank != 0:
@@ -423,6 +449,22 @@ def run_gpu(args, w: workloads.Workload):
                             "traffic": None, "flops_per_launch": fwd_ops(w)}
         line.pop("bwd_call", None)
         line["gpu_launches"] = 6 * args.steps        # K-mean, FP4 quantise, 3 widen, forward
+    if args.qat:
+        line["metric"] = "Attn-QAT fwd+bwd effective TOPS (N=8192,d=128)"
+        line["dtype"] = ("NVFP4 fake-quantised Q, K, V and P in " + w.dtype + " operands (f32 accumulate); "
+                         "16-bit backward")
+        line["config"]["qat"] = True
+        line["config"]["smooth_k"] = False
+        line["roofline"] = {"kernel": "sage_qat_bwd call (prologue + tcgen05 backward kernel)",
+                            "bound": "tensor", "achieved": round(bwd_tflops, 1), "peak": peak,
+                            "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
+                            "traffic": None, "flops_per_launch": bwd_ops(w)}
+        line["fwd_call"]["note"] = "two forward passes (O and L, then O'); tflops counts the 6 N^2 d of the method"
+        line["quantise_call"] = {"ms": round(quant_ms, 4), "bound": "hbm", "bytes": 12 * w.B * w.H * w.N * w.d,
+                                 "gbs": round(12 * w.B * w.H * w.N * w.d / (quant_ms * 1e-3) / 1e9, 1),
+                                 "peak_gbs": hbm_peak}
+        line["quantise_call"]["frac"] = round(line["quantise_call"]["gbs"] / hbm_peak, 4)
+        line["gpu_launches"] = 5 * args.steps        # fake quantise, 2 forward passes, prologue, backward
     return line
 
 
@@ -455,12 +497,35 @@ def oracle_sample(w: workloads.Workload, q_blocks, kv_blocks, seed: int = 0) -> 
     return secs, 4.0 * tile * n_f + 10.0 * tile * n_b
 
 
-def cpu_baseline_subprocess(w: workloads.Workload, q_blocks, kv_blocks, label: str) -> dict:
+def qat_oracle_sample(w: workloads.Workload, q_blocks, kv_blocks, seed: int = 0) -> tuple[float, float]:
+    """Time the Attn-QAT oracle on head (0, 0): fake quantisation, the whole forward (the backward
+    needs O', L and R of every row) and the backward over ``kv_blocks`` (None = all).
+    Returns (seconds, algorithmic ops)."""
+    import numpy as np
+    from oracle import qat as oqat
+    x = workloads.make_inputs(w, seed=seed, heads=1)
+    x = {k: np.ascontiguousarray(v[:1, :1]) for k, v in x.items()}
+    T = w.N // 64
+    kb = list(range(T)) if kv_blocks is None else list(kv_blocks)
+    rnd = lambda a: workloads.round_to(a, w.dtype)
+    t0 = time.perf_counter()
+    fq = oqat.fake_quant(x["Q"], x["K"], x["V"])
+    O, Op, L, R = oqat.qat_forward(fq, w.causal, rnd)
+    oqat.qat_backward(fq, Op.astype(np.float32), L.astype(np.float32), R, x["dO"], w.causal, rnd,
+                      kv_blocks=None if kv_blocks is None else kb, q_blocks=None if kv_blocks is None else [])
+    secs = time.perf_counter() - t0
+    tile = 64 * 64 * w.d
+    n_f = sum((i + 1) if w.causal else T for i in range(T))
+    n_b = sum((T - j) if w.causal else T for j in kb)
+    return secs, 6.0 * tile * n_f + 10.0 * tile * n_b
+
+
+def cpu_baseline_subprocess(w: workloads.Workload, q_blocks, kv_blocks, label: str, fn: str = "oracle_sample") -> dict:
     """Run the oracle in a fresh interpreter (single BLAS thread) and describe the sample."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = ("import json, sys; sys.path.insert(0, %r); import bench, workloads; "
-            "w = workloads.get(%r, causal=%r); s, ops = bench.oracle_sample(w, %r, %r); "
-            "print(json.dumps({'s': s, 'ops': ops}))" % (ROOT, w.name, w.causal, q_blocks, kv_blocks))
+            "w = workloads.get(%r, causal=%r); s, ops = bench.%s(w, %r, %r); "
+            "print(json.dumps({'s': s, 'ops': ops}))" % (ROOT, w.name, w.causal, fn, q_blocks, kv_blocks))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label,
@@ -514,6 +579,8 @@ def main():
                     help="QK-norm fused into the quantise call, and its gradient after the backward")
     ap.add_argument("--fp4", action="store_true",
                     help="the SageAttention3 FP4 inference forward (quantise + forward only)")
+    ap.add_argument("--qat", action="store_true",
+                    help="the Attn-QAT training step (NVFP4 fake quantisation, O', 16-bit backward)")
     ap.add_argument("--workload", default="headline", choices=["headline", "qknorm", "outlier", "longseq"],
                     help="the workload (default: the headline B2 H16 N8192 d128 fp16); the others are the "
                          "parity workloads of workloads.py, timed the same way")
@@ -543,7 +610,12 @@ def main():
     if line is None:
         return
     rank, world, _ = rank_info()
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and args.qat:
+        line["cpu_baseline"] = cpu_baseline_subprocess(
+            w, None, [0, 1], "head (0,0) of 32: fake quantisation, the whole forward and the backward over 2 of "
+                             f"{w.N // 64} key blocks, value = their 6 / 10 x 64^2 d ops per tile / CPU seconds",
+            fn="qat_oracle_sample")
+    elif not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline_subprocess(
             w, None, None, "head (0,0) of 32: full quantise + forward + backward of one head, "
                            "value = its 14 N^2 d ops / CPU seconds")

@@ -52,8 +52,10 @@
 //        rounded to the input type (A operand of dK, B operand of dQ);
 //   P^ = the forward's quantised P rebuilt: e = ex2(fl32(acc c - r)) with the forward's row
 //        maximum r of this (key block, query), phi(e) one-level NVFP4 over the 16 keys of a block
-//        (16 lanes of a warp: shuffles), P^ = rnd16(fl32(phi(e) fl32(ex2(fl32(r - L2))))) (A of dV).
-// One pass over S^T and dP^T suffices: nothing waits for a tile maximum.
+//        (16 lanes of a warp), P^ = rnd16(fl32(phi(e) fl32(ex2(fl32(r - L2))))) (A of dV).
+// A short pass over S^T forms each 16-key block's scale once (a reduce-scatter of the block
+// maxima over the lanes, one column's scale math per lane); the second pass reads S^T and dP^T.
+// Nothing waits for a tile maximum, so no barrier joins the score warps.
 #include "sage_device.cuh"
 #include "sage_internal.h"
 
@@ -103,6 +105,7 @@ struct Smem {
     alignas(16) float L2s[3][64];                      // [stage][q]: -fl32(L log2 e), negated
     alignas(16) float Ds[3][64];                       // [stage][q]: D
     alignas(16) float Rs[3][2][64];                    // Attn-QAT: [stage][key block][q] forward row maxima
+    float4 qscal[8][64];                               // Attn-QAT: [16-key block][q] (s, 1/s, g, r)
     float red[4][2][2];                                // [warp][step parity][P max, |dS| max]
     float sps[kScaleSlots][2];                         // [step % 8][key block] P tile scales
     float sds[kScaleSlots][2];                         // [step % 8][key block] dS tile scales
@@ -300,16 +303,6 @@ __device__ __forceinline__ void score_pass2(uint32_t s_col, uint32_t dp_col, con
     });
 }
 
-// Attn-QAT row data of 8 query columns: -L2, D and the forward's row maxima r of this key block
-struct RowData8Q : RowData8 {
-    float rr[8];
-    __device__ __forceinline__ void load(const float *L2s, const float *Ds, const float *Rs, int col0) {
-        RowData8::load(L2s, Ds, col0);
-        *reinterpret_cast<float4 *>(&rr[0]) = *reinterpret_cast<const float4 *>(&Rs[col0]);
-        *reinterpret_cast<float4 *>(&rr[4]) = *reinterpret_cast<const float4 *>(&Rs[col0 + 4]);
-    }
-};
-
 __device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool bf16) {
     if (bf16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -319,67 +312,94 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Attn-QAT: the single score pass over the 64 query columns of a block (same staging as
-// score_walk).  Per column: P and dS as score_p_ds_8; e = ex2(fl32(acc c - r)) (masked to 0 where
-// EDGE says the pair is not live); the NVFP4 block maximum over the 16 keys = 16 lanes; s, 1/s and
-// the E2M1 codes as the forward forms them; P^ = rnd16(fl32(phi(e) g)), g = ex2(fl32(r - L2)),
-// zero where phi(e) is zero (r may be undefined for a pair the forward never visited, all of
-// whose entries are masked).  P^ goes to TMEM over read S^T columns, dS to this key's dS row.
+// Attn-QAT pass A: the NVFP4 block data of every query column for this thread's 16-key block
+// (the 16 lanes of its half-warp).  The block maximum of e = ex2(fl32(acc c - r)) is e of the block
+// maximum of acc (the float32 rounding and ex2 are monotonic), so the lanes first reduce acc:
+// a reduce-scatter over the 16 lanes (offsets 8, 4, 2, 1, each step keeping half the columns)
+// leaves lane L with the maxima of columns 2L and 2L + 1 of each 32-column chunk.  Each lane then
+// forms, for its 4 columns, s = e4m3(fl32(max e / 6)), 1/s, g = ex2(fl32(r - L2)) and r, and stores
+// them in `scal` (this half-warp's 64 columns); a column with no live key in the block gets s = 0.
+template <bool EDGE>
+__device__ __forceinline__ void qat_block_scales(uint32_t s_col, const float *L2s, const float *Rs,
+                                                 float cq, int qlo, bool key_ok, float4 *scal) {
+    const int lane = static_cast<int>(lane_id());
+    const int L = lane & 15;
+    float own[4];
+#pragma unroll
+    for (int chunk = 0; chunk < 2; ++chunk) {
+        uint32_t a[32];
+        tmem_ld16(s_col + 32 * chunk, *reinterpret_cast<uint32_t(*)[16]>(&a[0]));
+        tmem_ld16(s_col + 32 * chunk + 16, *reinterpret_cast<uint32_t(*)[16]>(&a[16]));
+        tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&a[0]));
+        tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&a[16]));
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[i] = __uint_as_float(a[i]);
+            if (EDGE) v[i] = (key_ok && 32 * chunk + i >= qlo) ? v[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int o = 8, w = 32; o >= 1; o >>= 1, w >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < w / 2; ++i) {
+                const float send = up ? v[i] : v[i + w / 2];
+                const float keep = up ? v[i + w / 2] : v[i];
+                v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+        }
+        own[2 * chunk] = v[0];
+        own[2 * chunk + 1] = v[1];
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int col = 32 * (t >> 1) + 2 * L + (t & 1);
+        const float r = Rs[col];
+        float sc = 0.0f, inv = 0.0f, g = 0.0f;
+        if (own[t] != -INFINITY) {
+            const float em = ex2_approx(__fmaf_rn(own[t], cq, -r));
+            sc = e4m3_round_f(__fdiv_rn(em, 6.0f));
+            inv = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+            g = ex2_approx(__fadd_rn(r, L2s[col]));     // L2s holds -L2
+        }
+        scal[col] = make_float4(sc, inv, g, r);
+    }
+    __syncwarp();
+}
+
+// Attn-QAT pass B over the 64 query columns of a block (the staging of score_walk): P and dS as
+// score_p_ds_8; e = ex2(fl32(acc c - r)) (masked to 0 where EDGE says the pair is not live);
+// code = e2m1(fl32(e / s as e fl32(1/s))); P^ = rnd16(fl32((code s) g)), zero where the code is
+// zero (r may be undefined for a pair the forward never visited, all of whose entries are masked).
+// P^ goes to TMEM over read S^T columns, dS to this key's row of the shared dS tile.
 template <bool EDGE, bool BF16>
 __device__ __forceinline__ void score_pass_qat(uint32_t s_col, uint32_t dp_col, const float *L2s,
-                                               const float *Ds, const float *Rs, float cq, int qlo,
+                                               const float *Ds, const float4 *scal, float cq, int qlo,
                                                bool key_ok, uint8_t *dss_row, int swz) {
-    auto half = [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8Q &rd, int col0) {
+    score_walk(s_col, dp_col, L2s, Ds, [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8 &rd, int col0) {
         float pv[8], ds[8];
         score_p_ds_8<EDGE, false, false>(sr, dr, rd, col0, cq, 0.0f, qlo, key_ok, 1.0f, pv, ds);
         uint32_t pk[4], dk[4];
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
-            float e[2], sc[2], g[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                float x = __fmaf_rn(__uint_as_float(sr[k + u]), cq, -rd.rr[k + u]);
-                if (EDGE) x = (key_ok && col0 + k + u >= qlo) ? x : -INFINITY;
-                e[u] = ex2_approx(x);
-                float m = e[u];
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                sc[u] = e4m3_round_f(__fdiv_rn(m, 6.0f));
-                g[u] = ex2_approx(__fadd_rn(rd.rr[k + u], rd.l2[k + u]));
+            const float4 q0 = scal[col0 + k], q1 = scal[col0 + k + 1];
+            float x0 = __fmaf_rn(__uint_as_float(sr[k]), cq, -q0.w);
+            float x1 = __fmaf_rn(__uint_as_float(sr[k + 1]), cq, -q1.w);
+            if (EDGE) {
+                x0 = (key_ok && col0 + k >= qlo) ? x0 : -INFINITY;
+                x1 = (key_ok && col0 + k + 1 >= qlo) ? x1 : -INFINITY;
             }
-            const float i0 = sc[0] > 0.0f ? __frcp_rn(sc[0]) : 0.0f;
-            const float i1 = sc[1] > 0.0f ? __frcp_rn(sc[1]) : 0.0f;
-            const f2 y = mul2(f2{e[0], e[1]}, f2{i0, i1});
-            const uint32_t h = hmul2(e2m1x2_to_f16x2(e2m1x2(y.x, y.y)), pack_half2(sc[0], sc[1]));
-            const float2 ph = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-            const float p0 = ph.x != 0.0f ? __fmul_rn(ph.x, g[0]) : 0.0f;
-            const float p1 = ph.y != 0.0f ? __fmul_rn(ph.y, g[1]) : 0.0f;
+            const f2 y = mul2(f2{ex2_approx(x0), ex2_approx(x1)}, f2{q0.y, q1.y});
+            const uint32_t h = e2m1x2_to_f16x2(e2m1x2(y.x, y.y));
+            const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+            const float p0 = c.x != 0.0f ? __fmul_rn(c.x * q0.x, q0.z) : 0.0f;   // c s is exact
+            const float p1 = c.y != 0.0f ? __fmul_rn(c.y * q1.x, q1.z) : 0.0f;
             pk[k / 2] = pack16x2(p0, p1, BF16);
             dk[k / 2] = pack16x2(ds[k], ds[k + 1], BF16);
         }
         tmem_st4(s_col + col0 / 2, pk);
         *reinterpret_cast<uint4 *>(dss_row + (((col0 >> 3) ^ swz) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-    };
-    uint32_t sA[8], dA[8], sB[8], dB[8];
-    RowData8Q rA, rB;
-    tmem_ld8(s_col, sA);
-    tmem_ld8(dp_col, dA);
-    rA.load(L2s, Ds, Rs, 0);
-#pragma unroll 1
-    for (int col0 = 0; col0 < 64; col0 += 16) {
-        tmem_wait_ld_regs(sA, dA);
-        tmem_ld8(s_col + col0 + 8, sB);
-        tmem_ld8(dp_col + col0 + 8, dB);
-        rB.load(L2s, Ds, Rs, col0 + 8);
-        half(sA, dA, rA, col0);
-        tmem_wait_ld_regs(sB, dB);
-        if (col0 + 16 < 64) {
-            tmem_ld8(s_col + col0 + 16, sA);
-            tmem_ld8(dp_col + col0 + 16, dA);
-            rA.load(L2s, Ds, Rs, col0 + 16);
-        }
-        half(sB, dB, rB, col0 + 8);
-    }
+    });
 }
 
 // d = 128: this warpgroup's 32 query rows [32 half, 32 half + 32) of the step's two transposed dQ
@@ -639,12 +659,16 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
             if (D != 128 && c >= 2 && !mbar_wait(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
             const uint32_t s_col = lane_base + 128 * b;
             uint8_t *dss_row = s.dss[b] + tq * 128;
-            if (edge)
-                score_pass_qat<true, DPK == kDpBf16>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], s.Rs[m3][kb], a.sl2, qlo,
+            float4 *scal = s.qscal[tq >> 4];
+            if (edge) {
+                qat_block_scales<true>(s_col, s.L2s[m3], s.Rs[m3][kb], a.sl2, qlo, key_ok, scal);
+                score_pass_qat<true, DPK == kDpBf16>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], scal, a.sl2, qlo,
                                                      key_ok, dss_row, tq & 7);
-            else
-                score_pass_qat<false, DPK == kDpBf16>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], s.Rs[m3][kb], a.sl2, qlo,
+            } else {
+                qat_block_scales<false>(s_col, s.L2s[m3], s.Rs[m3][kb], a.sl2, qlo, key_ok, scal);
+                score_pass_qat<false, DPK == kDpBf16>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], scal, a.sl2, qlo,
                                                       key_ok, dss_row, tq & 7);
+            }
             tmem_wait_st();
             fence_view_async_shared();
             tc_fence_before();
