@@ -11,4 +11,5 @@ from .binding import (  # noqa: F401
     sage_device_status, sage_dump_bytes, sage_qknorm_bwd, sage_quantize_smooth,
     sage_quantize_smooth_noalloc, sage_quantize_smooth_qknorm, sage_status_string, sage_version,
 )
-from .autograd import SageAttentionFunction, sage_attention  # noqa: F401,E402
+from .autograd import (SageAttentionFunction, SageQatAttentionFunction, sage_attention,  # noqa: F401,E402
+                       sage_attention_qat)

@@ -12,11 +12,16 @@ summary, K-smoothing).  With Q-smoothing the library adds the dK bias term itsel
 With ``qk_norm`` the quantiser first RMS-normalises Q and K per token ("SageBwd ..." (structured
 summary), QK-norm: x / sqrt(mean x^2 + eps) * gamma) and the backward chains the attention
 gradients through ``sage_qknorm_bwd``, which also gives the gradients of the two gammas.
+
+``sage_attention_qat`` is Attn-QAT ("Attn-QAT: 4-Bit Attention With Quantization-Aware Training",
+technical summary, section 2.2): the forward runs on NVFP4 fake-quantised Q, K, V with an FP4 P
+and keeps the high-precision output O'; the backward rebuilds the forward's quantised P and forms
+D from O'.  Fake quantisation passes the gradient straight through.
 """
 import torch
 
-from .binding import (sage_attn_bwd, sage_attn_fwd, sage_qknorm_bwd, sage_quantize_smooth,
-                      sage_quantize_smooth_qknorm)
+from .binding import (sage_attn_bwd, sage_attn_fwd, sage_qat_bwd, sage_qat_fwd, sage_qat_quantize,
+                      sage_qknorm_bwd, sage_quantize_smooth, sage_quantize_smooth_qknorm)
 
 
 class SageAttentionFunction(torch.autograd.Function):
@@ -73,3 +78,26 @@ def sage_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal:
         raise ValueError("gamma_q / gamma_k need qk_norm=True")
     return SageAttentionFunction.apply(Q, K, V, gamma_q, gamma_k, causal, smooth_q, dp_int8, fp8,
                                        qk_norm, eps)
+
+
+class SageQatAttentionFunction(torch.autograd.Function):
+    """O = Attn-QAT attention(Q, K, V); inputs (B, H, N, d) fp16 or bf16 CUDA tensors."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, causal: bool):
+        Qf, Kf, Vf = sage_qat_quantize(Q.contiguous(), K.contiguous(), V.contiguous())
+        O, Op, L, R = sage_qat_fwd(Qf, Kf, Vf, causal=causal)
+        ctx.causal = causal
+        ctx.save_for_backward(Qf, Kf, Vf, Op, L, R)
+        return O
+
+    @staticmethod
+    def backward(ctx, dO):
+        Qf, Kf, Vf, Op, L, R = ctx.saved_tensors
+        dQ, dK, dV = sage_qat_bwd(Qf, Kf, Vf, Op, L, R, dO.to(Qf.dtype).contiguous(), causal=ctx.causal)
+        return dQ.to(Qf.dtype), dK.to(Qf.dtype), dV.to(Qf.dtype), None
+
+
+def sage_attention_qat(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False) -> torch.Tensor:
+    """Differentiable Attn-QAT attention: 4-bit (NVFP4) fake-quantised forward, 16-bit backward."""
+    return SageQatAttentionFunction.apply(Q, K, V, causal)

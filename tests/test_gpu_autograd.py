@@ -40,3 +40,30 @@ def test_autograd_matches_direct_calls_and_fpa(causal, dtype):
         a, b = got.detach().float().flatten(), ref.detach().float().flatten()
         cos = float(torch.dot(a, b) / (a.norm() * b.norm()))
         assert cos > 0.99, cos
+
+
+@pytest.mark.parametrize("causal,dtype", [(False, "bf16"), (True, "fp16")])
+def test_qat_autograd_matches_direct_calls(causal, dtype):
+    """sage_attention_qat: the output and the gradients (cast to the input dtype) are those of the
+    three Attn-QAT calls (dQ up to the order of its float32 reductions), and the QAT output is
+    an approximation of full-precision attention (cos > 0.98 at 4 bits)."""
+    import bit_trainable_attention_sage_gb300 as sg
+    w, x = make_case(256, 64, dtype, causal)
+    Q, K, V, dO = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V", "dO"))
+    Qr, Kr, Vr = (t.clone().requires_grad_(True) for t in (Q, K, V))
+    O = sg.sage_attention_qat(Qr, Kr, Vr, causal=causal)
+    O.backward(dO)
+    Qf, Kf, Vf = sg.sage_qat_quantize(Q, K, V)
+    O2, Op, L, R = sg.sage_qat_fwd(Qf, Kf, Vf, causal=causal)
+    dQ, dK, dV = sg.sage_qat_bwd(Qf, Kf, Vf, Op, L, R, dO, causal=causal)
+    assert sg.sage_device_status() == 0
+    assert torch.equal(O, O2)
+    for g, ref in ((Kr.grad, dK), (Vr.grad, dV)):
+        assert g.dtype == Q.dtype and torch.equal(g, ref.to(Q.dtype))
+    assert rel_l2(Qr.grad.float().cpu().numpy(), dQ.to(Q.dtype).float().cpu().numpy()) <= 1e-3
+    S = Q.float() @ K.float().transpose(-1, -2) / np.sqrt(w.d)
+    if causal:
+        S = S.masked_fill(torch.ones(w.N, w.N, dtype=torch.bool, device=S.device).triu(1), float("-inf"))
+    Ofp = torch.softmax(S, -1) @ V.float()
+    cos = torch.nn.functional.cosine_similarity(O.float().flatten(), Ofp.flatten(), dim=0).item()
+    assert cos > 0.98, cos

@@ -140,3 +140,58 @@ def test_full_size_fp4_headline():
     O_stored = workloads.round_to(Oref.astype(np.float32), w.dtype)
     assert rel_l2(O.float().cpu().numpy()[b, h], O_stored[b, h]) <= 1e-3
     assert np.max(np.abs(L.cpu().numpy()[b, h] - Lref[b, h])) <= 1e-3 * max(1.0, float(np.max(np.abs(Lref[b, h]))))
+
+
+@pytest.mark.parametrize("name,head,fwd_sel,q_sel,kv_sel", [
+    ("headline", (1, 7), None, [2, 101], [0, 127]),
+    ("longseq", (0, 5), "ends", [0, 1, -1], [-1, -2]),
+], ids=["headline", "longseq"])
+def test_full_size_qat(name, head, fwd_sel, q_sel, kv_sel):
+    """Attn-QAT at full size, in the benchmark's launch configuration: the sampled head's
+    fake-quantised Q', K', V' bit for bit, its forward R on the rows computed, O, O' and L on those
+    rows, and dQ, dK, dV on the sampled blocks within rel-l2 1e-3 of the oracle."""
+    import bit_trainable_attention_sage_gb300 as sg
+    from oracle import qat as oqat
+    w = workloads.get(name)
+    x = workloads.make_inputs(w, seed=2)
+    Q, K, V, dO = (to_dev(x[k], w.dtype) for k in ("Q", "K", "V", "dO"))
+    Qf, Kf, Vf = sg.sage_qat_quantize(Q, K, V)
+    O, Op, L, R = sg.sage_qat_fwd(Qf, Kf, Vf, causal=w.causal)
+    dQ, dK, dV = sg.sage_qat_bwd(Qf, Kf, Vf, Op, L, R, dO, causal=w.causal)
+    assert sg.sage_device_status() == 0
+    b, h = head
+    T = w.N // 64
+    q_blocks = sorted({i % T for i in q_sel})
+    kv_blocks = sorted({j % T for j in kv_sel})
+    one = lambda k: np.ascontiguousarray(x[k][b:b + 1, h:h + 1])
+    fq = oqat.fake_quant(one("Q"), one("K"), one("V"))
+    for k, t in (("Qf", Qf), ("Kf", Kf), ("Vf", Vf)):
+        assert np.array_equal(t[b, h].float().cpu().numpy(), fq[k][0, 0].astype(np.float32)), k
+    if fwd_sel is None:
+        fwd_blocks = None
+    else:
+        need = set(q_blocks)
+        for j in kv_blocks:
+            need.update(range(j, T))
+        fwd_blocks = sorted(need)
+    rnd = lambda a: workloads.round_to(a, w.dtype)
+    Oref, Opref, Lref, Rref = oqat.qat_forward(fq, w.causal, rnd, q_blocks=fwd_blocks)
+    rows = np.concatenate([np.arange(64 * i, 64 * i + 64) for i in (range(T) if fwd_blocks is None else fwd_blocks)])
+    assert rel_l2(O[b, h].float().cpu().numpy()[rows], rnd(Oref[0, 0].astype(np.float32))[rows]) <= 1e-3
+    assert rel_l2(Op[b, h].cpu().numpy()[rows], Opref[0, 0][rows]) <= 1e-3
+    Lg = L[b, h].cpu().numpy()[rows]
+    assert np.max(np.abs(Lg - Lref[0, 0][rows])) <= 1e-3 * max(1.0, float(np.max(np.abs(Lref[0, 0][rows]))))
+    Rg = R[b, h].cpu().numpy()[:, rows]
+    Rr = Rref[0, 0][:, rows]
+    fin = np.isfinite(Rr)
+    assert np.array_equal(np.isneginf(Rg[~np.isnan(Rr)]), np.isneginf(Rr[~np.isnan(Rr)]))
+    assert np.max(np.abs(Rg[fin] - Rr[fin]) / np.maximum(1.0, np.abs(Rr[fin]))) < 1e-5
+    g = oqat.qat_backward(fq, Opref.astype(np.float32), Lref.astype(np.float32), Rref, one("dO"), w.causal, rnd,
+                          q_blocks=q_blocks, kv_blocks=kv_blocks)
+    qrows = np.concatenate([np.arange(64 * i, 64 * i + 64) for i in q_blocks])
+    krows = np.concatenate([np.arange(64 * j, 64 * j + 64) for j in kv_blocks])
+    for nm, got, want, r in (("dQ", dQ, g["dQ"], qrows), ("dK", dK, g["dK"], krows), ("dV", dV, g["dV"], krows)):
+        gv = got[b, h].cpu().numpy()[r]
+        assert np.all(np.isfinite(gv)), nm
+        err = rel_l2(gv, want[0, 0][r])
+        assert err <= 1e-3, (nm, err)
