@@ -716,12 +716,10 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
             score_pass1<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
                                                            key_ok, dps, mp, md, cs, dump_s0, N);
         // tile maxima of (this query block, this key block): over the 32 lanes, then over the
-        // two warps of the key block
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
-            md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, o));
-        }
+        // two warps of the key block.  Both are non-negative floats (P >= +0, |dS|), whose bit
+        // patterns order as unsigned integers: one warp-wide integer max each.
+        mp = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mp)));
+        md = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(md)));
         if (lane_id() == 0) {
             s.red[warp][c & 1][0] = mp;
             s.red[warp][c & 1][1] = md;
