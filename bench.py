@@ -12,8 +12,9 @@ value, the end-to-end value through the public API with host buffers (``e2e``), 
 the dominant call, the clocks seen during the timed region, the number of library kernels
 launched, and the CPU oracle timed on a bounded sample (``cpu_baseline``).
 
-``--impl reference`` times the CPU oracle alone (the reference arm of this build: there is no
-published GPU implementation of the method), each step a bounded sample of the same workload.
+``--impl reference`` times the CPU oracle alone (the reference arm: the method has no published
+GPU implementation to run), each step a bounded sample of the same workload.  ``--qat`` times the
+Attn-QAT step instead of SageBwd's, with the Attn-QAT oracle as its CPU baseline.
 """
 from __future__ import annotations
 
