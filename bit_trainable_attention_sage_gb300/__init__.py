@@ -3,7 +3,8 @@
 The compute path is the C-ABI library libsage_gb300.so (include/sage.h); this package holds its
 CUDA sources (csrc/), the in-tree build (build.py) and a thin ctypes binding (binding.py) whose
 functions carry the C entry points' names.  ``autograd.sage_attention`` wraps the calls as a
-differentiable PyTorch operation.
+differentiable PyTorch operation; ``autograd.sage_attention_qat`` does the same for the Attn-QAT
+calls (4-bit fake-quantised forward with a high-precision O', 16-bit backward).
 """
 from .binding import (  # noqa: F401
     Fp4Quantized, Quantized, SageError, SageParams, lib, make_params, sage_attn_bwd, sage_attn_fwd,

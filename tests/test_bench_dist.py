@@ -51,3 +51,19 @@ def test_weak_scaling_value():
     # block scales and the K mean
     n = 2 * 16 * 8192 * 128
     assert bench.quant_bytes(w) == 11 * n + 4 * (3 * 2 * 16 * 128 + 2 * 16 * 128)
+
+
+def test_qat_step_ops_and_cli():
+    """The Attn-QAT leg counts the method's 16 B H N^2 d tensor ops a step (6 forward: S, P^ V',
+    P~ V'; 10 backward), halved when causal, and the CLI offers it."""
+    import subprocess
+    import sys
+    import bench
+    import workloads
+    w = workloads.get("headline")
+    assert bench.qat_step_ops(w) == 16.0 * 2 * 16 * 8192 * 8192 * 128
+    assert bench.qat_step_ops(workloads.get("headline", causal=True)) == bench.qat_step_ops(w) / 2
+    assert bench.qat_step_ops(w) == bench.step_ops(w) + 2.0 * 2 * 16 * 8192 * 8192 * 128
+    out = subprocess.run([sys.executable, "bench.py", "--help"], capture_output=True, text=True,
+                         cwd=bench.ROOT, timeout=120).stdout
+    assert "--qat" in out
