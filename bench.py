@@ -521,12 +521,35 @@ def qat_oracle_sample(w: workloads.Workload, q_blocks, kv_blocks, seed: int = 0)
     return secs, 6.0 * tile * n_f + 10.0 * tile * n_b
 
 
+def regime_sample(w: workloads.Workload, seed: int = 0, rows: int = 128) -> dict:
+    """RMS of P, dP and dS of float64 full-precision attention (the oracle's FPA) on the first and
+    last ``rows`` // 2 query rows of head (0, 0), every key: how close the synthetic workload comes
+    to the gradient magnitudes the pages report for trained models (their dS near 1e-7)."""
+    import numpy as np
+    from oracle import fpa
+    x = workloads.make_inputs(w, seed=seed, heads=1)
+    Q, K, V, dO = (np.asarray(x[k][0, 0], np.float64) for k in ("Q", "K", "V", "dO"))
+    h = rows // 2
+    idx = np.r_[0:h, w.N - h:w.N]
+    S = Q[idx] @ K.T / math.sqrt(w.d)
+    if w.causal:
+        S = np.where(np.arange(w.N)[None, :] > idx[:, None], -np.inf, S)
+    P = fpa.softmax_rows(S)
+    dP = dO[idx] @ V.T
+    D = (P * dP).sum(axis=1, keepdims=True)
+    dS = P * (dP - D)
+    rms = lambda a: float(np.sqrt(np.mean(a * a)))
+    return {"rms_P": rms(P), "rms_dP": rms(dP), "rms_dS": rms(dS),
+            "sample": f"head (0,0), query rows 0-{h - 1} and {w.N - h}-{w.N - 1}, every key, float64 FPA"}
+
+
 def cpu_baseline_subprocess(w: workloads.Workload, q_blocks, kv_blocks, label: str, fn: str = "oracle_sample") -> dict:
     """Run the oracle in a fresh interpreter (single BLAS thread) and describe the sample."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = ("import json, sys; sys.path.insert(0, %r); import bench, workloads; "
             "w = workloads.get(%r, causal=%r); s, ops = bench.%s(w, %r, %r); "
-            "print(json.dumps({'s': s, 'ops': ops}))" % (ROOT, w.name, w.causal, fn, q_blocks, kv_blocks))
+            "print(json.dumps({'s': s, 'ops': ops, 'regime': bench.regime_sample(w)}))"
+            % (ROOT, w.name, w.causal, fn, q_blocks, kv_blocks))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label,
@@ -534,7 +557,7 @@ def cpu_baseline_subprocess(w: workloads.Workload, q_blocks, kv_blocks, label: s
     out = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": round(out["ops"] / out["s"] / 1e12, 8), "unit": UNIT, "cores": 1,
             "kind": "oracle", "sample": label, "seconds": round(out["s"], 2),
-            "host_cores_available": len(os.sched_getaffinity(0))}
+            "host_cores_available": len(os.sched_getaffinity(0)), "regime": out["regime"]}
 
 
 def run_reference(args, w: workloads.Workload):
