@@ -101,6 +101,10 @@ def lib() -> ctypes.CDLL:
     L.sage_status_string.restype = ctypes.c_char_p
     L.sage_version.argtypes = []
     L.sage_version.restype = ctypes.c_char_p
+    L.sage_quantize_noalloc_max_partials.argtypes = []
+    L.sage_quantize_noalloc_max_partials.restype = sz
+    L.sage_quantize_noalloc_partials_needed.argtypes = [P]
+    L.sage_quantize_noalloc_partials_needed.restype = sz
     _lib = L
     return L
 

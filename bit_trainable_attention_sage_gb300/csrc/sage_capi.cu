@@ -169,7 +169,8 @@ static BwdDump bwd_dump(const sage_params &p, void *w, size_t *bytes) {
 // ------------------------------------------------------------------------------------------
 static bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-static int check_params(const sage_params *p) {
+// shared with sage_noalloc.cu (declared in sage_internal.h)
+int check_params(const sage_params *p) {
     if (!p) return SAGE_ERR_ARG;
     if (p->B <= 0 || p->H <= 0 || p->N <= 0 || p->d <= 0) return SAGE_ERR_ARG;
     if (p->causal != 0 && p->causal != 1) return SAGE_ERR_ARG;

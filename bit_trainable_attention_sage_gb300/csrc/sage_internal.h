@@ -91,6 +91,9 @@ struct BwdArgs {
     float sl2, inv_sqrt_d;
 };
 
+// sage_capi.cu: the parameter rules every entry point applies (SAGE_OK or a status code)
+int check_params(const sage_params *p);
+
 // sage_quant.cu
 int kmean_splits(const sage_params &p);
 cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st,

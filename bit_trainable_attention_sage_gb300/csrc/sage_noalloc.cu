@@ -19,20 +19,30 @@ constexpr size_t kNoallocPartials = 131072;
 
 static __device__ __align__(256) double g_noalloc_kpartial[kNoallocPartials];
 
-// Device address of the array on each device, looked up once per device (the host-side name of
-// the array is not a device address and must never be handed to a kernel).
+// Device address of the array on each device.  The host-side name of the array is not a device
+// address and must never be handed to a kernel, so the address is looked up with
+// cudaGetSymbolAddress, once per device with that device current, and kept.  A failed lookup is
+// not kept: the next call on that device tries again.
 static constexpr int kMaxDevices = 64;
 static double *g_noalloc_ptr[kMaxDevices];
-static std::once_flag g_noalloc_once[kMaxDevices];
-static cudaError_t g_noalloc_status[kMaxDevices];
+static std::mutex g_noalloc_mutex;
 
 static double *noalloc_scratch(int device) {
-    std::call_once(g_noalloc_once[device], [device]() {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[device]) {
         void *ptr = nullptr;
-        g_noalloc_status[device] = cudaGetSymbolAddress(&ptr, g_noalloc_kpartial);
-        g_noalloc_ptr[device] = g_noalloc_status[device] == cudaSuccess ? static_cast<double *>(ptr) : nullptr;
-    });
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_kpartial) == cudaSuccess)
+            g_noalloc_ptr[device] = static_cast<double *>(ptr);
+        else
+            (void)cudaGetLastError();    // clear the error so that the next call starts clean
+    }
     return g_noalloc_ptr[device];
+}
+
+// Partial sums a call with these parameters keeps in the array (0 without K-smoothing).
+static size_t partials_needed(const sage_params &p) {
+    if (!p.smooth_k) return 0;
+    return static_cast<size_t>(p.B) * p.H * kmean_splits(p) * p.d;
 }
 
 }  // namespace sage
@@ -41,18 +51,19 @@ using namespace sage;
 
 extern "C" size_t sage_quantize_noalloc_max_partials(void) { return kNoallocPartials; }
 
+extern "C" size_t sage_quantize_noalloc_partials_needed(const sage_params *p) {
+    if (check_params(p) != SAGE_OK) return 0;
+    return partials_needed(*p);
+}
+
 extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, const void *K,
                                             const void *V, int8_t *Qh, int8_t *Kh, int8_t *Vh,
                                             float *sQ, float *sK, float *sV, float *muK,
                                             float *muQ, sage_stream_t stream) {
-    // same argument rules as sage_quantize_smooth; the caller passes no workspace
-    if (!p) return SAGE_ERR_ARG;
-    if (p->B <= 0 || p->H <= 0 || p->N <= 0 || p->d <= 0) return SAGE_ERR_ARG;
-    if ((p->causal | p->smooth_k | p->smooth_q) & ~1) return SAGE_ERR_ARG;
+    // the rules of sage_quantize_smooth, less its workspace; no debug dump, no INT8-dP flag
+    const int st = check_params(p);
+    if (st != SAGE_OK) return st;
     if (p->flags & ~SAGE_FLAG_FP8) return SAGE_ERR_ARG;
-    if (p->dtype != SAGE_FP16 && p->dtype != SAGE_BF16) return SAGE_ERR_UNSUPPORTED;
-    if ((p->d != 64 && p->d != 128) || p->N % 64 != 0) return SAGE_ERR_UNSUPPORTED;
-    if (static_cast<long long>(p->B) * p->H > 65535) return SAGE_ERR_UNSUPPORTED;
     const void *ptrs[] = {Q, K, V, Qh, Kh, Vh, sQ, sK, sV, muK};
     for (const void *q : ptrs) {
         if (!q) return SAGE_ERR_ARG;
@@ -62,9 +73,7 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
         if (!muQ) return SAGE_ERR_ARG;
         if (reinterpret_cast<uintptr_t>(muQ) & 15u) return SAGE_ERR_ALIGN;
     }
-    const int splits = kmean_splits(*p);
-    const size_t need = static_cast<size_t>(p->B) * p->H * splits * p->d;
-    if (p->smooth_k && need > kNoallocPartials) return SAGE_ERR_WORKSPACE;   // beyond the static scratch
+    if (partials_needed(*p) > kNoallocPartials) return SAGE_ERR_WORKSPACE;   // beyond the array
 
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return SAGE_ERR_CUDA;
@@ -76,7 +85,7 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
     a.Qh = Qh; a.Kh = Kh; a.Vh = Vh;
     a.sQ = sQ; a.sK = sK; a.sV = sV;
     a.muK = muK; a.muQ = p->smooth_q ? muQ : nullptr;
-    a.ksplits = splits;
+    a.ksplits = kmean_splits(*p);
     // every partial sum the quantiser reads is written by the K-mean pass of the same call, so the
     // array needs no clearing; calls that overlap on the GPU share it and race
     a.kpartial = p->smooth_k ? scratch : nullptr;

@@ -13,8 +13,10 @@
  *   - Tensors are contiguous, row-major (B, H, N, d): token n of head (b, h) starts at element
  *     ((b * H + h) * N + n) * d.  Per-block scales are float32 (B, H, N / 64).
  *   - Every pointer is DEVICE memory allocated and owned by the caller, except `p` (host).  The
- *     library allocates nothing and keeps no state between calls; scratch memory is the caller's
- *     `workspace` of at least the size the matching *_workspace_bytes() query returns.
+ *     library allocates nothing.  Scratch memory is the caller's `workspace` of at least the size
+ *     the matching *_workspace_bytes() query returns, except for sage_quantize_smooth_noalloc,
+ *     which keeps its scratch in a fixed array inside the library.  The only other state kept
+ *     between calls is the device error word that sage_device_status() reads and clears.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  The
  *     return value reports argument and launch errors only; a device-side timeout of a bounded
  *     wait is reported by sage_device_status().
@@ -239,20 +241,26 @@ SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t 
  * For callers that cannot allocate device memory while they run -- for example a plug-in whose
  * host framework owns all device memory and offers it no allocator, or a latency-critical loop
  * that must not pay for (or synchronise on) an allocation.  Same inputs, outputs, results and
- * errors as sage_quantize_smooth, but the float64 K-mean partial sums live in a fixed array
- * inside the library (sage_quantize_noalloc_max_partials() entries, 1 MiB, held on every device
- * that loads the library until the process exits) instead of in a caller workspace.
+ * parameter rules as sage_quantize_smooth, but the float64 K-mean partial sums live in a fixed
+ * array inside the library (sage_quantize_noalloc_max_partials() entries, 1 MiB, held on every
+ * device that loads the library until the process exits) instead of in a caller workspace.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - Returns SAGE_ERR_WORKSPACE when B * H * splits * d exceeds that capacity (splits is the
- *     K-mean split count the library chooses: about ceil(304 / (B*H)), at most N / 64).
+ *   - A call needs sage_quantize_noalloc_partials_needed(p) entries: B * H * splits * d with
+ *     K-smoothing, 0 without, where splits = ceil(608 / (B * H)) clamped to [1, N / 64] is the
+ *     K-mean split count the library chooses.  Refusal therefore depends on B * H * splits, not on
+ *     B * H alone.  A call needing more than the capacity returns SAGE_ERR_WORKSPACE before any
+ *     launch.  The query returns 0 for parameters the call would refuse.
  *   - The first call on a device looks up the array's device address on that device (the
- *     current device); make that first call before any stream capture.
+ *     current device) and keeps it; make that first call before any stream capture.  The kept
+ *     address is not refreshed after cudaDeviceReset: do not use this entry point on a device
+ *     after resetting it in the same process.
  *   - Every call shares the one array, which keeps the last call's partial sums.  Nothing has to
  *     start at zero (each call writes every entry it reads first), but calls that overlap on the
  *     GPU -- on different streams, or from different host threads -- race on it.
- *   - `flags` must be 0 or SAGE_FLAG_FP8 (no debug dump).
+ *   - `flags` must be 0 or SAGE_FLAG_FP8 (no debug dump): SAGE_ERR_ARG otherwise.
  * ------------------------------------------------------------------------------------------ */
 SAGE_API size_t sage_quantize_noalloc_max_partials(void);
+SAGE_API size_t sage_quantize_noalloc_partials_needed(const sage_params *p);
 SAGE_API int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, const void *K,
                                           const void *V, int8_t *Qh, int8_t *Kh, int8_t *Vh,
                                           float *sQ, float *sK, float *sV, float *muK, float *muQ,

@@ -154,3 +154,21 @@ def test_qat_argument_checks(sg):
     assert L.sage_qat_bwd(ctypes.byref(p), *f[:10], f[11], 100, None) == 6
     assert L.sage_qat_bwd(ctypes.byref(p), *f[:10], None, 1 << 20, None) == 6
     assert L.sage_qat_bwd(ctypes.byref(p), *f[:9], f[9] + 8, f[11], 1 << 20, None) == 3
+
+
+def test_noalloc_partials_query(sg):
+    """The allocation-free quantise call needs B*H*splits*d K-mean partial sums with K-smoothing
+    (splits = ceil(608 / (B*H)) clamped to [1, N/64]) and none without; the host-only query says
+    so, and returns 0 for parameters the call would refuse."""
+    L = sg.lib()
+    cap = L.sage_quantize_noalloc_max_partials()
+    assert cap == 131072
+    for B, H, N, d in ((1, 3, 320, 64), (2, 16, 8192, 128), (1, 600, 8192, 128), (1, 608, 8192, 128)):
+        p = sg.make_params(B, H, N, d, 0, False)
+        splits = min(max(-(-608 // (B * H)), 1), N // 64)
+        assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == B * H * splits * d
+    # B*H = 600 takes 2 splits and exceeds the array; B*H = 608 takes 1 and fits
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 600, 8192, 128, 0, False))) > cap
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 608, 8192, 128, 0, False))) <= cap
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 256, 64, 0, False, smooth_k=False))) == 0
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 100, 64, 0, False))) == 0

@@ -51,17 +51,21 @@ def test_noalloc_matches_quantize_two_calls(B, H, N, d, dtype, smooth_q):
 
 
 def test_noalloc_rejects_beyond_capacity():
+    """B*H = 2048 heads of d = 128 need 2048 * 128 partial sums (one K-mean split each): more than
+    the array holds.  The call gets real device tensors of the right size (about 150 MiB), so even
+    a launch by mistake would stay inside its buffers; it must return SAGE_ERR_WORKSPACE, and the
+    partials-needed query must agree."""
     from bit_trainable_attention_sage_gb300 import build
     build.build()
     import bit_trainable_attention_sage_gb300 as sg
     L = sg.lib()
-    L.sage_quantize_noalloc_max_partials.restype = ctypes.c_size_t
     cap = L.sage_quantize_noalloc_max_partials()
     assert cap == 131072
-    # B*H = 2048 heads of d = 128 need 2048 * 128 partial sums (one split each): too many
-    p = sg.make_params(1, 2048, 64, 128, sg.binding.SAGE_FP16, False)
-    fake = [0x10000 * (i + 1) for i in range(10)] + [None]      # never dereferenced: refused first
-    fn = L.sage_quantize_smooth_noalloc
-    fn.argtypes = [ctypes.POINTER(sg.SageParams)] + [ctypes.c_void_p] * 12
-    fn.restype = ctypes.c_int
-    assert fn(ctypes.byref(p), *fake, None) == sg.binding.SAGE_ERR_WORKSPACE
+    B, H, N, d = 1, 2048, 64, 128
+    p = sg.make_params(B, H, N, d, sg.binding.SAGE_FP16, False)
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == B * H * d > cap
+    Q, K, V = (torch.zeros((B, H, N, d), dtype=torch.float16, device="cuda") for _ in range(3))
+    with pytest.raises(sg.binding.SageError) as e:
+        sg.sage_quantize_smooth_noalloc(Q, K, V)
+    assert e.value.status == sg.binding.SAGE_ERR_WORKSPACE
+    assert sg.sage_device_status() == 0
