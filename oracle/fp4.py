@@ -18,12 +18,15 @@ Readings where the pages leave a step open:
     e2m1(fl32(x / s)) with IEEE float32 division; a block whose scale is 0 has all-zero codes;
   * Q and K (after smoothing) are blocked along d, V along the tokens (the contraction of P V),
     16 consecutive tokens per channel;
-  * the softmax follows the INT8 path's per-tile form (R7): with r the row max of the 64-key tile
-    and x = fl32(acc c - r), c = fl32(log2(e) / sqrt(d)) (the block scales live inside the
-    dequantised operands), P~2 = fl32(2688 fl32(2^x)) and s_P1 = 2^(r - m) / 2688, which is
-    eq. (6) with rowmax(P~) = 2^(r - m); the second level quantises P~2 in 1 x 16 blocks along the
-    keys with codes e2m1(fl32(v * fl32(1 / s_P2))) (a reciprocal, as the kernel forms it);
-  * l accumulates the unquantised P~ as in eq. (1); Q-smoothing adds the same bias as R5.
+  * the softmax follows the INT8 path's per-tile form (R7): the logits are the float32 values
+    S = fl32(acc c), c = fl32(log2(e) / sqrt(d)) (the block scales live inside the dequantised
+    operands), r is the row max of S over the 64-key tile and x = fl32(S - r);
+    P~2 = fl32(2688 fl32(2^x)) and s_P1 = 2^(r - m) / 2688, which is eq. (6) with
+    rowmax(P~) = 2^(r - m); the second level quantises P~2 in 1 x 16 blocks along the keys with
+    codes e2m1(fl32(v * fl32(1 / s_P2))): the reciprocal of each block scale formed once, as the
+    backward's INT8 tiles form theirs (R8);
+  * l accumulates the unquantised P~ as in eq. (1); Q-smoothing adds the same bias as R5, in a
+    second float32 rounding S = fl32(fl32(acc c) + b).
 
 The block products of dequantised FP4 operands are computed in float64 (each operand has at most
 6 significant bits, an E2M1 value 1.1b times an E4M3 scale 1.xxxb, so each product at most 12; a
@@ -152,14 +155,12 @@ def sage_fp4_forward(prep: dict, causal: bool, heads=None):
                 cols = slice(64 * j, 64 * j + 64)
                 s = Qd[b, h, rows] @ Kd[b, h, cols].T
                 valid = ~tri if (causal and j == i) else np.ones((64, 64), bool)
-                if bias is None:
-                    amax = np.where(valid, s, -np.inf).max(axis=1)
-                    r = (amax * c).astype(np.float32)
-                    x = (s * c - r.astype(np.float64)[:, None]).astype(np.float32)
-                else:
-                    t = (s * c + bias[cols].astype(np.float64)[None, :]).astype(np.float32)
-                    r = np.where(valid, t, -np.inf).max(axis=1).astype(np.float32)
-                    x = (t - r[:, None]).astype(np.float32)
+                # the logits as float32 values S = fl32(acc c) (+ bias: fl32(S + b)), x = fl32(S - r)
+                S = (s * c).astype(np.float32)
+                if bias is not None:
+                    S = (S + bias[cols][None, :]).astype(np.float32)
+                r = np.where(valid, S, -np.inf).max(axis=1).astype(np.float32)
+                x = (S - np.where(np.isfinite(r), r, F32(0))[:, None]).astype(np.float32)
                 x = np.where(valid, x, -np.inf)
                 e64, pd = p_two_level(x)
                 m_new = np.maximum(m, r.astype(np.float64))

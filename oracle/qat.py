@@ -15,30 +15,31 @@ Readings where the pages leave a step open (the plainest ones the rest supports)
       (Q, K blocked along d, V along the tokens, the contraction axis of P V), no smoothing.  The
       values s * code have at most 6 significant bits and lie in [2^-10, 2688], so they are exact
       in fp16 and in bf16: every matrix product below runs on the input 16-bit type.
-  Q2  forward logits and softmax follow the library's per-tile form: per 64-key block,
-      acc = Q' K'^T (exact), c = fl32(log2(e)/sqrt(d)), r = fl32(max_k acc_k * c) over the
-      unmasked keys, x_k = fl32(acc_k c - r), e_k = fl32(2^x_k); l accumulates the unquantised e
-      (eq. (1) of "SageAttention3 ..." (review)), m the running max of r.
+  Q2  forward logits and softmax follow the per-tile form of the INT8 forward: per 64-key block,
+      acc = Q' K'^T (exact), c = fl32(log2(e)/sqrt(d)), the logits S_k = fl32(acc_k c) as float32
+      values, r = max_k S_k over the unmasked keys, x_k = fl32(S_k - r), e_k = fl32(2^x_k); l
+      accumulates the unquantised e (eq. (1) of "SageAttention3 ..." (review)), m the running max
+      of r.
   Q3  phi, the P fake quantiser, is one-level NVFP4 along the keys: per 16 keys of a row,
       s = e4m3(fl32(max e / 6)), codes e2m1(fl32(e * fl32(1/s))), P^ = codes * s (a zero scale
       gives zero codes).  The forward applies it to e (each 64-key block normalised by its own
       row max r, so the block's largest entry is 1) and keeps r (float32, one per row and key
       block).  "The same quantisation as the forward" in the backward is read as rebuilding the
-      forward's quantised P exactly: e from the stored r, phi(e), then normalised,
-      P^ = rnd16(fl32(phi(e) * fl32(2^(fl32(r - L2))))), so that dV is the gradient of the
+      forward's quantised P exactly: e = fl32(2^fl32(S - r)) from the stored r, phi(e), then
+      normalised, P^ = rnd16(fl32(phi(e) * fl32(2^(fl32(r - L2))))), so that dV is the gradient of the
       forward's own O with respect to V'.  (phi of the normalised P itself would not do: in a
       diffuse row of 8192 keys P is near 1.2e-4 and max / 6 lies far below the smallest E4M3
       scale 2^-9, so whole blocks would quantise to zero.)
   Q4  O = sum_j 2^(r_j - m) P^_j V'_j / l in the input dtype; O' = sum_j 2^(r_j - m) rnd16(e_j) V'_j
       / l kept in float32: the unquantised P~ enters its product as a 16-bit operand (BF16 is the
       pages' "high precision"), exactly as the backward's products do.
-  Q5  backward: P = fl32(2^(fl32(acc c - L2))) with L2 = fl32(L log2(e)); D = rowsum(dO o O');
+  Q5  backward: P = fl32(2^(fl32(S - L2))) with L2 = fl32(L log2(e)); D = rowsum(dO o O');
       dP = fl32(dO V'^T); dS = fl32(P fl32(dP - D)) rounded to the input dtype for the two
       products it feeds; dV = P^^T dO (P^ of Q3), dQ = dS K' / sqrt(d), dK = dS^T Q' / sqrt(d)
       (the fake quantisers pass the gradient straight through, so these are also the gradients
       of Q, K and V).
 
-Exactness: every float32 rounding the kernels take is taken here at the same step (fl32 below);
+Exactness: each float32 rounding the readings name is taken here (fl32 below);
 products of fake-quantised operands are exact in float64 (at most 12 significant bits each, a
 row of 128 sums stays exact unless its products span more than 2^34); everything that only
 accumulates (m, l, O, O', D, dQ, dK, dV) is float64.  ``exact=True`` replaces every quantiser and
@@ -124,10 +125,10 @@ def qat_forward(fq: dict, causal: bool, dtype_round, exact: bool = False, heads=
                 cols = slice(BLOCK * j, BLOCK * j + BLOCK)
                 valid = _mask(causal, i, j)
                 acc = Qf[b, h, rows] @ Kf[b, h, cols].T
-                amax = np.where(valid, acc, -np.inf).max(axis=1)
-                r = _fl32(amax * c, exact)
+                S = _fl32(acc * c, exact)
+                r = np.where(valid, S, -np.inf).max(axis=1)
                 R[b, h, j, rows] = r
-                x = np.where(valid, _fl32(acc * c - r[:, None], exact), -np.inf)
+                x = np.where(valid, _fl32(S - np.where(np.isfinite(r), r, 0.0)[:, None], exact), -np.inf)
                 e = _fl32(np.exp2(x), exact)
                 p_hat = e if exact else p_fake_quant(e)
                 p_16 = e if exact else np.asarray(dtype_round(e.astype(np.float32)), np.float64)
@@ -174,7 +175,8 @@ def qat_backward(fq: dict, Op_stored, L_stored, R, dO, causal: bool, dtype_round
         cols = slice(BLOCK * j, BLOCK * j + BLOCK)
         valid = _mask(causal, i, j)
         acc = Qf[b, h, rows] @ Kf[b, h, cols].T
-        x = np.where(valid, _fl32(acc * c - L2[b, h, rows][:, None], exact), -np.inf)
+        S = _fl32(acc * c, exact)
+        x = np.where(valid, _fl32(S - L2[b, h, rows][:, None], exact), -np.inf)
         P = _fl32(np.exp2(x), exact)
         dP = _fl32(dO[b, h, rows] @ Vf[b, h, cols].T, exact)
         dS = _fl32(P * _fl32(dP - D32[b, h, rows][:, None], exact), exact)
@@ -187,7 +189,7 @@ def qat_backward(fq: dict, Op_stored, L_stored, R, dO, causal: bool, dtype_round
                 r = np.asarray(R[b, h, j, rows], np.float64)
                 live = valid.any(axis=1)
                 r0 = np.where(live, r, 0.0)
-                e = np.where(valid, _fl32(np.exp2(_fl32(acc * c - r0[:, None], False)), False), 0.0)
+                e = np.where(valid, _fl32(np.exp2(_fl32(S - r0[:, None], False)), False), 0.0)
                 g = _fl32(np.exp2(_fl32(r0 - L2[b, h, rows], False)), False)
                 p_hat = np.where(live[:, None], _fl32(p_fake_quant(e) * g[:, None], False), 0.0)
                 p_hat = np.asarray(dtype_round(p_hat.astype(np.float32)), np.float64)

@@ -6,11 +6,12 @@ key vector is RMS-normalised, RMSNorm(x) = x / sqrt((1/d) sum_i x_i^2) * gamma w
 scale vector gamma; reproduction paragraph: norm epsilon 1e-6 (read as added to the mean square).
 
 Readings where the pages leave a step open:
-  * the sum of squares is the exact sum rounded once to float32, S = fl32(sum_c x_c^2); then, in
-    IEEE float32 operations, ms = S / d (exact, d a power of two), v = fl32(ms + eps),
-    s = fl32(sqrt(v)), r = fl32(1 / s); eps is a float32 value (1e-6 rounded to float32 in the
-    pages' setup).  Every step is a correctly rounded float32 operation on a uniquely defined
-    value, so the result does not depend on any summation order;
+  * r = 1 / sqrt(ms + eps) is the float32 nearest to its exact value, ms = (1/d) sum_c x_c^2 the
+    exact mean square of the 16-bit inputs and eps the float32 value the caller passes (1e-6 in
+    the pages' setup): computed here as the exact sum of squares rounded once to float64
+    (math.fsum), divided by d (a power of two, exact), then IEEE float64 steps and one final
+    rounding to float32, which is correctly rounded unless the exact value lies within about
+    2^-52 of a float32 rounding boundary;
   * the normalised value is y = round_dtype(fl32(fl32(x * r) * gamma_c)): the fused prologue
     produces exactly what a separate norm writing a 16-bit tensor would, and everything after it
     (K-mean, smoothing, quantisation) runs on those 16-bit values;
@@ -19,46 +20,28 @@ Readings where the pages leave a step open:
     y = gamma * x * r in float64: dx = r (gamma * dy - xh * mean_c(gamma_c dy_c xh_c)),
     xh = x * r; dgamma_c = sum over all tokens of dy_c xh_c.
 
-Parity: pinned by tests/test_oracle_qknorm.py (central finite differences of the float64
+Parity: pinned by tests/test_oracle_qknorm.py (r against the exact value by bracketing its
+float32 neighbours' midpoints in rational arithmetic, central finite differences of the float64
 function, the gradient's orthogonality to x at eps = 0, bit-exact invariance under power-of-two
 scaling, a hand-worked row).
 """
 from __future__ import annotations
 
-from fractions import Fraction
+import math
 
 import numpy as np
 
 F32 = np.float32
 
 
-def round_f32(q: Fraction) -> np.float32:
-    """The float32 nearest to a non-negative rational (ties to even); normal range only."""
-    if q == 0:
-        return F32(0)
-    e = q.numerator.bit_length() - q.denominator.bit_length()     # 2^e <= q < 2^(e+2)
-    if Fraction(2) ** e > q:
-        e -= 1
-    if Fraction(2) ** (e + 1) <= q:
-        e += 1
-    scaled = q / Fraction(2) ** (e - 23)                             # in [2^23, 2^24)
-    n = scaled.numerator // scaled.denominator
-    rem = scaled - n
-    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
-        n += 1
-    return F32(n * 2.0 ** (e - 23))
-
-
 def row_factor(x, eps: float) -> np.ndarray:
-    """r = fl32(1 / fl32(sqrt(fl32(fl32(sum x^2) / d + eps)))) per row of (..., d) 16-bit values,
-    the sum exact before its one rounding."""
-    x = np.asarray(x, np.float32)
+    """r = fl32(1 / sqrt(fl64(fsum(x^2)) / d + eps)) per row of (..., d) 16-bit values."""
+    x = np.asarray(x, np.float32).astype(np.float64)
     d = x.shape[-1]
     flat = x.reshape(-1, d)
-    S = np.array([round_f32(sum(Fraction(float(v)) ** 2 for v in row)) for row in flat], np.float32)
-    ms = S / F32(d)
-    v = ms + F32(eps)
-    r = F32(1) / np.sqrt(v)
+    ss = np.array([math.fsum(v * v for v in row) for row in flat])    # exact sum, one rounding
+    ms = ss / d
+    r = 1.0 / np.sqrt(ms + float(F32(eps)))
     return r.astype(np.float32).reshape(x.shape[:-1])
 
 

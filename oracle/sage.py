@@ -13,20 +13,19 @@ backward (1)-(7); "SageAttention3 ..." (review), INT8 backward (Algorithm 3 equa
 
 Readings where the pages are silent, garbled or at odds:
   R1  the softmax scale 1/sqrt(d) is applied after dequantisation, in float32, folded with
-      log2(e) into c = fl32(fl32(s_Q s_K) * fl32(log2(e)/sqrt(d))): the logits in log2 units are
-      acc * c; dQ and dK carry 1/sqrt(d) by the chain rule.
-  R7  forward P^ is per token per 64-key tile: with r = fl32(max_k(acc_k) * c) the row max over the
-      tile's unmasked entries and x_k = fl32(acc_k * c - r) (one rounding, as a fused
-      multiply-add), P^_k = rne(fl32(127 * fl32(2^x_k))); s_P = 2^(r - m)/127; l accumulates the
+      log2(e) into c = fl32(fl32(s_Q s_K) * fl32(log2(e)/sqrt(d))).  The logits are float32
+      values in log2 units, S_k = fl32(acc_k * c) (with Q-smoothing S_k = fl32(fl32(acc_k * c) +
+      bias_k)); dQ and dK carry 1/sqrt(d) by the chain rule.
+  R7  forward P^ is per token per 64-key tile: with r = max_k S_k the row max over the tile's
+      unmasked entries and x_k = fl32(S_k - r), P^_k = rne(fl32(127 * fl32(2^x_k))), where 2^x
+      is the float32 nearest to the exact power; s_P = 2^(r - m)/127; l accumulates the
       unquantised P~ (eq. 1); eq. (8)'s inverted rescale "diag(...)^-1" is read as eq. (1)'s
-      non-inverted one.  With Q-smoothing t_k = fl32(acc_k * c + bias_k), r = max t_k,
-      x_k = fl32(t_k - r).
-  R8  backward P_k = fl32(2^(fl32(acc_k * c - L2))) with L2 = fl32(L * fl32(log2(e))) (with
-      Q-smoothing fl32(t_k - L2)); P and dS are quantised per 64x64 tile: s = fl32(max|x|/127),
-      q = rne16(fl32(x * fl32(1/s) + 1536)) - 1536, i.e. the value x/s rounded once to float32
-      at the 2^-13 spacing of [1024, 2048) and then to the nearest integer, ties to even (the
-      pages say only "round"; this is the kernel's two-instruction rounding); a tile whose
-      max|x| is below 2^-120 (zero, or so small that 1/s would overflow float32) gets s = 0, q = 0.
+      non-inverted one.
+  R8  backward P_k = fl32(2^(fl32(S_k - L2))) with L2 = fl32(L * fl32(log2(e))); P and dS are
+      quantised per 64x64 tile: s = fl32(max|x|/127), its reciprocal inv = fl32(1/s) formed once
+      per tile, q = clamp(rne(fl32(x * inv)), -127, 127) (the pages say only "round"); a tile
+      whose max|x| is below 2^-120 (zero, or so small that 1/s is not a finite float32) gets
+      s = 0, q = 0.
   R9  dP = dO V^T uses the unquantised 16-bit dO and V, float32 result, never rounded to 16 bits.
   R10 D = rowsum(dO o O) uses the stored 16-bit O.
   R11 no K-smoothing correction in the backward pass.
@@ -35,8 +34,9 @@ Readings where the pages are silent, garbled or at odds:
   R5  with Q-smoothing, S gets the bias mu_Qi K_sm,j^T (before 1/sqrt(d)) and dK gets
       (dS_ij^T 1) mu_Qi^T / sqrt(d) from the unquantised dS.
 
-Where float decides an integer code (P^, dS^), the decision is taken in float32 as the kernel
-does; everything that only accumulates (m, l, O, dV, dQ, dK, D) is float64.
+Where float decides an integer code (P^, dS^), the decision is taken in float32, each named
+step one correctly rounded float32 operation; everything that only accumulates (m, l, O, dV,
+dQ, dK, D) is float64.
 
 FP8 variant (``QUANTISED_FP8``; "SageAttention3 ..." (review), "INT8 vs FP8 training"): every
 INT8 code becomes an E4M3 code with 448 in place of 127 (see oracle.quant): block scales
@@ -44,7 +44,8 @@ fl32(max|x|/448); forward P^_k = e4m3_round(fl32(448 * fl32(2^x_k))), s_P = 2^(r
 backward tile codes e4m3_round(fl32(x * fl32(1/s))), s = fl32(max|x|/448), a tile whose max|x|
 is below 2^-110 being a zero tile (1/s stays finite).  Block products of E4M3 values are exact in
 float64: each product is a multiple of 2^-18 below 2^18, a sum of at most 128 of them stays
-below 2^25, so 43 bits suffice.
+below 2^25, so 43 bits suffice.  (Their logits fl32(acc * c) take one float64 rounding before the
+float32 one, since acc * c may need 67 bits; integer products need at most 45 and are exact.)
 
 The ``DEQUANTISED`` arithmetic replaces every quantiser by the identity and drops every float32
 rounding; the very same tiled code must then equal float64 full-precision attention, which pins
@@ -102,40 +103,28 @@ class Arith:
         assert np.array_equal(r, p), "integer block product is not integral"
         return r.astype(np.int64)
 
-    def fma_logits(self, s_int, c, sub=None, bias=None):
-        """Logits in log2 units minus ``sub`` (a per-row array), as the kernel forms them.
-
-        Without a bias: fl32(acc * c - sub) with a single rounding (a fused multiply-add; acc * c
-        is exact in float64 and so is the difference, so one cast rounds once).
-        With a bias: t = fl32(acc * c + bias) (one rounding), then fl32(t - sub).
-        """
+    def logits(self, s_int, c, bias=None):
+        """The logits in log2 units as float32 values (R1): S = fl32(acc * c), then with a bias
+        S = fl32(S + bias).  acc * c of an integer product (|acc| < 2^21 times a 24-bit c) is
+        exact in float64, so one cast rounds once."""
         acc = np.asarray(s_int, np.float64)
         if not self.quantised:
-            t = acc * c + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
-            return t if sub is None else t - np.asarray(sub, np.float64)[:, None]
-        c64 = float(F32(c))
-        if bias is None:
-            if sub is None:
-                return (acc * c64).astype(np.float32)
-            return (acc * c64 - np.asarray(sub, np.float32).astype(np.float64)[:, None]).astype(np.float32)
-        t = (acc * c64 + np.asarray(bias, np.float32).astype(np.float64)[None, :]).astype(np.float32)
-        if sub is None:
-            return t
-        return t - np.asarray(sub, np.float32)[:, None]
+            return acc * c + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+        S = (acc * float(F32(c))).astype(np.float32)
+        if bias is not None:
+            S = S + np.asarray(bias, np.float32)[None, :]        # float32 add, one rounding
+        return S
 
-    def row_max_logit(self, s_int, c, valid, bias=None):
-        """r = the row max of the logits over ``valid`` entries, -inf where a row has none.
-        Without a bias it is formed from the integer maximum: fl32(max_k(acc_k) * c), c >= 0."""
-        acc = np.asarray(s_int, np.float64)
-        anyv = valid.any(axis=1)
-        if bias is None:
-            amax = np.where(valid, acc, -np.inf).max(axis=1)
-            if self.quantised:
-                r = (np.where(anyv, amax, 0.0) * float(F32(c))).astype(np.float32)
-                return np.where(anyv, r, np.float32(-np.inf)).astype(np.float32)
-            return np.where(anyv, np.where(anyv, amax, 0.0) * c, -np.inf)
-        t = self.fma_logits(s_int, c, None, bias)
-        return np.where(valid, t, -np.inf).max(axis=1).astype(np.float32 if self.quantised else np.float64)
+    def minus(self, S, sub):
+        """x = fl32(S - sub) with ``sub`` one value per row (a row max r or L2)."""
+        if not self.quantised:
+            return np.asarray(S, np.float64) - np.asarray(sub, np.float64)[:, None]
+        return (np.asarray(S, np.float32) - np.asarray(sub, np.float32)[:, None]).astype(np.float32)
+
+    @staticmethod
+    def row_max(S, valid):
+        """r = the row max of S over ``valid`` entries, -inf where a row has none."""
+        return np.where(valid, S, -np.inf).max(axis=1)
 
     # -- the quantisers --------------------------------------------------------------------
     def block_quant(self, x):
@@ -145,38 +134,42 @@ class Arith:
         x = np.asarray(x, np.float64)
         return x, np.ones(x.shape[:-2] + (x.shape[-2] // BLOCK,))
 
-    def token_quant(self, x):
+    def token_quant(self, x, unrounded: bool = False):
         """Forward per-token P^ of one tile (R7) from x = logits - r.
-        Returns (2^x in float64, P^)."""
+        Returns (2^x in float64, P^), and with ``unrounded`` also the float32 values
+        fl32(127 * fl32(2^x)) that the rounding decides from."""
         e64 = np.exp2(np.asarray(x, np.float64))
         if not self.quantised:
-            return e64, 127.0 * e64
+            y = 127.0 * e64
+            return (e64, y, y) if unrounded else (e64, y)
         e32 = e64.astype(np.float32)
+        y = (F32(self.qmax) * e32).astype(np.float32)
         if self.fmt == "e4m3":
-            return e64, e4m3_round(F32(448) * e32)
-        return e64, np.clip(np.rint(F32(127) * e32), 0, 127).astype(np.int64)
+            q = e4m3_round(y)
+        else:
+            q = np.clip(np.rint(y), 0, 127).astype(np.int64)
+        return (e64, q, y) if unrounded else (e64, q)
 
-    def tile_quant(self, x):
-        """Backward per-tile quantiser of P and dS (R8).  Returns (scale, codes)."""
+    def tile_quant(self, x, unrounded: bool = False):
+        """Backward per-tile quantiser of P and dS (R8).  Returns (scale, codes), and with
+        ``unrounded`` also the float32 values fl32(x * inv) that the rounding decides from."""
         if not self.quantised:
-            return 1.0, np.asarray(x, np.float64)
+            x = np.asarray(x, np.float64)
+            return (1.0, x, x) if unrounded else (1.0, x)
         x = np.asarray(x, np.float32)
         mx = np.max(np.abs(x)) if x.size else F32(0)
-        if self.fmt == "e4m3":
-            if mx < TILE_ZERO_BELOW_FP8:
-                return F32(0), np.zeros(x.shape)
-            s = F32(mx) / F32(448)
+        zero = mx < (TILE_ZERO_BELOW_FP8 if self.fmt == "e4m3" else TILE_ZERO_BELOW)
+        if zero:
+            s, inv = F32(0), F32(0)
+        else:
+            s = F32(mx) / F32(self.qmax)
             inv = F32(1) / s
-            return s, e4m3_round(x * inv)          # float32 product, one rounding, then E4M3
-        if mx < TILE_ZERO_BELOW:
-            return F32(0), np.zeros(x.shape, np.int64)
-        s = F32(mx) / F32(127)
-        inv = F32(1) / s
-        # round half to even of y = fl32(x * inv + 1536) at fp16 resolution (1 in [1024, 2048)):
-        # x * inv is exact in float64 and so is the sum, so one cast gives the fused rounding
-        y = (x.astype(np.float64) * float(inv) + 1536.0).astype(np.float32)
-        q = y.astype(np.float16).astype(np.int64) - 1536
-        return s, q
+        y = (x * inv).astype(np.float32)                     # float32 product, one rounding
+        if self.fmt == "e4m3":
+            q = e4m3_round(y)
+        else:
+            q = np.clip(np.rint(y), -127, 127).astype(np.int64)   # rint: ties to even
+        return (s, q, y) if unrounded else (s, q)
 
     def exp2_32(self, x):
         if self.quantised:
@@ -228,8 +221,9 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
     """SageBwd forward (steps a3-a6).  Returns (O float64 (B,H,N,d), L float64 (B,H,N)).
 
     ``q_blocks`` limits the query blocks computed (others stay zero), ``heads`` the (b, h) pairs.
-    ``record`` (small N only) receives, per head, the S block products, the P^ codes and the
-    P^ V^ block products of every tile (integers for INT8 codes, float64 for E4M3).
+    ``record`` (small N only) receives, per head, the S block products, the float32 logits S, the
+    P^ codes, the float32 values their rounding decides from (P_y) and the P^ V^ block products of
+    every tile (integers for INT8 codes, float64 for E4M3).
     """
     Qh, Kh, Vh = prep["Qh"], prep["Kh"], prep["Vh"]
     sQ, sK, sV = prep["sQ"], prep["sK"], prep["sV"]
@@ -245,7 +239,9 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
             rec = record.setdefault((b, h), {})
             rtype = np.int64 if arith.fmt == "int8" else np.float64
             rec["S_int"] = np.zeros((N, N), rtype)
+            rec["S"] = np.zeros((N, N), np.float32)
             rec["P_hat"] = np.zeros((N, N), rtype)
+            rec["P_y"] = np.zeros((N, N), np.float32)
             rec["PV_int"] = {}
         for i in (range(T) if q_blocks is None else q_blocks):
             rows = slice(i * BLOCK, (i + 1) * BLOCK)
@@ -260,16 +256,16 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
                 # (3) S_ij = MM(Q^_i, K^_j) * s_Q * s_K  (and * 1/sqrt(d), in log2 units)
                 s_int = arith.int_mm(Qh[b, h, rows], np.swapaxes(Kh[b, h, cols], 0, 1))
                 c = arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2)
-                bias_j = None if bias is None else bias[cols]
+                S = arith.logits(s_int, c, None if bias is None else bias[cols])
                 valid = ~mask if (causal and j == i) else np.ones((BLOCK, BLOCK), bool)
                 # (4) online softmax statistics and per-token quantisation of P~
-                r = arith.row_max_logit(s_int, c, valid, bias_j)
-                x = arith.fma_logits(s_int, c, np.where(np.isfinite(r), r, 0), bias_j)
+                r = arith.row_max(S, valid)
+                x = arith.minus(S, np.where(np.isfinite(r), r, 0))
                 x = np.where(valid, x, -np.inf)
-                m_new = np.maximum(m, r.astype(np.float64))
-                e64, p_hat = arith.token_quant(x)
+                m_new = np.maximum(m, np.asarray(r, np.float64))
+                e64, p_hat, p_y = arith.token_quant(x, unrounded=True)
                 alpha = np.exp2(m - m_new)
-                grow = np.exp2(r.astype(np.float64) - m_new)
+                grow = np.exp2(np.asarray(r, np.float64) - m_new)
                 s_p = grow / arith.qmax
                 l = alpha * l + grow * e64.sum(axis=1)
                 # (5) O_ij = diag(e^{m_old - m_new}) O + MM(P^_ij, V^_j) * s_P * s_V
@@ -278,7 +274,9 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
                 m = m_new
                 if record is not None:
                     rec["S_int"][rows, cols] = s_int
+                    rec["S"][rows, cols] = S
                     rec["P_hat"][rows, cols] = p_hat
+                    rec["P_y"][rows, cols] = p_y
                     rec["PV_int"][(i, j)] = pv
             O[b, h, rows] = acc / l[:, None]
             L[b, h, rows] = (m + np.log2(l)) * LN2
@@ -287,7 +285,7 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
 
 def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUANTISED,
                   q_blocks=None, kv_blocks=None, heads=None, record: dict | None = None,
-                  dp_int8: bool = False):
+                  dp_int8: bool = False, products: bool = False):
     """SageBwd backward (steps a7-a13).  Returns dict(dQ, dK, dV float64 (B,H,N,d), D, dOh, sdO).
 
     ``dp_int8`` selects the ablation of "SageAttention3 ..." (review), Table 1c: dP from the INT8
@@ -297,7 +295,10 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
     ``O_stored`` is the forward output as stored (16-bit values), ``L`` the stored float32 LSE.
     ``q_blocks`` / ``kv_blocks`` restrict which dQ rows / dK, dV rows are completed (for sampled
     checks at large N); by default everything is computed, looping over key/value blocks and,
-    inside, query blocks.  ``record`` receives the per-tile dequantised P, dP, dequantised dS.
+    inside, query blocks.  ``record`` receives, per head, the per-tile dequantised P, dP and
+    dequantised dS, the P and dS codes, the float32 values their rounding decides from (P_y, dS_y),
+    the logits (S_bwd) and the tile scales (sP, sdS); with ``products`` also the integer block
+    products MM(P^^T, dO^_i), MM(dS^, K^_j) and MM(dS^^T, Q^_i) of every tile (i, j).
     """
     if dp_int8 and arith.fmt != "int8":
         raise ValueError("the INT8-dP ablation applies to INT8 codes only")
@@ -329,14 +330,16 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
         # (2) recompute S_ij (same formula as the forward) and P_ij = exp(S_ij - L_i)
         s_int = arith.int_mm(Qh[b, h, rows], np.swapaxes(Kh[b, h, cols], 0, 1))
         c = arith.logit_scale(sQ[b, h, i], sK[b, h, j], sl2)
-        x = arith.fma_logits(s_int, c, L2[b, h, rows], None if bias is None else bias[cols])
+        S = arith.logits(s_int, c, None if bias is None else bias[cols])
+        x = arith.minus(S, L2[b, h, rows])
         if causal and i == j:
             x = np.where(mask, -np.inf, x)
         P = arith.exp2_32(x)
         # (3) dV_j += MM(P^_ij^T, dO^_i) * s_P * s_dO
-        s_p, p_hat = arith.tile_quant(P)
+        s_p, p_hat, p_y = arith.tile_quant(P, unrounded=True)
+        dv_int = arith.int_mm(p_hat.T, dOh[b, h, rows]) if (want_dkv or products) else None
         if want_dkv:
-            dV[b, h, cols] += (float(s_p) * float(sdO[b, h, i])) * arith.int_mm(p_hat.T, dOh[b, h, rows])
+            dV[b, h, cols] += (float(s_p) * float(sdO[b, h, i])) * dv_int
         # (4) dP_ij = dO_i V_j^T, 16-bit operands, float32 result (ablation: INT8 codes, exact
         # integer product times the float32 product of the two block scales)
         if dp_int8:
@@ -346,13 +349,15 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
             dP = arith.r32(dO[b, h, rows].astype(np.float64) @ V64[b, h, cols].T)
         # (5) dS_ij = P_ij o (dP_ij - D_i), then per-tile quantisation
         dS = arith.r32(P * arith.r32(dP - D32[b, h, rows][:, None]))
-        s_ds, ds_hat = arith.tile_quant(dS)
+        s_ds, ds_hat, ds_y = arith.tile_quant(dS, unrounded=True)
         # (6) dQ_i += MM(dS^_ij, K^_j) * s_dS * s_K   (and * 1/sqrt(d))
+        dq_int = arith.int_mm(ds_hat, Kh[b, h, cols]) if (want_dq or products) else None
         if want_dq:
-            dQ[b, h, rows] += (float(s_ds) * float(sK[b, h, j]) * inv_sqrt_d) * arith.int_mm(ds_hat, Kh[b, h, cols])
+            dQ[b, h, rows] += (float(s_ds) * float(sK[b, h, j]) * inv_sqrt_d) * dq_int
         # (7) dK_j += MM(dS^_ij^T, Q^_i) * s_dS * s_Q   (and * 1/sqrt(d))
+        dk_int = arith.int_mm(ds_hat.T, Qh[b, h, rows]) if (want_dkv or products) else None
         if want_dkv:
-            dK[b, h, cols] += (float(s_ds) * float(sQ[b, h, i]) * inv_sqrt_d) * arith.int_mm(ds_hat.T, Qh[b, h, rows])
+            dK[b, h, cols] += (float(s_ds) * float(sQ[b, h, i]) * inv_sqrt_d) * dk_int
             if prep.get("muQ") is not None:
                 colsum = np.asarray(dS, np.float64).sum(axis=0)
                 dK[b, h, cols] += inv_sqrt_d * np.outer(colsum, np.asarray(prep["muQ"][b, h, i], np.float64))
@@ -360,9 +365,27 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
             rec = record.setdefault((b, h), {})
             for key in ("P", "dP", "dS"):
                 rec.setdefault(key, np.zeros((N, N)))
+            ctype = np.int64 if arith.fmt == "int8" else np.float64
+            for key in ("P_hat", "dS_hat"):
+                rec.setdefault(key, np.zeros((N, N), ctype))
+            for key in ("P_y", "dS_y", "S_bwd"):
+                rec.setdefault(key, np.zeros((N, N), np.float32))
+            for key in ("sP", "sdS"):
+                rec.setdefault(key, np.zeros((T, T), np.float32))
             rec["P"][rows, cols] = float(s_p) * np.asarray(p_hat, np.float64)
             rec["dP"][rows, cols] = dP
             rec["dS"][rows, cols] = float(s_ds) * np.asarray(ds_hat, np.float64)
+            rec["P_hat"][rows, cols] = p_hat
+            rec["dS_hat"][rows, cols] = ds_hat
+            rec["P_y"][rows, cols] = p_y
+            rec["dS_y"][rows, cols] = ds_y
+            rec["S_bwd"][rows, cols] = S
+            rec["sP"][i, j] = s_p
+            rec["sdS"][i, j] = s_ds
+            if products:
+                rec.setdefault("dV_int", {})[(i, j)] = dv_int
+                rec.setdefault("dQ_int", {})[(i, j)] = dq_int
+                rec.setdefault("dK_int", {})[(i, j)] = dk_int
 
     for (b, h) in heads:
         biases = {}
@@ -387,7 +410,8 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
 
 
 def run(Q, K, V, dO, causal: bool, dtype_round, smooth_k: bool = True, smooth_q: bool = False,
-        arith: Arith = QUANTISED, record: dict | None = None, dp_int8: bool = False):
+        arith: Arith = QUANTISED, record: dict | None = None, dp_int8: bool = False,
+        products: bool = False):
     """Whole path on full tensors: quantise, forward, backward.  ``dtype_round`` rounds O to the
     stored 16-bit type (identity in the dequantised limit)."""
     prep = prepare(Q, K, V, smooth_k=smooth_k, smooth_q=smooth_q, arith=arith)
@@ -395,5 +419,6 @@ def run(Q, K, V, dO, causal: bool, dtype_round, smooth_k: bool = True, smooth_q:
     O, L = sage_forward(prep, causal, arith=arith, record=record)
     O_stored = dtype_round(O.astype(np.float32)) if arith.quantised else O
     L_stored = L.astype(np.float32) if arith.quantised else L
-    g = sage_backward(prep, O_stored, L_stored, dO, causal, arith=arith, record=record, dp_int8=dp_int8)
+    g = sage_backward(prep, O_stored, L_stored, dO, causal, arith=arith, record=record, dp_int8=dp_int8,
+                      products=products)
     return dict(prep=prep, O=O, L=L, O_stored=O_stored, L_stored=L_stored, **g)

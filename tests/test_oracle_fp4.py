@@ -97,7 +97,8 @@ def _inputs(N, d, seed, q_off=0.0, k_off=0.0):
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp4_forward_closed_form(causal):
     """O_i = sum_j 2^(r_ij - M_i) / 2688 (P'_ij V'_j) / sum_j 2^(r_ij - M_i) sum_k 2^(x_ijk), with
-    P' the brute-force NVFP4 of fl32(2688 fl32(2^x)) per 16 keys, evaluated without tiling."""
+    x = fl32(fl32(acc c) - r) and P' the brute-force NVFP4 of fl32(2688 fl32(2^x)) per 16 keys,
+    evaluated without tiling."""
     N, d = 192, 64
     Q, K, V = _inputs(N, d, seed=4)
     prep = fp4.quantize_fp4(Q, K, V)
@@ -118,7 +119,8 @@ def test_fp4_forward_closed_form(causal):
         vj = valid[:, 64 * j:64 * j + 64]
         live = vj.any(axis=1)
         r = np.where(live, (np.where(vj, a, -np.inf).max(axis=1) * c).astype(np.float32), -np.inf)
-        x = np.where(vj, (a * c - np.where(live, r, 0)[:, None]).astype(np.float32), -np.inf)
+        S = (a * c).astype(np.float32)
+        x = np.where(vj, (S - np.where(live, r, 0)[:, None].astype(np.float32)).astype(np.float32), -np.inf)
         e = np.exp2(x.astype(np.float64))
         v = (np.float32(2688) * e.astype(np.float32)).astype(np.float32)
         pd = np.zeros_like(e)

@@ -149,8 +149,8 @@ def _inputs(N, d, seed, scale=1.0):
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_forward_closed_form(causal):
     """O_i = sum_j 2^(r_ij - M_i) (s_V,j / 448) P^_ij V^_j / sum_j 2^(r_ij - M_i) sum_k 2^(x_ijk),
-    with P^ the nearest E4M3 value to fl32(448 fl32(2^x)) (brute-force search here), evaluated
-    row by row without tiling."""
+    with x = fl32(fl32(acc c) - r) and P^ the nearest E4M3 value to fl32(448 fl32(2^x))
+    (brute-force search here), evaluated row by row without tiling."""
     N, d = 256, 64
     Q, K, V, _ = _inputs(N, d, seed=12, scale=2.0)
     prep = sage.prepare(Q, K, V, arith=sage.QUANTISED_FP8)
@@ -165,7 +165,8 @@ def test_fp8_forward_closed_form(causal):
     live = vj.any(axis=2)
     amax = np.where(vj, accj, -np.inf).max(axis=2)
     r = np.where(live, (np.where(live, amax, 0) * cj).astype(np.float32), -np.inf)
-    x = np.where(vj, (accj * cj[:, :, None] - np.where(live, r, 0)[:, :, None]).astype(np.float32), -np.inf)
+    Sj = (accj * cj[:, :, None]).astype(np.float32)
+    x = np.where(vj, (Sj - np.where(live, r, 0)[:, :, None].astype(np.float32)).astype(np.float32), -np.inf)
     e64 = np.exp2(x.astype(np.float64))
     p_hat = _nearest_brute(np.float32(448) * e64.astype(np.float32)).reshape(N, T, 64)
     r64 = r.astype(np.float64)

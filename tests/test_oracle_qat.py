@@ -96,7 +96,8 @@ def test_p_fake_quant_against_brute_force():
 
 
 def _closed_form_forward(fq, N, d, causal, dtype):
-    """Untiled: for each row and 64-key block j, r_j = fl32(max acc c), e = fl32(2^fl32(acc c - r_j));
+    """Untiled: for each row and 64-key block j, the float32 logits S = fl32(acc c), r_j = max S,
+    e = fl32(2^fl32(S - r_j));
     O = sum_j 2^(r_j - M) phi(e_j) V'_j / sum_j 2^(r_j - M) sum e_j, phi by grid search;
     O' the same with rnd16(e_j)."""
     Qf, Kf, Vf = (fq[k][0, 0] for k in ("Qf", "Kf", "Vf"))
@@ -113,7 +114,8 @@ def _closed_form_forward(fq, N, d, causal, dtype):
                 continue
             acc = Kf[keys] @ Qf[i]
             r = float(np.float32(np.where(valid, acc, -np.inf).max() * c))
-            x = np.where(valid, (acc * c - r).astype(np.float32), -np.inf)
+            S = (acc * c).astype(np.float32)
+            x = np.where(valid, (S - np.float32(r)).astype(np.float32), -np.inf)
             e = np.exp2(x.astype(np.float64)).astype(np.float32)
             rs.append(r)
             ph.append(_phi_brute(e))
@@ -192,7 +194,8 @@ def test_dv_is_the_gradient_of_the_forward_output(causal):
                 continue
             acc = Kf[keys] @ Qf[i]
             r = float(np.float32(np.where(valid, acc, -np.inf).max() * c))
-            e = np.exp2(np.where(valid, (acc * c - r).astype(np.float32), -np.inf).astype(np.float64)).astype(np.float32)
+            S = (acc * c).astype(np.float32)
+            e = np.exp2(np.where(valid, (S - np.float32(r)).astype(np.float32), -np.inf).astype(np.float64)).astype(np.float32)
             rs[j], ph[j], sums[j] = r, _phi_brute(e), e.astype(np.float64).sum()
         M = max(rs.values())
         den = sum(2.0 ** (rs[j] - M) * sums[j] for j in rs)

@@ -3,14 +3,12 @@
 own formulas: finite differences, invariants and a hand-worked row."""
 from __future__ import annotations
 
-import math
 from fractions import Fraction as Fr
 
 import numpy as np
 
 import workloads
 from oracle import qknorm
-from tests.exact import fl32
 
 
 def _f64(x, g, eps):
@@ -76,29 +74,19 @@ def test_hand_worked_row():
     assert y2.tolist() == [[2.400390625, 0.7998046875, 0.0, 0.0]]
 
 
-def _sqrt_rn32(v: Fr) -> Fr:
-    """Correctly rounded float32 square root of a rational: the candidate near sqrt whose
-    midpoints with its neighbours bracket v when squared."""
-    c0 = np.float32(math.sqrt(float(v)))
-    for c in (c0, np.nextafter(c0, np.float32(0)), np.nextafter(c0, np.float32(np.inf))):
-        cf = Fr(float(c))
-        lo = (cf + Fr(float(np.nextafter(c, np.float32(0))))) / 2
-        hi = (cf + Fr(float(np.nextafter(c, np.float32(np.inf))))) / 2
-        if lo * lo < v < hi * hi:
-            return cf
-    raise AssertionError("no candidate brackets v")
-
-
-def test_row_factor_against_exact_rationals():
-    """r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))), S = fl32(exact sum of squares), re-derived in
-    exact rationals (the square root by bracketing midpoints)."""
+def test_row_factor_is_the_correctly_rounded_exact_value():
+    """r must be the float32 nearest to the exact 1 / sqrt(sum(x^2)/d + eps), eps the float32 value
+    passed: with m_lo, m_hi the midpoints between r and its float32 neighbours,
+    1/m_hi^2 < v < 1/m_lo^2 in exact rationals (v = the exact mean square + eps)."""
     rng = np.random.default_rng(3)
-    eps = Fr(float(np.float32(1e-6)))
+    eps = np.float32(1e-6)
     for scale in (1.0, 1e-3, 40.0):
-        x = workloads.round_fp16((rng.standard_normal((60, 128)) * scale).astype(np.float32))
-        r = qknorm.row_factor(x, np.float32(1e-6))
+        x = workloads.round_fp16((rng.standard_normal((100, 128)) * scale).astype(np.float32))
+        r = qknorm.row_factor(x, eps)
         for row, rv in zip(x, r):
-            S = fl32(sum(Fr(float(a)) ** 2 for a in row))
-            v = fl32(S / 128 + eps)
-            want = fl32(1 / _sqrt_rn32(v))
-            assert Fr(float(rv)) == want
+            v = sum(Fr(float(a)) ** 2 for a in row) / 128 + Fr(float(eps))
+            lo = Fr(float(np.nextafter(rv, np.float32(0))))
+            hi = Fr(float(np.nextafter(rv, np.float32(np.inf))))
+            c = Fr(float(rv))
+            m_lo, m_hi = (c + lo) / 2, (c + hi) / 2
+            assert 1 / (m_hi * m_hi) < v < 1 / (m_lo * m_lo)
