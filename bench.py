@@ -32,16 +32,24 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+HOST_CORES = len(os.sched_getaffinity(0))
 if "reference" in sys.argv:
-    # the reference arm times the oracle on one host core: pin BLAS before numpy loads
+    # the reference arm times the oracle on every host core this process may use: set the BLAS
+    # thread count before numpy loads
     for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[_v] = "1"
+        os.environ[_v] = str(HOST_CORES)
 
 import workloads  # noqa: E402
 
 METRIC = "fwd+bwd effective TOPS (N=8192,d=128) and % of INT8/FP16 tensor-core roofline"
 UNIT = "TOPS"
 KERNELS_PER_STEP = 10   # kmean_partial, quantize, 3 widen + fwd, 2 widen + bwd prologue + bwd
+# The rate of the legacy warp-level integer MMA (mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32),
+# the only INT8 tensor-core instruction sm_103a has (ptxas rejects tcgen05 kind::i8 there), as
+# measured on GB300 by a probe kernel when the integer GEMMs' instruction was chosen.  It stands in
+# for the "INT8 peak" of the literal roofline reading.
+INT8_MMA_SYNC_TOPS = 152.0
+BURST_REGION_MS = 1000.0  # a timed region shorter than this compares with the burst peak
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "bwd_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "bit_trainable_attention_sage_gb300", "csrc", f)
                   for f in ("sage_bwd.cu", "sage_device.cuh", "sage_internal.h")]
@@ -79,6 +87,27 @@ def max_over_ranks(dist, value: float, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def config_of(w: workloads.Workload) -> dict:
+    """The ``config`` object both arms report for a workload."""
+    return {"workload": f"{w.name} {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "causal": w.causal, "smooth_k": True, "smooth_q": w.smooth_q, "per_rank": "own batch",
+            "l2": f"inputs larger than L2 (Q,K,V,dO = {8 * w.B * w.H * w.N * w.d // 2**20} MiB per step)"}
+
+
+def step_roofline(w: workloads.Workload, step_ms: float, p16_tflops: float) -> dict:
+    """The step's combined roofline, t_roof = 12 BHN^2d / P_int + 2 BHN^2d / P_16 (x 1/2 causal),
+    read two ways: P_int = the fp16 tcgen05 peak (the instruction the integer GEMMs execute, the
+    honest figure) and P_int = the measured legacy INT8 mma.sync rate (the literal INT8 reading)."""
+    unit = w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
+    t16 = 14.0 * unit / (p16_tflops * 1e12) * 1e3
+    t8 = (12.0 * unit / (INT8_MMA_SYNC_TOPS * 1e12) + 2.0 * unit / (p16_tflops * 1e12)) * 1e3
+    return {"fp16_reading": {"p_int_tflops": p16_tflops, "t_roof_ms": round(t16, 4), "frac": round(t16 / step_ms, 4)},
+            "int8_literal_reading": {"p_int_tops": INT8_MMA_SYNC_TOPS, "t_roof_ms": round(t8, 4),
+                                     "frac": round(t8 / step_ms, 4),
+                                     "caveat": "P_int is the legacy mma.sync s8 rate, 12x below the fp16 tcgen05 "
+                                               "rate that actually runs the integer GEMMs, so this fraction exceeds 1"}}
 
 
 def step_ops(w: workloads.Workload) -> float:
@@ -397,8 +426,15 @@ def run_gpu(args, w: workloads.Workload):
 
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-    peak = peaks.get("bf16_tflops_sustained", 1700.0)
-    peak_src = "measured (bf16_tflops_sustained; fp16 runs at the bf16 rate)" if peaks else "fallback"
+    # the timed region's length decides which measured peak applies: burst for a sub-second region
+    burst = ms_max < BURST_REGION_MS
+    if peaks:
+        peak = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+        peak_src = (f"of measured ({'bf16_tflops, burst' if burst else 'bf16_tflops_sustained'}: timed region "
+                    f"{ms_max:.0f} ms; fp16 runs at the bf16 rate)")
+    else:
+        peak = 1900.0 if burst else 1700.0
+        peak_src = f"of fallback ({'burst' if burst else 'sustained'})"
     bwd_tflops = bwd_ops(w) / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else 0.0
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     quant_gbs = quant_bytes(w) / (quant_ms * 1e-3) / 1e9
@@ -414,9 +450,7 @@ def run_gpu(args, w: workloads.Workload):
         "dtype": ("e4m3" if args.fp8 else "s8") + " codes as f16 (f32 accumulate); dP "
                  + ("s8 codes (ablation)" if args.dp_int8 else "f16"),
         "data": "synthetic",
-        "config": {"workload": f"{w.name} {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "smooth_k": True, "smooth_q": w.smooth_q,
-                   "per_rank": "own batch", "l2": f"inputs larger than L2 (Q,K,V,dO = {8 * w.B * w.H * w.N * w.d // 2**20} MiB per step)"},
+        "config": config_of(w),
         "roofline": {"kernel": "sage_attn_bwd call (bwd prologue + tcgen05 backward kernel)",
                      "bound": "tensor", "achieved": round(bwd_tflops, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
@@ -427,6 +461,7 @@ def run_gpu(args, w: workloads.Workload):
                           "gbs": round(quant_gbs, 1), "peak_gbs": hbm_peak,
                           "frac": round(quant_gbs / hbm_peak, 4)},
         "step_frac_of_fp16_peak": round(value / world / peak, 4),
+        "step_roofline": step_roofline(w, ms_max / args.steps, peak),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "mode": "pinned host buffers; copies of step k+1 in and step k-1 out overlap step k"},
@@ -544,20 +579,22 @@ def regime_sample(w: workloads.Workload, seed: int = 0, rows: int = 128) -> dict
 
 
 def cpu_baseline_subprocess(w: workloads.Workload, q_blocks, kv_blocks, label: str, fn: str = "oracle_sample") -> dict:
-    """Run the oracle in a fresh interpreter (single BLAS thread) and describe the sample."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    """Run the oracle in a fresh interpreter with one BLAS thread per host core this process may use,
+    and describe the sample."""
+    n = str(HOST_CORES)
+    env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n)
     code = ("import json, sys; sys.path.insert(0, %r); import bench, workloads; "
             "w = workloads.get(%r, causal=%r); s, ops = bench.%s(w, %r, %r); "
             "print(json.dumps({'s': s, 'ops': ops, 'regime': bench.regime_sample(w)}))"
             % (ROOT, w.name, w.causal, fn, q_blocks, kv_blocks))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label,
+        return {"value": None, "unit": UNIT, "cores": HOST_CORES, "kind": "oracle", "sample": label,
                 "error": r.stderr[-300:]}
     out = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": round(out["ops"] / out["s"] / 1e12, 8), "unit": UNIT, "cores": 1,
-            "kind": "oracle", "sample": label, "seconds": round(out["s"], 2),
-            "host_cores_available": len(os.sched_getaffinity(0)), "regime": out["regime"]}
+    return {"value": round(out["ops"] / out["s"] / 1e12, 8), "unit": UNIT, "cores": HOST_CORES,
+            "threads": f"BLAS threads = {HOST_CORES} (the host cores this process may use)",
+            "kind": "oracle", "sample": label, "seconds": round(out["s"], 2), "regime": out["regime"]}
 
 
 def run_reference(args, w: workloads.Workload):
@@ -582,8 +619,9 @@ def run_reference(args, w: workloads.Workload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (f32 codes)",
         "data": "synthetic",
-        "config": {"workload": f"{w.name} {w.tag}", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
-        "cpu_baseline": {"value": round(value, 8), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": label},
+        "config": config_of(w),
+        "cpu_baseline": {"value": round(value, 8), "unit": UNIT, "cores": HOST_CORES, "kind": "oracle",
+                         "sample": label, "threads": f"BLAS threads = {HOST_CORES}"},
         "e2e": {"value": round(value, 8), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

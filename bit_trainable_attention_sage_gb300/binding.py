@@ -105,6 +105,8 @@ def lib() -> ctypes.CDLL:
     L.sage_quantize_noalloc_max_partials.restype = sz
     L.sage_quantize_noalloc_partials_needed.argtypes = [P]
     L.sage_quantize_noalloc_partials_needed.restype = sz
+    L.sage_quantize_smooth_noalloc.argtypes = [P] + [vp] * 12
+    L.sage_quantize_smooth_noalloc.restype = ci
     _lib = L
     return L
 
@@ -458,8 +460,6 @@ def sage_quantize_smooth_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
                         dt, smooth_k, smooth_q, fp8)
     L = lib()
     fn = L.sage_quantize_smooth_noalloc
-    fn.argtypes = [ctypes.POINTER(SageParams)] + [ctypes.c_void_p] * 12
-    fn.restype = ctypes.c_int
     p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
     st = fn(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(out.Qh), _ptr(out.Kh), _ptr(out.Vh),
             _ptr(out.sQ), _ptr(out.sK), _ptr(out.sV), _ptr(out.muK), _ptr(out.muQ), _stream(stream))

@@ -39,18 +39,22 @@
 //   warp 13     TMEM allocation and the single MMA-issuing thread.
 //   warp 14     TMA producer of the dO^ codes (one stage).
 //
-// Numerics (the CPU oracle mirrors these float32 steps):
+// Numerics.  The method's steps are S = fl32(acc c), P = fl32(2^fl32(S - L2)) and per tile
+// code = rne(fl32(x fl32(1/s))); the kernel forms fl32(acc c - L2) with one rounding, 2^x by the
+// hardware approximation, and the code by rounding the exact product x * fl32(1/s), which differs
+// from rne(fl32(x * inv)) only within |x * inv| 2^-24 of a half-integer.  A code can therefore
+// differ from the method's only where x / s lies within rounding distance of a half-integer:
 //   c = fl32(fl32(sQ sK) * fl32(log2(e)/sqrt(d)));  L2 = fl32(L * fl32(log2(e)))
 //   P = fl32(ex2(fl32(acc * c - L2)))   (with Q-smoothing ex2(fl32(fl32(acc * c + bias) - L2)))
 //   dS = fl32(P * fl32(dP - D))
-//   per 64x64 tile: s = fl32(max|x| / 127), code = rne16(fl32(x * fl32(1/s) + 1536)) - 1536;
-//   max|x| < 2^-120 -> zero tile
+//   per 64x64 tile: s = fl32(max|x| / 127), code = rne(x * fl32(1/s)) (the exact product rounded
+//   once, codes2); max|x| < 2^-120 -> zero tile
 // Attn-QAT variant ("Attn-QAT: 4-Bit Attention With Quantization-Aware Training", technical
 // summary, sections 2.2-2.3): every operand is a 16-bit value of the input type -- the
 // fake-quantised Q', K', V' and the plain dO (also the B operand of dV) -- and the scales are 1:
 //   P  = fl32(ex2(fl32(acc c - L2))), D from the high-precision O', dS = fl32(P fl32(dP - D))
 //        rounded to the input type (A operand of dK, B operand of dQ);
-//   P^ = the forward's quantised P rebuilt: e = ex2(fl32(acc c - r)) with the forward's row
+//   P^ = the forward's quantised P rebuilt: e = ex2(fl32(fl32(acc c) - r)) with the forward's row
 //        maximum r of this (key block, query), phi(e) one-level NVFP4 over the 16 keys of a block
 //        (16 lanes of a warp), P^ = rnd16(fl32(phi(e) fl32(ex2(fl32(r - L2))))) (A of dV).
 // A short pass over S^T forms each 16-key block's scale once (a reduce-scatter of the block
@@ -58,6 +62,13 @@
 // Nothing waits for a tile maximum, so no barrier joins the score warps.
 #include "sage_device.cuh"
 #include "sage_internal.h"
+
+// Test builds only (default 0): the TMA producer never issues step 1's Q^ block, so nothing
+// ever arrives on that stage's barrier and the bounded waits run out.  The library's timeout
+// test builds a copy of the library with this set and a short SAGE_WAIT_CYCLES.
+#ifndef SAGE_TEST_SKIP_Q_ARRIVAL
+#define SAGE_TEST_SKIP_Q_ARRIVAL 0
+#endif
 
 namespace sage {
 
@@ -149,20 +160,15 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
                  : "memory");
 }
 
-// Two tile codes packed as fp16: rne16(fl32(x * inv + 1536)) - 1536 (inv = 0 for a zero tile).
-// Values x * inv lie in [-127, 127], so x * inv + 1536 lies in [1024, 2048) where fp16 spacing is
-// 1: the fp16 conversion rounds to an integer and the subtraction is exact.
+// Two tile codes packed as fp16: the nearest integer (ties to even) to x * inv (inv = 0 for a zero
+// tile).  fl32(x * inv + 1.5 * 2^23) rounds the exact product to an integer in one rounding (the
+// float32 spacing is 1 there, and |x * inv| <= 127 * (1 + 2^-23)); the subtraction is exact and the
+// integer converts to fp16 exactly.
 __device__ __forceinline__ uint32_t codes2(float x0, float x1, float inv) {
-    const f2 y = fma2(f2{x0, x1}, f2{inv, inv}, f2{1536.0f, 1536.0f});
-    const float y0 = y.x, y1 = y.y;
-    uint32_t r;
-    // cvt packs its first source into the upper half; 0x6600 is 1536 in fp16
-    asm("{\n\t.reg .b32 t;\n\t"
-        "cvt.rn.f16x2.f32 t, %2, %1;\n\t"
-        "sub.rn.f16x2 %0, t, %3;\n\t}"
-        : "=r"(r)
-        : "f"(y0), "f"(y1), "r"(0x66006600u));
-    return r;
+    constexpr float kRound = 12582912.0f;          // 1.5 * 2^23
+    const f2 y = fma2(f2{x0, x1}, f2{inv, inv}, f2{kRound, kRound});
+    const f2 q = sub2(y, f2{kRound, kRound});
+    return pack_half2(q.x, q.y);
 }
 
 // FP8 variant: two E4M3 tile codes e4m3(fl32(x * inv)) as fp16 values (inv = 0 for a zero tile)
@@ -258,7 +264,7 @@ template <bool EDGE, bool BIAS, bool DUMP, bool DP8>
 __device__ __forceinline__ void score_pass1(uint32_t s_col, uint32_t dp_col, const float *L2s,
                                             const float *Ds, float cq, float bias, int qlo,
                                             bool key_ok, float dps, float &mp, float &md, float &cs,
-                                            int32_t *dump_col0, int N) {
+                                            int32_t *dump_col0, float *dump_dp0, int N) {
     score_walk(s_col, dp_col, L2s, Ds, [&](const uint32_t(&sr)[8], const uint32_t(&dr)[8], const RowData8 &rd, int col0) {
         float pv[8], ds[8];
         score_p_ds_8<EDGE, BIAS, DP8>(sr, dr, rd, col0, cq, bias, qlo, key_ok, dps, pv, ds);
@@ -267,8 +273,11 @@ __device__ __forceinline__ void score_pass1(uint32_t s_col, uint32_t dp_col, con
             mp = fmaxf(mp, pv[k]);
             md = fmaxf(md, fabsf(ds[k]));
             if (BIAS) cs += ds[k];
-            if (DUMP && key_ok && (!EDGE || col0 + k >= qlo))
+            if (DUMP && key_ok && (!EDGE || col0 + k >= qlo)) {
                 dump_col0[static_cast<size_t>(col0 + k) * N] = static_cast<int32_t>(__uint_as_float(sr[k]));
+                dump_dp0[static_cast<size_t>(col0 + k) * N] =
+                    DP8 ? __fmul_rn(__uint_as_float(dr[k]), dps) : __uint_as_float(dr[k]);
+            }
         }
     });
 }
@@ -313,8 +322,8 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool bf16) {
 }
 
 // Attn-QAT pass A: the NVFP4 block data of every query column for this thread's 16-key block
-// (the 16 lanes of its half-warp).  The block maximum of e = ex2(fl32(acc c - r)) is e of the block
-// maximum of acc (the float32 rounding and ex2 are monotonic), so the lanes first reduce acc:
+// (the 16 lanes of its half-warp).  The block maximum of e = ex2(fl32(fl32(acc c) - r)) is e of the
+// block maximum of acc (the float32 roundings and ex2 are monotonic), so the lanes first reduce acc:
 // a reduce-scatter over the 16 lanes (offsets 8, 4, 2, 1, each step keeping half the columns)
 // leaves lane L with the maxima of columns 2L and 2L + 1 of each 32-column chunk.  Each lane then
 // forms, for its 4 columns, s = e4m3(fl32(max e / 6)), 1/s, g = ex2(fl32(r - L2)) and r, and stores
@@ -357,7 +366,7 @@ __device__ __forceinline__ void qat_block_scales(uint32_t s_col, const float *L2
         const float r = Rs[col];
         float sc = 0.0f, inv = 0.0f, g = 0.0f;
         if (own[t] != -INFINITY) {
-            const float em = ex2_approx(__fmaf_rn(own[t], cq, -r));
+            const float em = ex2_approx(__fsub_rn(__fmul_rn(own[t], cq), r));   // as the forward
             sc = e4m3_round_f(__fdiv_rn(em, 6.0f));
             inv = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
             g = ex2_approx(__fadd_rn(r, L2s[col]));     // L2s holds -L2
@@ -368,7 +377,7 @@ __device__ __forceinline__ void qat_block_scales(uint32_t s_col, const float *L2
 }
 
 // Attn-QAT pass B over the 64 query columns of a block (the staging of score_walk): P and dS as
-// score_p_ds_8; e = ex2(fl32(acc c - r)) (masked to 0 where EDGE says the pair is not live);
+// score_p_ds_8; e = ex2(fl32(fl32(acc c) - r)) (masked to 0 where EDGE says the pair is not live);
 // code = e2m1(fl32(e / s as e fl32(1/s))); P^ = rnd16(fl32((code s) g)), zero where the code is
 // zero (r may be undefined for a pair the forward never visited, all of whose entries are masked).
 // P^ goes to TMEM over read S^T columns, dS to this key's row of the shared dS tile.
@@ -383,8 +392,9 @@ __device__ __forceinline__ void score_pass_qat(uint32_t s_col, uint32_t dp_col, 
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             const float4 q0 = scal[col0 + k], q1 = scal[col0 + k + 1];
-            float x0 = __fmaf_rn(__uint_as_float(sr[k]), cq, -q0.w);
-            float x1 = __fmaf_rn(__uint_as_float(sr[k + 1]), cq, -q1.w);
+            // e as the forward formed it: fl32(fl32(acc c) - r)
+            float x0 = __fsub_rn(__fmul_rn(__uint_as_float(sr[k]), cq), q0.w);
+            float x1 = __fsub_rn(__fmul_rn(__uint_as_float(sr[k + 1]), cq), q1.w);
             if (EDGE) {
                 x0 = (key_ok && col0 + k >= qlo) ? x0 : -INFINITY;
                 x1 = (key_ok && col0 + k + 1 >= qlo) ? x1 : -INFINITY;
@@ -406,8 +416,12 @@ __device__ __forceinline__ void score_pass_qat(uint32_t s_col, uint32_t dp_col, 
 // products in R_A (thread = d column, TMEM columns = query rows): the scaled sum is added to
 // global dQ by float32 reductions, one row at a time, so a warp's 32 lanes cover 32 consecutive
 // floats of the row.  R_A is released once read.
+// With DUMP the raw integer products of key block 0 and 1 also go to dump_g0 / dump_g1 (element
+// [q][tq] of the tile's 64 x 128 product, or NULL for a key block past N).
+template <bool DUMP>
 __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, float sg0, float sg1,
-                                               int tq, float *dq_rows, uint64_t *aq_free) {
+                                               int tq, float *dq_rows, uint64_t *aq_free,
+                                               int32_t *dump_g0, int32_t *dump_g1) {
     float *dst = dq_rows + (32 * half) * 128 + tq;
 #pragma unroll 1
     for (int r0 = 0; r0 < 32; r0 += 8) {
@@ -415,6 +429,14 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
         tmem_ld8(lane_base + R_A + 32 * half + r0, v0);
         tmem_ld8(lane_base + R_A + 64 + 32 * half + r0, v1);
         tmem_wait_ld_regs(v0, v1);
+        if (DUMP) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int q = 32 * half + r0 + k;
+                if (dump_g0) dump_g0[q * 128] = static_cast<int32_t>(__uint_as_float(v0[k]));
+                if (dump_g1) dump_g1[q * 128] = static_cast<int32_t>(__uint_as_float(v1[k]));
+            }
+        }
         float dq[8];
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
@@ -484,6 +506,7 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
                         bulk_load(s.Rs[s3][g], a.R + (static_cast<size_t>(bh) * nblk + min(2 * jt + g, nblk - 1)) * N + q0,
                                   64 * 4, &s.meta_full[s3]);
                 last_meta[s3] = c;
+                if (SAGE_TEST_SKIP_Q_ARRIVAL && c == 1) continue;
                 if (c >= 3 && !mbar_wait(&s.q_free[s3], (c / 3 - 1) & 1, abort_flag, &g_bwd_err, 3)) break;
                 mbar_arrive_expect_tx(&s.q_full[s3], kBlkBytes);
                 for (int dc = 0; dc < D / 64; ++dc) tma_load_3d(s.qc[s3][dc], mapQ, &s.q_full[s3], 64 * dc, q0, bh);
@@ -653,10 +676,10 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
             const int b = c & 1, m3 = c % 3;
             const int qlo = a.causal ? max(0, key - q0) : 0;
             const bool edge = (a.causal && q0 < k0 + 128) || k0 + 128 > N;
-            if (!mbar_wait(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19)) break;
-            if (!mbar_wait(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20)) break;
+            if (!mbar_wait_warp(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19)) break;
+            if (!mbar_wait_warp(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20)) break;
             tc_fence_after();
-            if (D != 128 && c >= 2 && !mbar_wait(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
+            if (D != 128 && c >= 2 && !mbar_wait_warp(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
             const uint32_t s_col = lane_base + 128 * b;
             uint8_t *dss_row = s.dss[b] + tq * 128;
             float4 *scal = s.qscal[tq >> 4];
@@ -689,6 +712,7 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const float *sdOh = a.sdO + static_cast<size_t>(bh) * nblk;
     const float sv = (DPK == kDpInt8 && key_ok) ? a.sV[static_cast<size_t>(bh) * nblk + kblk] : 0.0f;
     float sdo_next = DPK == kDpInt8 ? sdOh[c_first] : 0.0f;
+    bool alive = true;                               // false once one of this warp's waits gave up
     for (int c = 0; c < n; ++c) {
         const int qb = c_first + c;
         const int q0 = 64 * qb;
@@ -703,31 +727,43 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         }
         const int qlo = a.causal ? max(0, key - q0) : 0;
         const bool edge = (a.causal && q0 < k0 + 128) || k0 + 128 > N;
-        if (!mbar_wait(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19)) break;
-        if (!mbar_wait(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20)) break;
-        tc_fence_after();
+        // A warp whose wait gave up still takes part in this step's tile-maximum barrier, with a
+        // negative maximum as its flag (P maxima are never negative): after the barrier all four
+        // warps read the same four slots and leave the loop together.  A warp leaving alone would
+        // leave the others blocked at the barrier.
+        const bool ok = alive && mbar_wait_warp(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19) &&
+                        mbar_wait_warp(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20);
         const uint32_t s_col = lane_base + 128 * b;
         float mp = 0.0f, md = 0.0f, cs = 0.0f;
-        int32_t *dump_s0 = DUMP ? a.dump_s + (bhN + q0) * N + key : nullptr;
-        if (edge)
-            score_pass1<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
-                                                          key_ok, dps, mp, md, cs, dump_s0, N);
-        else
-            score_pass1<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
-                                                           key_ok, dps, mp, md, cs, dump_s0, N);
-        // tile maxima of (this query block, this key block): over the 32 lanes, then over the
-        // two warps of the key block.  Both are non-negative floats (P >= +0, |dS|), whose bit
-        // patterns order as unsigned integers: one warp-wide integer max each.
-        mp = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mp)));
-        md = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(md)));
+        if (ok) {
+            tc_fence_after();
+            int32_t *dump_s0 = DUMP ? a.dump_s + (bhN + q0) * N + key : nullptr;
+            float *dump_dp0 = DUMP ? a.dump_dp + (bhN + q0) * N + key : nullptr;
+            if (edge)
+                score_pass1<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                                              key_ok, dps, mp, md, cs, dump_s0, dump_dp0, N);
+            else
+                score_pass1<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                                               key_ok, dps, mp, md, cs, dump_s0, dump_dp0, N);
+            // tile maxima of (this query block, this key block): over the 32 lanes, then over the
+            // two warps of the key block.  Both are non-negative floats (P >= +0, |dS|), whose bit
+            // patterns order as unsigned integers: one warp-wide integer max each.
+            mp = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mp)));
+            md = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(md)));
+        }
         if (lane_id() == 0) {
-            s.red[warp][c & 1][0] = mp;
+            s.red[warp][c & 1][0] = ok ? mp : -1.0f;
             s.red[warp][c & 1][1] = md;
         }
         if (BIAS) s.colsum[c & 3][tq] = cs;
         named_bar_sync(1, 128);
+        // a slot [w][c & 1] is written again only at step c + 2, after every warp has passed the
+        // barrier of step c + 1 and so has read it here
+        const float f0 = s.red[0][c & 1][0], f1 = s.red[1][c & 1][0];
+        const float f2 = s.red[2][c & 1][0], f3 = s.red[3][c & 1][0];
+        if (fminf(fminf(f0, f1), fminf(f2, f3)) < 0.0f) break;
         const int w0 = warp & ~1;
-        const float mxp = fmaxf(s.red[w0][c & 1][0], s.red[w0 + 1][c & 1][0]);
+        const float mxp = w0 == 0 ? fmaxf(f0, f1) : fmaxf(f2, f3);
         const float mxd = fmaxf(s.red[w0][c & 1][1], s.red[w0 + 1][c & 1][1]);
         // FP8: s = max/448, and a tile below 2^-110 is zero so that 1/s stays finite
         constexpr float kZero = FP8 ? kTileZeroFp8 : kTileZero;
@@ -748,7 +784,11 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         // the dQ MMAs that read this dS^ tile two steps ago must be done: d = 128 they ran before
         // this step's S^T / dP^T (the tensor pipe runs in issue order), d = 64 they are those of
         // the previous step pair
-        if (D != 128 && c >= 2 && !mbar_wait(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) break;
+        // (a warp giving up here skips pass 2; the flag of its next step ends the loop for all four)
+        if (D != 128 && c >= 2 && !mbar_wait_warp(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) {
+            alive = false;
+            continue;
+        }
         int16_t *dump_p0 = DUMP ? a.dump_p + (bhN + q0) * N + key : nullptr;
         int16_t *dump_ds0 = DUMP ? a.dump_ds + (bhN + q0) * N + key : nullptr;
         uint8_t *dss_row = s.dss[b] + tq * 128;
@@ -808,15 +848,22 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
         const float sdo = sdo_next;
         if (!QAT && c + 1 < n) sdo_next = sdOh[qb + 1];
         // dV += s_P s_dO (P^T dO^)
-        if (!mbar_wait(&s.a_full, c & 1, abort_flag, &g_bwd_err, 23)) break;
+        if (!mbar_wait_warp(&s.a_full, c & 1, abort_flag, &g_bwd_err, 23)) break;
         tc_fence_after();
         {
             const float sc = QAT ? 1.0f : __fmul_rn(s.sps[z][kb], sdo);
+            int32_t *dump_row = (DUMP && key_ok)
+                ? a.dump_dv + (((static_cast<size_t>(bh) * nblk + qb) * nblk + 2 * jt + kb) * 64 + (tq & 63)) * D
+                : nullptr;
 #pragma unroll
             for (int cc = 0; cc < D; cc += 8) {
                 uint32_t r[8];
                 tmem_ld8(lane_base + R_A + cc, r);
                 tmem_wait_ld_regs(r);
+                if (DUMP && dump_row) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dump_row[cc + k] = static_cast<int32_t>(__uint_as_float(r[k]));
+                }
 #pragma unroll
                 for (int k = 0; k < 8; k += 2) {
                     const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(r[k]), __uint_as_float(r[k + 1])},
@@ -832,16 +879,22 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
         if (D == 128) {
             // dQ rows 0-31 of this step: both key blocks' products, each scaled by its own
             // s_dS s_K / sqrt(d), summed
-            if (!mbar_wait(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 24)) break;
+            if (!mbar_wait_warp(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 24)) break;
             tc_fence_after();
             const float sg0 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
             const float sg1 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
-            dq_consume_128(lane_base, 0, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free);
+            int32_t *dq0 = nullptr, *dq1 = nullptr;
+            if (DUMP) {
+                const size_t t0 = (static_cast<size_t>(bh) * nblk + qb) * nblk + 2 * jt;
+                if (k0 < N) dq0 = a.dump_dq + t0 * 64 * D + tq;
+                if (k0 + 64 < N) dq1 = a.dump_dq + (t0 + 1) * 64 * D + tq;
+            }
+            dq_consume_128<DUMP>(lane_base, 0, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free, dq0, dq1);
         } else if ((c & 1) || c == n - 1) {
             // d = 64, step pair (c - 1, c) (or the last step alone): thread = query row of the
             // pair, vector atomics along the row
             const int pr = c >> 1;
-            if (!mbar_wait(&s.rq_full, pr & 1, abort_flag, &g_bwd_err, 25)) break;
+            if (!mbar_wait_warp(&s.rq_full, pr & 1, abort_flag, &g_bwd_err, 25)) break;
             tc_fence_after();
             const int zq = (2 * pr + (tq >> 6)) & (kScaleSlots - 1);
             const int qrow = 64 * (c_first + 2 * pr) + tq;
@@ -855,6 +908,15 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
                 tmem_ld8(lane_base + R_Q + cc, r0);
                 tmem_ld8(lane_base + R_Q + 64 + cc, r1);
                 tmem_wait_ld_regs(r0, r1);
+                if (DUMP && live) {
+                    const size_t t0 = (static_cast<size_t>(bh) * nblk + c_first + 2 * pr + (tq >> 6)) * nblk + 2 * jt;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (k0 < N) a.dump_dq[(t0 * 64 + (tq & 63)) * D + cc + e] = static_cast<int32_t>(__uint_as_float(r0[e]));
+                        if (k0 + 64 < N)
+                            a.dump_dq[((t0 + 1) * 64 + (tq & 63)) * D + cc + e] = static_cast<int32_t>(__uint_as_float(r1[e]));
+                    }
+                }
                 if (live) {
 #pragma unroll
                     for (int k = 0; k < 8; k += 4) {
@@ -918,15 +980,22 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
         const float sq = sq_next;
         if (!QAT && c + 1 < n) sq_next = sQh[qb + 1];
         // dK += s_dS s_Q / sqrt(d) (dS^T Q^)   (+ Q-smoothing bias (dS^T 1) mu_Q / sqrt(d))
-        if (!mbar_wait(&s.b_full, c & 1, abort_flag, &g_bwd_err, 30)) break;
+        if (!mbar_wait_warp(&s.b_full, c & 1, abort_flag, &g_bwd_err, 30)) break;
         tc_fence_after();
         {
             const float sc = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][kb], sq), a.inv_sqrt_d);
+            int32_t *dump_row = (DUMP && key_ok)
+                ? a.dump_dk + (((static_cast<size_t>(bh) * nblk + qb) * nblk + 2 * jt + kb) * 64 + (tq & 63)) * D
+                : nullptr;
 #pragma unroll
             for (int cc = 0; cc < D; cc += 8) {
                 uint32_t r[8];
                 tmem_ld8(lane_base + R_B + cc, r);
                 tmem_wait_ld_regs(r);
+                if (DUMP && dump_row) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dump_row[cc + k] = static_cast<int32_t>(__uint_as_float(r[k]));
+                }
 #pragma unroll
                 for (int k = 0; k < 8; k += 2) {
                     const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(r[k]), __uint_as_float(r[k + 1])},
@@ -947,11 +1016,17 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
         if (lane_id() == 0) mbar_arrive(&s.b_free);
         if (D == 128) {
             // dQ rows 32-63 of this step
-            if (!mbar_wait(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 31)) break;
+            if (!mbar_wait_warp(&s.aq_full, c & 1, abort_flag, &g_bwd_err, 31)) break;
             tc_fence_after();
             const float sg0 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][0], skb[0]), a.inv_sqrt_d);
             const float sg1 = QAT ? a.inv_sqrt_d : __fmul_rn(__fmul_rn(s.sds[z][1], skb[1]), a.inv_sqrt_d);
-            dq_consume_128(lane_base, 1, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free);
+            int32_t *dq0 = nullptr, *dq1 = nullptr;
+            if (DUMP) {
+                const size_t t0 = (static_cast<size_t>(bh) * nblk + qb) * nblk + 2 * jt;
+                if (k0 < N) dq0 = a.dump_dq + t0 * 64 * D + tq;
+                if (k0 + 64 < N) dq1 = a.dump_dq + (t0 + 1) * 64 * D + tq;
+            }
+            dq_consume_128<DUMP>(lane_base, 1, sg0, sg1, tq, a.dQ + (bhN + q0) * D, &s.aq_free, dq0, dq1);
         }
     }
     if (key_ok && !*abort_flag) {

@@ -147,11 +147,14 @@ struct BwdDump {
     float *sp, *sds;
     int8_t *doh;
     float *sdO, *D;
+    float *dp;
+    int32_t *dv, *dq, *dk;
 };
 static BwdDump bwd_dump(const sage_params &p, void *w, size_t *bytes) {
     Carve c(w);
     BwdDump r;
     const size_t nn = rows(p) * p.N;
+    const size_t prod = nblocks(p) * (p.N / 64) * 64 * p.d;    // one 64 x d product per tile
     r.s = c.take<int32_t>(nn);
     r.p = c.take<int16_t>(nn);
     r.ds = c.take<int16_t>(nn);
@@ -160,6 +163,10 @@ static BwdDump bwd_dump(const sage_params &p, void *w, size_t *bytes) {
     r.doh = c.take<int8_t>(elems(p));
     r.sdO = c.take<float>(nblocks(p));
     r.D = c.take<float>(rows(p));
+    r.dp = c.take<float>(nn);
+    r.dv = c.take<int32_t>(prod);
+    r.dq = c.take<int32_t>(prod);
+    r.dk = c.take<int32_t>(prod);
     if (bytes) *bytes = c.off;
     return r;
 }
@@ -445,6 +452,7 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     a.dQ = dQ; a.dK = dK; a.dV = dV;
     if (p->flags & SAGE_FLAG_DUMP) {
         a.dump_s = dd.s; a.dump_p = dd.p; a.dump_ds = dd.ds; a.dump_sp = dd.sp; a.dump_sds = dd.sds;
+        a.dump_dp = dd.dp; a.dump_dv = dd.dv; a.dump_dq = dd.dq; a.dump_dk = dd.dk;
         SAGE_CUDA(cudaMemcpyAsync(dd.sdO, w.sdO, nblocks(*p) * sizeof(float), cudaMemcpyDeviceToDevice, st));
         SAGE_CUDA(cudaMemcpyAsync(dd.D, w.D, rows(*p) * sizeof(float), cudaMemcpyDeviceToDevice, st));
     }

@@ -111,6 +111,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Warp-wide bounded wait: every lane of the warp calls it and all get the same answer (false if
+// any lane's wait gave up).  The lanes of a waiting warp may leave the sleeping wait at different
+// times, and a warp whose lanes disagreed would split before its next warp-collective instruction
+// (a tcgen05.ld / st .sync.aligned, a named barrier); the vote keeps the warp whole.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               unsigned int *err_word, uint32_t where) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err_word, where));
+}
+
 // Bounded wait that ignores the abort flag: used to drain a CTA's own copies and MMAs in flight
 // before it frees its shared and tensor memory.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,

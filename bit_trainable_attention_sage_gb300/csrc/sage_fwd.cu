@@ -25,12 +25,17 @@
 // While one warpgroup turns S into codes the tensor core works on the other tile, so the two
 // softmax warpgroups and the MMA pipe overlap.  TMEM: all 512 columns; one CTA per SM.
 
-// Numerics (the CPU oracle mirrors these float32 steps):
+// Numerics (the method's steps, with 2^x by the hardware approximation: a code can therefore
+// differ from the one exact powers give only where 127 * 2^x lies within rounding distance of a
+// half-integer).  The logit is rounded before r is subtracted, as the method forms S and then
+// exponentiates S - r: fusing the two roundings moved the row sums l by up to 1e-5 relative at
+// logits near 500 (sigma = 10 inputs), enough to change the 16-bit O and, through
+// D = rowsum(dO o O), the backward's gradients by more than 1e-3.
 //   c   = fl32(fl32(sQ_i sK_j) * fl32(log2(e)/sqrt(d)))
-//   r   = fl32(max_k(acc_k) * c)                 (row max of the 64-key block, log2 units)
-//   x_k = fl32(acc_k * c - r)                    (one rounding: fused multiply-add)
-//   P^_k = rint(fl32(127 * ex2(x_k)))            (round half to even)
-//   with Q-smoothing: t_k = fl32(acc_k * c + bias_k), r = max t_k, x_k = fl32(t_k - r)
+//   S_k = fl32(acc_k * c);  r = max_k S_k = fl32(max_k(acc_k) * c)   (64-key block, log2 units)
+//   x_k = fl32(S_k - r)
+//   P^_k = rint(127 * ex2(x_k))                  (the exact product, round half to even)
+//   with Q-smoothing: S_k = fl32(fl32(acc_k * c) + bias_k), r = max S_k
 //   l <- 2^(m - m') l + 2^(r - m') sum_k ex2(x_k);  O <- 2^(m - m') O + (2^(r - m') / 127) s_V PV
 //   O_out = O / l;  L = (m + log2 l) ln 2
 // FP8 variant (SAGE_FLAG_FP8, "SageAttention3 ..." (review), INT8 vs FP8 training): the codes are
@@ -123,7 +128,7 @@ __device__ __forceinline__ float fwd_row_max(uint32_t (&raw)[64], float c, const
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float acc = __uint_as_float(raw[k + e]);
-            v[e] = BIAS ? __fmaf_rn(acc, c, bias[k + e]) : acc;
+            v[e] = BIAS ? __fadd_rn(__fmul_rn(acc, c), bias[k + e]) : acc;   // S = fl32(fl32(acc c) + b)
             if (BIAS) raw[k + e] = __float_as_uint(v[e]);
             if (MASKED) v[e] = (k + e < nvalid) ? v[e] : -INFINITY;
         }
@@ -133,18 +138,25 @@ __device__ __forceinline__ float fwd_row_max(uint32_t (&raw)[64], float c, const
     return fmaxf(rp[0], rp[1]);
 }
 
-// Codes of a 64-key block: P^ = rint(fl32(127 ex2(x))), x = fl32(acc c - r) (or with Q-smoothing
-// fl32(t - r), t = fl32(acc c + bias) left in `raw` by the row maximum), packed as fp16 pairs into
-// the 32 TMEM columns at `code_col`;
-// returns the row sum of ex2(x) (four partial sums).  rint is done with the float32 add of
-// 1.5 * 2^23 and its subtraction (exact for the values 0..127 here, and a full-rate instruction,
-// unlike the conversion unit's round-to-integer).
+// Codes of a 64-key block: P^ = rint(fl32(127 ex2(x))), x = fl32(S - r) with the logit
+// S = fl32(acc c) (with Q-smoothing S = fl32(fl32(acc c) + bias), left in `raw` by the row
+// maximum), packed as fp16 pairs into the 32 TMEM columns at `code_col`;
+// returns the row sum of ex2(x) (four partial sums).  rint is a fused multiply-add of 1.5 * 2^23
+// (float32 spacing 1 there, so the exact product 127 ex2(x) is rounded to an integer once) and an
+// exact subtraction: full-rate instructions, unlike the conversion unit's round-to-integer.  This
+// differs from rint(fl32(127 ex2(x))) only within 127 ex2(x) 2^-24 of a half-integer.
 // FP8: P^ = e4m3(fl32(448 ex2(x))) instead, converted to fp16 in two instructions per pair.
 // FP4: each 16-key group is an NVFP4 block of v = fl32(2688 ex2(x)) (two passes over the group:
 // its maximum, then the codes), written as the dequantised fp16 values.
 constexpr int kFmtInt8 = 0, kFmtFp8 = 1, kFmtFp4 = 2, kFmtQat = 3, kFmtQatHp = 4;
 // formats whose block scales live inside the dequantised operands: c = log2(e)/sqrt(d) alone
 __host__ __device__ constexpr bool scales_inside(int fmt) { return fmt == kFmtFp4 || fmt == kFmtQat || fmt == kFmtQatHp; }
+
+// The logits S = fl32(acc c) of a column pair, rounded on their own.  The code generator contracts
+// a multiply followed by an add into one fused multiply-add even when both are packed .rn
+// instructions (measured: the forward's O then matched the one-rounding form bit for bit), so the
+// product is formed as a fused multiply-add with a zero addend, which it leaves alone.
+__device__ __forceinline__ f2 logit2(f2 a, f2 c) { return fma2(a, c, f2{0.0f, 0.0f}); }
 
 // an fp16 pair -> the same values as a bf16 pair (exact for the fake-quantised P values)
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
@@ -169,7 +181,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
                 const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
-                f2 x2 = fma2(a2, c2, nrs2);
+                f2 x2 = add2(logit2(a2, c2), nrs2);            // fl32(fl32(acc c) - r)
                 if (MASKED) {
                     x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
                     x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
@@ -200,7 +212,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
                 const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
-                f2 x2 = BIAS ? sub2(a2, rs2) : fma2(a2, c2, nrs2);
+                f2 x2 = BIAS ? sub2(a2, rs2) : add2(logit2(a2, c2), nrs2);   // fl32(S - r), S = fl32(acc c)
                 if (MASKED) {
                     x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
                     x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
@@ -224,7 +236,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
             for (int k = 0; k < 16; k += 2) {
                 // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
                 const f2 a2{__uint_as_float(raw[cc + k]), __uint_as_float(raw[cc + k + 1])};
-                f2 x2 = BIAS ? sub2(a2, rs2) : fma2(a2, c2, nrs2);
+                f2 x2 = BIAS ? sub2(a2, rs2) : add2(logit2(a2, c2), nrs2);   // fl32(S - r), S = fl32(acc c)
                 if (MASKED) {
                     x2.x = (cc + k < nvalid) ? x2.x : -INFINITY;
                     x2.y = (cc + k + 1 < nvalid) ? x2.y : -INFINITY;
@@ -235,7 +247,7 @@ __device__ __forceinline__ float fwd_codes(const uint32_t (&raw)[64], float c, f
                     const f2 v2 = mul2(k448, e2);
                     pk[k / 2] = e4m3x2_f16x2(v2.x, v2.y);
                 } else {
-                    const f2 p2 = sub2(add2(mul2(k127, e2), kr2), kr2);
+                    const f2 p2 = sub2(fma2(k127, e2, kr2), kr2);   // rint of the exact 127 ex2(x)
                     const float p0 = p2.x, p1 = p2.y;
                     pk[k / 2] = pack_half2(p0, p1);
                     if (DUMP && dump_row) {
@@ -417,7 +429,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         float m = -INFINITY, l = 0.0f;
         int pv_uses = 0;
         for (int j = 0; j < my_steps; ++j) {
-            if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, &g_fwd_err, 10)) break;
+            if (!mbar_wait_warp(&s.s_full[t], j & 1, abort_flag, &g_fwd_err, 10)) break;
             tc_fence_after();
             const bool has_b = 128 * j + 64 < kv_end;
             float r_h0 = -INFINITY, r_h1 = -INFINITY, sum_h0 = 0.0f, sum_h1 = 0.0f;
@@ -490,7 +502,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (h == 1 && !has_b) break;
-                if (!mbar_wait(&s.pv_full[t], pv_uses & 1, abort_flag, &g_fwd_err, 11)) break;
+                if (!mbar_wait_warp(&s.pv_full[t], pv_uses & 1, abort_flag, &g_fwd_err, 11)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D; cc += 32) {

@@ -14,7 +14,7 @@ namespace sage {
 
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e) rounded to float32
 
-// log2(e) / sqrt(d) rounded once to float32 (the double is formed first, as the oracle does)
+// log2(e) / sqrt(d) rounded once to float32 (the double quotient is formed first)
 inline float scale_log2(int d) {
     return static_cast<float>(1.4426950408889634 / __builtin_sqrt(static_cast<double>(d)));
 }
@@ -86,6 +86,10 @@ struct BwdArgs {
     int16_t *dump_ds;     // debug: (B,H,N,N) dS codes
     float *dump_sp;       // debug: (B,H,N/64,N/64) P tile scales
     float *dump_sds;      // debug: (B,H,N/64,N/64) dS tile scales
+    float *dump_dp;       // debug: (B,H,N,N) dP as the score warpgroup uses it
+    int32_t *dump_dv;     // debug: (B,H,N/64,N/64,64,d) integer P^T dO^ block products [i][j][key][c]
+    int32_t *dump_dq;     // debug: (B,H,N/64,N/64,64,d) integer dS^ K^ block products [i][j][q][c]
+    int32_t *dump_dk;     // debug: (B,H,N/64,N/64,64,d) integer dS^T Q^ block products [i][j][key][c]
     const float *R;       // Attn-QAT: the forward's row maxima (B,H,N/64,N), else NULL
     int N, H, causal, dtype;
     float sl2, inv_sqrt_d;

@@ -6,7 +6,7 @@
 // rows of query block i); method steps, forward (2) and backward (1).
 // "SageAttention3 ..." (review), eq. (7).
 //
-// Bit-exact contract (the CPU oracle computes the same thing):
+// Bit-exact contract:
 //   block        = 64 tokens x d
 //   mu           = float64 sum, float64 divide, one rounding to float32
 //   x            = fl32(v - mu)
@@ -15,8 +15,8 @@
 // FP8 variant ("SageAttention3 ..." (review), INT8 vs FP8 training): delta = fl32(max|x| / 448)
 // and code = E4M3(fl32(x / delta)), round to nearest even, saturating at +-448.
 // QK-norm prologue ("SageBwd ..." (structured summary), QK-norm; norm epsilon 1e-6): Q and K rows
-// become y = rnd16(fl32(fl32(x r) gamma_c)), r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))) with
-// S = fl32(exact sum of x^2), before the K-mean, the smoothing and the quantiser see them.
+// become y = rnd16(fl32(fl32(x r) gamma_c)), r the float32 nearest to 1 / sqrt(S / d + eps) with
+// S the exact sum of x^2, before the K-mean, the smoothing and the quantiser see them.
 //
 // All kernels here stream through HBM once; they are bound by memory bandwidth.
 #include "sage_device.cuh"
@@ -123,13 +123,63 @@ struct Sum3 {
     }
 };
 
+// r = the float32 nearest to 1 / sqrt(v), v = S / d + eps, with S = h + l + t the exact sum of
+// squares held as an unevaluated float32 triple and d a power of two.
+//   1. v as a float32 pair vh + vl (two-sums; relative error about 2^-46) and a candidate
+//      r0 = fl32(1 / fl32(sqrt(vh))), within about two ulps of the exact value r*.
+//   2. The residual rho = 1 - r0^2 v in compensated float32: r0^2 = a + b exactly (a two-product
+//      by fused multiply-add), then 1 - a vh, - b vh and - a vl by fused multiply-adds; |rho| is
+//      below about 2^-21 and its error below about 2^-43.
+//   3. r* = r0 (1 - rho)^(-1/2) = r0 (1 + rho/2 + 3 rho^2 / 8 + O(rho^3)), so r* lies
+//      z = (rho/2 + 3 rho^2/8) r0 / ulp(r0) ulps above r0, z known to within about 2^-19.
+//      The nearest float32 is r0 + rint(z) ulp.
+//   4. Where z lies within 2^-16 of a half-integer (about one row in 10 000), or in the corner
+//      cases (|rint(z)| > 2, r0 within four ulps of either end of its binade, v outside
+//      [2^-100, 2^100]), float64 decides:
+//      fl32(1 / sqrt(fl64(S / d + eps))) with the IEEE float64 square root and division.
+__device__ __noinline__ float rsqrt_rn_fallback(float h, float l, float t, int d, float eps) {
+    const double S = (static_cast<double>(h) + static_cast<double>(l)) + static_cast<double>(t);
+    const double v = fma(S, 1.0 / static_cast<double>(d), static_cast<double>(eps));
+    return static_cast<float>(1.0 / sqrt(v));
+}
+
+__device__ __forceinline__ float rsqrt_rn(float h, float l, float t, int d, float eps) {
+    const float inv_d = 1.0f / static_cast<float>(d);              // exact: d = 64 or 128
+    float s1, e1, sh, sl;
+    two_sum(h, l, s1, e1);
+    two_sum(s1, __fadd_rn(e1, t), sh, sl);                         // S = sh + sl
+    sh = __fmul_rn(sh, inv_d);
+    sl = __fmul_rn(sl, inv_d);
+    float a1, b1, vh, vl;
+    two_sum(sh, eps, a1, b1);
+    two_sum(a1, __fadd_rn(b1, sl), vh, vl);                        // v = vh + vl
+    if (!(vh >= 0x1p-100f && vh <= 0x1p100f)) return rsqrt_rn_fallback(h, l, t, d, eps);
+    const float r0 = __frcp_rn(__fsqrt_rn(vh));
+    const float a = __fmul_rn(r0, r0);
+    const float b = __fmaf_rn(r0, r0, -a);                         // r0^2 = a + b
+    float rho = __fmaf_rn(-a, vh, 1.0f);
+    rho = __fmaf_rn(-b, vh, rho);
+    rho = __fmaf_rn(-a, vl, rho);
+    const float rel = __fmaf_rn(__fmul_rn(0.375f, rho), rho, __fmul_rn(0.5f, rho));
+    const uint32_t mant = __float_as_uint(r0) & 0x7FFFFFu;
+    const float z = __fmul_rn(rel, static_cast<float>(mant | 0x800000u));   // r0 / ulp(r0) = 1.mant * 2^23
+    const float k = rintf(z);
+    // candidates and midpoints up to 2.5 ulps away keep r0's spacing when r0 is at least four
+    // ulps from both ends of its binade
+    if (fabsf(__fsub_rn(fabsf(__fsub_rn(z, k)), 0.5f)) < 0x1p-16f || fabsf(k) > 2.0f || mant < 4u ||
+        mant > 0x7FFFFBu)
+        return rsqrt_rn_fallback(h, l, t, d, eps);
+    const float ulp = __uint_as_float(__float_as_uint(r0) & 0x7F800000u) * 0x1p-23f;
+    return __fmaf_rn(k, ulp, r0);                                  // exact: r0 or a neighbour
+}
+
 // QK-norm of this lane's 8 values of a row whose d / 8 slices sit in `lanes` consecutive lanes
 // (every lane of the warp takes part).  The squares of 16-bit values are exact in float32 (bf16:
 // for 2^-63 <= |x| < 2^63).  They are summed as an unevaluated float32 triple h + l + t with
 // two-sums, whose only rounding is in t (relative 2^-65 over a row); a butterfly of the same
-// exact steps leaves the same triple in every lane of the row.  h then becomes fl32(h + l + t),
-// the exact sum rounded once (a tie in h + l is settled by the sign of t).
-// Returns r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))) and replaces v by rnd_T(fl32(fl32(v r) g_c)).
+// exact steps leaves the same triple in every lane of the row.
+// Returns r, the float32 nearest to 1 / sqrt(S / d + eps) (rsqrt_rn), and replaces v by
+// rnd_T(fl32(fl32(v r) g_c)).
 template <typename T>
 __device__ __forceinline__ float qk_norm8(float (&v)[8], const float *gamma, int c0, int lanes,
                                           int d, float eps) {
@@ -151,20 +201,7 @@ __device__ __forceinline__ float qk_norm8(float (&v)[8], const float *gamma, int
         two_sum(l, e1, l, e3);
         t = __fadd_rn(__fadd_rn(__fadd_rn(t, to), e2), e3);
     }
-    // S = h + l + t exactly (up to t's own roundings): round it once to float32
-    {
-        float e;
-        two_sum(l, t, l, t);                      // l = fl32(l + t), t = its error
-        two_sum(h, l, h, e);                      // h = fl32(h + l), e = h + l - h (exact)
-        // h + e on a midpoint between floats: the sign of t decides (S >= 0, h >= 0).  The
-        // midpoint above h lies half an ulp of h's binade away; below a power of two, half that.
-        float half_ulp = __uint_as_float((__float_as_uint(h) & 0x7F800000u)) * 0x1p-24f;
-        if (e < 0.0f && (__float_as_uint(h) & 0x7FFFFFu) == 0u) half_ulp *= 0.5f;
-        if (t != 0.0f && h > 0.0f && fabsf(e) == half_ulp && ((e > 0.0f) == (t > 0.0f)))
-            h = __fadd_rn(h, __fmul_rn(2.0f, e));
-    }
-    const float ms = __fmul_rn(h, 1.0f / static_cast<float>(d));         // exact: d = 64 or 128
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+    const float r = rsqrt_rn(h, l, t, d, eps);
     float g[8] = {1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f};
     if (gamma) {
         *reinterpret_cast<float4 *>(&g[0]) = *reinterpret_cast<const float4 *>(gamma + c0);

@@ -121,9 +121,9 @@ SAGE_API int sage_quantize_smooth(const sage_params *p, const void *Q, const voi
  * scale vector; the reproduction paragraph gives the norm epsilon 1e-6 (added to the mean square).
  *
  * sage_quantize_smooth_qknorm: as sage_quantize_smooth, on the normalised Q and K:
- *   r = fl32(1 / fl32(sqrt(fl32(S / d + eps)))) per token, S = fl32(sum_c x_c^2), the exact sum
- *       rounded once (every step a correctly rounded float32 operation, independent of any
- *       summation order; bf16 inputs need 2^-63 <= |x| < 2^63 or x = 0 for exact squares);
+ *   r = the float32 nearest to 1 / sqrt(S / d + eps) per token, S = sum_c x_c^2 exactly
+ *       (independent of any summation order; bf16 inputs need 2^-63 <= |x| < 2^63 or x = 0 for
+ *       exact squares);
  *   y = rnd(fl32(fl32(x r) * gamma_c)) rounded to the input dtype, so the call equals a separate
  *       norm writing a 16-bit tensor followed by sage_quantize_smooth.  V is not normalised.
  *   Same workspace as sage_quantize_smooth.  With smooth_q = 1, Kn is required and is the K to
@@ -201,9 +201,9 @@ SAGE_API int sage_attn_fwd_fp4(const sage_params *p, const uint8_t *Qc, const ui
  * Out: O  (B,H,N,d) fp16/bf16 (the dtype of p).
  *      L  (B,H,N) float32 natural-log log-sum-exp of the scaled logits S / sqrt(d) as formed
  *         (with K-smoothing these differ from the unsmoothed logits by a per-row constant).
- * Logits: t = acc * fl32(fl32(sQ sK) * fl32(log2(e) / sqrt(d))) in log2 units; P codes are
- * round-half-even of 2^(t - r) * 127 with r the row max over the 64-key tile; the running sum l
- * accumulates the unquantised probabilities.
+ * Logits: S = fl32(acc * fl32(fl32(sQ sK) * fl32(log2(e) / sqrt(d)))) in log2 units; P codes are
+ * round-half-even of fl32(127 * 2^fl32(S - r)) with r the row max of S over the 64-key tile; the
+ * running sum l accumulates the unquantised probabilities.
  * ------------------------------------------------------------------------------------------ */
 SAGE_API size_t sage_fwd_workspace_bytes(const sage_params *p);
 SAGE_API int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, const int8_t *Vh,
@@ -224,8 +224,9 @@ SAGE_API int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t 
  *      L                       (B,H,N) float32 from sage_attn_fwd.
  * Out: dQ, dK, dV              (B,H,N,d) float32, fully overwritten (the library zeroes them).
  * P and dS are quantised per 64x64 tile: s = fl32(max|x| / 127), code = the nearest integer
- * (ties to even) of fl32(x * fl32(1 / s) + 1536), minus 1536; a tile whose max|x| is below
- * 2^-120 is a zero tile.  dO is quantised per 64-token block like Q.  dQ sums the tiles with
+ * (ties to even) to the exact product x * fl32(1 / s) -- the nearest integer to
+ * fl32(x * fl32(1 / s)) except within |x / s| 2^-24 of a half-integer; a tile whose max|x| is
+ * below 2^-120 is a zero tile.  dO is quantised per 64-token block like Q.  dQ sums the tiles with
  * float32 reductions into global memory, so its last bits vary from run to run.
  * ------------------------------------------------------------------------------------------ */
 SAGE_API size_t sage_bwd_workspace_bytes(const sage_params *p);
@@ -283,7 +284,7 @@ SAGE_API int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, c
  *   In: Q, K, V (B,H,N,d) fp16/bf16.  Out: Qf, Kf, Vf (B,H,N,d) same type.
  *
  * sage_qat_fwd -- per 64-key block, r = fl32(max acc * c) (c = fl32(log2(e) / sqrt(d)), acc the
- *   product Q' K'^T), e = ex2(fl32(acc c - r)); P^ = phi(e), phi one-level NVFP4 over 16 keys
+ *   product Q' K'^T), e = ex2(fl32(fl32(acc c) - r)); P^ = phi(e), phi one-level NVFP4 over 16 keys
  *   (s = e4m3(fl32(max e / 6)), code = e2m1(fl32(e fl32(1/s)))); O = sum 2^(r - m) P^ V' / l,
  *   O' = sum 2^(r - m) rnd16(e) V' / l, l the running sum of e.
  *   In: Qf, Kf, Vf from sage_qat_quantize.
@@ -293,7 +294,7 @@ SAGE_API int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q, c
  *
  * sage_qat_bwd -- P = ex2(fl32(acc c - L2)), L2 = fl32(L log2(e)); D = rowsum(dO o O');
  *   dP = dO V'^T; dS = fl32(P fl32(dP - D)) rounded to the input type; P^ = the forward's
- *   phi(ex2(fl32(acc c - r))) times fl32(ex2(fl32(r - L2))), rounded to the input type;
+ *   phi(ex2(fl32(fl32(acc c) - r))) times fl32(ex2(fl32(r - L2))), rounded to the input type;
  *   dV = P^^T dO; dQ = dS K' / sqrt(d); dK = dS^T Q' / sqrt(d) (fake quantisation passes the
  *   gradient straight through: these are the gradients of Q, K and V).
  *   In: Qf, Kf, Vf; Op, L, R from sage_qat_fwd; dO (B,H,N,d) input type.

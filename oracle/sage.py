@@ -221,8 +221,8 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
     """SageBwd forward (steps a3-a6).  Returns (O float64 (B,H,N,d), L float64 (B,H,N)).
 
     ``q_blocks`` limits the query blocks computed (others stay zero), ``heads`` the (b, h) pairs.
-    ``record`` (small N only) receives, per head, the S block products, the float32 logits S, the
-    P^ codes, the float32 values their rounding decides from (P_y) and the P^ V^ block products of
+    ``record`` (small N only) receives, per head, the S block products, the float32 logits S and
+    the products acc c they are rounded from, the P^ codes, the float32 values their rounding decides from (P_y) and the P^ V^ block products of
     every tile (integers for INT8 codes, float64 for E4M3).
     """
     Qh, Kh, Vh = prep["Qh"], prep["Kh"], prep["Vh"]
@@ -240,6 +240,7 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
             rtype = np.int64 if arith.fmt == "int8" else np.float64
             rec["S_int"] = np.zeros((N, N), rtype)
             rec["S"] = np.zeros((N, N), np.float32)
+            rec["acc_c"] = np.zeros((N, N))
             rec["P_hat"] = np.zeros((N, N), rtype)
             rec["P_y"] = np.zeros((N, N), np.float32)
             rec["PV_int"] = {}
@@ -275,6 +276,7 @@ def sage_forward(prep: dict, causal: bool, arith: Arith = QUANTISED, q_blocks=No
                 if record is not None:
                     rec["S_int"][rows, cols] = s_int
                     rec["S"][rows, cols] = S
+                    rec["acc_c"][rows, cols] = np.asarray(s_int, np.float64) * float(c)
                     rec["P_hat"][rows, cols] = p_hat
                     rec["P_y"][rows, cols] = p_y
                     rec["PV_int"][(i, j)] = pv
@@ -297,7 +299,7 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
     checks at large N); by default everything is computed, looping over key/value blocks and,
     inside, query blocks.  ``record`` receives, per head, the per-tile dequantised P, dP and
     dequantised dS, the P and dS codes, the float32 values their rounding decides from (P_y, dS_y),
-    the logits (S_bwd) and the tile scales (sP, sdS); with ``products`` also the integer block
+    the logits (S_bwd) and acc c (acc_c_bwd), and the tile scales (sP, sdS); with ``products`` also the integer block
     products MM(P^^T, dO^_i), MM(dS^, K^_j) and MM(dS^^T, Q^_i) of every tile (i, j).
     """
     if dp_int8 and arith.fmt != "int8":
@@ -370,6 +372,7 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
                 rec.setdefault(key, np.zeros((N, N), ctype))
             for key in ("P_y", "dS_y", "S_bwd"):
                 rec.setdefault(key, np.zeros((N, N), np.float32))
+            rec.setdefault("acc_c_bwd", np.zeros((N, N)))
             for key in ("sP", "sdS"):
                 rec.setdefault(key, np.zeros((T, T), np.float32))
             rec["P"][rows, cols] = float(s_p) * np.asarray(p_hat, np.float64)
@@ -380,6 +383,7 @@ def sage_backward(prep: dict, O_stored, L, dO, causal: bool, arith: Arith = QUAN
             rec["P_y"][rows, cols] = p_y
             rec["dS_y"][rows, cols] = ds_y
             rec["S_bwd"][rows, cols] = S
+            rec["acc_c_bwd"][rows, cols] = np.asarray(s_int, np.float64) * float(c)
             rec["sP"][i, j] = s_p
             rec["sdS"][i, j] = s_ds
             if products:

@@ -36,27 +36,50 @@ def fwd_dump_views(buf, B, H, N, d):
 def bwd_dump_views(buf, B, H, N, d):
     nn = B * H * N * N
     nb = B * H * (N // 64)
-    s, p, ds, sp, sds, doh, sdo, D = carve(buf, [
-        (torch.int32, nn), (torch.int16, nn), (torch.int16, nn), (torch.float32, nb * (N // 64)),
-        (torch.float32, nb * (N // 64)), (torch.int8, B * H * N * d), (torch.float32, nb),
-        (torch.float32, B * H * N)])
+    T = N // 64
+    prod = nb * T * 64 * d
+    s, p, ds, sp, sds, doh, sdo, D, dp, dv, dq, dk = carve(buf, [
+        (torch.int32, nn), (torch.int16, nn), (torch.int16, nn), (torch.float32, nb * T),
+        (torch.float32, nb * T), (torch.int8, B * H * N * d), (torch.float32, nb),
+        (torch.float32, B * H * N), (torch.float32, nn), (torch.int32, prod), (torch.int32, prod),
+        (torch.int32, prod)])
     return dict(S=s.view(B, H, N, N), P=p.view(B, H, N, N), dS=ds.view(B, H, N, N),
-                sP=sp.view(B, H, N // 64, N // 64), sdS=sds.view(B, H, N // 64, N // 64),
-                dOh=doh.view(B, H, N, d), sdO=sdo.view(B, H, N // 64), D=D.view(B, H, N))
+                sP=sp.view(B, H, T, T), sdS=sds.view(B, H, T, T),
+                dOh=doh.view(B, H, N, d), sdO=sdo.view(B, H, N // 64), D=D.view(B, H, N),
+                dP=dp.view(B, H, N, N), dV_int=dv.view(B, H, T, T, 64, d),
+                dQ_int=dq.view(B, H, T, T, 64, d), dK_int=dk.view(B, H, T, T, 64, d))
 
 
 def make_case(N, d, dtype, causal, B=1, H=2, seed=0, qk="normal", sigma=1.0, k_offset_var=0.0,
-              do_var=1e-2, smooth_q=False):
+              do_var=1e-2, smooth_q=False, special=None):
+    """A seeded case; ``special`` reshapes the draws into one of the method's degenerate inputs:
+      "const_k"    every key of a head equal (K-smoothing makes K_sm = 0: zero K blocks, s_K = 0)
+      "zero_do"    dO = 0 (every dS tile zero)
+      "tiny_ds"    bf16 dO scaled per 64-row block by 2^-110, 2^-117, 2^-121, 2^-126, ... so that
+                   dS tile maxima fall on both sides of the 2^-120 zero-tile bound"""
     w = workloads.Workload("case", B, H, N, d, dtype, causal, qk=qk, sigma=sigma,
                            k_offset_var=k_offset_var, do_var=do_var, smooth_q=smooth_q)
-    return w, workloads.make_inputs(w, seed=seed)
+    x = workloads.make_inputs(w, seed=seed)
+    if special == "const_k":
+        x["K"] = np.ascontiguousarray(np.broadcast_to(x["K"][:, :, :1, :], x["K"].shape))
+    elif special == "zero_do":
+        x["dO"] = np.zeros_like(x["dO"])
+    elif special == "tiny_ds":
+        assert dtype == "bf16", "the 2^-120 range needs the bf16 exponent range"
+        exps = [-110, -117, -121, -126]
+        per_tok = np.repeat([2.0 ** exps[i % len(exps)] for i in range(N // 64)], 64)
+        x["dO"] = workloads.round_bf16((x["dO"].astype(np.float64) * per_tok[None, None, :, None]).astype(np.float32))
+    elif special is not None:
+        raise ValueError(special)
+    return w, x
 
 
-def oracle_run(w, x, record=True, dp_int8=False, fp8=False):
+def oracle_run(w, x, record=True, dp_int8=False, fp8=False, products=False):
     rec = {} if record else None
     out = osage.run(x["Q"], x["K"], x["V"], x["dO"], w.causal,
                     lambda a: workloads.round_to(a, w.dtype), smooth_q=w.smooth_q, record=rec,
-                    dp_int8=dp_int8, arith=osage.QUANTISED_FP8 if fp8 else osage.QUANTISED)
+                    dp_int8=dp_int8, arith=osage.QUANTISED_FP8 if fp8 else osage.QUANTISED,
+                    products=products)
     out["record"] = rec
     return out
 

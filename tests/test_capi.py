@@ -172,3 +172,11 @@ def test_noalloc_partials_query(sg):
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 608, 8192, 128, 0, False))) <= cap
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 256, 64, 0, False, smooth_k=False))) == 0
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 100, 64, 0, False))) == 0
+
+
+def test_binding_types_every_declared_call(sg):
+    """Every entry point the header declares gets its argument types when the binding loads the
+    library: a ctypes call without them passes 64-bit pointers as C ints."""
+    L = sg.lib()
+    for name in _declared():
+        assert getattr(L, name).argtypes is not None, name

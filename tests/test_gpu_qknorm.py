@@ -139,3 +139,36 @@ def test_qknorm_refuses_bad_eps():
     Q, K, V, _, _ = _raw(128, 64, "fp16", seed=1)
     with pytest.raises(sg.SageError):
         sg.sage_quantize_smooth_qknorm(to_dev(Q, "fp16"), to_dev(K, "fp16"), to_dev(V, "fp16"), eps=-1.0)
+
+
+@pytest.mark.parametrize("dtype,d", [("fp16", 128), ("bf16", 64)])
+def test_qknorm_row_factor_many_rows(dtype, d):
+    """The row factor is the float32 nearest to 1 / sqrt(mean x^2 + eps) on every one of 2 x 32768
+    rows whose per-token scales span four decades (the kernel's float32 candidate is corrected from
+    its residual, with a float64 decision near rounding boundaries); the normalised tensors, codes,
+    scales and means that follow stay bit-exact."""
+    import bit_trainable_attention_sage_gb300 as sg
+    B, H, N = 1, 8, 4096
+    rng = np.random.default_rng(17)
+    rnd = lambda a: workloads.round_to(a.astype(np.float32), dtype)
+    tok = lambda: np.exp(rng.normal(0.0, 2.0, (B, H, N, 1)))
+    Q = rnd(rng.standard_normal((B, H, N, d)) * tok())
+    K = rnd(rng.standard_normal((B, H, N, d)) * tok())
+    V = rnd(rng.standard_normal((B, H, N, d)))
+    q = sg.sage_quantize_smooth_qknorm(to_dev(Q, dtype), to_dev(K, dtype), to_dev(V, dtype), eps=float(EPS),
+                                       keep_normed=True)
+    torch.cuda.synchronize()
+    Yq, rq, Yk, rk = _oracle_prologue(Q, K, None, None, dtype)
+    for name, got, want in (("rQ", q.rQ, rq), ("rK", q.rK, rk)):
+        g = got.cpu().numpy()
+        ulps = np.abs(g.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
+        print(f"\n{name}: {int((ulps != 0).sum())} of {ulps.size} rows differ, largest {int(ulps.max())} ulp")
+        assert ulps.max() <= 1, name
+        assert np.array_equal(g.view(np.uint32), want.view(np.uint32)), name
+    assert np.array_equal(q.Qn.float().cpu().numpy(), Yq)
+    assert np.array_equal(q.Kn.float().cpu().numpy(), Yk)
+    prep = quant.quantize_smooth(Yq, Yk, V)
+    for k in ("Qh", "Kh", "Vh"):
+        assert np.array_equal(getattr(q, k).cpu().numpy(), prep[k]), k
+    for k in ("sQ", "sK", "muK"):
+        assert np.array_equal(getattr(q, k).cpu().numpy().view(np.uint32), np.asarray(prep[k], np.float32).view(np.uint32)), k
