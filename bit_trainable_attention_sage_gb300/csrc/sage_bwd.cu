@@ -187,13 +187,27 @@ __device__ __forceinline__ int16_t code_hi(uint32_t w) {
 // Row data of 8 query columns (-L2 = -fl32(L log2 e) and D), loaded ahead of use: the MMAs read
 // their operands from shared memory at a high rate, so a shared-memory load waited for at once
 // would stall the score warps.
+#ifndef SAGE_ROWDATA_LDS
+#define SAGE_ROWDATA_LDS 1
+#endif
 struct RowData8 {
     float l2[8], dd[8];
     __device__ __forceinline__ void load(const float *L2s, const float *Ds, int col0) {
+#if SAGE_ROWDATA_LDS
+        // explicit shared-memory loads: through a plain pointer the compiler cannot tell the
+        // address space and issues generic loads, which take the slower generic path
+        const uint32_t a = smem_u32(L2s) + 4u * static_cast<uint32_t>(col0);
+        const uint32_t b = smem_u32(Ds) + 4u * static_cast<uint32_t>(col0);
+        *reinterpret_cast<float4 *>(&l2[0]) = lds128(a);
+        *reinterpret_cast<float4 *>(&l2[4]) = lds128(a + 16u);
+        *reinterpret_cast<float4 *>(&dd[0]) = lds128(b);
+        *reinterpret_cast<float4 *>(&dd[4]) = lds128(b + 16u);
+#else
         *reinterpret_cast<float4 *>(&l2[0]) = *reinterpret_cast<const float4 *>(&L2s[col0]);
         *reinterpret_cast<float4 *>(&l2[4]) = *reinterpret_cast<const float4 *>(&L2s[col0 + 4]);
         *reinterpret_cast<float4 *>(&dd[0]) = *reinterpret_cast<const float4 *>(&Ds[col0]);
         *reinterpret_cast<float4 *>(&dd[4]) = *reinterpret_cast<const float4 *>(&Ds[col0 + 4]);
+#endif
     }
 };
 
@@ -712,7 +726,6 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const float *sdOh = a.sdO + static_cast<size_t>(bh) * nblk;
     const float sv = (DPK == kDpInt8 && key_ok) ? a.sV[static_cast<size_t>(bh) * nblk + kblk] : 0.0f;
     float sdo_next = DPK == kDpInt8 ? sdOh[c_first] : 0.0f;
-    bool alive = true;                               // false once one of this warp's waits gave up
     for (int c = 0; c < n; ++c) {
         const int qb = c_first + c;
         const int q0 = 64 * qb;
@@ -730,29 +743,32 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         // A warp whose wait gave up still takes part in this step's tile-maximum barrier, with a
         // negative maximum as its flag (P maxima are never negative): after the barrier all four
         // warps read the same four slots and leave the loop together.  A warp leaving alone would
-        // leave the others blocked at the barrier.
-        const bool ok = alive && mbar_wait_warp(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19) &&
-                        mbar_wait_warp(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20);
+        // leave the others blocked at the barrier.  (The give-up path is a branch of its own, so
+        // that the common path keeps its register allocation.)
+        if (!mbar_wait_warp(&s.meta_full[m3], (c / 3) & 1, abort_flag, &g_bwd_err, 19) ||
+            !mbar_wait_warp(&s.sd_full[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 20)) {
+            if (lane_id() == 0) s.red[warp][c & 1][0] = -1.0f;
+            named_bar_sync(1, 128);
+            break;
+        }
+        tc_fence_after();
         const uint32_t s_col = lane_base + 128 * b;
         float mp = 0.0f, md = 0.0f, cs = 0.0f;
-        if (ok) {
-            tc_fence_after();
-            int32_t *dump_s0 = DUMP ? a.dump_s + (bhN + q0) * N + key : nullptr;
-            float *dump_dp0 = DUMP ? a.dump_dp + (bhN + q0) * N + key : nullptr;
-            if (edge)
-                score_pass1<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
-                                                              key_ok, dps, mp, md, cs, dump_s0, dump_dp0, N);
-            else
-                score_pass1<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
-                                                               key_ok, dps, mp, md, cs, dump_s0, dump_dp0, N);
-            // tile maxima of (this query block, this key block): over the 32 lanes, then over the
-            // two warps of the key block.  Both are non-negative floats (P >= +0, |dS|), whose bit
-            // patterns order as unsigned integers: one warp-wide integer max each.
-            mp = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mp)));
-            md = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(md)));
-        }
+        int32_t *dump_s0 = DUMP ? a.dump_s + (bhN + q0) * N + key : nullptr;
+        float *dump_dp0 = DUMP ? a.dump_dp + (bhN + q0) * N + key : nullptr;
+        if (edge)
+            score_pass1<true, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                                          key_ok, dps, mp, md, cs, dump_s0, dump_dp0, N);
+        else
+            score_pass1<false, BIAS, DUMP, DPK == kDpInt8>(s_col, s_col + 64, s.L2s[m3], s.Ds[m3], cq, bias, qlo,
+                                                           key_ok, dps, mp, md, cs, dump_s0, dump_dp0, N);
+        // tile maxima of (this query block, this key block): over the 32 lanes, then over the
+        // two warps of the key block.  Both are non-negative floats (P >= +0, |dS|), whose bit
+        // patterns order as unsigned integers: one warp-wide integer max each.
+        mp = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mp)));
+        md = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(md)));
         if (lane_id() == 0) {
-            s.red[warp][c & 1][0] = ok ? mp : -1.0f;
+            s.red[warp][c & 1][0] = mp;
             s.red[warp][c & 1][1] = md;
         }
         if (BIAS) s.colsum[c & 3][tq] = cs;
@@ -784,10 +800,15 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
         // the dQ MMAs that read this dS^ tile two steps ago must be done: d = 128 they ran before
         // this step's S^T / dP^T (the tensor pipe runs in issue order), d = 64 they are those of
         // the previous step pair
-        // (a warp giving up here skips pass 2; the flag of its next step ends the loop for all four)
+        // (a warp giving up here skips pass 2 and, unless this was the last step, flags the next
+        // step's barrier at once: every warp has passed this step's barrier, so none still reads
+        // that step's slots, and every warp reaches the next one)
         if (D != 128 && c >= 2 && !mbar_wait_warp(&s.dss_free, ((c >> 1) - 1) & 1, abort_flag, &g_bwd_err, 22)) {
-            alive = false;
-            continue;
+            if (c + 1 < n) {
+                if (lane_id() == 0) s.red[warp][(c + 1) & 1][0] = -1.0f;
+                named_bar_sync(1, 128);
+            }
+            break;
         }
         int16_t *dump_p0 = DUMP ? a.dump_p + (bhN + q0) * N + key : nullptr;
         int16_t *dump_ds0 = DUMP ? a.dump_ds + (bhN + q0) * N + key : nullptr;

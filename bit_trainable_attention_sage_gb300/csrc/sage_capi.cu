@@ -80,7 +80,10 @@ struct QuantWs {
 static QuantWs quant_ws(const sage_params &p, void *w, size_t *bytes) {
     Carve c(w);
     QuantWs r;
-    r.kpartial = c.take<double>(static_cast<size_t>(p.B) * p.H * kmean_splits(p) * p.d);
+    // the FP4 quantiser's per-split partial sums, or the INT8 pass's per-CTA partials and barrier
+    const size_t split = static_cast<size_t>(p.B) * p.H * kmean_splits(p) * p.d;
+    const size_t fused = quant_fused_doubles(p);
+    r.kpartial = c.take<double>(split > fused ? split : fused);
     if (bytes) *bytes = c.off;
     return r;
 }
@@ -532,7 +535,7 @@ size_t sage_dump_bytes(const sage_params *p, int which) {
 int sage_device_status(sage_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SAGE_ERR_CUDA;
-    const unsigned int e = take_fwd_error() | take_bwd_error();
+    const unsigned int e = take_fwd_error() | take_bwd_error() | take_quant_error();
     if (cudaGetLastError() != cudaSuccess) return SAGE_ERR_CUDA;
     return e ? SAGE_ERR_TIMEOUT : SAGE_OK;
 }

@@ -95,20 +95,36 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 }
 
 // Bounded wait for phase `parity` of `bar`.  Returns false (and raises the abort flag and the
-// device error word) if the wait expired or the CTA had already aborted.
+// device error word) if the wait expired or the CTA had already aborted.  The clock and the abort
+// flag are read on every 16th round only: a waiting warp then issues fewer instructions into the
+// sub-partition's issue slots, which the working warps share (measured on the backward: 4.39 ->
+// 4.36 ms against reading them every round; polling with the non-blocking test_wait instead of
+// the sleeping try_wait made the backward 5 % and the forward 2 % slower).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int *err_word, uint32_t where) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = clock64();
-    while (true) {
-        if (*abort_flag) return false;
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (clock64() - t0 > SAGE_WAIT_CYCLES) {
-            *abort_flag = 1;
-            atomicOr(err_word, 1u | (where << 8));
-            return false;
+        if ((it & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > SAGE_WAIT_CYCLES) {
+                *abort_flag = 1;
+                atomicOr(err_word, 1u | (where << 8));
+                return false;
+            }
         }
     }
+}
+
+// ld.shared of four floats at a shared-memory address (16-byte aligned).  Volatile so that it is
+// not moved above the barrier wait that makes the data visible.
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
 // Warp-wide bounded wait: every lane of the warp calls it and all get the same answer (false if

@@ -13,8 +13,8 @@
 //
 // One CTA owns two 128-row query tiles (four 64-row quantisation blocks) of one head and walks
 // the keys in steps of 128 (two 64-key blocks); both tiles share every K and V tile it loads:
-//   warp 8      TMA producer: both Q tiles once, then K and V tiles (single-buffered each; K(j+1)
-//               streams in while the softmax and PV of step j run)
+//   warp 8      TMA producer: both Q tiles once, then K and V tiles, double-buffered (step j in
+//               stage j & 1; step j + 1's tiles stream in while step j's MMAs read the other)
 //   warp 9      allocates TMEM; one lane issues every MMA, for each tile t:
 //                 S_t    = Q^_t K^T                 M=128 N=128 K=d  -> TMEM cols 256t + [0,128)
 //                 PV_t,h = P^_t[:,64h:64h+64] V^_h  M=128 N=d   K=64 -> TMEM cols 256t + [128,256)
@@ -77,9 +77,9 @@ constexpr uint32_t kRegsControl = 40;
 template <int D>
 struct Smem {
     alignas(1024) uint8_t q[2][D / 64][128 * 128];   // [tile][chunk][row][64 halves], 128B swizzle
-    alignas(1024) uint8_t k[D / 64][128 * 128];
-    alignas(1024) uint8_t v[D / 64][128 * 128];
-    uint64_t q_full, k_full, k_free, v_full, v_free, mma_done;
+    alignas(1024) uint8_t k[2][D / 64][128 * 128];   // two stages: step j's tile in stage j & 1
+    alignas(1024) uint8_t v[2][D / 64][128 * 128];
+    uint64_t q_full, k_full[2], k_free[2], v_full[2], v_free[2], mma_done;
     uint64_t s_full[2], p_full[2][2], pv_full[2], pv_free[2];   // p_full[tile][64-key half]
     uint32_t tmem_base;
     int abort_flag;
@@ -292,10 +292,12 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (threadIdx.x == 0) {
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);
-        mbar_init(&s.k_full, 1);
-        mbar_init(&s.k_free, 1);
-        mbar_init(&s.v_full, 1);
-        mbar_init(&s.v_free, 1);
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(&s.k_full[st], 1);
+            mbar_init(&s.k_free[st], 1);
+            mbar_init(&s.v_full[st], 1);
+            mbar_init(&s.v_free[st], 1);
+        }
         mbar_init(&s.mma_done, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s.s_full[t], 1);
@@ -323,31 +325,37 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             for (int t = 0; t < 2; ++t)
                 for (int c = 0; c < D / 64; ++c) tma_load_3d(s.q[t][c], &mapQ, &s.q_full, 64 * c, q0 + 128 * t, bh);
             int k_issued = 0, v_issued = 0;
+            // K and V tiles of step j go to stage j & 1: the next step's tiles stream in while
+            // this step's MMAs still read the other stage
             for (int j = 0; j < nsteps; ++j) {
-                if (j > 0 && !mbar_wait(&s.k_free, (j - 1) & 1, abort_flag, &g_fwd_err, 1)) break;
-                mbar_arrive_expect_tx(&s.k_full, kTileBytes);
-                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.k[c], &mapK, &s.k_full, 64 * c, 128 * j, bh);
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(&s.k_free[st], ((j >> 1) - 1) & 1, abort_flag, &g_fwd_err, 1)) break;
+                mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.k[st][c], &mapK, &s.k_full[st], 64 * c, 128 * j, bh);
                 k_issued = j + 1;
-                if (j > 0 && !mbar_wait(&s.v_free, (j - 1) & 1, abort_flag, &g_fwd_err, 2)) break;
-                mbar_arrive_expect_tx(&s.v_full, kTileBytes);
-                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.v[c], &mapV, &s.v_full, 64 * c, 128 * j, bh);
+                if (j >= 2 && !mbar_wait(&s.v_free[st], ((j >> 1) - 1) & 1, abort_flag, &g_fwd_err, 2)) break;
+                mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(s.v[st][c], &mapV, &s.v_full[st], 64 * c, 128 * j, bh);
                 v_issued = j + 1;
             }
-            // drain: every load issued must land before the CTA may exit
+            // drain: every load issued must land before the CTA may exit (the last one of each
+            // stage; an earlier one into the same stage was consumed before it was reissued)
             mbar_wait_drain(&s.q_full, 0, &g_fwd_err, 3);
-            if (k_issued > 0) mbar_wait_drain(&s.k_full, (k_issued - 1) & 1, &g_fwd_err, 3);
-            if (v_issued > 0) mbar_wait_drain(&s.v_full, (v_issued - 1) & 1, &g_fwd_err, 4);
+            for (int jj = k_issued > 2 ? k_issued - 2 : 0; jj < k_issued; ++jj)
+                mbar_wait_drain(&s.k_full[jj & 1], (jj >> 1) & 1, &g_fwd_err, 3);
+            for (int jj = v_issued > 2 ? v_issued - 2 : 0; jj < v_issued; ++jj)
+                mbar_wait_drain(&s.v_full[jj & 1], (jj >> 1) & 1, &g_fwd_err, 4);
         }
         } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (elect_one()) {
             constexpr uint32_t idS = idesc_f16(128, 128, BF16OPS, false, false);
             constexpr uint32_t idPV = idesc_f16(128, D, BF16OPS, false, true);
-            const uint32_t k_addr = smem_u32(s.k[0]), v_addr = smem_u32(s.v[0]);
             int pv_count[2] = {0, 0};
-            // S_t = Q^_t K^(j)^T into the tile's S columns
-            auto issue_s = [&](int t) {
+            // S_t = Q^_t K^(j)^T into the tile's S columns, K^(j) from stage kst = j & 1
+            auto issue_s = [&](int t, int kst) {
                 const uint32_t q_addr = smem_u32(s.q[t][0]);
+                const uint32_t k_addr = smem_u32(s.k[kst][0]);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -357,51 +365,56 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 umma_commit(&s.s_full[t]);
             };
             bool ok = mbar_wait(&s.q_full, 0, abort_flag, &g_fwd_err, 5) &&
-                      mbar_wait(&s.k_full, 0, abort_flag, &g_fwd_err, 6);
+                      mbar_wait(&s.k_full[0], 0, abort_flag, &g_fwd_err, 6);
             if (ok) {
                 tc_fence_after();
                 for (int t = 0; t < 2; ++t)
-                    if (0 < nsteps_t[t]) issue_s(t);
-                umma_commit(&s.k_free);
+                    if (0 < nsteps_t[t]) issue_s(t, 0);
+                umma_commit(&s.k_free[0]);
             }
             // Per step j: the PV MMAs of both tiles, half by half; a tile's S of step j + 1 goes in
             // right after its last PV of step j (the PV MMAs have then taken its P codes: the pipe
             // runs in issue order), so its next softmax need not wait for the other tile's PVs.
             for (int j = 0; j < nsteps && ok; ++j) {
-                if (!(ok = mbar_wait(&s.v_full, j & 1, abort_flag, &g_fwd_err, 8))) break;
+                if (!(ok = mbar_wait(&s.v_full[j & 1], (j >> 1) & 1, abort_flag, &g_fwd_err, 8))) break;
+                const uint32_t v_addr = smem_u32(s.v[j & 1][0]);
                 bool k_next = false;                              // K of step j + 1 has landed
                 int s_left = (j + 1 < nsteps_t[0]) + (j + 1 < nsteps_t[1]);
-                for (int h = 0; h < 2 && ok; ++h) {
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (j >= nsteps_t[t]) continue;
-                        if (h == 1 && 128 * j + 64 >= kv_end_t[t]) continue;   // (then j is its last step)
-                        // this half's P codes are in place (each half has its own barrier, so the
-                        // first half's PV runs while the second half is being coded)
-                        if (!mbar_wait(&s.p_full[t][h], j & 1, abort_flag, &g_fwd_err, 7)) { ok = false; break; }
-                        // the tile's PV accumulator must have been read out
-                        if (pv_count[t] > 0 &&
-                            !mbar_wait(&s.pv_free[t], (pv_count[t] - 1) & 1, abort_flag, &g_fwd_err, 9)) { ok = false; break; }
-                        tc_fence_after();
+                // half h of tile t; called with constant h and t, so that every per-tile value
+                // stays in a register (indexing the small arrays at run time put them in local
+                // memory, which the large shared-memory carve-out leaves to L2)
+                auto pv_half = [&](const int h, const int t) -> bool {
+                    if (j >= nsteps_t[t]) return true;
+                    if (h == 1 && 128 * j + 64 >= kv_end_t[t]) return true;   // (then j is its last step)
+                    // this half's P codes are in place (each half has its own barrier, so the
+                    // first half's PV runs while the second half is being coded)
+                    if (!mbar_wait(&s.p_full[t][h], j & 1, abort_flag, &g_fwd_err, 7)) return false;
+                    // the tile's PV accumulator must have been read out
+                    if (pv_count[t] > 0 &&
+                        !mbar_wait(&s.pv_free[t], (pv_count[t] - 1) & 1, abort_flag, &g_fwd_err, 9)) return false;
+                    tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t vrow = 64 * h + 16 * kk;
-                            umma_ts(tmem + 256 * t + 128, tmem + 256 * t + 32 * h + 8 * kk,
-                                    sdesc_sw128(v_addr + vrow * 128, 16384, 1024), idPV, kk > 0);
-                        }
-                        umma_commit(&s.pv_full[t]);
-                        ++pv_count[t];
-                        if (h == 1 && j + 1 < nsteps_t[t]) {
-                            if (!k_next) {
-                                if (!(ok = mbar_wait(&s.k_full, (j + 1) & 1, abort_flag, &g_fwd_err, 6))) break;
-                                tc_fence_after();
-                                k_next = true;
-                            }
-                            issue_s(t);
-                            if (--s_left == 0) umma_commit(&s.k_free);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t vrow = 64 * h + 16 * kk;
+                        umma_ts(tmem + 256 * t + 128, tmem + 256 * t + 32 * h + 8 * kk,
+                                sdesc_sw128(v_addr + vrow * 128, 16384, 1024), idPV, kk > 0);
                     }
-                }
-                umma_commit(&s.v_free);
+                    umma_commit(&s.pv_full[t]);
+                    ++pv_count[t];
+                    if (h == 1 && j + 1 < nsteps_t[t]) {
+                        if (!k_next) {
+                            if (!mbar_wait(&s.k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, &g_fwd_err, 6)) return false;
+                            tc_fence_after();
+                            k_next = true;
+                        }
+                        issue_s(t, (j + 1) & 1);
+                        if (--s_left == 0) umma_commit(&s.k_free[(j + 1) & 1]);
+                    }
+                    return true;
+                };
+                ok = pv_half(0, 0) && pv_half(0, 1) && pv_half(1, 0) && pv_half(1, 1);
+                if (!ok) break;
+                umma_commit(&s.v_free[j & 1]);
             }
             // every MMA must have finished before the tensor memory is released
             umma_commit(&s.mma_done);
@@ -418,8 +431,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int qblk = min(grow, N - 1) >> 6;
         const size_t bhN = static_cast<size_t>(bh) * N;
         const int nblk = N >> 6;
-        const int kv_end = kv_end_t[t];
-        const int my_steps = nsteps_t[t];
+        const int kv_end = t ? kv_end_t[1] : kv_end_t[0];
+        const int my_steps = t ? nsteps_t[1] : nsteps_t[0];
         // FP4: the block scales live inside the dequantised operands
         const float sq = scales_inside(FMT) ? 1.0f : a.sQ[static_cast<size_t>(bh) * nblk + qblk];
         const uint32_t lane_base = tmem_addr(tmem, 32 * quarter, 256 * t);

@@ -26,7 +26,6 @@ struct QuantArgs {
     const double *kpartial;   // (B*H, ksplits, d) float64 partial sums of K (workspace)
     int ksplits;
     int N, d, smooth_k, smooth_q;
-    int z_base;               // first tensor of the launch: 0 = Q, 1 = K, 2 = V
     int fp8;                  // 1: E4M3 codes, delta = max|x| / 448 (SAGE_FLAG_FP8)
     int qk_norm;              // 1: QK-norm prologue (arguments in QkNormArgs)
 };
@@ -103,6 +102,9 @@ int kmean_splits(const sage_params &p);
 cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st,
                             const QkNormArgs *qn = nullptr);
 cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st);   // V only
+unsigned int take_quant_error();
+// float64 words of quantiser scratch the INT8 pass needs with K-smoothing (partial sums, barrier)
+size_t quant_fused_doubles(const sage_params &p);
 // NVFP4 quantisation of Q, K (along d) and V (along the tokens), smoothed as for INT8
 cudaError_t launch_quantize_fp4(const sage_params &p, QuantArgs a, Fp4Out o, cudaStream_t st);
 // NVFP4 codes and scales -> the exact fp16 values s * code (along_tokens: V's scale layout)

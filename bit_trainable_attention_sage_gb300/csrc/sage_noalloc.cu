@@ -42,7 +42,7 @@ static double *noalloc_scratch(int device) {
 // Partial sums a call with these parameters keeps in the array (0 without K-smoothing).
 static size_t partials_needed(const sage_params &p) {
     if (!p.smooth_k) return 0;
-    return static_cast<size_t>(p.B) * p.H * kmean_splits(p) * p.d;
+    return quant_fused_doubles(p);
 }
 
 }  // namespace sage
@@ -86,8 +86,9 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
     a.sQ = sQ; a.sK = sK; a.sV = sV;
     a.muK = muK; a.muQ = p->smooth_q ? muQ : nullptr;
     a.ksplits = kmean_splits(*p);
-    // every partial sum the quantiser reads is written by the K-mean pass of the same call, so the
-    // array needs no clearing; calls that overlap on the GPU share it and race
+    // every partial sum the quantiser reads is written by the K-mean phase of the same call, and
+    // the two barrier words at the end are cleared on the stream before the launch, so the array
+    // needs no other clearing; calls that overlap on the GPU share it and race
     a.kpartial = p->smooth_k ? scratch : nullptr;
     a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
     a.fp8 = (p->flags & SAGE_FLAG_FP8) != 0;

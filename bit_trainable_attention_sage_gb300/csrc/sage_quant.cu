@@ -47,6 +47,24 @@ __device__ __forceinline__ void load8(const T *p, float (&v)[8]) {
     }
 }
 
+// 8 consecutive 16-bit values (one 16-byte word) -> 8 floats (exact)
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<T, __half>::value) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        } else {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+}
+
 __device__ __forceinline__ int quant_code(float x, float delta) {
     if (delta == 0.0f) return 0;
     int q = __float2int_rn(__fdiv_rn(x, delta));
@@ -253,6 +271,16 @@ __device__ __forceinline__ float block_max_256(float v, float *red) {
     return m;
 }
 
+// 16-byte read-only global load; volatile so that a batch of them is issued in program order,
+// all before the first use
+__device__ __forceinline__ uint4 ldg128_nc(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // fp16 value as an exact integer multiple of 2^-24 (the smallest fp16 subnormal): every finite
 // fp16 is m 2^-24 (subnormal) or (1024 + m) 2^(e - 25), so the multiple is m or
 // (1024 + m) << (e - 1), below 2^40 in magnitude.
@@ -263,7 +291,7 @@ __device__ __forceinline__ long long half_fixed24(uint32_t h) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// a1: partial sums of K over token ranges, exact, one (head, split) per CTA.
+// a1 (FP4 quantiser): partial sums of K over token ranges, exact, one (head, split) per CTA.
 // partial[(bh * S + s) * d + c] = sum_{n in split s} K[bh, n, c]
 // fp16 input: int64 multiples of 2^-24 (integer adds, far faster than float64 ones here and just
 // as exact: a sum of 32768 values stays below 2^55, and any sum below 2^53 is exact in both);
@@ -326,6 +354,11 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
             }
         }
     } else if constexpr (std::is_same<T, __half>::value) {
+        // fp16 values v = hi + lo exactly, hi = v rounded to a multiple of 2^-4 (adding 1.5 2^19
+        // rounds there) and lo = v - hi, a multiple of 2^-24 with |lo| <= 2^-5.  Sixteen his stay
+        // below 2^20 (multiples of 2^-4: 24 bits) and sixteen los below 2^-1 (multiples of
+        // 2^-24: 23 bits), so packed float32 adds sum them exactly; every sixteen rows both join
+        // the int64 total in units of 2^-24.
         __shared__ long long redi[256 * 8];
         const int bh = blockIdx.x, s = blockIdx.y;
         const int vec_per_row = d / 8;
@@ -334,16 +367,37 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
         const int n0 = s * rows_per_split;
         const int n1 = min(N, n0 + rows_per_split);
         long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        const T *base = K + static_cast<size_t>(bh) * N * d;
-        // unrolled so that several rows' loads are in flight at once
-#pragma unroll 4
-        for (int n = n0 + rg; n < n1; n += rows_in_flight) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(base + static_cast<size_t>(n) * d + cv * 8);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        const T *base = K + static_cast<size_t>(bh) * N * d + cv * 8;
+        const f2 c2{786432.0f, 786432.0f};               // 1.5 * 2^19
+        for (int nb = n0 + rg; nb < n1; nb += 16 * rows_in_flight) {
+            f2 hs[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+            f2 ls[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+            // all sixteen rows' loads in flight before any is used (rows past the split are zeros)
+            uint4 w[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int n = nb + u * rows_in_flight;
+                w[u] = n < n1 ? ldg128_nc(base + static_cast<size_t>(n) * d) : make_uint4(0, 0, 0, 0);
+            }
+            // (every use below depends on this statement, which comes after the last load)
+#pragma unroll
+            for (int u = 0; u < 16; ++u) asm volatile("" : "+r"(w[u].x), "+r"(w[u].y), "+r"(w[u].z), "+r"(w[u].w));
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                float v[8];
+                unpack8<T>(w[u], v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const f2 x{v[2 * i], v[2 * i + 1]};
+                    const f2 hi = sub2(add2(x, c2), c2);
+                    hs[i] = add2(hs[i], hi);
+                    ls[i] = add2(ls[i], sub2(x, hi));
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += half_fixed24(u[i] & 0xFFFFu);
-                acc[2 * i + 1] += half_fixed24(u[i] >> 16);
+                acc[2 * i] += (__float2ll_rn(hs[i].x * 16.0f) << 20) + __float2ll_rn(ls[i].x * 16777216.0f);
+                acc[2 * i + 1] += (__float2ll_rn(hs[i].y * 16.0f) << 20) + __float2ll_rn(ls[i].y * 16777216.0f);
             }
         }
 #pragma unroll
@@ -385,7 +439,7 @@ __global__ void __launch_bounds__(256) kmean_partial_kernel(const T *__restrict_
     }
 }
 
-// Per-channel mean that tensor z of 64-row block blk has subtracted before quantisation, into
+// (FP4 quantiser) Per-channel mean that tensor z of 64-row block blk has subtracted before quantisation, into
 // mu_s: mu_K from the K-mean partial sums (z = 1 with smooth_k), or the block's own mean of Q
 // (z = 0 with smooth_q; with NORM the rows pass through the QK-norm first).  Writes muK / muQ and
 // returns whether the tensor is smoothed.  Ends with a CTA barrier.
@@ -468,63 +522,463 @@ __device__ __forceinline__ bool smoothing_mean(const SmoothIn a, const T *src, i
 }
 
 // ---------------------------------------------------------------------------------------------
-// a2: smoothing + per-block quantisation of Q (z=0), K (z=1), V (z=2).  One 64 x d block per CTA.
+// a1 + a2: the K-mean, the smoothing and the per-block quantisation of Q (z=0), K (z=1), V (z=2)
+// in one persistent, pipelined pass.
+//
+// Every 64 x d block is contiguous in memory, so one bulk copy (cp.async.bulk, completion counted
+// in bytes on an mbarrier) brings it into a shared-memory stage; the stages keep the next blocks'
+// loads in flight while the CTA works on the current one.  A CTA walks one sequence of blocks:
+//   1. (K-smoothing) its contiguous share of K's blocks, summed column by column into one partial
+//      sum per head it touches (exact: int64 multiples of 2^-24 for fp16; float32 triples, then
+//      float64, for bf16), stored at slot (CTA + head), which no other CTA uses.  The last CTA to
+//      add a partial of head h adds all of them in CTA order, writes mu_K = fl32(sum / N) and
+//      raises the head's flag;
+//   2. the blocks w = blockIdx.x + j gridDim.x of K, Q, V in that order (K's blocks first: the
+//      K-mean has just read them and most are still in L2), each smoothed, reduced to its
+//      maximum |x| and written as codes; a K block first waits for its head's flag (a
+//      cooperative launch keeps every CTA resident, so every flag is raised).
+//
+// Codes: rne(fl32(x / delta)) is taken as q = fl32(x r), r = fl32(1 / delta), rounded to the
+// nearest integer k.  For normal delta, |q - x/delta| < 2^-16 and |fl32(x/delta) - x/delta| <=
+// 2^-18 (|x/delta| <= 127 / (1 - 2^-24)), so where q lies more than 2^-15 from a half-integer
+// (|q - k| < 1/2 - 2^-15) both x / delta and its rounding lie on k's side of it and k is the code.
+// Eight values whose q comes nearer (about 6e-5 of them), or a subnormal delta, take the
+// correctly rounded division itself.
 // ---------------------------------------------------------------------------------------------
-template <typename T, bool NORM, bool FP8>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, QkNormArgs qn) {
-    __shared__ float red[8];
-    __shared__ float mu_s[128];
-    __shared__ double colsum[256 * 8];
-    const int blk = blockIdx.x, bh = blockIdx.y, z = blockIdx.z + a.z_base;
-    const int d = a.d, N = a.N;
-    const T *src = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
-    int8_t *dst = z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh);
-    const bool norm = NORM && z < 2;                   // uniform over the CTA
-    // selected by value: indexing the parameter's arrays with z would copy them to local memory
-    const float *gamma = norm ? (z == 0 ? qn.gamma[0] : qn.gamma[1]) : nullptr;
-    float *scale = z == 0 ? a.sQ : (z == 1 ? a.sK : a.sV);
-    const int vec_per_row = d / 8;
-    const int rows_in_flight = 256 / vec_per_row;
-    const int cv = threadIdx.x % vec_per_row, rg = threadIdx.x / vec_per_row;
-    const int iters = 64 / rows_in_flight;            // 4 for d = 128, 2 for d = 64
-    const size_t blk_off = (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * d;
+constexpr int kQuantThreads = 256;
+constexpr int kQuantStageBytes = 65536;      // bytes of block stages per CTA (4 x 16 KB at d = 128)
+constexpr int kQuantMaxStages = 8;
+constexpr int kQuantGridMax = 304;           // CTAs of the pass at most: two on each of 152 SMs
 
-    const SmoothIn si{a.kpartial, a.muK, a.muQ, a.ksplits, N, d, a.smooth_k, a.smooth_q};
-    const bool smooth = smoothing_mean<T, NORM>(si, src, z, blk, bh, blk_off, cv, rg, vec_per_row,
-                                                 rows_in_flight, iters, gamma, qn.eps, mu_s, colsum);
+__device__ unsigned int g_quant_err;
 
-    float x[4][8];
-    float mx = 0.0f;
+size_t quant_fused_doubles(const sage_params &p) {
+    // partial sums (kQuantGridMax + B*H slots of d), then two 32-bit words a head (the count of
+    // CTAs that have added their partial, and the flag that mu_K of the head is written)
+    return static_cast<size_t>(kQuantGridMax + p.B * p.H) * p.d + static_cast<size_t>(p.B) * p.H;
+}
+
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned int *p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// INT8 codes of 8 values as bytes: delta > 0 normal, r = fl32(1 / delta).  Packed float32 pairs:
+// q = fl32(x r); adding 1.5 2^23 rounds q to the nearest integer k (ties to even) and leaves
+// k mod 256 in the low byte of the sum; |q - k| over the eight values decides whether any lies
+// near a half-integer, and then all eight take the correctly rounded division.  (Should the code
+// generator fuse the product into the addition, k is the rounding of the exact x r, which the
+// same test places on the same side of every half-integer.)
+__device__ __forceinline__ uint2 pack_codes8_rcp(const float (&x)[8], float delta, float r) {
+    constexpr float kMagic = 12582912.0f;
+    const f2 r2{r, r}, m2{kMagic, kMagic};
+    f2 t[4];
+    float dmax = 0.0f;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        if (it >= iters) break;
-        const int r = rg + it * rows_in_flight;
-        load8(src + blk_off + static_cast<size_t>(r) * d + cv * 8, x[it]);
+    for (int i = 0; i < 4; ++i) {
+        const f2 q = mul2(f2{x[2 * i], x[2 * i + 1]}, r2);
+        t[i] = add2(q, m2);
+        const f2 e = sub2(q, sub2(t[i], m2));
+        dmax = max3f(dmax, fabsf(e.x), fabsf(e.y));
+    }
+    if (dmax >= 0.499969482421875f) {                  // 1/2 - 2^-15
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float k0 = fminf(fmaxf(rintf(__fdiv_rn(x[2 * i], delta)), -127.0f), 127.0f);
+            const float k1 = fminf(fmaxf(rintf(__fdiv_rn(x[2 * i + 1], delta)), -127.0f), 127.0f);
+            t[i] = add2(f2{k0, k1}, m2);
+        }
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = __byte_perm(__float_as_uint(t[i].x), __float_as_uint(t[i].y), 0x0040);
+    return make_uint2(__byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410));
+}
+
+struct QuantSched {
+    int per_z;               // blocks of one tensor: B*H*N/64
+    int nz;                  // tensors: 3 (K, Q, V), or 1 (V alone)
+    int nA;                  // K-mean blocks: per_z with K-smoothing, else 0
+    void *kpart;             // (kQuantGridMax + B*H, d) partial sums: int64 (fp16) or float64 (bf16)
+    unsigned int *sync;      // [h] CTAs that added head h's partial, [B*H + h] mu_K of head h
+                             // written (zeroed before the launch)
+};
+
+// CTA c's share of the K-mean blocks is [c nA / grid, (c + 1) nA / grid); the CTA whose share
+// holds block kb, and whether a share holds any block
+__device__ __forceinline__ int kmean_owner(long long kb, int nA, int grid) {
+    return static_cast<int>(((kb + 1) * grid - 1) / nA);
+}
+__device__ __forceinline__ bool kmean_share_nonempty(int c, int nA, int grid) {
+    return static_cast<long long>(c) * nA / grid < static_cast<long long>(c + 1) * nA / grid;
+}
+// the CTAs whose shares hold blocks of head h: [c0, c1], and how many of them are non-empty
+__device__ __forceinline__ int kmean_contributors(int h, int nb, int nA, int grid, int &c0, int &c1) {
+    c0 = kmean_owner(static_cast<long long>(h) * nb, nA, grid);
+    c1 = kmean_owner(static_cast<long long>(h) * nb + nb - 1, nA, grid);
+    int n = 0;
+    for (int c = c0; c <= c1; ++c) n += kmean_share_nonempty(c, nA, grid);
+    return n;
+}
+
+template <typename T, bool NORM, bool FP8, int D>
+__global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(QuantArgs a, QkNormArgs qn, QuantSched sc) {
+    constexpr int kVec = D / 8;                               // threads a row
+    constexpr int kRows = kQuantThreads / kVec;               // rows in one pass of the CTA
+    constexpr int kIters = 64 / kRows;                        // rows a thread in a block: 4 (d = 128) or 2
+    constexpr uint32_t kBlkBytes = 64u * D * sizeof(T);
+    constexpr int kStages = kQuantStageBytes / kBlkBytes < kQuantMaxStages ? kQuantStageBytes / kBlkBytes : kQuantMaxStages;
+    constexpr bool kHalf = std::is_same<T, __half>::value;
+    extern __shared__ __align__(128) uint8_t qsm[];
+    __shared__ uint64_t full[kStages];
+    __shared__ int4 info[kStages];                            // (z, bh, blk) of the block in each stage
+    __shared__ float red[2][8];
+    __shared__ float mu_s[D];
+    __shared__ int abort_s, fin_s;
+    const int tid = threadIdx.x;
+    const int N = a.N, nb = N / 64;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    const int nwork = sc.per_z * sc.nz;
+    // this CTA's K-mean share and quantise blocks
+    const int a_lo = static_cast<int>(static_cast<long long>(cta) * sc.nA / grid);
+    const int a_hi = static_cast<int>(static_cast<long long>(cta + 1) * sc.nA / grid);
+    const int nAc = a_hi - a_lo;
+    const int mine = nAc + (nwork - cta + grid - 1) / grid;
+    double *colsum = reinterpret_cast<double *>(qsm + kStages * kBlkBytes);   // smooth_q / K-mean only
+    const int cv = tid % kVec, rg = tid / kVec;
+
+    auto issue = [&](int j) {
+        const int s = j % kStages;
+        int z, bh, blk;
+        if (j < nAc) {
+            const int kb = a_lo + j;
+            z = 1;
+            bh = kb / nb;
+            blk = kb - bh * nb;
+        } else {
+            const int w = cta + (j - nAc) * grid;
+            const int zi = w / sc.per_z, rem = w - zi * sc.per_z;
+            z = sc.nz == 1 ? 2 : (zi == 0 ? 1 : (zi == 1 ? 0 : 2));
+            bh = rem / nb;
+            blk = rem - bh * nb;
+        }
+        info[s] = make_int4(z, bh, blk, 0);
+        const T *base = static_cast<const T *>(z == 0 ? a.Q : (z == 1 ? a.K : a.V));
+        mbar_arrive_expect_tx(&full[s], kBlkBytes);
+        bulk_load(qsm + s * kBlkBytes, base + (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * D,
+                  kBlkBytes, &full[s]);
+    };
+    if (tid == 0) {
+        abort_s = 0;
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        for (int j = 0; j < kStages && j < mine; ++j) issue(j);
+    }
+    __syncthreads();
+    // this thread's kIters rows of the block in stage st (16-byte slices, 8 values each)
+    auto read_block = [&](int st, float (&x)[kIters][8]) {
+        const uint8_t *buf = qsm + st * kBlkBytes;
+#pragma unroll
+        for (int k = 0; k < kIters; ++k)
+            unpack8<T>(*reinterpret_cast<const uint4 *>(buf + ((rg + k * kRows) * D + cv * 8) * sizeof(T)), x[k]);
+    };
+
+    int i = 0;
+    bool failed = false;
+    // ---------------------------------------------------------------- 1. K-mean share
+    if (sc.nA > 0) {
+        // fp16: v = hi + lo exactly, hi = v rounded to a multiple of 2^-4 (adding 1.5 2^19 rounds
+        // there), lo = v - hi a multiple of 2^-24 with |lo| <= 2^-5; sixteen his stay below 2^20
+        // (24 bits) and sixteen los below 2^-1 (23 bits), so packed float32 adds sum them exactly,
+        // and every sixteen rows they join the int64 total in units of 2^-24.
+        long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        f2 hs[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+        f2 ls[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+        Sum3 acc3[8];
+        int rows_acc = 0;
+        const f2 c2{786432.0f, 786432.0f};                    // 1.5 * 2^19
+        auto fold = [&]() {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += (__float2ll_rn(hs[e].x * 16.0f) << 20) + __float2ll_rn(ls[e].x * 16777216.0f);
+                acc[2 * e + 1] += (__float2ll_rn(hs[e].y * 16.0f) << 20) + __float2ll_rn(ls[e].y * 16777216.0f);
+                hs[e] = f2{0.0f, 0.0f};
+                ls[e] = f2{0.0f, 0.0f};
+            }
+        };
+        for (; i < nAc; ++i) {
+            const int st = i % kStages;
+            const bool ok = mbar_wait_warp(&full[st], (i / kStages) & 1, &abort_s, &g_quant_err, 1);
+            const int4 inf = info[st];
+            const int bh = inf.y, blk = inf.z;
+            float x[kIters][8];
+            read_block(st, x);
+#pragma unroll
+            for (int k = 0; k < kIters; ++k) {
+                if (NORM) qk_norm8<T>(x[k], qn.gamma[1], cv * 8, kVec, D, qn.eps);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    if constexpr (kHalf) {
+                        const f2 v{x[k][e], x[k][e + 1]};
+                        const f2 hi = sub2(add2(v, c2), c2);
+                        hs[e / 2] = add2(hs[e / 2], hi);
+                        ls[e / 2] = add2(ls[e / 2], sub2(v, hi));
+                    } else {
+                        acc3[e].add(x[k][e]);
+                        acc3[e + 1].add(x[k][e + 1]);
+                    }
+                }
+            }
+            if (kHalf && (rows_acc += kIters) == 16) {
+                fold();
+                rows_acc = 0;
+            }
+            // every thread has read the stage (and a wait that gave up is seen by all)
+            if (__syncthreads_or(!ok)) {
+                failed = true;
+                break;
+            }
+            if (tid == 0 && i + kStages < mine) {
+                fence_view_async_shared();
+                issue(i + kStages);
+            }
+            if (blk == nb - 1 || i == nAc - 1) {
+                // the end of this CTA's run of head bh: its partial sum, in a fixed order
+                if (kHalf) {
+                    fold();
+                    rows_acc = 0;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if constexpr (kHalf) reinterpret_cast<long long *>(colsum)[tid * 8 + e] = acc[e];
+                    else colsum[tid * 8 + e] = acc3[e].value();
+                    acc[e] = 0;
+                    acc3[e] = Sum3();
+                }
+                __syncthreads();
+                if (tid < D) {
+                    const int cvv = tid / 8, ci = tid % 8;
+                    if constexpr (kHalf) {
+                        long long sum = 0;
+                        for (int g = 0; g < kRows; ++g) sum += reinterpret_cast<long long *>(colsum)[(g * kVec + cvv) * 8 + ci];
+                        static_cast<long long *>(sc.kpart)[static_cast<size_t>(cta + bh) * D + tid] = sum;
+                    } else {
+                        double sum = 0.0;
+                        for (int g = 0; g < kRows; ++g) sum += colsum[(g * kVec + cvv) * 8 + ci];
+                        static_cast<double *>(sc.kpart)[static_cast<size_t>(cta + bh) * D + tid] = sum;
+                    }
+                }
+                __syncthreads();
+                // the last CTA to add a partial of head bh writes the head's mean
+                int c0, c1;
+                const int ncontrib = kmean_contributors(bh, nb, sc.nA, grid, c0, c1);
+                if (tid == 0) {
+                    __threadfence();
+                    fin_s = atomicAdd(&sc.sync[bh], 1u) + 1u == static_cast<unsigned int>(ncontrib);
+                }
+                __syncthreads();
+                if (fin_s) {
+                    __threadfence();
+                    if (tid < D) {
+                        // (with more CTAs than K blocks, some shares are empty and wrote no partial)
+                        double sum;
+                        if constexpr (kHalf) {
+                            long long si = 0;
+                            for (int cc = c0; cc <= c1; ++cc)
+                                if (kmean_share_nonempty(cc, sc.nA, grid))
+                                    si += __ldcg(static_cast<const long long *>(sc.kpart) + static_cast<size_t>(cc + bh) * D + tid);
+                            sum = static_cast<double>(si) * 0x1p-24;
+                        } else {
+                            sum = 0.0;
+                            for (int cc = c0; cc <= c1; ++cc)
+                                if (kmean_share_nonempty(cc, sc.nA, grid))
+                                    sum += __ldcg(static_cast<const double *>(sc.kpart) + static_cast<size_t>(cc + bh) * D + tid);
+                        }
+                        a.muK[static_cast<size_t>(bh) * D + tid] = static_cast<float>(sum / static_cast<double>(N));
+                    }
+                    __syncthreads();
+                    if (tid == 0) {
+                        __threadfence();
+                        st_release_gpu(&sc.sync[sc.per_z / nb + bh], 1u);
+                    }
+                }
+            }
+        }
+    }
+    // ---------------------------------------------------------------- 2. smoothing + codes
+    for (; i < mine && !failed; ++i) {
+        const int st = i % kStages;
+        // Every warp waits for the stage itself.  A warp whose bounded wait gave up goes on with
+        // whatever the stage holds and posts a negative maximum: after the block-maximum barrier,
+        // the one CTA barrier of a block, every warp sees it and the CTA stops before writing.
+        bool ok = mbar_wait_warp(&full[st], (i / kStages) & 1, &abort_s, &g_quant_err, 1);
+        // (info[st] is rewritten only after the block-maximum barrier below, which every thread
+        // reaches after reading it here)
+        const int4 inf = info[st];
+        const int z = inf.x, bh = inf.y, blk = inf.z;
+        const size_t blk_off = (static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64) * D;
+        float x[kIters][8];
+        read_block(st, x);
+        const bool norm = NORM && z < 2;               // uniform over the CTA
         if (norm) {
-            const float rf = qk_norm8<T>(x[it], gamma, cv * 8, vec_per_row, d, qn.eps);
+            // selected by value: indexing the parameter's arrays with z would copy them to local memory
+            const float *gamma = z == 0 ? qn.gamma[0] : qn.gamma[1];
             float *rnorm = z == 0 ? qn.rnorm[0] : qn.rnorm[1];
             void *xnorm = z == 0 ? qn.xnorm[0] : qn.xnorm[1];
-            if (cv == 0) rnorm[static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r] = rf;
-            if (xnorm)
-                *reinterpret_cast<uint4 *>(static_cast<T *>(xnorm) + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-                    pack8<T>(x[it]);
-        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (smooth) x[it][i] = __fsub_rn(x[it][i], mu_s[cv * 8 + i]);
-            mx = fmaxf(mx, fabsf(x[it][i]));
+            for (int k = 0; k < kIters; ++k) {
+                const int r = rg + k * kRows;
+                const float rf = qk_norm8<T>(x[k], gamma, cv * 8, kVec, D, qn.eps);
+                if (cv == 0) rnorm[static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * 64 + r] = rf;
+                if (xnorm)
+                    *reinterpret_cast<uint4 *>(static_cast<T *>(xnorm) + blk_off + static_cast<size_t>(r) * D + cv * 8) =
+                        pack8<T>(x[k]);
+            }
+        }
+        // per-channel mean to subtract: mu_K (written before the grid-wide barrier; read through
+        // L2), or the block's own mean of Q (float64 sum of its exact values, one rounding of
+        // sum / 64)
+        bool smooth = false;
+        float mu[8];
+        if (z == 1 && a.smooth_k) {
+            smooth = true;
+            // mu_K of head bh is final once the head's flag is up (one lane polls, bounded)
+            bool up = true;
+            if (lane_id() == 0) {
+                const unsigned int *flag = &sc.sync[sc.per_z / nb + bh];
+                if (ld_acquire_gpu(flag) == 0u) {
+                    const unsigned long long t0 = clock64();
+                    while (ld_acquire_gpu(flag) == 0u) {
+                        if (*reinterpret_cast<volatile int *>(&abort_s) || clock64() - t0 > SAGE_WAIT_CYCLES) {
+                            abort_s = 1;
+                            atomicOr(&g_quant_err, 1u | (3u << 8));
+                            up = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+            }
+            // (the warp barrier orders the lanes' reads of mu_K after lane 0's acquire of the flag;
+            // a shuffle alone would let those reads move above the poll)
+            __syncwarp();
+            up = __shfl_sync(0xffffffffu, up, 0);
+            ok = ok && up;
+            const float4 *m = reinterpret_cast<const float4 *>(a.muK + static_cast<size_t>(bh) * D + cv * 8);
+            *reinterpret_cast<float4 *>(&mu[0]) = __ldcg(m);
+            *reinterpret_cast<float4 *>(&mu[4]) = __ldcg(m + 1);
+        } else if (z == 1) {
+            if (blk == 0 && tid < D) a.muK[static_cast<size_t>(bh) * D + tid] = 0.0f;
+        } else if (z == 0 && a.smooth_q) {
+            smooth = true;
+            // per thread: fp16 values as exact int64 multiples of 2^-24 (no float64 adds, slow on
+            // GB300); bf16 in float64
+            long long acci[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            double accd[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int k = 0; k < kIters; ++k) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if constexpr (kHalf)
+                        acci[e] += half_fixed24(__half_as_ushort(__float2half_rn(x[k][e])));
+                    else
+                        accd[e] += static_cast<double>(x[k][e]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if constexpr (kHalf)
+                    colsum[tid * 8 + e] = static_cast<double>(acci[e]) * 0x1p-24;
+                else
+                    colsum[tid * 8 + e] = accd[e];
+            }
+            __syncthreads();
+            if (tid < D) {
+                const int cvv = tid / 8, ci = tid % 8;
+                double sum = 0.0;
+                for (int g = 0; g < kRows; ++g) sum += colsum[(g * kVec + cvv) * 8 + ci];
+                const float m = static_cast<float>(sum / 64.0);
+                mu_s[tid] = m;
+                a.muQ[(static_cast<size_t>(bh) * nb + blk) * D + tid] = m;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mu[e] = mu_s[cv * 8 + e];
+        }
+        float mxr[kIters];                                    // one running maximum a row: short chains
+#pragma unroll
+        for (int k = 0; k < kIters; ++k) {
+            mxr[k] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                f2 v{x[k][e], x[k][e + 1]};
+                if (smooth) v = sub2(v, f2{mu[e], mu[e + 1]});   // fl32(v - mu), lane by lane
+                x[k][e] = v.x;
+                x[k][e + 1] = v.y;
+                mxr[k] = max3f(mxr[k], fabsf(v.x), fabsf(v.y));
+            }
+        }
+        float mx = mxr[0];
+#pragma unroll
+        for (int k = 1; k < kIters; ++k) mx = fmaxf(mx, mxr[k]);
+        // block maximum; red is double-buffered (its slot is written again two blocks on, after
+        // the next block's barrier, which every thread reaches only after reading it here).
+        // Non-negative floats order like their bit patterns: one integer maximum over the warp.
+        mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
+        if ((tid & 31) == 0) red[i & 1][tid >> 5] = ok ? mx : -1.0f;
+        __syncthreads();
+        float mn = red[i & 1][0];
+        mx = mn;
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            mx = fmaxf(mx, red[i & 1][w]);
+            mn = fminf(mn, red[i & 1][w]);
+        }
+        if (mn < 0.0f) {
+            failed = true;
+            break;
+        }
+        // every thread has read its values out of this stage: refill it
+        if (tid == 0 && i + kStages < mine) {
+            fence_view_async_shared();
+            issue(i + kStages);
+        }
+        const float delta = __fdiv_rn(mx, FP8 ? 448.0f : 127.0f);
+        int8_t *dst = (z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh)) + blk_off + cv * 8;
+        if (FP8) {
+#pragma unroll
+            for (int k = 0; k < kIters; ++k)
+                *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8_e4m3(x[k], delta);
+        } else if (delta >= 0x1p-126f) {
+            const float rcp = __frcp_rn(delta);
+#pragma unroll
+            for (int k = 0; k < kIters; ++k)
+                *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8_rcp(x[k], delta, rcp);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kIters; ++k)
+                *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8(x[k], delta);
+        }
+        if (tid == 0) {
+            float *scale = z == 0 ? a.sQ : (z == 1 ? a.sK : a.sV);
+            scale[static_cast<size_t>(bh) * nb + blk] = delta;
         }
     }
-    mx = block_max_256(mx, red);
-    const float delta = __fdiv_rn(mx, FP8 ? 448.0f : 127.0f);
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        if (it >= iters) break;
-        const int r = rg + it * rows_in_flight;
-        *reinterpret_cast<uint2 *>(dst + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-            FP8 ? pack_codes8_e4m3(x[it], delta) : pack_codes8(x[it], delta);
+    if (failed && tid == 0) {
+        // gave up: wait (bounded) for the copies still in flight into this CTA's stages
+        for (int j = i; j < i + kStages && j < mine; ++j)
+            mbar_wait_drain(&full[j % kStages], (j / kStages) & 1, &g_quant_err, 2);
     }
-    if (threadIdx.x == 0) scale[static_cast<size_t>(bh) * (N / 64) + blk] = delta;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -914,60 +1368,104 @@ __global__ void __launch_bounds__(256) qbias_kernel(const T *__restrict__ K,
 // ---------------------------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------------------------
-template <typename T>
-static void launch_quantize_t(const QuantArgs &a, const QkNormArgs &qn, dim3 g, cudaStream_t st) {
-    if (a.qk_norm) {
-        if (a.fp8) quantize_kernel<T, true, true><<<g, 256, 0, st>>>(a, qn);
-        else quantize_kernel<T, true, false><<<g, 256, 0, st>>>(a, qn);
-    } else {
-        if (a.fp8) quantize_kernel<T, false, true><<<g, 256, 0, st>>>(a, qn);
-        else quantize_kernel<T, false, false><<<g, 256, 0, st>>>(a, qn);
-    }
+// SMs of the current device (cached per device; a repeated query is harmless)
+static int sm_count() {
+    static int cached[16] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 16 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 16) cached[dev] = n;
+    return n;
 }
 
-static void launch_quantize_grid(const sage_params &p, const QuantArgs &a, const QkNormArgs &qn,
-                                 dim3 g, cudaStream_t st) {
-    if (p.dtype == SAGE_FP16) launch_quantize_t<__half>(a, qn, g, st);
-    else launch_quantize_t<__nv_bfloat16>(a, qn, g, st);
+template <typename T, bool NORM, bool FP8, int D>
+static cudaError_t launch_quantize_k(const sage_params &p, const QuantArgs &a, const QkNormArgs &qn, int nz,
+                                     cudaStream_t st) {
+    constexpr int blk_bytes = 64 * D * static_cast<int>(sizeof(T));
+    constexpr int nstages = kQuantStageBytes / blk_bytes < kQuantMaxStages ? kQuantStageBytes / blk_bytes : kQuantMaxStages;
+    const int nb = p.N / 64;
+    QuantSched sc;
+    sc.per_z = p.B * p.H * nb;
+    sc.nz = nz;
+    sc.nA = (nz == 3 && p.smooth_k) ? sc.per_z : 0;
+    const bool colsum = a.smooth_q || sc.nA > 0;
+    const int smem = nstages * blk_bytes + (colsum ? kQuantThreads * 8 * static_cast<int>(sizeof(double)) : 0);
+    auto kern = quantize_kernel<T, NORM, FP8, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // CTAs resident together: the K-mean's grid-wide barrier needs every CTA of the launch resident
+    static int occ_cache[2] = {0, 0};
+    int occ = occ_cache[colsum];
+    if (occ <= 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kQuantThreads, smem);
+        if (e != cudaSuccess) return e;
+        occ_cache[colsum] = occ;
+    }
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    int per_sm = occ < 2 ? occ : 2;
+    int cap = per_sm * sms;
+    if (cap > kQuantGridMax) cap = kQuantGridMax;
+    const int nwork = sc.per_z * nz;
+    const int grid = nwork < cap ? nwork : cap;
+    if (grid <= 0) return cudaSuccess;
+    double *scratch = const_cast<double *>(a.kpartial);   // the caller's workspace (written here)
+    sc.kpart = scratch;
+    sc.sync = nullptr;
+    if (sc.nA > 0) {
+        if (!a.kpartial || !a.muK) return cudaErrorInvalidValue;
+        sc.sync = reinterpret_cast<unsigned int *>(scratch + static_cast<size_t>(kQuantGridMax + p.B * p.H) * D);
+        e = cudaMemsetAsync(sc.sync, 0, 2 * sizeof(unsigned int) * static_cast<size_t>(p.B) * p.H, st);
+        if (e != cudaSuccess) return e;
+        QuantArgs ca = a;
+        QkNormArgs cq = qn;
+        void *args[] = {&ca, &cq, &sc};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kQuantThreads), args,
+                                           static_cast<size_t>(smem), st);
+    }
+    kern<<<grid, kQuantThreads, smem, st>>>(a, qn, sc);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_quantize_t(const sage_params &p, const QuantArgs &a, const QkNormArgs &qn, int nz, cudaStream_t st) {
+    if (a.qk_norm)
+        return a.fp8 ? launch_quantize_k<T, true, true, D>(p, a, qn, nz, st)
+                     : launch_quantize_k<T, true, false, D>(p, a, qn, nz, st);
+    return a.fp8 ? launch_quantize_k<T, false, true, D>(p, a, qn, nz, st)
+                 : launch_quantize_k<T, false, false, D>(p, a, qn, nz, st);
+}
+
+static cudaError_t launch_quantize_grid(const sage_params &p, const QuantArgs &a, const QkNormArgs &qn,
+                                        int nz, cudaStream_t st) {
+    if (p.B * p.H * (p.N / 64) == 0) return cudaSuccess;
+    if (p.dtype == SAGE_FP16)
+        return p.d == 128 ? launch_quantize_t<__half, 128>(p, a, qn, nz, st) : launch_quantize_t<__half, 64>(p, a, qn, nz, st);
+    return p.d == 128 ? launch_quantize_t<__nv_bfloat16, 128>(p, a, qn, nz, st)
+                      : launch_quantize_t<__nv_bfloat16, 64>(p, a, qn, nz, st);
 }
 
 int kmean_splits(const sage_params &p) {
     const int bh = p.B * p.H;
-    int s = (4 * 152 + bh - 1) / bh;                   // about four CTAs per SM
-    const int max_s = p.N / 64;
-    return s < 1 ? 1 : (s > max_s ? max_s : s);
+    int s = (8 * 152 + bh - 1) / bh;                   // about eight CTAs per SM
+    // at least 16 rows a thread (256 threads, d / 8 of them a row), all of them loaded at once
+    const int max_s = static_cast<int>(static_cast<long long>(p.N) * p.d / 32768);
+    return s < 1 ? 1 : (s > max_s ? (max_s < 1 ? 1 : max_s) : s);
 }
 
 cudaError_t launch_quantize(const sage_params &p, QuantArgs a, cudaStream_t st, const QkNormArgs *qn) {
     QkNormArgs nq{};
     if (qn) nq = *qn;
-    const int bh = p.B * p.H;
-    if (p.smooth_k) {
-        const int S = a.ksplits;
-        const int rows = (p.N + S - 1) / S;
-        dim3 g(bh, S);
-        double *part = const_cast<double *>(a.kpartial);
-        if (p.dtype == SAGE_FP16) {
-            const __half *K = static_cast<const __half *>(a.K);
-            if (a.qk_norm) kmean_partial_kernel<__half, true><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nq.gamma[1], nq.eps);
-            else kmean_partial_kernel<__half, false><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nullptr, 0.0f);
-        } else {
-            const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.K);
-            if (a.qk_norm) kmean_partial_kernel<__nv_bfloat16, true><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nq.gamma[1], nq.eps);
-            else kmean_partial_kernel<__nv_bfloat16, false><<<g, 256, 0, st>>>(K, part, p.N, p.d, S, rows, nullptr, 0.0f);
-        }
-    }
-    dim3 g(p.N / 64, bh, 3);
-    launch_quantize_grid(p, a, nq, g, st);
-    return cudaGetLastError();
+    if (!a.muK) return cudaErrorInvalidValue;
+    return launch_quantize_grid(p, a, nq, 3, st);
 }
 
 // V alone (no smoothing applies to V): codes to a.Vh, scales to a.sV
 cudaError_t launch_quantize_v(const sage_params &p, QuantArgs a, cudaStream_t st) {
-    a.z_base = 2;
-    dim3 g(p.N / 64, p.B * p.H, 1);
-    launch_quantize_grid(p, a, QkNormArgs{}, g, st);
-    return cudaGetLastError();
+    return launch_quantize_grid(p, a, QkNormArgs{}, 1, st);
 }
 
 cudaError_t launch_quantize_fp4(const sage_params &p, QuantArgs a, Fp4Out o, cudaStream_t st) {
@@ -1133,6 +1631,13 @@ cudaError_t launch_qbias(const sage_params &p, const void *K, const float *muK, 
     else
         qbias_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(K), muK, muQ, bias, p.N, p.d, sl2);
     return cudaGetLastError();
+}
+
+unsigned int take_quant_error() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_quant_err, sizeof(v));
+    cudaMemcpyToSymbol(g_quant_err, &zero, sizeof(zero));
+    return v;
 }
 
 }  // namespace sage

@@ -246,18 +246,20 @@ SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t 
  * array inside the library (sage_quantize_noalloc_max_partials() entries, 1 MiB, held on every
  * device that loads the library until the process exits) instead of in a caller workspace.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - A call needs sage_quantize_noalloc_partials_needed(p) entries: B * H * splits * d with
- *     K-smoothing, 0 without, where splits = ceil(608 / (B * H)) clamped to [1, N / 64] is the
- *     K-mean split count the library chooses.  Refusal therefore depends on B * H * splits, not on
- *     B * H alone.  A call needing more than the capacity returns SAGE_ERR_WORKSPACE before any
- *     launch.  The query returns 0 for parameters the call would refuse.
+ *   - A call needs sage_quantize_noalloc_partials_needed(p) entries: (304 + B * H) * d + B * H
+ *     with K-smoothing (a partial-sum slot of d entries for each of the pass's at most 304 CTAs
+ *     and each head, and one entry of two 32-bit counters for each head), 0 without.  At
+ *     d = 128 that admits B * H <= 714.  A call needing more than the capacity returns
+ *     SAGE_ERR_WORKSPACE before any launch.  The query returns 0 for parameters the call would
+ *     refuse.
  *   - The first call on a device looks up the array's device address on that device (the
  *     current device) and keeps it; make that first call before any stream capture.  The kept
  *     address is not refreshed after cudaDeviceReset: do not use this entry point on a device
  *     after resetting it in the same process.
  *   - Every call shares the one array, which keeps the last call's partial sums.  Nothing has to
- *     start at zero (each call writes every entry it reads first), but calls that overlap on the
- *     GPU -- on different streams, or from different host threads -- race on it.
+ *     start at zero (each call writes every partial sum it reads first, and clears the counters
+ *     on its stream before the launch), but calls that overlap on the GPU -- on different
+ *     streams, or from different host threads -- race on it.
  *   - `flags` must be 0 or SAGE_FLAG_FP8 (no debug dump): SAGE_ERR_ARG otherwise.
  * ------------------------------------------------------------------------------------------ */
 SAGE_API size_t sage_quantize_noalloc_max_partials(void);

@@ -56,7 +56,10 @@ def make_case(N, d, dtype, causal, B=1, H=2, seed=0, qk="normal", sigma=1.0, k_o
       "const_k"    every key of a head equal (K-smoothing makes K_sm = 0: zero K blocks, s_K = 0)
       "zero_do"    dO = 0 (every dS tile zero)
       "tiny_ds"    bf16 dO scaled per 64-row block by 2^-110, 2^-117, 2^-121, 2^-126, ... so that
-                   dS tile maxima fall on both sides of the 2^-120 zero-tile bound"""
+                   dS tile maxima fall on both sides of the 2^-120 zero-tile bound
+      "tiny_qkv"   bf16 Q and V scaled per 64-row block by 1, 2^-100, 2^-125, 2^-131, ... and K by
+                   2^-127: block scales max / 127 that are subnormal in float32 (and subnormal
+                   inputs)"""
     w = workloads.Workload("case", B, H, N, d, dtype, causal, qk=qk, sigma=sigma,
                            k_offset_var=k_offset_var, do_var=do_var, smooth_q=smooth_q)
     x = workloads.make_inputs(w, seed=seed)
@@ -69,6 +72,13 @@ def make_case(N, d, dtype, causal, B=1, H=2, seed=0, qk="normal", sigma=1.0, k_o
         exps = [-110, -117, -121, -126]
         per_tok = np.repeat([2.0 ** exps[i % len(exps)] for i in range(N // 64)], 64)
         x["dO"] = workloads.round_bf16((x["dO"].astype(np.float64) * per_tok[None, None, :, None]).astype(np.float32))
+    elif special == "tiny_qkv":
+        assert dtype == "bf16", "subnormal block scales need the bf16 exponent range"
+        exps = [0, -100, -125, -131]
+        per_tok = np.repeat([2.0 ** exps[i % len(exps)] for i in range(N // 64)], 64)[None, None, :, None]
+        for k in ("Q", "V"):
+            x[k] = workloads.round_bf16((x[k].astype(np.float64) * per_tok).astype(np.float32))
+        x["K"] = workloads.round_bf16((x["K"].astype(np.float64) * 2.0 ** -127).astype(np.float32))
     elif special is not None:
         raise ValueError(special)
     return w, x

@@ -157,19 +157,19 @@ def test_qat_argument_checks(sg):
 
 
 def test_noalloc_partials_query(sg):
-    """The allocation-free quantise call needs B*H*splits*d K-mean partial sums with K-smoothing
-    (splits = ceil(608 / (B*H)) clamped to [1, N/64]) and none without; the host-only query says
-    so, and returns 0 for parameters the call would refuse."""
+    """The allocation-free quantise call needs (304 + B*H)*d + B*H float64 words of K-mean scratch
+    with K-smoothing (a partial-sum slot of d for each of the pass's at most 304 CTAs and each
+    head, and a word of two 32-bit counters for each head) and none without; the host-only query
+    says so, and returns 0 for parameters the call would refuse."""
     L = sg.lib()
     cap = L.sage_quantize_noalloc_max_partials()
     assert cap == 131072
-    for B, H, N, d in ((1, 3, 320, 64), (2, 16, 8192, 128), (1, 600, 8192, 128), (1, 608, 8192, 128)):
+    for B, H, N, d in ((1, 3, 320, 64), (2, 16, 8192, 128), (1, 714, 8192, 128), (1, 715, 8192, 128)):
         p = sg.make_params(B, H, N, d, 0, False)
-        splits = min(max(-(-608 // (B * H)), 1), N // 64)
-        assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == B * H * splits * d
-    # B*H = 600 takes 2 splits and exceeds the array; B*H = 608 takes 1 and fits
-    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 600, 8192, 128, 0, False))) > cap
-    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 608, 8192, 128, 0, False))) <= cap
+        assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == (304 + B * H) * d + B * H
+    # at d = 128, B*H = 715 exceeds the array and 714 fits
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 715, 8192, 128, 0, False))) > cap
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 714, 8192, 128, 0, False))) <= cap
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 256, 64, 0, False, smooth_k=False))) == 0
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 100, 64, 0, False))) == 0
 

@@ -13,7 +13,7 @@ import torch
 
 from tests import parity
 from tests.gpu_common import (causal_mask_full, fwd_dump_views, gpu_fwd, make_case, oracle_fwd,
-                              rel_l2, visited_blocks)
+                              rel_l2, to_dev, visited_blocks)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +52,57 @@ def test_quantize_bit_exact(case):
     assert np.array_equal(q.muK.cpu().numpy().view(np.uint32), prep["muK"].view(np.uint32))
     if w.smooth_q:
         assert np.array_equal(q.muQ.cpu().numpy().view(np.uint32), prep["muQ"].view(np.uint32))
+
+
+# the quantiser alone on more blocks than its grid has CTAs: every CTA walks several blocks and
+# reuses each of its shared-memory stages (8 at d = 64, 4 at d = 128); and bf16 blocks whose scale
+# is subnormal in float32
+QUANT_CASES = [
+    # B, H, N, d, dtype, extra
+    (1, 16, 4096, 64, "bf16", dict(smooth_q=True)),
+    (2, 16, 2048, 128, "fp16", dict(k_offset_var=4.0)),
+    (1, 16, 4096, 64, "fp16", dict(qk="outlier")),
+    (1, 4, 1024, 128, "bf16", dict(special="tiny_qkv")),
+    (1, 4, 1024, 64, "bf16", dict(special="tiny_qkv", smooth_q=True)),
+]
+
+
+@pytest.mark.parametrize("case", QUANT_CASES, ids=[f"B{c[0]}H{c[1]}N{c[2]}d{c[3]}-{c[4]}-" + "-".join(f"{k}={v}" for k, v in c[5].items()) for c in QUANT_CASES])
+def test_quantize_many_blocks_bit_exact(case):
+    import bit_trainable_attention_sage_gb300 as sg
+    from oracle import sage as osage
+    B, H, N, d, dtype, extra = case
+    w, x = make_case(N, d, dtype, False, B=B, H=H, **extra)
+    Q, K, V = (to_dev(x[k], dtype) for k in ("Q", "K", "V"))
+    q = sg.sage_quantize_smooth(Q, K, V, smooth_q=w.smooth_q)
+    assert sg.sage_device_status() == 0
+    prep = osage.prepare(x["Q"], x["K"], x["V"], smooth_q=w.smooth_q)
+    for name in ("Qh", "Kh", "Vh"):
+        assert np.array_equal(getattr(q, name).cpu().numpy(), prep[name]), name
+    for name in ("sQ", "sK", "sV", "muK") + (("muQ",) if w.smooth_q else ()):
+        got = getattr(q, name).cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), np.asarray(prep[name], np.float32).view(np.uint32)), name
+    if extra.get("special") == "tiny_qkv":
+        s = np.concatenate([prep[k].ravel() for k in ("sQ", "sK", "sV")])
+        assert np.any((s > 0) & (s < np.finfo(np.float32).tiny)), "no subnormal block scale"
+
+
+def test_quantize_repeatable():
+    """Ten quantise calls on the same inputs (every CTA waits for mu_K of the heads of its K blocks,
+    which other CTAs finalise) give bit-identical codes, scales and means, equal to the oracle's."""
+    import bit_trainable_attention_sage_gb300 as sg
+    from oracle import sage as osage
+    w, x = make_case(2048, 128, "fp16", False, B=2, H=16, k_offset_var=4.0)
+    Q, K, V = (to_dev(x[k], "fp16") for k in ("Q", "K", "V"))
+    prep = osage.prepare(x["Q"], x["K"], x["V"], smooth_q=False)
+    for _ in range(10):
+        q = sg.sage_quantize_smooth(Q, K, V)
+        assert sg.sage_device_status() == 0
+        for name in ("Qh", "Kh", "Vh"):
+            assert np.array_equal(getattr(q, name).cpu().numpy(), prep[name]), name
+        for name in ("sQ", "sK", "sV", "muK"):
+            got = getattr(q, name).cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), np.asarray(prep[name], np.float32).view(np.uint32)), name
 
 
 @pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
