@@ -43,7 +43,7 @@ import workloads  # noqa: E402
 
 METRIC = "fwd+bwd effective TOPS (N=8192,d=128) and % of INT8/FP16 tensor-core roofline"
 UNIT = "TOPS"
-KERNELS_PER_STEP = 11   # kmean_partial, kmean_final, quantize, 3 widen + fwd, 2 widen + bwd prologue + bwd
+KERNELS_PER_STEP = 9    # quantise pass, 3 widen + fwd, bwd prologue + 2 widen + bwd
 # The rate of the legacy warp-level integer MMA (mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32),
 # the only INT8 tensor-core instruction sm_103a has (ptxas rejects tcgen05 kind::i8 there), as
 # measured on GB300 by a probe kernel when the integer GEMMs' instruction was chosen.  It stands in
