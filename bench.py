@@ -110,6 +110,14 @@ def step_roofline(w: workloads.Workload, step_ms: float, p16_tflops: float) -> d
                                                "rate that actually runs the integer GEMMs, so this fraction exceeds 1"}}
 
 
+def leg_roofline(ops: float, step_ms: float, p16_tflops: float, note: str) -> dict:
+    """The roofline of a leg with no INT8 GEMM (the FP4 forward on dequantised fp16 operands, the
+    16-bit Attn-QAT step): its own tensor ops at the fp16 rate."""
+    t16 = ops / (p16_tflops * 1e12) * 1e3
+    return {"fp16_reading": {"p_int_tflops": p16_tflops, "t_roof_ms": round(t16, 4), "frac": round(t16 / step_ms, 4)},
+            "note": note}
+
+
 def step_ops(w: workloads.Workload) -> float:
     """Algorithmic tensor ops of one quantise + forward + backward: 14 B H N^2 d (x 1/2 causal)."""
     ops = 14.0 * w.B * w.H * w.N * w.N * w.d
@@ -485,6 +493,8 @@ def run_gpu(args, w: workloads.Workload):
                             "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(fwd_tflops / peak, 4),
                             "traffic": None, "flops_per_launch": fwd_ops(w)}
         line.pop("bwd_call", None)
+        line["step_roofline"] = leg_roofline(fwd_ops(w), ms_max / args.steps, peak,
+                                             "quantise + forward only: the forward's 4 N^2 d at the fp16 rate")
         line["gpu_launches"] = 6 * args.steps        # K-mean, FP4 quantise, 3 widen, forward
     if args.qat:
         line["metric"] = "Attn-QAT fwd+bwd effective TOPS (N=8192,d=128)"
@@ -501,6 +511,8 @@ def run_gpu(args, w: workloads.Workload):
                                  "gbs": round(12 * w.B * w.H * w.N * w.d / (quant_ms * 1e-3) / 1e9, 1),
                                  "peak_gbs": hbm_peak}
         line["quantise_call"]["frac"] = round(line["quantise_call"]["gbs"] / hbm_peak, 4)
+        line["step_roofline"] = leg_roofline(qat_step_ops(w), ms_max / args.steps, peak,
+                                             "16-bit operands throughout: the method's 16 N^2 d at the fp16 rate")
         line["gpu_launches"] = 5 * args.steps        # fake quantise, 2 forward passes, prologue, backward
     return line
 
