@@ -43,7 +43,7 @@ import workloads  # noqa: E402
 
 METRIC = "fwd+bwd effective TOPS (N=8192,d=128) and % of INT8/FP16 tensor-core roofline"
 UNIT = "TOPS"
-KERNELS_PER_STEP = 9    # quantise pass, 3 widen + fwd, bwd prologue + 2 widen + bwd
+KERNELS_PER_STEP = 4    # quantise pass (it also writes the fp16 operand copies), fwd, bwd prologue, bwd
 # The rate of the legacy warp-level integer MMA (mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32),
 # the only INT8 tensor-core instruction sm_103a has (ptxas rejects tcgen05 kind::i8 there), as
 # measured on GB300 by a probe kernel when the integer GEMMs' instruction was chosen.  It stands in
@@ -131,14 +131,15 @@ def qknorm_bwd_bytes(w: workloads.Workload) -> int:
     return 10 * n + 4 * w.B * w.H * w.N
 
 
-def quant_bytes(w: workloads.Workload) -> int:
+def quant_bytes(w: workloads.Workload, ops16: bool = True) -> int:
     """Algorithmic HBM bytes of one sage_quantize_smooth call: Q, K, V read once (2 B an element),
-    int8 codes written (1 B), plus the float32 block scales and means.  The K-mean pass reads K a
-    second time, but a one-pass schedule could take that read from L2 (K of the headline workload
-    is 64 MiB of a 126 MiB L2), so it is not counted: the minimum DRAM traffic of the call."""
+    int8 codes written (1 B) and, with the operand copies (SAGE_FLAG_OPS16, the binding's default),
+    their fp16 values (2 B), plus the float32 block scales and means.  The K-mean phase reads K a
+    second time, but that read comes from L2 (K of the headline workload is 64 MiB of a 126 MiB
+    L2), so it is not counted: the minimum DRAM traffic of the call."""
     n = w.B * w.H * w.N * w.d
     reads = 2 * n * 3
-    writes = 3 * n
+    writes = 3 * n + (6 * n if ops16 else 0)
     small = 4 * (3 * w.B * w.H * (w.N // 64) + w.B * w.H * w.d
                  + (w.B * w.H * (w.N // 64) * w.d if w.smooth_q else 0))
     return reads + writes + small
@@ -474,7 +475,7 @@ def run_gpu(args, w: workloads.Workload):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "mode": "pinned host buffers; copies of step k+1 in and step k-1 out overlap step k"},
-        "gpu_launches": (KERNELS_PER_STEP + (2 if args.qk_norm else 0)) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (2 if args.qk_norm else 0) + (2 if args.dp_int8 else 0)) * args.steps,
         "clocks": clk,
     }
     if args.qk_norm:

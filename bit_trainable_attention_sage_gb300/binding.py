@@ -21,6 +21,7 @@ SAGE_FP16, SAGE_BF16 = 0, 1
 SAGE_FLAG_DUMP = 1
 SAGE_FLAG_DP_INT8 = 2
 SAGE_FLAG_FP8 = 4
+SAGE_FLAG_OPS16 = 8
 
 EXPORTED = (
     "sage_quantize_workspace_bytes", "sage_quantize_smooth", "sage_fwd_workspace_bytes",
@@ -35,7 +36,7 @@ class SageParams(ctypes.Structure):
         ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int), ("d", ctypes.c_int),
         ("dtype", ctypes.c_int), ("causal", ctypes.c_int), ("smooth_k", ctypes.c_int),
         ("smooth_q", ctypes.c_int), ("flags", ctypes.c_uint), ("dump", ctypes.c_void_p),
-        ("dump_bytes", ctypes.c_size_t),
+        ("dump_bytes", ctypes.c_size_t), ("ops16", ctypes.c_void_p),
     ]
 
 
@@ -135,10 +136,14 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_params(B: int, H: int, N: int, d: int, dtype: int, causal: bool, smooth_k: bool = True,
-                smooth_q: bool = False, dump: torch.Tensor | None = None, fp8: bool = False) -> SageParams:
-    p = SageParams(B, H, N, d, dtype, int(causal), int(smooth_k), int(smooth_q), 0, None, 0)
+                smooth_q: bool = False, dump: torch.Tensor | None = None, fp8: bool = False,
+                ops16: torch.Tensor | None = None) -> SageParams:
+    p = SageParams(B, H, N, d, dtype, int(causal), int(smooth_k), int(smooth_q), 0, None, 0, None)
     if fp8:
         p.flags |= SAGE_FLAG_FP8
+    if ops16 is not None:
+        p.flags |= SAGE_FLAG_OPS16
+        p.ops16 = ops16.data_ptr()
     if dump is not None:
         p.flags |= SAGE_FLAG_DUMP
         p.dump = dump.data_ptr()
@@ -180,17 +185,27 @@ class Quantized:
     rK: torch.Tensor | None = None
     Qn: torch.Tensor | None = None
     Kn: torch.Tensor | None = None
+    # SAGE_FLAG_OPS16: (3,B,H,N,d) fp16 values of the Q^, K^, V^ codes, read by the forward and
+    # backward calls instead of widening the codes again
+    ops16: torch.Tensor | None = None
+
+
+def _ops16_buffer(B, H, N, d, dev, want: bool) -> torch.Tensor | None:
+    return torch.empty((3, B, H, N, d), dtype=torch.float16, device=dev) if want else None
 
 
 def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, smooth_k: bool = True,
-                         smooth_q: bool = False, fp8: bool = False, stream=None) -> Quantized:
+                         smooth_q: bool = False, fp8: bool = False, ops16: bool = True,
+                         stream=None) -> Quantized:
     """K-smoothing (+ optional Q-smoothing) and per-block INT8 (``fp8``: E4M3) quantisation of
-    (B,H,N,d) Q, K, V."""
+    (B,H,N,d) Q, K, V.  With ``ops16`` (the default) the call also writes the codes' fp16 values,
+    which the forward and backward calls on the result then read instead of widening the codes."""
     _require_cuda(Q, K, V)
     B, H, N, d = Q.shape
     dt = _dtype_code(Q)
     dev = Q.device
-    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
+    o16 = _ops16_buffer(B, H, N, d, dev, ops16)
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8, ops16=o16)
     Qh = torch.empty((B, H, N, d), dtype=torch.int8, device=dev)
     Kh, Vh = torch.empty_like(Qh), torch.empty_like(Qh)
     sQ = torch.empty((B, H, N // 64), dtype=torch.float32, device=dev)
@@ -204,13 +219,14 @@ def sage_quantize_smooth(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, s
                                 _ptr(sQ), _ptr(sK), _ptr(sV), _ptr(muK), _ptr(muQ), _ptr(ws), nws,
                                 _stream(stream))
     _check("sage_quantize_smooth", st)
-    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8)
+    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8, ops16=o16)
 
 
 def sage_quantize_smooth_qknorm(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *,
                                 gamma_q: torch.Tensor | None = None, gamma_k: torch.Tensor | None = None,
                                 eps: float = 1e-6, smooth_k: bool = True, smooth_q: bool = False,
-                                fp8: bool = False, keep_normed: bool = False, stream=None) -> Quantized:
+                                fp8: bool = False, keep_normed: bool = False, ops16: bool = True,
+                                stream=None) -> Quantized:
     """QK-norm (per-token RMSNorm of Q and K, float32 gammas of d entries or None) fused into
     sage_quantize_smooth.  The result carries the row factors rQ, rK and, with ``keep_normed``
     (forced when ``smooth_q``), the normalised Q and K; pass ``q.Kn`` as K to the forward and
@@ -219,7 +235,8 @@ def sage_quantize_smooth_qknorm(Q: torch.Tensor, K: torch.Tensor, V: torch.Tenso
     B, H, N, d = Q.shape
     dt = _dtype_code(Q)
     dev = Q.device
-    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
+    o16 = _ops16_buffer(B, H, N, d, dev, ops16)
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8, ops16=o16)
     Qh = torch.empty((B, H, N, d), dtype=torch.int8, device=dev)
     Kh, Vh = torch.empty_like(Qh), torch.empty_like(Qh)
     sQ = torch.empty((B, H, N // 64), dtype=torch.float32, device=dev)
@@ -239,7 +256,7 @@ def sage_quantize_smooth_qknorm(Q: torch.Tensor, K: torch.Tensor, V: torch.Tenso
                                        _ptr(Qh), _ptr(Kh), _ptr(Vh), _ptr(sQ), _ptr(sK), _ptr(sV),
                                        _ptr(muK), _ptr(muQ), _ptr(ws), nws, _stream(stream))
     _check("sage_quantize_smooth_qknorm", st)
-    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8, rQ, rK, Qn, Kn)
+    return Quantized(Qh, Kh, Vh, sQ, sK, sV, muK, muQ, dt, smooth_k, smooth_q, fp8, rQ, rK, Qn, Kn, ops16=o16)
 
 
 def sage_qknorm_bwd(X: torch.Tensor, r: torch.Tensor, dY: torch.Tensor, *, gamma: torch.Tensor | None = None,
@@ -327,7 +344,7 @@ def sage_attn_fwd(q: Quantized, *, causal: bool, K: torch.Tensor | None = None,
     """SageBwd forward.  Returns (O (B,H,N,d) in the input dtype, L (B,H,N) float32)."""
     B, H, N, d = q.Qh.shape
     dev = q.Qh.device
-    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump, q.fp8)
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump, q.fp8, q.ops16)
     odt = torch.float16 if q.dtype == SAGE_FP16 else torch.bfloat16
     O = torch.empty((B, H, N, d), dtype=odt, device=dev) if out is None else out
     Lse = torch.empty((B, H, N), dtype=torch.float32, device=dev) if lse is None else lse
@@ -351,7 +368,7 @@ def sage_attn_bwd(q: Quantized, V: torch.Tensor, O: torch.Tensor, L: torch.Tenso
     _require_cuda(V, O, L, dO, K)
     B, H, N, d = q.Qh.shape
     dev = q.Qh.device
-    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump, q.fp8)
+    p = make_params(B, H, N, d, q.dtype, causal, q.smooth_k, q.smooth_q, dump, q.fp8, q.ops16)
     if dp_int8:
         p.flags |= SAGE_FLAG_DP_INT8
     if grads is None:
@@ -443,7 +460,7 @@ def sage_status_string(status: int) -> str:
 
 def sage_quantize_smooth_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *,
                                  smooth_k: bool = True, smooth_q: bool = False, fp8: bool = False,
-                                 out=None, stream=None) -> Quantized:
+                                 ops16: bool = True, out=None, stream=None) -> Quantized:
     """sage_quantize_smooth for callers that cannot allocate device memory while they run: the
     K-mean scratch lives in a fixed array inside the library.  ``out`` (a Quantized whose tensors
     the caller allocated beforehand) receives the results; without it they are allocated here."""
@@ -457,10 +474,10 @@ def sage_quantize_smooth_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
         out = Quantized(Qh, torch.empty_like(Qh), torch.empty_like(Qh), sQ, torch.empty_like(sQ),
                         torch.empty_like(sQ), torch.empty((B, H, d), dtype=torch.float32, device=dev),
                         torch.empty((B, H, N // 64, d), dtype=torch.float32, device=dev) if smooth_q else None,
-                        dt, smooth_k, smooth_q, fp8)
+                        dt, smooth_k, smooth_q, fp8, ops16=_ops16_buffer(B, H, N, d, dev, ops16))
     L = lib()
     fn = L.sage_quantize_smooth_noalloc
-    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8)
+    p = make_params(B, H, N, d, dt, False, smooth_k, smooth_q, fp8=fp8, ops16=out.ops16)
     st = fn(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(out.Qh), _ptr(out.Kh), _ptr(out.Vh),
             _ptr(out.sQ), _ptr(out.sK), _ptr(out.sV), _ptr(out.muK), _ptr(out.muQ), _stream(stream))
     _check("sage_quantize_smooth_noalloc", st)

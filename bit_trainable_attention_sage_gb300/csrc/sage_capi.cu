@@ -95,9 +95,11 @@ struct FwdWs {
 static FwdWs fwd_ws(const sage_params &p, void *w, size_t *bytes) {
     Carve c(w);
     FwdWs r;
-    r.q16 = c.take<__half>(elems(p));
-    r.k16 = c.take<__half>(elems(p));
-    r.v16 = c.take<__half>(elems(p));
+    // (with SAGE_FLAG_OPS16 the operand copies come from the caller's p->ops16)
+    const bool own = !(p.flags & SAGE_FLAG_OPS16);
+    r.q16 = own ? c.take<__half>(elems(p)) : nullptr;
+    r.k16 = own ? c.take<__half>(elems(p)) : nullptr;
+    r.v16 = own ? c.take<__half>(elems(p)) : nullptr;
     r.qbias = p.smooth_q ? c.take<float>(nblocks(p) * p.N) : nullptr;
     if (bytes) *bytes = c.off;
     return r;
@@ -113,8 +115,9 @@ struct BwdWs {
 static BwdWs bwd_ws(const sage_params &p, void *w, size_t *bytes) {
     Carve c(w);
     BwdWs r;
-    r.q16 = c.take<__half>(elems(p));
-    r.k16 = c.take<__half>(elems(p));
+    const bool own = !(p.flags & SAGE_FLAG_OPS16);
+    r.q16 = own ? c.take<__half>(elems(p)) : nullptr;
+    r.k16 = own ? c.take<__half>(elems(p)) : nullptr;
     r.do16 = c.take<__half>(elems(p));
     r.D = c.take<float>(rows(p));
     r.L2 = c.take<float>(rows(p));
@@ -186,7 +189,11 @@ int check_params(const sage_params *p) {
     if (p->causal != 0 && p->causal != 1) return SAGE_ERR_ARG;
     if (p->smooth_k != 0 && p->smooth_k != 1) return SAGE_ERR_ARG;
     if (p->smooth_q != 0 && p->smooth_q != 1) return SAGE_ERR_ARG;
-    if (p->flags & ~(SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8 | SAGE_FLAG_FP8)) return SAGE_ERR_ARG;
+    if (p->flags & ~(SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8 | SAGE_FLAG_FP8 | SAGE_FLAG_OPS16)) return SAGE_ERR_ARG;
+    if (p->flags & SAGE_FLAG_OPS16) {
+        if (!p->ops16) return SAGE_ERR_ARG;
+        if (reinterpret_cast<uintptr_t>(p->ops16) & 15u) return SAGE_ERR_ALIGN;
+    }
     if ((p->flags & SAGE_FLAG_FP8) && (p->flags & (SAGE_FLAG_DUMP | SAGE_FLAG_DP_INT8))) return SAGE_ERR_UNSUPPORTED;
     if (p->dtype != SAGE_FP16 && p->dtype != SAGE_BF16) return SAGE_ERR_UNSUPPORTED;
     if (p->d != 64 && p->d != 128) return SAGE_ERR_UNSUPPORTED;
@@ -274,6 +281,7 @@ static int quantize_call(const sage_params *p, const sage_qknorm *qn, const void
     a.kpartial = w.kpartial;
     a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
     a.fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
+    a.ops16 = (p->flags & SAGE_FLAG_OPS16) ? static_cast<__half *>(p->ops16) : nullptr;
     QkNormArgs na{};
     if (qn) {
         a.qk_norm = 1;
@@ -337,9 +345,17 @@ int sage_attn_fwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     FwdWs w = fwd_ws(*p, workspace, nullptr);
     const size_t n = elems(*p);
     const bool fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
-    SAGE_CUDA(launch_widen(Qh, w.q16, n, fp8, st));
-    SAGE_CUDA(launch_widen(Kh, w.k16, n, fp8, st));
-    SAGE_CUDA(launch_widen(Vh, w.v16, n, fp8, st));
+    if (p->flags & SAGE_FLAG_OPS16) {
+        // the quantiser wrote the operand copies (Q^, K^, V^ in that order)
+        const __half *o16 = static_cast<const __half *>(p->ops16);
+        w.q16 = const_cast<__half *>(o16);
+        w.k16 = const_cast<__half *>(o16 + n);
+        w.v16 = const_cast<__half *>(o16 + 2 * n);
+    } else {
+        SAGE_CUDA(launch_widen(Qh, w.q16, n, fp8, st));
+        SAGE_CUDA(launch_widen(Kh, w.k16, n, fp8, st));
+        SAGE_CUDA(launch_widen(Vh, w.v16, n, fp8, st));
+    }
     const float sl2 = scale_log2(p->d);
     if (p->smooth_q) SAGE_CUDA(launch_qbias(*p, K, muK, muQ, w.qbias, sl2, st));
     FwdArgs a;
@@ -429,8 +445,14 @@ int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t *Kh, cons
     memset(&dd, 0, sizeof(dd));
     if (p->flags & SAGE_FLAG_DUMP) dd = bwd_dump(*p, p->dump, nullptr);
     const bool fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
-    SAGE_CUDA(launch_widen(Qh, w.q16, n, fp8, st));
-    SAGE_CUDA(launch_widen(Kh, w.k16, n, fp8, st));
+    if (p->flags & SAGE_FLAG_OPS16) {
+        const __half *o16 = static_cast<const __half *>(p->ops16);
+        w.q16 = const_cast<__half *>(o16);
+        w.k16 = const_cast<__half *>(o16 + n);
+    } else {
+        SAGE_CUDA(launch_widen(Qh, w.q16, n, fp8, st));
+        SAGE_CUDA(launch_widen(Kh, w.k16, n, fp8, st));
+    }
     const bool dp8 = (p->flags & SAGE_FLAG_DP_INT8) != 0;
     if (dp8) {
         // V codes for dP (the ablation): the same per-block quantiser as sage_quantize_smooth

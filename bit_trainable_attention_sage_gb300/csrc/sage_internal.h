@@ -28,6 +28,7 @@ struct QuantArgs {
     int N, d, smooth_k, smooth_q;
     int fp8;                  // 1: E4M3 codes, delta = max|x| / 448 (SAGE_FLAG_FP8)
     int qk_norm;              // 1: QK-norm prologue (arguments in QkNormArgs)
+    __half *ops16;            // SAGE_FLAG_OPS16: (3,B,H,N,d) fp16 copies of the codes, else NULL
 };
 
 // QK-norm prologue: Q (index 0) and K (index 1) are RMS-normalised per token.  A kernel parameter

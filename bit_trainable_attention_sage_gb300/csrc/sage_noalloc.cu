@@ -63,7 +63,7 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
     // the rules of sage_quantize_smooth, less its workspace; no debug dump, no INT8-dP flag
     const int st = check_params(p);
     if (st != SAGE_OK) return st;
-    if (p->flags & ~SAGE_FLAG_FP8) return SAGE_ERR_ARG;
+    if (p->flags & ~(SAGE_FLAG_FP8 | SAGE_FLAG_OPS16)) return SAGE_ERR_ARG;
     const void *ptrs[] = {Q, K, V, Qh, Kh, Vh, sQ, sK, sV, muK};
     for (const void *q : ptrs) {
         if (!q) return SAGE_ERR_ARG;
@@ -92,6 +92,7 @@ extern "C" int sage_quantize_smooth_noalloc(const sage_params *p, const void *Q,
     a.kpartial = p->smooth_k ? scratch : nullptr;
     a.N = p->N; a.d = p->d; a.smooth_k = p->smooth_k; a.smooth_q = p->smooth_q;
     a.fp8 = (p->flags & SAGE_FLAG_FP8) != 0;
+    a.ops16 = (p->flags & SAGE_FLAG_OPS16) ? static_cast<__half *>(p->ops16) : nullptr;
     if (launch_quantize(*p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SAGE_ERR_CUDA;
     return SAGE_OK;
 }

@@ -546,9 +546,14 @@ __device__ __forceinline__ bool smoothing_mean(const SmoothIn a, const T *src, i
 // correctly rounded division itself.
 // ---------------------------------------------------------------------------------------------
 constexpr int kQuantThreads = 256;
-constexpr int kQuantStageBytes = 65536;      // bytes of block stages per CTA (4 x 16 KB at d = 128)
+// CTAs per SM (the QK-norm variants, which need more registers, keep two).  Measured with the L2
+// flushed between calls: two 0.0959 ms, three 0.0928, four 0.0980 at B2 H16 N8192 d128; two
+// 0.1338, three 0.1154 at B2 H32 N8192 d64.
+constexpr int kQuantCtas = 3;
+// bytes of block stages per CTA: 3 x 16 KB at d = 128
+constexpr int kQuantStageBytes = 49152;
 constexpr int kQuantMaxStages = 8;
-constexpr int kQuantGridMax = 304;           // CTAs of the pass at most: two on each of 152 SMs
+constexpr int kQuantGridMax = kQuantCtas * 152;   // CTAs of the pass at most
 
 __device__ unsigned int g_quant_err;
 
@@ -579,26 +584,43 @@ __device__ __forceinline__ void st_release_gpu(unsigned int *p, unsigned int v) 
 // near a half-integer, and then all eight take the correctly rounded division.  (Should the code
 // generator fuse the product into the addition, k is the rounding of the exact x r, which the
 // same test places on the same side of every half-integer.)
-__device__ __forceinline__ uint2 pack_codes8_rcp(const float (&x)[8], float delta, float r) {
+// fp16 values of 8 int8 codes (exact)
+__device__ __forceinline__ uint4 codes8_to_f16(uint2 c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t src = i < 2 ? c.x : c.y;
+        const int lo = static_cast<int8_t>((src >> (16 * (i & 1))) & 0xFFu);
+        const int hi = static_cast<int8_t>((src >> (16 * (i & 1) + 8)) & 0xFFu);
+        w[i] = pack_half2(static_cast<float>(lo), static_cast<float>(hi));
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool H16 = false>
+__device__ __forceinline__ uint2 pack_codes8_rcp(const float (&x)[8], float delta, float r, uint4 *h16 = nullptr) {
     constexpr float kMagic = 12582912.0f;
     const f2 r2{r, r}, m2{kMagic, kMagic};
-    f2 t[4];
+    f2 t[4], k[4];
     float dmax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const f2 q = mul2(f2{x[2 * i], x[2 * i + 1]}, r2);
         t[i] = add2(q, m2);
-        const f2 e = sub2(q, sub2(t[i], m2));
+        k[i] = sub2(t[i], m2);
+        const f2 e = sub2(q, k[i]);
         dmax = max3f(dmax, fabsf(e.x), fabsf(e.y));
     }
     if (dmax >= 0.499969482421875f) {                  // 1/2 - 2^-15
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float k0 = fminf(fmaxf(rintf(__fdiv_rn(x[2 * i], delta)), -127.0f), 127.0f);
-            const float k1 = fminf(fmaxf(rintf(__fdiv_rn(x[2 * i + 1], delta)), -127.0f), 127.0f);
-            t[i] = add2(f2{k0, k1}, m2);
+            k[i].x = fminf(fmaxf(rintf(__fdiv_rn(x[2 * i], delta)), -127.0f), 127.0f);
+            k[i].y = fminf(fmaxf(rintf(__fdiv_rn(x[2 * i + 1], delta)), -127.0f), 127.0f);
+            t[i] = add2(k[i], m2);
         }
     }
+    if (H16) *h16 = make_uint4(pack_half2(k[0].x, k[0].y), pack_half2(k[1].x, k[1].y), pack_half2(k[2].x, k[2].y),
+                               pack_half2(k[3].x, k[3].y));
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = __byte_perm(__float_as_uint(t[i].x), __float_as_uint(t[i].y), 0x0040);
@@ -632,7 +654,7 @@ __device__ __forceinline__ int kmean_contributors(int h, int nb, int nA, int gri
 }
 
 template <typename T, bool NORM, bool FP8, int D>
-__global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(QuantArgs a, QkNormArgs qn, QuantSched sc) {
+__global__ void __launch_bounds__(kQuantThreads, NORM ? 2 : kQuantCtas) quantize_kernel(QuantArgs a, QkNormArgs qn, QuantSched sc) {
     constexpr int kVec = D / 8;                               // threads a row
     constexpr int kRows = kQuantThreads / kVec;               // rows in one pass of the CTA
     constexpr int kIters = 64 / kRows;                        // rows a thread in a block: 4 (d = 128) or 2
@@ -955,19 +977,38 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(QuantArgs a,
         }
         const float delta = __fdiv_rn(mx, FP8 ? 448.0f : 127.0f);
         int8_t *dst = (z == 0 ? a.Qh : (z == 1 ? a.Kh : a.Vh)) + blk_off + cv * 8;
+        // SAGE_FLAG_OPS16: the codes' exact fp16 values too, the tensor cores' operands
+        __half *h16 = a.ops16 ? a.ops16 + static_cast<size_t>(z) * sc.per_z * 64 * D + blk_off + cv * 8 : nullptr;
         if (FP8) {
 #pragma unroll
-            for (int k = 0; k < kIters; ++k)
-                *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8_e4m3(x[k], delta);
+            for (int k = 0; k < kIters; ++k) {
+                const size_t r = static_cast<size_t>(rg + k * kRows) * D;
+                *reinterpret_cast<uint2 *>(dst + r) = pack_codes8_e4m3(x[k], delta);
+                if (h16) *reinterpret_cast<uint4 *>(h16 + r) = pack_codes8_e4m3_f16(x[k], delta);
+            }
         } else if (delta >= 0x1p-126f) {
             const float rcp = __frcp_rn(delta);
+            if (h16) {
 #pragma unroll
-            for (int k = 0; k < kIters; ++k)
-                *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8_rcp(x[k], delta, rcp);
+                for (int k = 0; k < kIters; ++k) {
+                    const size_t r = static_cast<size_t>(rg + k * kRows) * D;
+                    uint4 hv;
+                    *reinterpret_cast<uint2 *>(dst + r) = pack_codes8_rcp<true>(x[k], delta, rcp, &hv);
+                    *reinterpret_cast<uint4 *>(h16 + r) = hv;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kIters; ++k)
+                    *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8_rcp(x[k], delta, rcp);
+            }
         } else {
 #pragma unroll
-            for (int k = 0; k < kIters; ++k)
-                *reinterpret_cast<uint2 *>(dst + static_cast<size_t>(rg + k * kRows) * D) = pack_codes8(x[k], delta);
+            for (int k = 0; k < kIters; ++k) {
+                const size_t r = static_cast<size_t>(rg + k * kRows) * D;
+                const uint2 c = pack_codes8(x[k], delta);
+                *reinterpret_cast<uint2 *>(dst + r) = c;
+                if (h16) *reinterpret_cast<uint4 *>(h16 + r) = codes8_to_f16(c);
+            }
         }
         if (tid == 0) {
             float *scale = z == 0 ? a.sQ : (z == 1 ? a.sK : a.sV);
@@ -1321,15 +1362,25 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(BwdPrologueArgs a) {
     }
     mx = block_max_256(mx, red);
     const float delta = __fdiv_rn(mx, a.fp8 ? 448.0f : 127.0f);
+    // INT8 codes of a normal delta: the reciprocal product with the exact tie test (see
+    // pack_codes8_rcp), which gives the codes and their fp16 values together
+    const bool rcp_path = !a.fp8 && delta >= 0x1p-126f;
+    const float rcp = rcp_path ? __frcp_rn(delta) : 0.0f;
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         if (it >= iters) break;
         const int r = rg + it * rows_in_flight;
-        *reinterpret_cast<uint4 *>(a.dO16 + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-            a.fp8 ? pack_codes8_e4m3_f16(x[it], delta) : pack_codes8_f16(x[it], delta);
-        if (a.dOh)
-            *reinterpret_cast<uint2 *>(a.dOh + blk_off + static_cast<size_t>(r) * d + cv * 8) =
-                pack_codes8(x[it], delta);
+        const size_t off = blk_off + static_cast<size_t>(r) * d + cv * 8;
+        if (rcp_path) {
+            uint4 h;
+            const uint2 c = pack_codes8_rcp<true>(x[it], delta, rcp, &h);
+            *reinterpret_cast<uint4 *>(a.dO16 + off) = h;
+            if (a.dOh) *reinterpret_cast<uint2 *>(a.dOh + off) = c;
+        } else {
+            *reinterpret_cast<uint4 *>(a.dO16 + off) =
+                a.fp8 ? pack_codes8_e4m3_f16(x[it], delta) : pack_codes8_f16(x[it], delta);
+            if (a.dOh) *reinterpret_cast<uint2 *>(a.dOh + off) = pack_codes8(x[it], delta);
+        }
     }
     if (threadIdx.x == 0) a.sdO[static_cast<size_t>(bh) * (N / 64) + blk] = delta;
 }
@@ -1406,7 +1457,8 @@ static cudaError_t launch_quantize_k(const sage_params &p, const QuantArgs &a, c
     if (occ < 1) return cudaErrorInvalidConfiguration;
     int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    int per_sm = occ < 2 ? occ : 2;
+    const int want = NORM ? 2 : kQuantCtas;
+    int per_sm = occ < want ? occ : want;
     int cap = per_sm * sms;
     if (cap > kQuantGridMax) cap = kQuantGridMax;
     const int nwork = sc.per_z * nz;

@@ -68,6 +68,17 @@ extern "C" {
                                    bit patterns.  Pass it to all three calls of one pass; it
                                    cannot be combined with SAGE_FLAG_DUMP or SAGE_FLAG_DP_INT8
                                    (SAGE_ERR_UNSUPPORTED). */
+#define SAGE_FLAG_OPS16 8u      /* operand copies in fp16: the tensor cores take the codes as their
+                                   exact fp16 values, and without this flag the forward and backward
+                                   calls widen the codes into their workspaces (5 passes a step).
+                                   sage_quantize_smooth (and its QK-norm and no-allocation forms)
+                                   then also writes those values to p->ops16: Q^, K^, V^ in that
+                                   order, each (B,H,N,d) fp16, 16-byte aligned.  sage_attn_fwd and
+                                   sage_attn_bwd read them from p->ops16 instead of widening (they
+                                   must be the copies of the same codes) and their workspace
+                                   queries drop the widened copies.  The tensor cores see the
+                                   same operands as without the flag.  The FP4 and Attn-QAT entry
+                                   points refuse it (SAGE_ERR_UNSUPPORTED). */
 
 typedef struct CUstream_st *sage_stream_t;   /* identical to cudaStream_t */
 
@@ -90,6 +101,7 @@ typedef struct sage_params {
     unsigned flags;  /* SAGE_FLAG_*                                                          */
     void *dump;      /* device buffer for SAGE_FLAG_DUMP, else NULL                          */
     size_t dump_bytes;
+    void *ops16;     /* device buffer for SAGE_FLAG_OPS16, else NULL: (3,B,H,N,d) fp16       */
 } sage_params;
 
 /* ------------------------------------------------------------------------------------------ *
@@ -246,10 +258,10 @@ SAGE_API int sage_attn_bwd(const sage_params *p, const int8_t *Qh, const int8_t 
  * array inside the library (sage_quantize_noalloc_max_partials() entries, 1 MiB, held on every
  * device that loads the library until the process exits) instead of in a caller workspace.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - A call needs sage_quantize_noalloc_partials_needed(p) entries: (304 + B * H) * d + B * H
- *     with K-smoothing (a partial-sum slot of d entries for each of the pass's at most 304 CTAs
+ *   - A call needs sage_quantize_noalloc_partials_needed(p) entries: (456 + B * H) * d + B * H
+ *     with K-smoothing (a partial-sum slot of d entries for each of the pass's at most 456 CTAs
  *     and each head, and one entry of two 32-bit counters for each head), 0 without.  At
- *     d = 128 that admits B * H <= 714.  A call needing more than the capacity returns
+ *     d = 128 that admits B * H <= 563.  A call needing more than the capacity returns
  *     SAGE_ERR_WORKSPACE before any launch.  The query returns 0 for parameters the call would
  *     refuse.
  *   - The first call on a device looks up the array's device address on that device (the

@@ -47,9 +47,12 @@ def test_weak_scaling_value():
     assert ops == 14.0 * 2 * 16 * 8192 * 8192 * 128
     assert bench.step_ops(workloads.get("headline", causal=True)) == ops / 2
     assert bench.fwd_ops(w) + bench.bwd_ops(w) == ops
-    # quantise call: Q, K, V read once, int8 codes written, float32 block scales and the K mean
+    # quantise call: Q, K, V read once, int8 codes and their fp16 operand copies written, float32
+    # block scales and the K mean
     n = 2 * 16 * 8192 * 128
-    assert bench.quant_bytes(w) == 9 * n + 4 * (3 * 2 * 16 * 128 + 2 * 16 * 128)
+    small = 4 * (3 * 2 * 16 * 128 + 2 * 16 * 128)
+    assert bench.quant_bytes(w) == 15 * n + small
+    assert bench.quant_bytes(w, ops16=False) == 9 * n + small
 
 
 def test_qat_step_ops_and_cli():

@@ -105,6 +105,31 @@ def test_null_misaligned_and_workspace(sg):
     assert L.sage_quantize_smooth(ctypes.byref(p), *qargs, 1 << 30, None) == 1
 
 
+def test_ops16_flag_checks(sg):
+    """SAGE_FLAG_OPS16 needs a 16-byte aligned p->ops16 (SAGE_ERR_ARG / SAGE_ERR_ALIGN), drops the
+    widened operand copies from the forward (3 of them) and backward (2) workspaces, and is refused
+    by the FP4 entry points (fake device pointers are never dereferenced)."""
+    L = sg.lib()
+    n = 1 * 2 * 256 * 128
+    p = sg.make_params(1, 2, 256, 128, 0, False)
+    po = sg.make_params(1, 2, 256, 128, 0, False)
+    po.flags |= sg.binding.SAGE_FLAG_OPS16
+    po.ops16 = _fake(30)
+    # the copies sit first in both workspaces, each 256-byte aligned
+    assert L.sage_fwd_workspace_bytes(ctypes.byref(p)) - L.sage_fwd_workspace_bytes(ctypes.byref(po)) == 3 * 2 * n
+    assert L.sage_bwd_workspace_bytes(ctypes.byref(p)) - L.sage_bwd_workspace_bytes(ctypes.byref(po)) == 2 * 2 * n
+    assert L.sage_quantize_workspace_bytes(ctypes.byref(po)) == L.sage_quantize_workspace_bytes(ctypes.byref(p))
+    args = [_fake(i) for i in range(12)]
+    po.ops16 = None
+    assert L.sage_attn_fwd(ctypes.byref(po), *args, 1 << 30, None) == 1
+    po.ops16 = _fake(30) + 8
+    assert L.sage_attn_fwd(ctypes.byref(po), *args, 1 << 30, None) == 3
+    assert L.sage_quantize_smooth(ctypes.byref(po), *args, 1 << 30, None) == 3
+    po.ops16 = _fake(30)
+    assert L.sage_quantize_fp4(ctypes.byref(po), *args, 1 << 30, None) == 2
+    assert L.sage_attn_fwd_fp4(ctypes.byref(po), *args, 1 << 30, None) == 2
+
+
 def test_qknorm_argument_checks(sg):
     """The QK-norm calls refuse bad arguments before any launch (fake device pointers are never
     dereferenced)."""
@@ -157,19 +182,19 @@ def test_qat_argument_checks(sg):
 
 
 def test_noalloc_partials_query(sg):
-    """The allocation-free quantise call needs (304 + B*H)*d + B*H float64 words of K-mean scratch
-    with K-smoothing (a partial-sum slot of d for each of the pass's at most 304 CTAs and each
+    """The allocation-free quantise call needs (456 + B*H)*d + B*H float64 words of K-mean scratch
+    with K-smoothing (a partial-sum slot of d for each of the pass's at most 456 CTAs and each
     head, and a word of two 32-bit counters for each head) and none without; the host-only query
     says so, and returns 0 for parameters the call would refuse."""
     L = sg.lib()
     cap = L.sage_quantize_noalloc_max_partials()
     assert cap == 131072
-    for B, H, N, d in ((1, 3, 320, 64), (2, 16, 8192, 128), (1, 714, 8192, 128), (1, 715, 8192, 128)):
+    for B, H, N, d in ((1, 3, 320, 64), (2, 16, 8192, 128), (1, 563, 8192, 128), (1, 564, 8192, 128)):
         p = sg.make_params(B, H, N, d, 0, False)
-        assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == (304 + B * H) * d + B * H
-    # at d = 128, B*H = 715 exceeds the array and 714 fits
-    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 715, 8192, 128, 0, False))) > cap
-    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 714, 8192, 128, 0, False))) <= cap
+        assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == (456 + B * H) * d + B * H
+    # at d = 128, B*H = 564 exceeds the array and 563 fits
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 564, 8192, 128, 0, False))) > cap
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 563, 8192, 128, 0, False))) <= cap
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 256, 64, 0, False, smooth_k=False))) == 0
     assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(sg.make_params(1, 2, 100, 64, 0, False))) == 0
 

@@ -80,9 +80,15 @@ def test_sagebwd_calls_stay_inside_their_buffers(B, H, N, d, dt, causal, smooth_
     Q, K, V, dO = _inputs(B, H, N, d, dt, seed=N + d)
     snaps = [t.clone() for t in (Q, K, V, dO)]
     es = 2
-    for dump in (False, True):
+    for dump, ops in ((False, False), (True, False), (False, True)):
         bufs = {}
         p = sg.make_params(B, H, N, d, code, causal, smooth_q=smooth_q)
+        if ops:
+            # SAGE_FLAG_OPS16: the quantiser also writes the codes' fp16 values, which the
+            # forward and backward then read
+            bufs["ops16"] = Guarded(3 * 2 * n)
+            p.flags |= sg.binding.SAGE_FLAG_OPS16
+            p.ops16 = bufs["ops16"].ptr
         # ---- quantise (with workspace), then the allocation-free variant into fresh buffers
         for k, nbytes in (("Qh", n), ("Kh", n), ("Vh", n), ("sQ", 4 * nb), ("sK", 4 * nb), ("sV", 4 * nb),
                           ("muK", 4 * B * H * d), ("muQ", 4 * nb * d)):
@@ -95,13 +101,21 @@ def test_sagebwd_calls_stay_inside_their_buffers(B, H, N, d, dt, causal, smooth_
         assert st == 0
         _check(bufs, (Q, K, V), snaps[:3], "sage_quantize_smooth")
         na = {k: Guarded(bufs[k].n) for k in ("Qh", "Kh", "Vh", "sQ", "sK", "sV", "muK", "muQ")}
-        st = L.sage_quantize_smooth_noalloc(ctypes.byref(p), Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+        pn = sg.make_params(B, H, N, d, code, causal, smooth_q=smooth_q)
+        if ops:
+            na["ops16"] = Guarded(3 * 2 * n)
+            pn.flags |= sg.binding.SAGE_FLAG_OPS16
+            pn.ops16 = na["ops16"].ptr
+        st = L.sage_quantize_smooth_noalloc(ctypes.byref(pn), Q.data_ptr(), K.data_ptr(), V.data_ptr(),
                                             *[na[k].ptr for k in ("Qh", "Kh", "Vh", "sQ", "sK", "sV", "muK", "muQ")],
                                             _stream())
         assert st == 0
         _check(na, (Q, K, V), snaps[:3], "sage_quantize_smooth_noalloc")
         # ---- forward (optionally with the debug dump)
         pf = sg.make_params(B, H, N, d, code, causal, smooth_q=smooth_q)
+        if ops:
+            pf.flags |= sg.binding.SAGE_FLAG_OPS16
+            pf.ops16 = bufs["ops16"].ptr
         if dump:
             bufs["dump_f"] = Guarded(L.sage_dump_bytes(ctypes.byref(pf), 0))
             pf.flags |= sg.binding.SAGE_FLAG_DUMP
@@ -116,9 +130,12 @@ def test_sagebwd_calls_stay_inside_their_buffers(B, H, N, d, dt, causal, smooth_
                              bufs["muK"].ptr if smooth_q else None, bufs["muQ"].ptr if smooth_q else None,
                              bufs["O"].ptr, bufs["L"].ptr, bufs["ws_f"].ptr, wf, _stream())
         assert st == 0
-        _check(bufs, (Q, K, V), snaps[:3], f"sage_attn_fwd dump={dump}")
+        _check(bufs, (Q, K, V), snaps[:3], f"sage_attn_fwd dump={dump} ops16={ops}")
         # ---- backward (optionally with the debug dump)
         pb = sg.make_params(B, H, N, d, code, causal, smooth_q=smooth_q)
+        if ops:
+            pb.flags |= sg.binding.SAGE_FLAG_OPS16
+            pb.ops16 = bufs["ops16"].ptr
         if dump:
             bufs["dump_b"] = Guarded(L.sage_dump_bytes(ctypes.byref(pb), 1))
             pb.flags |= sg.binding.SAGE_FLAG_DUMP
@@ -134,7 +151,7 @@ def test_sagebwd_calls_stay_inside_their_buffers(B, H, N, d, dt, causal, smooth_
                              dO.data_ptr(), bufs["dQ"].ptr, bufs["dK"].ptr, bufs["dV"].ptr, bufs["ws_b"].ptr, wb,
                              _stream())
         assert st == 0
-        _check(bufs, (Q, K, V, dO), snaps, f"sage_attn_bwd dump={dump}")
+        _check(bufs, (Q, K, V, dO), snaps, f"sage_attn_bwd dump={dump} ops16={ops}")
         assert sg.sage_device_status() == 0
 
 

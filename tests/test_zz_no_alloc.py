@@ -51,8 +51,8 @@ def test_noalloc_matches_quantize_two_calls(B, H, N, d, dtype, smooth_q):
 
 
 def test_noalloc_rejects_beyond_capacity():
-    """B*H = 2048 heads of d = 128 need (304 + 2048) * 128 partial sums (one slot of d for each
-    of up to 304 CTAs and each head) and 2048 words of per-head counters: more than the array
+    """B*H = 2048 heads of d = 128 need (456 + 2048) * 128 partial sums (one slot of d for each
+    of up to 456 CTAs and each head) and 2048 words of per-head counters: more than the array
     holds.  The call gets real device tensors of the right size (about 150 MiB), so even
     a launch by mistake would stay inside its buffers; it must return SAGE_ERR_WORKSPACE, and the
     partials-needed query must agree."""
@@ -64,7 +64,7 @@ def test_noalloc_rejects_beyond_capacity():
     assert cap == 131072
     B, H, N, d = 1, 2048, 64, 128
     p = sg.make_params(B, H, N, d, sg.binding.SAGE_FP16, False)
-    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == (304 + B * H) * d + B * H > cap
+    assert L.sage_quantize_noalloc_partials_needed(ctypes.byref(p)) == (456 + B * H) * d + B * H > cap
     Q, K, V = (torch.zeros((B, H, N, d), dtype=torch.float16, device="cuda") for _ in range(3))
     with pytest.raises(sg.binding.SageError) as e:
         sg.sage_quantize_smooth_noalloc(Q, K, V)
