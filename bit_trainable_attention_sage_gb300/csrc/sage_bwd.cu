@@ -248,9 +248,11 @@ __device__ __forceinline__ void score_p_ds_8(const uint32_t (&sr)[8], const uint
 // their row data go out together, one wait covers them, and the two halves are computed back to
 // back, which gives the compiler eight independent column pairs to interleave.  (One 8-column
 // half per wait, with the next half's loads in flight, left each wait's work too short: 2 % slower
-// at d = 128 and 8 % at d = 64.  32 columns per wait, with 16 more registers for this warpgroup,
-// was 9 % slower at d = 128.)  The loop is kept rolled: the four warp roles run different code on
-// each SM sub-partition, and unrolled bodies overflow the instruction cache.
+// at d = 128 and 8 % at d = 64.  Bodies of four halves were slower still: 32 columns per wait,
+// with 16 more registers for this warpgroup, by 9 % at d = 128, and 16 columns per wait with the
+// next 16 columns' loads in flight (two alternating buffer sets) by 8 %.)  The loop is kept
+// rolled: the four warp roles run different code on each SM sub-partition, and larger bodies
+// overflow the instruction cache.
 __device__ __forceinline__ void reg_fence(uint32_t (&a)[8], uint32_t (&b)[8]) {
     asm volatile("" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
                  "+r"(a[7]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]),
