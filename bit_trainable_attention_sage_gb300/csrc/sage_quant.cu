@@ -690,6 +690,8 @@ __global__ void __launch_bounds__(kQuantThreads, NORM ? 2 : kQuantCtas) quantize
         } else {
             const int w = cta + (j - nAc) * grid;
             const int zi = w / sc.per_z, rem = w - zi * sc.per_z;
+            // K first (still in L2 after the K-mean); measured against K last, the order moves the
+            // pass by under 3 % either way (d = 128: K first 1.6 % faster; d = 64: 2.5 % slower)
             z = sc.nz == 1 ? 2 : (zi == 0 ? 1 : (zi == 1 ? 0 : 2));
             bh = rem / nb;
             blk = rem - bh * nb;
