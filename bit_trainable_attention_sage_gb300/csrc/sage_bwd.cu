@@ -482,8 +482,9 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
                                       const CUtensorMap *mapdOh) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
-    const int bh = blockIdx.y;
-    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const TileHead th = tile_order(a.causal);        // causal: key tile 0, the longest, first
+    const int bh = th.bh;
+    const int jt = th.rank;                          // key tile: keys [128 jt, 128 jt + 128)
     const int k0 = 128 * jt;
     const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
     const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
@@ -670,8 +671,9 @@ template <int D, int DPK, bool BIAS, bool DUMP, bool FP8, bool QAT>
 __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
-    const int bh = blockIdx.y;
-    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const TileHead th = tile_order(a.causal);        // causal: key tile 0, the longest, first
+    const int bh = th.bh;
+    const int jt = th.rank;                          // key tile: keys [128 jt, 128 jt + 128)
     const int k0 = 128 * jt;
     const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
     const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
@@ -840,8 +842,9 @@ template <int D, int DPK, bool BIAS, bool DUMP, bool QAT>
 __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
-    const int bh = blockIdx.y;
-    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const TileHead th = tile_order(a.causal);        // causal: key tile 0, the longest, first
+    const int bh = th.bh;
+    const int jt = th.rank;                          // key tile: keys [128 jt, 128 jt + 128)
     const int k0 = 128 * jt;
     const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
     const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair
@@ -971,8 +974,9 @@ template <int D, int DPK, bool BIAS, bool DUMP, bool QAT>
 __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
-    const int bh = blockIdx.y;
-    const int jt = blockIdx.x;                       // key tile: keys [128 jt, 128 jt + 128)
+    const TileHead th = tile_order(a.causal);        // causal: key tile 0, the longest, first
+    const int bh = th.bh;
+    const int jt = th.rank;                          // key tile: keys [128 jt, 128 jt + 128)
     const int k0 = 128 * jt;
     const int nblk = N >> 6;                         // 64-row blocks (N % 64 == 0)
     const int c_first = a.causal ? 2 * jt : 0;       // first query block with a live pair

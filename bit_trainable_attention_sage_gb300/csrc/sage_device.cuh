@@ -117,6 +117,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// The (tile rank, head) a CTA of a (tiles x heads) grid works on.  Causal tiles differ in length,
+// and CTAs start in linear block order as SMs free up: the heads are taken in groups of 8 and,
+// inside a group, rank 0 of every head first, then rank 1, ... (the caller maps rank 0 to its
+// longest tile).  The longest tiles then start first while a group's operands stay in L2; a
+// list-scheduling model of 152 SMs puts the causal makespan at 1.6 % (forward) and 1.2 %
+// (backward) above the ideal, against 16.7 % and 7.1 % head by head.  Non-causal tiles are all
+// alike: rank = blockIdx.x, head = blockIdx.y.
+struct TileHead {
+    int rank, bh;
+};
+__device__ __forceinline__ TileHead tile_order(int causal) {
+    if (!causal) return TileHead{static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y)};
+    constexpr int G = 8;
+    const int X = static_cast<int>(gridDim.x), BH = static_cast<int>(gridDim.y);
+    const int L = static_cast<int>(blockIdx.y) * X + static_cast<int>(blockIdx.x);
+    const int g = L / (X * G);
+    const int gs = min(G, BH - g * G);               // the last group may hold fewer heads
+    const int r = L - g * X * G;
+    return TileHead{r / gs, g * G + r % gs};
+}
+
 // ld.shared of four floats at a shared-memory address (16-byte aligned).  Volatile so that it is
 // not moved above the barrier wait that makes the data visible.
 __device__ __forceinline__ float4 lds128(uint32_t addr) {

@@ -271,10 +271,11 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
-    const int bh = blockIdx.y;
     const int npair = gridDim.x;
-    // causal: longest tile pairs first
-    const int ip = a.causal ? (npair - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    // causal: the longest tile pairs (the last ones) first
+    const TileHead th = tile_order(a.causal);
+    const int bh = th.bh;
+    const int ip = a.causal ? (npair - 1 - th.rank) : th.rank;
     const int q0 = ip * 256;
     int kv_end_t[2], nsteps_t[2];
 #pragma unroll
