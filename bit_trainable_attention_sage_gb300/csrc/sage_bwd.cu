@@ -15,9 +15,10 @@
 //   dP^T = V dO^T   (M=128 keys, N=64 q, K=d)   } [128b, 128b+64) and [128b+64, 128b+128)
 //   dK   = dS^T Q^  (M=128 keys, N=d, K=64 q; A = dS^ codes in shared memory)  -> R_B
 //   dV   = P^T dO^  (M=128 keys, N=d, K=64 q; A = P codes in TMEM over S^T)   -> R_A
-//   dQ   d = 128: dQ_g^T = K^_g^T dS^_g^T (M=d, N=64 q, K=64 keys of block g) -> R_A + 64 g,
-//          once the dV warpgroup has read the dV product out of R_A;  d = 64: dQ_g = dS^_g K^_g
-//          for two query blocks at once (M=128 q, N=d) into R_Q.
+//   dQ   d = 128: dQ_g^T = K^_g^T dS^_g^T (M=d, N=64 q, K=64 keys of block g) -> R_B + 64 g,
+//          once the dK warpgroup has read the dK product out of R_B (dK is issued first, so
+//          its read-out ends first);  d = 64: dQ_g = dS^_g K^_g for two query blocks at once
+//          (M=128 q, N=d) into R_Q.
 // With two score buffers the tensor core computes the next block's S^T and dP^T while the score
 // warpgroup turns the current block into codes, so the two overlap; a score buffer is free again
 // as soon as the dV MMA has read the P codes (the tensor pipe runs in issue order).
@@ -96,7 +97,8 @@ __device__ __forceinline__ void regs_to() {
     if constexpr (R > kRegsLaunch) regs_inc<R>();
     else if constexpr (R < kRegsLaunch) regs_dec<R>();
 }
-constexpr uint32_t R_A = 256;                         // dV product (d columns); d = 128: dQ^T
+constexpr uint32_t R_A = 256;                         // dV product (d columns)
+constexpr uint32_t R_B128 = R_A + 128;                // d = 128: dK product, then the dQ^T products
 constexpr uint32_t R_Q = 384;                         // d = 64: the two dQ products
 constexpr int kScaleSlots = 8;                        // tile scales kept for 8 steps
 // operands of the dP MMA: the unquantised fp16 or bf16 dO and V (the method), or their INT8 codes
@@ -124,7 +126,8 @@ struct Smem {
     uint64_t kv_full, q_full[3], q_free[3], do_full[2], do_free[2], doh_full, doh_free;
     uint64_t meta_full[3], meta_free[3], sd_full[2], codes_ready[2];
     uint64_t a_full, a_free, b_full, b_free;           // dV product in R_A, dK product in R_B
-    uint64_t aq_full, aq_free;                         // d = 128: dQ^T products in R_A
+    uint64_t aq_full, aq_free;                         // d = 128: dQ^T products in R_B
+    uint64_t dv_done;                                  // the dV MMAs of a step have completed
     uint64_t rq_full, rq_free;                         // d = 64: dQ products in R_Q
     uint64_t dss_free;                                 // d = 64: the dQ MMAs are done with both dS^ tiles
     uint64_t mma_done;
@@ -432,9 +435,9 @@ __device__ __forceinline__ void score_pass_qat(uint32_t s_col, uint32_t dp_col, 
 }
 
 // d = 128: this warpgroup's 32 query rows [32 half, 32 half + 32) of the step's two transposed dQ
-// products in R_A (thread = d column, TMEM columns = query rows): the scaled sum is added to
+// products in R_B (thread = d column, TMEM columns = query rows): the scaled sum is added to
 // global dQ by float32 reductions, one row at a time, so a warp's 32 lanes cover 32 consecutive
-// floats of the row.  R_A is released once read.
+// floats of the row.  R_B is released once read.  (Two 8-row loads per wait: four were slower.)
 // With DUMP the raw integer products of key block 0 and 1 also go to dump_g0 / dump_g1 (element
 // [q][tq] of the tile's 64 x 128 product, or NULL for a key block past N).
 template <bool DUMP>
@@ -445,8 +448,8 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
 #pragma unroll 1
     for (int r0 = 0; r0 < 32; r0 += 8) {
         uint32_t v0[8], v1[8];
-        tmem_ld8(lane_base + R_A + 32 * half + r0, v0);
-        tmem_ld8(lane_base + R_A + 64 + 32 * half + r0, v1);
+        tmem_ld8(lane_base + R_B128 + 32 * half + r0, v0);
+        tmem_ld8(lane_base + R_B128 + 64 + 32 * half + r0, v1);
         tmem_wait_ld_regs(v0, v1);
         if (DUMP) {
 #pragma unroll
@@ -465,7 +468,7 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
             dq[k + 1] = t.y;
         }
         if (r0 + 8 == 32) {
-            // every TMEM read of this warpgroup is done: R_A may be refilled
+            // every TMEM read of this warpgroup is done: R_B may be refilled
             tc_fence_before();
             __syncwarp();
             if (lane_id() == 0) mbar_arrive(aq_free);
@@ -473,6 +476,40 @@ __device__ __forceinline__ void dq_consume_128(uint32_t lane_base, int half, flo
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             red_add(dst + (r0 + k) * 128, dq[k]);
+    }
+}
+
+// acc[i] += sc * (product column i), i < D, from the TMEM columns [col, col + D) of this warp's
+// lanes (thread = key).  Four 8-column loads share one wait: the read-out of the dV product is on
+// the path to the dQ MMAs (they reuse its columns), and a wait per 8 columns left it waiting on
+// TMEM latency 16 times a step (2 % of the backward call at d = 128).  With DUMP the raw integer
+// products also go to dump_row (NULL for a key past N).
+template <int D, bool DUMP>
+__device__ __forceinline__ void add_scaled_product(uint32_t col, float sc, float (&acc)[D], int32_t *dump_row) {
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r0[8], r1[8], r2[8], r3[8];
+        tmem_ld8(col + cc, r0);
+        tmem_ld8(col + cc + 8, r1);
+        tmem_ld8(col + cc + 16, r2);
+        tmem_ld8(col + cc + 24, r3);
+        tmem_wait_ld_regs(r0, r1);
+        reg_fence(r2, r3);            // (the wait covers these loads too: no use may move above it)
+        const uint32_t *rr[4] = {r0, r1, r2, r3};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            if (DUMP && dump_row) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dump_row[cc + 8 * h + k] = static_cast<int32_t>(__uint_as_float(rr[h][k]));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k += 2) {
+                const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(rr[h][k]), __uint_as_float(rr[h][k + 1])},
+                                  f2{acc[cc + 8 * h + k], acc[cc + 8 * h + k + 1]});
+                acc[cc + 8 * h + k] = t.x;
+                acc[cc + 8 * h + k + 1] = t.y;
+            }
+        }
     }
 }
 
@@ -557,11 +594,15 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------------- MMA issuer
-        // Steady state per step c: dK(c), dV(c), dQ(c) (d = 128 into R_A once dV(c) has been read
+        // Steady state per step c: dK(c), dV(c), dQ(c) (d = 128 into R_B once dK(c) has been read
         // out of it), then S^T / dP^T of step c + 2 into the score buffer step c used.  S^T / dP^T
-        // of step c + 1 are already done, so the score warpgroup moves on at once; dQ(c) goes
-        // first because the score warpgroup's pass 2 of step c + 1 waits for it to release the
-        // dS^ tile.
+        // of step c + 1 are already done, so the score warpgroup moves on at once.  The dS^ tile
+        // of step c is written again at step c + 2, whose S^T / dP^T complete after dK(c) and
+        // dQ(c) (d = 128), which read it; d = 64 the score warpgroup waits for dss_free.  S^T of
+        // step c + 2 overwrites the P codes dV(c) reads as its A operand, and the tensor pipe's
+        // ordering covers MMAs into one accumulator only, so it waits for dV(c) to complete
+        // (dv_done; normally met by then: d = 128 the dK(c) read-out, d = 64 the dQ pair comes
+        // in between).
         if (elect_one()) {
             // Attn-QAT: every operand in the input type; otherwise codes as fp16, dP per dtype
             constexpr bool kOpsBf16 = QAT && DPK == kDpBf16;
@@ -605,7 +646,8 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
             for (int c = 0; c < n && ok; ++c) {
                 const int b = c & 1, s3 = c % 3;
                 if (!(ok = mbar_wait(&s.codes_ready[b], (c >> 1) & 1, abort_flag, &g_bwd_err, 10))) break;
-                if (c >= 1 && !(ok = mbar_wait(&s.b_free, (c - 1) & 1, abort_flag, &g_bwd_err, 11))) break;
+                // R_B must be empty: d = 128 the dQ(c - 1) products read out, d = 64 dK(c - 1)
+                if (c >= 1 && !(ok = mbar_wait(D == 128 ? &s.aq_free : &s.b_free, (c - 1) & 1, abort_flag, &g_bwd_err, 11))) break;
                 tc_fence_after();
                 // dK = dS^T Q^: A = this step's dS^ codes (K-major rows of 64 q), B = Q^ block
                 // read as MN-major (N = d)
@@ -620,26 +662,32 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
                 umma_commit(&s.q_free[s3]);
                 // dV = P^T dO^: A = the P codes in TMEM (8 columns per 16 q)
                 if (!(ok = mbar_wait(&s.doh_full, c & 1, abort_flag, &g_bwd_err, 12))) break;
-                // R_A must be empty: d = 128 the dQ(c - 1) products read out, d = 64 dV(c - 1)
-                if (c >= 1 && !(ok = mbar_wait(D == 128 ? &s.aq_free : &s.a_free, (c - 1) & 1, abort_flag, &g_bwd_err, 13))) break;
+                // R_A must be empty: dV(c - 1) read out
+                if (c >= 1 && !(ok = mbar_wait(&s.a_free, (c - 1) & 1, abort_flag, &g_bwd_err, 13))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk)
                     umma_ts(tmem + R_A, tmem + 128 * b + 8 * kk, dDoh + ((kk * 2048) >> 4), idKV, kk > 0);
                 umma_commit(&s.a_full);
                 umma_commit(&s.doh_free);
+                umma_commit(&s.dv_done);
                 if (D == 128) {
                     // dQ_g^T = K^_g^T dS^_g^T: A = K^ tile read as MN-major (M = d), B = the dS^
-                    // tile read as MN-major (N = q); product g into R_A + 64 g once the dV
-                    // warpgroup has read dV(c) out of R_A
-                    if (!(ok = mbar_wait(&s.a_free, c & 1, abort_flag, &g_bwd_err, 16))) break;
+                    // tile read as MN-major (N = q); product g into R_B + 64 g once the dK
+                    // warpgroup has read dK(c) out of R_B.  (Reusing R_A after the dV read-out,
+                    // which ends one product later, made the backward 4.5 % slower: S^T / dP^T
+                    // of step c + 2 queue behind dQ(c).)  dv_done first: S^T of step c + 2,
+                    // issued next, overwrites dV(c)'s A operand (waiting for it after the dQ
+                    // MMAs instead cost 1 %).
+                    if (c + 2 < n && !(ok = mbar_wait(&s.dv_done, c & 1, abort_flag, &g_bwd_err, 17))) break;
+                    if (!(ok = mbar_wait(&s.b_free, c & 1, abort_flag, &g_bwd_err, 16))) break;
                     tc_fence_after();
 #pragma unroll 1
                     for (int g = 0; g < 2; ++g)
 #pragma unroll 1
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t o = ((64 * g + 16 * kk) * 128) >> 4;
-                            umma_ss(tmem + R_A + 64 * g, dKmn + o, dDssM + ((b * 16384) >> 4) + o, idQ, kk > 0);
+                            umma_ss(tmem + R_B + 64 * g, dKmn + o, dDssM + ((b * 16384) >> 4) + o, idQ, kk > 0);
                         }
                     umma_commit(&s.aq_full);
                 } else if ((c & 1) || c == n - 1) {
@@ -658,7 +706,10 @@ __device__ __forceinline__ void control_role(Smem<D> &s, const BwdArgs &a, const
                     umma_commit(&s.rq_full);
                     umma_commit(&s.dss_free);
                 }
-                if (c + 2 < n && !(ok = issue_sd(c + 2))) break;
+                if (c + 2 < n) {
+                    if (D != 128 && !(ok = mbar_wait(&s.dv_done, c & 1, abort_flag, &g_bwd_err, 17))) break;
+                    if (!(ok = issue_sd(c + 2))) break;
+                }
             }
             umma_commit(&s.mma_done);
             mbar_wait_drain(&s.mma_done, 0, &g_bwd_err, 15);
@@ -884,23 +935,7 @@ __device__ __forceinline__ void dv_role(Smem<D> &s, const BwdArgs &a) {
             int32_t *dump_row = (DUMP && key_ok)
                 ? a.dump_dv + (((static_cast<size_t>(bh) * nblk + qb) * nblk + 2 * jt + kb) * 64 + (tq & 63)) * D
                 : nullptr;
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 8) {
-                uint32_t r[8];
-                tmem_ld8(lane_base + R_A + cc, r);
-                tmem_wait_ld_regs(r);
-                if (DUMP && dump_row) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) dump_row[cc + k] = static_cast<int32_t>(__uint_as_float(r[k]));
-                }
-#pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(r[k]), __uint_as_float(r[k + 1])},
-                                      f2{dv[cc + k], dv[cc + k + 1]});
-                    dv[cc + k] = t.x;
-                    dv[cc + k + 1] = t.y;
-                }
-            }
+            add_scaled_product<D, DUMP>(lane_base + R_A, sc, dv, dump_row);
         }
         tc_fence_before();
         __syncwarp();
@@ -1017,23 +1052,7 @@ __device__ __forceinline__ void dk_role(Smem<D> &s, const BwdArgs &a) {
             int32_t *dump_row = (DUMP && key_ok)
                 ? a.dump_dk + (((static_cast<size_t>(bh) * nblk + qb) * nblk + 2 * jt + kb) * 64 + (tq & 63)) * D
                 : nullptr;
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 8) {
-                uint32_t r[8];
-                tmem_ld8(lane_base + R_B + cc, r);
-                tmem_wait_ld_regs(r);
-                if (DUMP && dump_row) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) dump_row[cc + k] = static_cast<int32_t>(__uint_as_float(r[k]));
-                }
-#pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const f2 t = fma2(f2{sc, sc}, f2{__uint_as_float(r[k]), __uint_as_float(r[k + 1])},
-                                      f2{dk[cc + k], dk[cc + k + 1]});
-                    dk[cc + k] = t.x;
-                    dk[cc + k + 1] = t.y;
-                }
-            }
+            add_scaled_product<D, DUMP>(lane_base + R_B, sc, dk, dump_row);
         }
         if (BIAS) {
             const float w = __fmul_rn(s.colsum[c & 3][tq], a.inv_sqrt_d);
@@ -1087,7 +1106,7 @@ sage_bwd_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant_
                            &s.do_free[1], &s.doh_full, &s.doh_free, &s.meta_full[0],
                            &s.meta_full[1], &s.meta_full[2], &s.sd_full[0], &s.sd_full[1],
                            &s.a_full, &s.b_full, &s.aq_full, &s.rq_full, &s.dss_free,
-                           &s.mma_done};
+                           &s.dv_done, &s.mma_done};
         for (uint64_t *b : one) mbar_init(b, 1);
         uint64_t *four[] = {&s.meta_free[0], &s.meta_free[1], &s.meta_free[2], &s.codes_ready[0],
                             &s.codes_ready[1], &s.a_free, &s.b_free, &s.rq_free};
