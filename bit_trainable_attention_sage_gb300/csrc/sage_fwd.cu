@@ -18,6 +18,8 @@
 //   warp 9      allocates TMEM; one lane issues every MMA, for each tile t:
 //                 S_t    = Q^_t K^T                 M=128 N=128 K=d  -> TMEM cols 256t + [0,128)
 //                 PV_t,h = P^_t[:,64h:64h+64] V^_h  M=128 N=d   K=64 -> TMEM cols 256t + [128,256)
+//               (d = 64: half h into its own 64 columns 256t + 128 + 64h, so that PV_t,1 need
+//               not wait for the O update that reads PV_t,0)
 //   warps 0-3   softmax of tile 0, warps 4-7 of tile 1: thread = query row = TMEM lane.  Per step:
 //               logits, row max per 64-key block, P codes (written back to TMEM over the consumed
 //               S columns, as the A operand of the PV MMA), running max and sum, then
@@ -80,7 +82,8 @@ struct Smem {
     alignas(1024) uint8_t k[2][D / 64][128 * 128];   // two stages: step j's tile in stage j & 1
     alignas(1024) uint8_t v[2][D / 64][128 * 128];
     uint64_t q_full, k_full[2], k_free[2], v_full[2], v_free[2], mma_done;
-    uint64_t s_full[2], p_full[2][2], pv_full[2], pv_free[2];   // p_full[tile][64-key half]
+    uint64_t s_full[2], p_full[2][2];                  // p_full[tile][64-key half]
+    uint64_t pv_full[2][D == 64 ? 2 : 1], pv_free[2][D == 64 ? 2 : 1];   // [tile][PV buffer]
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -269,6 +272,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // PV accumulators a tile: d = 64 fits one per 64-key half into the tile's 128 PV columns
+    constexpr int kPvBuffers = D == 64 ? 2 : 1;
     const int warp = threadIdx.x >> 5;
     const int N = a.N;
     const int npair = gridDim.x;
@@ -304,8 +309,10 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mbar_init(&s.s_full[t], 1);
             mbar_init(&s.p_full[t][0], 4);
             mbar_init(&s.p_full[t][1], 4);
-            mbar_init(&s.pv_full[t], 1);
-            mbar_init(&s.pv_free[t], 4);
+            for (int pb = 0; pb < kPvBuffers; ++pb) {
+                mbar_init(&s.pv_full[t][pb], 1);
+                mbar_init(&s.pv_free[t][pb], 4);
+            }
         }
         fence_barrier_init();
     }
@@ -352,7 +359,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         if (elect_one()) {
             constexpr uint32_t idS = idesc_f16(128, 128, BF16OPS, false, false);
             constexpr uint32_t idPV = idesc_f16(128, D, BF16OPS, false, true);
-            int pv_count[2] = {0, 0};
+            int pv_count[2][kPvBuffers] = {};                   // [tile][PV buffer] uses
             // S_t = Q^_t K^(j)^T into the tile's S columns, K^(j) from stage kst = j & 1
             auto issue_s = [&](int t, int kst) {
                 const uint32_t q_addr = smem_u32(s.q[t][0]);
@@ -390,18 +397,20 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     // this half's P codes are in place (each half has its own barrier, so the
                     // first half's PV runs while the second half is being coded)
                     if (!mbar_wait(&s.p_full[t][h], j & 1, abort_flag, &g_fwd_err, 7)) return false;
-                    // the tile's PV accumulator must have been read out
-                    if (pv_count[t] > 0 &&
-                        !mbar_wait(&s.pv_free[t], (pv_count[t] - 1) & 1, abort_flag, &g_fwd_err, 9)) return false;
+                    // the PV buffer must have been read out (d = 128: the tile's one buffer, so the
+                    // O update of the previous half; d = 64: this half's buffer of the last step)
+                    const int pb = kPvBuffers == 2 ? h : 0;
+                    if (pv_count[t][pb] > 0 &&
+                        !mbar_wait(&s.pv_free[t][pb], (pv_count[t][pb] - 1) & 1, abort_flag, &g_fwd_err, 9)) return false;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t vrow = 64 * h + 16 * kk;
-                        umma_ts(tmem + 256 * t + 128, tmem + 256 * t + 32 * h + 8 * kk,
+                        umma_ts(tmem + 256 * t + 128 + 64 * pb, tmem + 256 * t + 32 * h + 8 * kk,
                                 sdesc_sw128(v_addr + vrow * 128, 16384, 1024), idPV, kk > 0);
                     }
-                    umma_commit(&s.pv_full[t]);
-                    ++pv_count[t];
+                    umma_commit(&s.pv_full[t][pb]);
+                    ++pv_count[t][pb];
                     if (h == 1 && j + 1 < nsteps_t[t]) {
                         if (!k_next) {
                             if (!mbar_wait(&s.k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, &g_fwd_err, 6)) return false;
@@ -441,7 +450,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < D; ++c) o[c] = 0.0f;
         float m = -INFINITY, l = 0.0f;
-        int pv_uses = 0;
+        int pv_uses[kPvBuffers] = {};                 // per PV buffer
         for (int j = 0; j < my_steps; ++j) {
             if (!mbar_wait_warp(&s.s_full[t], j & 1, abort_flag, &g_fwd_err, 10)) break;
             tc_fence_after();
@@ -516,14 +525,15 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (h == 1 && !has_b) break;
-                if (!mbar_wait_warp(&s.pv_full[t], pv_uses & 1, abort_flag, &g_fwd_err, 11)) break;
+                const int pb = kPvBuffers == 2 ? h : 0;
+                if (!mbar_wait_warp(&s.pv_full[t][pb], pv_uses[pb] & 1, abort_flag, &g_fwd_err, 11)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D; cc += 32) {
                     // 32 columns a wait: two loads in flight
                     uint32_t raw[32];
-                    tmem_ld16(lane_base + 128 + cc, *reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
-                    tmem_ld16(lane_base + 128 + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
+                    tmem_ld16(lane_base + 128 + 64 * pb + cc, *reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
+                    tmem_ld16(lane_base + 128 + 64 * pb + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
                     tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
                     tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
                     // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
@@ -548,8 +558,8 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane_id() == 0) mbar_arrive(&s.pv_free[t]);
-                ++pv_uses;
+                if (lane_id() == 0) mbar_arrive(&s.pv_free[t][pb]);
+                ++pv_uses[pb];
             }
         }
         // epilogue: O / l in the output type, L = (m + log2 l) ln 2 (the O' pass writes O' alone)

@@ -89,13 +89,19 @@ __device__ __forceinline__ uint2 pack_codes8_e4m3(const float (&x)[8], float del
     return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
-// fp16 copies of the E4M3 codes of 8 values
-__device__ __forceinline__ uint4 pack_codes8_e4m3_f16(const float (&x)[8], float delta) {
-    uint32_t w[4];
+// E4M3 codes of 8 values and, in *h16, their fp16 values: one division a value, the fp16 value
+// converted from the code (every E4M3 value is exact in fp16)
+__device__ __forceinline__ uint2 pack_codes8_e4m3_h16(const float (&x)[8], float delta, uint4 *h16) {
+    uint32_t w[4], h[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        w[i] = delta == 0.0f ? 0u : e4m3x2_f16x2(__fdiv_rn(x[2 * i], delta), __fdiv_rn(x[2 * i + 1], delta));
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i) {
+        const uint16_t c = delta == 0.0f ? static_cast<uint16_t>(0)
+                                         : e4m3x2(__fdiv_rn(x[2 * i], delta), __fdiv_rn(x[2 * i + 1], delta));
+        w[i] = c;
+        h[i] = e4m3x2_to_f16x2(c);
+    }
+    *h16 = make_uint4(h[0], h[1], h[2], h[3]);
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 // integer-valued fp16 copies of the codes (the tensor-core operand format on sm_103a)
@@ -985,8 +991,13 @@ __global__ void __launch_bounds__(kQuantThreads, NORM ? 2 : kQuantCtas) quantize
 #pragma unroll
             for (int k = 0; k < kIters; ++k) {
                 const size_t r = static_cast<size_t>(rg + k * kRows) * D;
-                *reinterpret_cast<uint2 *>(dst + r) = pack_codes8_e4m3(x[k], delta);
-                if (h16) *reinterpret_cast<uint4 *>(h16 + r) = pack_codes8_e4m3_f16(x[k], delta);
+                if (h16) {
+                    uint4 hv;
+                    *reinterpret_cast<uint2 *>(dst + r) = pack_codes8_e4m3_h16(x[k], delta, &hv);
+                    *reinterpret_cast<uint4 *>(h16 + r) = hv;
+                } else {
+                    *reinterpret_cast<uint2 *>(dst + r) = pack_codes8_e4m3(x[k], delta);
+                }
             }
         } else if (delta >= 0x1p-126f) {
             const float rcp = __frcp_rn(delta);
@@ -1379,8 +1390,10 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(BwdPrologueArgs a) {
             *reinterpret_cast<uint4 *>(a.dO16 + off) = h;
             if (a.dOh) *reinterpret_cast<uint2 *>(a.dOh + off) = c;
         } else {
-            *reinterpret_cast<uint4 *>(a.dO16 + off) =
-                a.fp8 ? pack_codes8_e4m3_f16(x[it], delta) : pack_codes8_f16(x[it], delta);
+            uint4 h;
+            if (a.fp8) (void)pack_codes8_e4m3_h16(x[it], delta, &h);
+            else h = pack_codes8_f16(x[it], delta);
+            *reinterpret_cast<uint4 *>(a.dO16 + off) = h;
             if (a.dOh) *reinterpret_cast<uint2 *>(a.dOh + off) = pack_codes8(x[it], delta);
         }
     }
