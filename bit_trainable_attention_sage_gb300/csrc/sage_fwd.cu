@@ -529,16 +529,17 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!mbar_wait_warp(&s.pv_full[t][pb], pv_uses[pb] & 1, abort_flag, &g_fwd_err, 11)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    // 32 columns a wait: two loads in flight
-                    uint32_t raw[32];
-                    tmem_ld16(lane_base + 128 + 64 * pb + cc, *reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
-                    tmem_ld16(lane_base + 128 + 64 * pb + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
-                    tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[0]));
-                    tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[16]));
+                for (int cc = 0; cc < D; cc += 64) {
+                    // 64 columns a wait, four loads in flight (32 a wait: the forward 1.2 % slower)
+                    uint32_t raw[64];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(lane_base + 128 + 64 * pb + cc + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&raw[16 * q]));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&raw[16 * q]));
                     // column pairs in packed float32 arithmetic (bit-identical to the scalar steps)
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
+                    for (int k = 0; k < 64; k += 2) {
                         const f2 pv2{__uint_as_float(raw[k]), __uint_as_float(raw[k + 1])};
                         const f2 o2{o[cc + k], o[cc + k + 1]};
                         const f2 r2 = (h == 0) ? fma2(f2{alpha, alpha}, o2, mul2(f2{cpv[0], cpv[0]}, pv2))
@@ -547,7 +548,7 @@ sage_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         o[cc + k + 1] = r2.y;
                     }
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
+                    for (int k = 0; k < 64; ++k) {
                         const float pv = __uint_as_float(raw[k]);
                         if (DUMP) {
                             if (grow < N)
