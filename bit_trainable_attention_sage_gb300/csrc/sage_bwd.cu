@@ -21,7 +21,8 @@
 //          (M=128 q, N=d) into R_Q.
 // With two score buffers the tensor core computes the next block's S^T and dP^T while the score
 // warpgroup turns the current block into codes, so the two overlap; a score buffer is free again
-// as soon as the dV MMA has read the P codes (the tensor pipe runs in issue order).
+// once the dV MMA that reads its P codes has completed (the MMA thread waits for it: the tensor
+// pipe's ordering covers MMAs into one accumulator only).
 // Shared-memory bandwidth (128 B per clock per SM) is the bound to respect: the N = 64 MMAs read
 // their A operand once per 64 queries, so nothing else goes through shared memory that need not
 // (no dQ staging: dQ is reduced into global memory straight from registers).
@@ -856,7 +857,7 @@ __device__ __forceinline__ void score_role(Smem<D> &s, const BwdArgs &a) {
             }
         }
         // the dQ MMAs that read this dS^ tile two steps ago must be done: d = 128 they ran before
-        // this step's S^T / dP^T (the tensor pipe runs in issue order), d = 64 they are those of
+        // this step's S^T / dP^T (whose commit tracks every MMA issued before), d = 64 they are those of
         // the previous step pair
         // (a warp giving up here skips pass 2 and, unless this was the last step, flags the next
         // step's barrier at once: every warp has passed this step's barrier, so none still reads
