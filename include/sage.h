@@ -15,8 +15,9 @@
  *   - Every pointer is DEVICE memory allocated and owned by the caller, except `p` (host).  The
  *     library allocates nothing.  Scratch memory is the caller's `workspace` of at least the size
  *     the matching *_workspace_bytes() query returns, except for sage_quantize_smooth_noalloc,
- *     which keeps its scratch in a fixed array inside the library.  The only other state kept
- *     between calls is the device error word that sage_device_status() reads and clears.
+ *     which keeps its scratch in a fixed array inside the library.  The other state kept between
+ *     calls is the device error word that sage_device_status() reads and clears, and host-side
+ *     caches (the quantise pass's occupancy-derived grid size, that array's address per device).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  The
  *     return value reports argument and launch errors only; a device-side timeout of a bounded
  *     wait is reported by sage_device_status().
