@@ -17,7 +17,8 @@
  *     the matching *_workspace_bytes() query returns, except for sage_quantize_smooth_noalloc,
  *     which keeps its scratch in a fixed array inside the library.  The other state kept between
  *     calls is the device error word that sage_device_status() reads and clears, and host-side
- *     caches (the quantise pass's occupancy-derived grid size, that array's address per device).
+ *     caches (the SM count per device, the quantise kernels' occupancy, that array's address
+ *     per device).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  The
  *     return value reports argument and launch errors only; a device-side timeout of a bounded
  *     wait is reported by sage_device_status().
